@@ -1,0 +1,7 @@
+"""Plain CPU oracle for vertical-slash sparse attention (test infrastructure).
+
+ONLY ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The product path never calls it.
+See ``oracle/vs_oracle.py`` for the functions and the passages they follow.
+"""
+from .vs_oracle import *  # noqa: F401,F403

@@ -1,0 +1,128 @@
+"""Pins for the oracle's masked attention forward and backward.
+
+Checks against (1) PyTorch's dense scaled-dot-product attention in fp64 on
+the CPU when every line is kept (the VS mask then equals the causal mask),
+(2) PyTorch autograd through an explicitly masked softmax, (3) central finite
+differences, and (4) explicit per-entry loops.  The online softmax across KV
+blocks in the ring-attention page (section 2.1) computes exactly this
+masked softmax, so the oracle is the definition itself.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import (attention_backward, attention_forward, attention_forward_rows,
+                    explicit_mask)
+
+
+def _inputs(L, Hq, Hkv, d, seed):
+    rng = np.random.default_rng(seed)
+    return (rng.standard_normal((L, Hq, d)), rng.standard_normal((L, Hkv, d)),
+            rng.standard_normal((L, Hkv, d)), rng.standard_normal((L, Hq, d)))
+
+
+def _torch_masked(Q, K, V, masks, dO):
+    Hq, G = Q.shape[1], Q.shape[1] // K.shape[1]
+    q = torch.tensor(Q, dtype=torch.float64).permute(1, 0, 2).requires_grad_()
+    k = torch.tensor(K, dtype=torch.float64).permute(1, 0, 2).requires_grad_()
+    v = torch.tensor(V, dtype=torch.float64).permute(1, 0, 2).requires_grad_()
+    ke, ve = k.repeat_interleave(G, 0), v.repeat_interleave(G, 0)
+    m = torch.tensor(np.stack(masks))
+    o = torch.nn.functional.scaled_dot_product_attention(q, ke, ve, attn_mask=m)
+    o.backward(torch.tensor(dO, dtype=torch.float64).permute(1, 0, 2))
+    return (o.detach().permute(1, 0, 2).numpy(), q.grad.permute(1, 0, 2).numpy(),
+            k.grad.permute(1, 0, 2).numpy(), v.grad.permute(1, 0, 2).numpy())
+
+
+@pytest.mark.parametrize("Hq,Hkv", [(1, 1), (4, 2), (4, 1)])
+def test_all_lines_kept_equals_dense_causal(Hq, Hkv):
+    L, d, bs = 256, 16, 64
+    Q, K, V, dO = _inputs(L, Hq, Hkv, d, Hq * 10 + Hkv)
+    index = [(np.array([], np.int64), np.arange(L // bs))] * Hq
+    O, LSE = attention_forward(Q, K, V, index)
+    G = Hq // Hkv
+    q = torch.tensor(Q).permute(1, 0, 2)
+    k = torch.tensor(K).permute(1, 0, 2).repeat_interleave(G, 0)
+    v = torch.tensor(V).permute(1, 0, 2).repeat_interleave(G, 0)
+    ref = torch.nn.functional.scaled_dot_product_attention(q, k, v, is_causal=True)
+    np.testing.assert_allclose(O, ref.permute(1, 0, 2).numpy(), atol=1e-12)
+    s = (q @ k.transpose(1, 2)) / math.sqrt(d)
+    s = s.masked_fill(~torch.ones(L, L, dtype=torch.bool).tril(), float("-inf"))
+    np.testing.assert_allclose(LSE, torch.logsumexp(s, -1).numpy(), atol=1e-12)
+    # all verticals kept, only band 0: also dense causal
+    index2 = [(np.arange(L), np.array([0]))] * Hq
+    O2, _ = attention_forward(Q, K, V, index2)
+    np.testing.assert_allclose(O2, O, atol=1e-12)
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_masked_fwd_bwd_vs_autograd(seed):
+    L, Hq, Hkv, d, bs = 128, 4, 2, 8, 16
+    Q, K, V, dO = _inputs(L, Hq, Hkv, d, 100 + seed)
+    rng = np.random.default_rng(seed)
+    index, masks = [], []
+    for h in range(Hq):
+        S = np.union1d(rng.choice(L // bs, 3, replace=False), [0])
+        Vv = np.sort(rng.choice(L, 9, replace=False))
+        index.append((Vv, S))
+        masks.append(explicit_mask(L, Vv, S, bs))
+    O, _ = attention_forward(Q, K, V, index, block=bs)
+    dQ, dK, dV = attention_backward(Q, K, V, dO, index, block=bs)
+    rO, rdQ, rdK, rdV = _torch_masked(Q, K, V, masks, dO)
+    for a, b in ((O, rO), (dQ, rdQ), (dK, rdK), (dV, rdV)):
+        np.testing.assert_allclose(a, b, atol=1e-11, rtol=1e-11)
+
+
+def test_backward_finite_differences():
+    L, Hq, Hkv, d, bs = 16, 2, 1, 4, 4
+    Q, K, V, dO = _inputs(L, Hq, Hkv, d, 9)
+    index = [(np.array([1, 6]), np.array([0, 2])), (np.array([0]), np.array([0, 1, 3]))]
+    dQ, dK, dV = attention_backward(Q, K, V, dO, index, block=bs)
+
+    def f(Qx, Kx, Vx):
+        O, _ = attention_forward(Qx, Kx, Vx, index, block=bs)
+        return float((O * dO).sum())
+
+    eps = 1e-6
+    rng = np.random.default_rng(0)
+    for X, G in ((Q, dQ), (K, dK), (V, dV)):
+        for _ in range(12):
+            idx = tuple(rng.integers(0, s) for s in X.shape)
+            old = X[idx]
+            X[idx] = old + eps
+            fp = f(Q, K, V)
+            X[idx] = old - eps
+            fm = f(Q, K, V)
+            X[idx] = old
+            num = (fp - fm) / (2 * eps)
+            assert abs(num - G[idx]) <= 1e-7 * max(1.0, abs(G[idx]))
+
+
+def test_forward_explicit_loops():
+    L, d, bs = 40, 3, 4
+    Q, K, V, _ = _inputs(L, 1, 1, d, 21)
+    Vv, S = np.array([2, 13, 30]), np.array([0, 3, 5])
+    O, LSE = attention_forward(Q, K, V, [(Vv, S)], block=bs)
+    for n in range(L):
+        act = [m for m in range(n + 1)
+               if (n // bs - m // bs) in (0, 3, 5) or m in (2, 13, 30)]
+        sc = [sum(Q[n, 0, c] * K[m, 0, c] for c in range(d)) / math.sqrt(d) for m in act]
+        mx = max(sc)
+        e = [math.exp(x - mx) for x in sc]
+        for c in range(d):
+            ref = sum(e[j] * V[act[j], 0, c] for j in range(len(act))) / sum(e)
+            assert abs(O[n, 0, c] - ref) < 1e-12
+        assert abs(LSE[0, n] - (mx + math.log(sum(e)))) < 1e-12
+
+
+def test_rows_subset_matches_full():
+    L, Hq, Hkv, d = 192, 2, 1, 8
+    Q, K, V, _ = _inputs(L, Hq, Hkv, d, 5)
+    index = [(np.array([3, 70]), np.array([0, 1])), (np.array([], np.int64), np.array([0, 2]))]
+    O, LSE = attention_forward(Q, K, V, index)
+    rows = np.array([0, 63, 64, 191, 100])
+    Or, LSEr = attention_forward_rows(Q, K, V, index, rows)
+    np.testing.assert_allclose(Or, O[rows], atol=1e-14)
+    np.testing.assert_allclose(LSEr, LSE[:, rows], atol=1e-14)
