@@ -1,0 +1,232 @@
+// extern "C" entry points of the VS sparse attention library: argument
+// validation (host, before any launch), workspace layout, and launches.
+#include <cmath>
+#include <cstring>
+
+#include "common.cuh"
+
+namespace vs {
+
+cudaError_t launch_index_scores(const IndexArgs& a, cudaStream_t s);
+cudaError_t launch_select(const IndexArgs& a, cudaStream_t s);
+size_t select_smem_bytes(int nbs);
+cudaError_t launch_attn_fwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
+                            void* O, float* lse, void* ws, cudaStream_t s);
+size_t attn_fwd_ws_bytes(const vs_params& p);
+cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
+                            const void* O, const float* lse, const void* dO, void* dQ, void* dK, void* dV, void* ws,
+                            cudaStream_t s);
+size_t attn_bwd_ws_bytes(const vs_params& p);
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+vs_status check_params(const vs_params* p) {
+  if (!p) return VS_ERR_INVALID_ARG;
+  if (p->L <= 0 || p->Hq <= 0 || p->Hkv <= 0 || p->d <= 0) return VS_ERR_INVALID_ARG;
+  if (p->Hq % p->Hkv != 0) return VS_ERR_INVALID_ARG;
+  if (p->block != kBlock) return VS_ERR_UNSUPPORTED;
+  if (p->stripes < 1) return VS_ERR_INVALID_ARG;
+  if (p->L % (kBlock * p->stripes) != 0) return VS_ERR_INVALID_ARG;
+  if (p->L > kMaxL) return VS_ERR_UNSUPPORTED;
+  if (p->d != 64 && p->d != 128) return VS_ERR_UNSUPPORTED;
+  if (p->last_q < 1 || p->last_q > p->L) return VS_ERR_INVALID_ARG;
+  if (!(p->top_p > 0.f && p->top_p <= 1.f)) return VS_ERR_INVALID_ARG;
+  if (!(p->density >= 0.f && p->density <= 1.f)) return VS_ERR_INVALID_ARG;
+  if (!(p->softmax_scale >= 0.f) || !std::isfinite(p->softmax_scale)) return VS_ERR_INVALID_ARG;
+  return VS_OK;
+}
+
+vs_status check_index_params(const vs_params* p) {
+  vs_status st = check_params(p);
+  if (st != VS_OK) return st;
+  if (p->last_q > 256) return VS_ERR_UNSUPPORTED;  // index rows per head kept within one CTA
+  return VS_OK;
+}
+
+struct IndexWs {
+  size_t status, part, rowstat, v, T64, S, total;
+};
+
+IndexWs index_ws(const vs_params& p) {
+  int tpc, nchunk, rs;
+  index_grid(p, &tpc, &nchunk, &rs);
+  const size_t qpad = (size_t)(p.last_q + 15) / 16 * 16;
+  const size_t bs = (size_t)kBlock * p.stripes;
+  const size_t nbs = (size_t)p.L / bs;
+  const size_t ntile = (size_t)p.L / kBlock;
+  WsLayout w;
+  IndexWs o;
+  o.status = w.take(sizeof(DevStatus));
+  o.part = w.take((size_t)nchunk * p.Hq * qpad * sizeof(float2));
+  o.rowstat = w.take((size_t)p.Hq * qpad * sizeof(float2));
+  o.v = w.take((size_t)p.Hq * p.L * sizeof(float));
+  o.T64 = w.take((size_t)p.Hq * p.last_q * ntile * sizeof(float));
+  o.S = w.take((size_t)p.Hq * nbs * sizeof(float));
+  o.total = w.off;
+  return o;
+}
+
+vs_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
+  if (!ws) return VS_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return VS_ERR_WORKSPACE;
+  if (ws_bytes < need) return VS_ERR_WORKSPACE;
+  return VS_OK;
+}
+
+vs_status check_index_ptrs(const vs_index* ix) {
+  if (!ix || !ix->v_idx || !ix->v_cnt || !ix->s_idx || !ix->s_cnt) return VS_ERR_INVALID_ARG;
+  return VS_OK;
+}
+
+}  // namespace
+}  // namespace vs
+
+using namespace vs;
+
+extern "C" {
+
+const char* vs_status_string(vs_status s) {
+  switch (s) {
+    case VS_OK: return "VS_OK";
+    case VS_ERR_INVALID_ARG: return "VS_ERR_INVALID_ARG: invalid argument";
+    case VS_ERR_UNSUPPORTED: return "VS_ERR_UNSUPPORTED: unsupported configuration";
+    case VS_ERR_WORKSPACE: return "VS_ERR_WORKSPACE: workspace missing, misaligned or too small";
+    case VS_ERR_CUDA: return "VS_ERR_CUDA: CUDA launch or runtime error";
+    case VS_ERR_TIMEOUT: return "VS_ERR_TIMEOUT: a bounded in-kernel wait gave up";
+  }
+  return "VS_ERR_UNKNOWN";
+}
+
+size_t vs_workspace_bytes(const vs_params* p, int op) {
+  if (op == VS_OP_ROPE) return 0;
+  if (op == VS_OP_INDEX) {
+    if (check_index_params(p) != VS_OK) return 0;
+    return index_ws(*p).total;
+  }
+  if (check_params(p) != VS_OK) return 0;
+  if (op == VS_OP_FWD) return attn_fwd_ws_bytes(*p);
+  if (op == VS_OP_BWD) return attn_bwd_ws_bytes(*p);
+  return 0;
+}
+
+vs_status vs_rope(const vs_params* p, int32_t H, const void* x, void* y, int32_t transpose, void* stream) {
+  if (!p || !x || !y || H <= 0 || p->L <= 0) return VS_ERR_INVALID_ARG;
+  if (p->d != 64 && p->d != 128) return VS_ERR_UNSUPPORTED;
+  if (!(p->rope_theta > 1.0) || !(p->yarn_factor >= 1.f)) return VS_ERR_INVALID_ARG;
+  if (p->yarn_factor > 1.f && p->yarn_orig_len <= 0) return VS_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y)) return VS_ERR_INVALID_ARG;
+  RopeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.x = x;
+  a.y = y;
+  a.L = p->L;
+  a.H = H;
+  a.d = p->d;
+  a.transpose = transpose ? 1 : 0;
+  // theta_i = base^(-2i/d); YaRN NTK-by-parts: gamma_i = clip((r_i - 1)/(32 - 1), 0, 1),
+  // r_i = orig_len * theta_i / (2 pi); theta'_i = theta_i (gamma_i + (1 - gamma_i)/s)
+  const double s = p->yarn_factor;
+  for (int i = 0; i < p->d / 2; ++i) {
+    double f = std::pow(p->rope_theta, -2.0 * i / p->d);
+    if (s > 1.0) {
+      const double r = p->yarn_orig_len * f / (2.0 * 3.14159265358979323846);
+      double g = (r - 1.0) / (32.0 - 1.0);
+      g = g < 0.0 ? 0.0 : (g > 1.0 ? 1.0 : g);
+      f = f * (g + (1.0 - g) / s);
+    }
+    a.inv_freq[i] = f;
+  }
+  a.mscale = s > 1.0 ? (float)(0.1 * std::log(s) + 1.0) : 1.0f;
+  return launch_rope(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? VS_OK : VS_ERR_CUDA;
+}
+
+vs_status vs_index_build(const vs_params* p, const void* Q, const void* K, const vs_index* out, void* ws,
+                         size_t ws_bytes, void* stream) {
+  vs_status st = check_index_params(p);
+  if (st != VS_OK) return st;
+  if (!Q || !K || !aligned16(Q) || !aligned16(K)) return VS_ERR_INVALID_ARG;
+  if ((st = check_index_ptrs(out)) != VS_OK) return st;
+  const IndexWs lay = index_ws(*p);
+  if ((st = check_ws(ws, ws_bytes, lay.total)) != VS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  if (cudaMemsetAsync(w + lay.status, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
+
+  IndexArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.Q = Q;
+  a.K = K;
+  a.L = p->L;
+  a.Hq = p->Hq;
+  a.Hkv = p->Hkv;
+  a.G = p->Hq / p->Hkv;
+  a.d = p->d;
+  a.last_q = p->last_q;
+  a.qpad = (p->last_q + 15) / 16 * 16;
+  a.bs = kBlock * p->stripes;
+  a.nbs = p->L / a.bs;
+  a.ntile = p->L / kBlock;
+  index_grid(*p, &a.tiles_per_chunk, &a.nchunk, &a.row_splits);
+  a.scale_log2 = default_scale(*p) * 1.4426950408889634f;
+  a.top_p = p->top_p;
+  a.density = p->density;
+  a.part = reinterpret_cast<float2*>(w + lay.part);
+  a.rowstat = reinterpret_cast<float2*>(w + lay.rowstat);
+  a.v = out->v_score ? out->v_score : reinterpret_cast<float*>(w + lay.v);
+  a.T64 = reinterpret_cast<float*>(w + lay.T64);
+  a.S = out->s_score ? out->s_score : reinterpret_cast<float*>(w + lay.S);
+  a.v_idx = out->v_idx;
+  a.v_cnt = out->v_cnt;
+  a.s_idx = out->s_idx;
+  a.s_cnt = out->s_cnt;
+  a.active = out->active_entries;
+  a.status = reinterpret_cast<DevStatus*>(w + lay.status);
+  if (select_smem_bytes(a.nbs) + 26 * 1024 > 227 * 1024) return VS_ERR_UNSUPPORTED;
+  if (launch_index_scores(a, s) != cudaSuccess) return VS_ERR_CUDA;
+  if (launch_select(a, s) != cudaSuccess) return VS_ERR_CUDA;
+  return VS_OK;
+}
+
+vs_status vs_sparse_attn_fwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,
+                             const void* V, void* O, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  vs_status st = check_params(p);
+  if (st != VS_OK) return st;
+  if ((st = check_index_ptrs(index)) != VS_OK) return st;
+  if (!Q || !K || !V || !O || !lse) return VS_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(lse)) return VS_ERR_INVALID_ARG;
+  if ((st = check_ws(ws, ws_bytes, attn_fwd_ws_bytes(*p))) != VS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
+  return launch_attn_fwd(*p, *index, Q, K, V, O, lse, ws, s) == cudaSuccess ? VS_OK : VS_ERR_CUDA;
+}
+
+vs_status vs_sparse_attn_bwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,
+                             const void* V, const void* O, const float* lse, const void* dO, void* dQ,
+                             void* dK, void* dV, void* ws, size_t ws_bytes, void* stream) {
+  vs_status st = check_params(p);
+  if (st != VS_OK) return st;
+  if ((st = check_index_ptrs(index)) != VS_OK) return st;
+  if (!Q || !K || !V || !O || !lse || !dO || !dQ || !dK || !dV) return VS_ERR_INVALID_ARG;
+  const void* ptrs[] = {Q, K, V, O, lse, dO, dQ, dK, dV};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return VS_ERR_INVALID_ARG;
+  if ((st = check_ws(ws, ws_bytes, attn_bwd_ws_bytes(*p))) != VS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
+  return launch_attn_bwd(*p, *index, Q, K, V, O, lse, dO, dQ, dK, dV, ws, s) == cudaSuccess ? VS_OK : VS_ERR_CUDA;
+}
+
+vs_status vs_device_status(void* ws, void* stream) {
+  if (!ws) return VS_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return VS_ERR_CUDA;
+  DevStatus h;
+  if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return VS_ERR_CUDA;
+  if (h.code == VS_OK) return VS_OK;
+  if (cudaMemset(ws, 0, sizeof(DevStatus)) != cudaSuccess) return VS_ERR_CUDA;
+  return h.code == VS_ERR_TIMEOUT ? VS_ERR_TIMEOUT : VS_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,84 @@
+// Shared definitions of the VS sparse attention library (host + device).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/vs.h"
+
+namespace vs {
+
+constexpr int kBlock = 64;                       // slash tile edge (keys and queries)
+constexpr uint64_t kWaitLimitNs = 2000000000ull; // bounded in-kernel waits: 2 s
+constexpr int kMaxL = 1 << 20;                   // supported sequence length ceiling
+
+// Device-side status word (first bytes of every workspace).
+struct DevStatus {
+  int32_t code;   // VS_OK or VS_ERR_TIMEOUT
+  int32_t where;  // which wait gave up (kernel-specific tag)
+  int32_t pad[2];
+};
+
+__device__ __forceinline__ void report_timeout(DevStatus* st, int where) {
+  if (st) {
+    atomicExch(&st->code, (int32_t)VS_ERR_TIMEOUT);
+    atomicExch(&st->where, where);
+  }
+}
+
+__host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Simple bump allocator over the caller's workspace (host side, computes offsets only).
+struct WsLayout {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  }
+};
+
+inline float default_scale(const vs_params& p) {
+  return p.softmax_scale > 0.f ? p.softmax_scale : 1.0f / sqrtf((float)p.d);
+}
+
+// ---------------------------------------------------------------- launchers
+// (implemented in the per-stage .cu files; all return cudaGetLastError())
+
+struct RopeArgs {
+  const void* x;
+  void* y;
+  int32_t L, H, d;
+  int32_t transpose;
+  float mscale;
+  double inv_freq[64];  // d/2 <= 64 frequencies, host-computed in fp64
+};
+cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s);
+
+struct IndexArgs {
+  const void* Q;
+  const void* K;
+  int32_t L, Hq, Hkv, G, d;
+  int32_t last_q, qpad;       // index rows; rows per head padded to 16
+  int32_t bs, nbs;            // slash tile (64 * stripes) and band count
+  int32_t ntile;              // L / 64
+  int32_t tiles_per_chunk, nchunk;
+  int32_t row_splits;         // CTAs along the row dimension per KV head
+  float scale_log2;           // softmax scale * log2(e)
+  float top_p, density;
+  float2* part;               // [nchunk][Hq*qpad] (max, sum) per chunk, log2 domain
+  float2* rowstat;            // [Hq*qpad] (max, 1/sum)
+  float* v;                   // [Hq][L]
+  float* T64;                 // [Hq][last_q][ntile] row mass per 64-key tile
+  float* S;                   // [Hq][nbs]
+  int32_t* v_idx;
+  int32_t* v_cnt;
+  int32_t* s_idx;
+  int32_t* s_cnt;
+  int64_t* active;            // [Hq] or null
+  DevStatus* status;
+};
+cudaError_t launch_index(const IndexArgs& a, cudaStream_t s);
+void index_grid(const vs_params& p, int* tiles_per_chunk, int* nchunk, int* row_splits);
+
+}  // namespace vs

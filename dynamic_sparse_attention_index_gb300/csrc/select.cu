@@ -1,0 +1,419 @@
+// Sparse-index approximation, selection stage, and the exact active-entry
+// count.  One CTA per query head.
+//
+// MTraining review, section "分布式稀疏索引近似": keep the minimum number of
+// vertical lines and slash bands that recall the target attention mass
+// ("online top-p budget" in the training-loss section).  Reading: each
+// direction independently keeps the smallest prefix of its masses sorted in
+// descending order (ties: lower index first) whose sum reaches top_p of the
+// direction's total; band 0 is always kept.  top_p >= 1 keeps every element
+// with positive mass.
+//
+// Budget-fill variant (the experiments fix sparsity at 95 %, section 八
+// item 4): verticals and bands >= 1 are ranked together by mass (both
+// directions total last_q) and the kept set is band 0 plus every candidate
+// with mass >= tau, tau the largest value whose set reaches the requested
+// active density.
+//
+// Selection by threshold: masses are non-negative fp32, so their bit
+// patterns order like the values.  A most-significant-digit-first radix
+// descent (11/11/10 bits) over a histogram of counts and masses finds the
+// threshold key; masses are summed as exact 64-bit fixed-point integers
+// (scale 2^sh, sum < 2^62), so every sum is order-independent and the
+// selection is deterministic.  Kept elements are then compacted in index
+// order, which yields ascending lists.
+//
+// Active entries (section 四 "核心公式" sparsity ratio): band B >= 1 covers
+// (nbs - B) full bs x bs tiles, band 0 the causal halves of the nbs diagonal
+// tiles, and a kept vertical m adds bs entries for each later row tile whose
+// band is not kept.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace vs {
+namespace {
+
+constexpr int kThreads = 1024;
+constexpr int kWarps = kThreads / 32;
+
+struct SelShared {
+  unsigned long long hsum[2048];
+  unsigned int hcnt[2048];
+  unsigned long long wsum[kWarps];
+  unsigned int wcnt[kWarps];
+  unsigned int wcnt2[kWarps];
+  unsigned long long bcast_u64[4];
+  unsigned int bcast_u32[4];
+};
+
+__device__ __forceinline__ uint32_t key_of(float x) { return __float_as_uint(x); }
+
+__device__ __forceinline__ unsigned long long quant(float x, int sh) {
+  // exact x * 2^sh (power-of-two scale), truncated to an integer
+  return (unsigned long long)__float2ull_rz(ldexpf(x, sh));
+}
+
+// Block-wide sum (all threads get the result).
+__device__ unsigned long long block_sum_u64(unsigned long long v, SelShared& sh) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) sh.wsum[warp] = v;
+  __syncthreads();
+  unsigned long long t = 0;
+  for (int w = 0; w < kWarps; ++w) t += sh.wsum[w];
+  __syncthreads();
+  return t;
+}
+
+// Largest key tau such that sum of quantised masses of elements with key >= tau
+// reaches `target` (target >= 1).  Also returns the mass/count strictly above
+// tau and the count/mass at tau.
+struct Thresh {
+  uint32_t tau;
+  unsigned long long sum_gt;
+  unsigned int cnt_gt;
+  unsigned int cnt_eq;
+  unsigned long long qtau;
+};
+
+__device__ Thresh radix_threshold(const float* x, int n, int sh, unsigned long long target, SelShared& s) {
+  uint32_t prefix = 0, pmask = 0;
+  unsigned long long above = 0;
+  unsigned int above_cnt = 0, eq_cnt = 0;
+  const int shifts[3] = {21, 10, 0};
+  const int bits[3] = {11, 11, 10};
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = shifts[pass], nb = 1 << bits[pass];
+    for (int b = threadIdx.x; b < nb; b += kThreads) {
+      s.hsum[b] = 0;
+      s.hcnt[b] = 0;
+    }
+    __syncthreads();
+    for (int base = 0; base < n; base += kThreads) {
+      const int i = base + threadIdx.x;
+      float xv = 0.f;
+      bool in = false;
+      uint32_t k = 0;
+      if (i < n) {
+        xv = x[i];
+        k = key_of(xv);
+        in = (k & pmask) == prefix;
+      }
+      const int bin = in ? (int)((k >> shift) & (uint32_t)(nb - 1)) : -1;
+      // aggregate equal bins within the warp before touching shared memory;
+      // the 61-bit masses are summed in three 21-bit parts (no overflow)
+      const unsigned same = __match_any_sync(0xffffffffu, bin);
+      if (in) {
+        const unsigned long long q = quant(xv, sh);
+        const unsigned s0 = __reduce_add_sync(same, (unsigned)(q & 0x1FFFFFull));
+        const unsigned s1 = __reduce_add_sync(same, (unsigned)((q >> 21) & 0x1FFFFFull));
+        const unsigned s2 = __reduce_add_sync(same, (unsigned)(q >> 42));
+        if ((__ffs(same) - 1) == (int)(threadIdx.x & 31)) {
+          atomicAdd(&s.hsum[bin], (unsigned long long)s0 + ((unsigned long long)s1 << 21) +
+                                      ((unsigned long long)s2 << 42));
+          atomicAdd(&s.hcnt[bin], (unsigned)__popc(same));
+        }
+      }
+    }
+    __syncthreads();
+    // suffix sums from the top bin down, done by warp 0
+    if (threadIdx.x < 32) {
+      const int lane = threadIdx.x;
+      const int per = nb / 32;  // contiguous bins per lane (64 or 32)
+      unsigned long long ls = 0;
+      unsigned lc = 0;
+      for (int b = lane * per; b < (lane + 1) * per; ++b) {
+        ls += s.hsum[b];
+        lc += s.hcnt[b];
+      }
+      // exclusive suffix over lanes: mass of all bins above this lane's range
+      unsigned long long suf = ls;
+      unsigned sufc = lc;
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long t = __shfl_down_sync(0xffffffffu, suf, o);
+        const unsigned tc = __shfl_down_sync(0xffffffffu, sufc, o);
+        if (lane + o < 32) {
+          suf += t;
+          sufc += tc;
+        }
+      }
+      const unsigned long long above_lane = suf - ls;  // bins strictly above my range
+      const unsigned above_lane_c = sufc - lc;
+      // the lane whose range contains the crossing
+      const bool hit = (above + above_lane < target) && (above + suf >= target);
+      const unsigned hb = __ballot_sync(0xffffffffu, hit);
+      int chosen_lane = hb ? (__ffs(hb) - 1) : -1;
+      if (chosen_lane < 0) chosen_lane = 0;  // target beyond total: take everything
+      if (lane == chosen_lane) {
+        unsigned long long acc = above + above_lane;
+        unsigned accc = above_lane_c;
+        int bsel = lane * per;
+        for (int b = (lane + 1) * per - 1; b >= lane * per; --b) {
+          if (acc + s.hsum[b] >= target || b == lane * per) {
+            bsel = b;
+            break;
+          }
+          acc += s.hsum[b];
+          accc += s.hcnt[b];
+        }
+        s.bcast_u64[0] = acc;
+        s.bcast_u32[0] = above_cnt + accc;
+        s.bcast_u32[1] = (uint32_t)bsel;
+        s.bcast_u32[2] = s.hcnt[bsel];
+      }
+    }
+    __syncthreads();
+    above = s.bcast_u64[0];
+    above_cnt = s.bcast_u32[0];
+    prefix |= s.bcast_u32[1] << shift;
+    pmask |= (uint32_t)(nb - 1) << shift;
+    eq_cnt = s.bcast_u32[2];
+    __syncthreads();
+  }
+  Thresh t;
+  t.tau = prefix;
+  t.sum_gt = above;
+  t.cnt_gt = above_cnt;
+  t.cnt_eq = eq_cnt;
+  t.qtau = quant(__uint_as_float(prefix), sh);
+  return t;
+}
+
+// Compact {i : key_i > tau} plus the first `n_tie` indices with key_i == tau,
+// in index order, into out[]; returns the count.  If accum_vert is set, also
+// returns (via *vert_entries) the sum over kept i of bs * notS[nbs-1-i/bs].
+__device__ int compact_select(const float* x, int n, uint32_t tau, unsigned n_tie, int32_t* out,
+                              const int32_t* notS, int nbs, int bs, unsigned long long* vert_entries,
+                              SelShared& s, int skip_index) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int base = 0;
+  unsigned tie_base = 0;
+  unsigned long long ve = 0;
+  for (int start = 0; start < n; start += kThreads) {
+    const int i = start + threadIdx.x;
+    bool gt = false, eq = false;
+    if (i < n && i != skip_index) {
+      const uint32_t k = key_of(x[i]);
+      gt = k > tau;
+      eq = k == tau;
+    }
+    const unsigned bgt = __ballot_sync(0xffffffffu, gt);
+    const unsigned beq = __ballot_sync(0xffffffffu, eq);
+    if (lane == 0) {
+      s.wcnt[warp] = __popc(bgt);
+      s.wcnt2[warp] = __popc(beq);
+    }
+    __syncthreads();
+    unsigned tie_before = 0, eq_total = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < warp) tie_before += s.wcnt2[w];
+      eq_total += s.wcnt2[w];
+    }
+    const unsigned lanemask = (1u << lane) - 1u;
+    const unsigned my_tie_rank = tie_base + tie_before + __popc(beq & lanemask);
+    const bool keep = gt || (eq && my_tie_rank < n_tie);
+    const unsigned bkeep = __ballot_sync(0xffffffffu, keep);
+    __syncthreads();
+    if (lane == 0) s.wcnt[warp] = __popc(bkeep);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < warp) before += s.wcnt[w];
+      total += s.wcnt[w];
+    }
+    if (keep) {
+      out[base + before + __popc(bkeep & lanemask)] = i;
+      if (notS) ve += (unsigned long long)bs * (unsigned long long)notS[nbs - 1 - i / bs];
+    }
+    base += total;
+    tie_base += eq_total;
+    __syncthreads();
+  }
+  if (vert_entries) *vert_entries = block_sum_u64(ve, s);
+  return base;
+}
+
+// notS[x] = #{B in [1, x] : B not kept}; kept given by inS (0/1 per band).
+__device__ void build_notS(const uint8_t* inS, int32_t* notS, int nbs, SelShared& s) {
+  // single-warp scan is plenty for nbs <= 16384
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int base = 0; base < nbs; base += 32) {
+      const int b = base + lane;
+      const int v = (b >= 1 && b < nbs && !inS[b]) ? 1 : 0;
+      int incl = v;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += t;
+      }
+      if (b < nbs) notS[b] = carry + incl;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  __syncthreads();
+}
+
+__device__ unsigned long long slash_entries(const uint8_t* inS, int nbs, int bs, SelShared& s) {
+  unsigned long long e = 0;
+  for (int B = threadIdx.x; B < nbs; B += kThreads) {
+    if (!inS[B]) continue;
+    e += (B == 0) ? (unsigned long long)nbs * (unsigned long long)(bs * (bs + 1) / 2)
+                  : (unsigned long long)(nbs - B) * (unsigned long long)bs * (unsigned long long)bs;
+  }
+  return block_sum_u64(e, s);
+}
+
+// Vertical entries for threshold key tau (keep m iff key(v[m]) >= tau).
+__device__ unsigned long long vert_entries_at(const float* v, int L, uint32_t tau, const int32_t* notS, int nbs,
+                                              int bs, SelShared& s) {
+  unsigned long long e = 0;
+  for (int m = threadIdx.x; m < L; m += kThreads)
+    if (key_of(v[m]) >= tau) e += (unsigned long long)notS[nbs - 1 - m / bs];
+  return block_sum_u64(e, s) * (unsigned long long)bs;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) {
+  extern __shared__ __align__(16) uint8_t dyn[];
+  __shared__ SelShared s;
+  const int h = blockIdx.x;
+  const int nbs = a.nbs, L = a.L, bs = a.bs;
+  uint8_t* inS = dyn;                                               // [nbs]
+  int32_t* notS = reinterpret_cast<int32_t*>(dyn + align_up(nbs, 16));  // [nbs]
+  const float* v = a.v + (size_t)h * L;
+  const float* S = a.S + (size_t)h * nbs;
+  int32_t* vout = a.v_idx + (size_t)h * L;
+  int32_t* sout = a.s_idx + (size_t)h * nbs;
+  // fixed-point scale: masses are <= last_q, so last_q * 2^sh < 2^62
+  int lg = 0;
+  while ((1 << lg) < a.last_q + 1) ++lg;
+  const int sh = 61 - lg;
+
+  unsigned long long slash_e = 0, vert_e = 0;
+  int nv = 0, ns = 0;
+  if (a.density <= 0.f) {
+    // ---------------- top-p, slash direction
+    unsigned long long tot = 0;
+    for (int B = threadIdx.x; B < nbs; B += kThreads) tot += quant(S[B], sh);
+    tot = block_sum_u64(tot, s);
+    uint32_t tau;
+    unsigned ntie;
+    if (a.top_p >= 1.f || tot == 0) {
+      tau = 1;  // every positive mass (key >= smallest positive denormal)
+      ntie = 0xffffffffu;
+      // keys > tau are kept; key == tau (the smallest denormal) kept too
+    } else {
+      unsigned long long target = (unsigned long long)((double)a.top_p * (double)tot);
+      if ((double)target < (double)a.top_p * (double)tot) ++target;
+      if (target < 1) target = 1;
+      const Thresh t = radix_threshold(S, nbs, sh, target, s);
+      tau = t.tau;
+      unsigned long long need = target > t.sum_gt ? target - t.sum_gt : 0;
+      unsigned long long k = t.qtau ? (need + t.qtau - 1) / t.qtau : 1;
+      if (k < 1) k = 1;
+      if (k > t.cnt_eq) k = t.cnt_eq;
+      ntie = (unsigned)k;
+    }
+    for (int B = threadIdx.x; B < nbs; B += kThreads) inS[B] = 0;
+    __syncthreads();
+    // compaction writes ascending band ids; band 0 forced separately
+    ns = compact_select(S, nbs, tau, ntie, sout, nullptr, nbs, bs, nullptr, s, -1);
+    // mark kept bands, then force band 0 in (keeping the list ascending)
+    for (int j = threadIdx.x; j < ns; j += kThreads) inS[sout[j]] = 1;
+    __syncthreads();
+    if (!inS[0]) {
+      // shift right by one and put 0 first (single thread; ns <= nbs - 1 here)
+      if (threadIdx.x == 0) {
+        for (int j = ns; j > 0; --j) sout[j] = sout[j - 1];
+        sout[0] = 0;
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) inS[0] = 1;
+      ++ns;
+    }
+    __syncthreads();
+    build_notS(inS, notS, nbs, s);
+    slash_e = slash_entries(inS, nbs, bs, s);
+    // ---------------- top-p, vertical direction
+    tot = 0;
+    for (int m = threadIdx.x; m < L; m += kThreads) tot += quant(v[m], sh);
+    tot = block_sum_u64(tot, s);
+    if (a.top_p >= 1.f || tot == 0) {
+      tau = 1;
+      ntie = 0xffffffffu;
+    } else {
+      unsigned long long target = (unsigned long long)((double)a.top_p * (double)tot);
+      if ((double)target < (double)a.top_p * (double)tot) ++target;
+      if (target < 1) target = 1;
+      const Thresh t = radix_threshold(v, L, sh, target, s);
+      tau = t.tau;
+      unsigned long long need = target > t.sum_gt ? target - t.sum_gt : 0;
+      unsigned long long k = t.qtau ? (need + t.qtau - 1) / t.qtau : 1;
+      if (k < 1) k = 1;
+      if (k > t.cnt_eq) k = t.cnt_eq;
+      ntie = (unsigned)k;
+    }
+    nv = compact_select(v, L, tau, ntie, vout, notS, nbs, bs, &vert_e, s, -1);
+  } else {
+    // ---------------- budget fill
+    const double T = (double)L * (double)(L + 1) * 0.5;
+    const unsigned long long target = (unsigned long long)ceil((double)a.density * T);
+    auto entries_at = [&](uint32_t tau) -> unsigned long long {
+      for (int B = threadIdx.x; B < nbs; B += kThreads) inS[B] = (B == 0) || (key_of(S[B]) >= tau);
+      __syncthreads();
+      build_notS(inS, notS, nbs, s);
+      const unsigned long long se = slash_entries(inS, nbs, bs, s);
+      const unsigned long long ve = vert_entries_at(v, L, tau, notS, nbs, bs, s);
+      return se + ve;
+    };
+    uint32_t tau;
+    if (entries_at(0x7f800001u) >= target) {
+      tau = 0x7f800001u;  // nothing beyond band 0
+    } else if (entries_at(1u) < target) {
+      tau = 1u;  // every positive candidate
+    } else {
+      tau = 0u;
+      for (int bit = 30; bit >= 0; --bit) {
+        const uint32_t cand = tau | (1u << bit);
+        if (cand > 0x7f800000u) continue;
+        if (entries_at(cand) >= target) tau = cand;
+      }
+    }
+    // final sets at tau: slash list (band 0 forced) and verticals
+    for (int B = threadIdx.x; B < nbs; B += kThreads) inS[B] = (B == 0) || (key_of(S[B]) >= tau);
+    __syncthreads();
+    build_notS(inS, notS, nbs, s);
+    slash_e = slash_entries(inS, nbs, bs, s);
+    // bands: keep key >= tau, i.e. key > tau - 1 ... use compaction with tie = all
+    ns = compact_select(S, nbs, tau - 1u, 0u, sout, nullptr, nbs, bs, nullptr, s, 0);
+    // band 0 forced: it was skipped above (skip_index = 0); prepend it
+    if (threadIdx.x == 0) {
+      for (int j = ns; j > 0; --j) sout[j] = sout[j - 1];
+      sout[0] = 0;
+    }
+    __syncthreads();
+    ++ns;
+    nv = compact_select(v, L, tau - 1u, 0u, vout, notS, nbs, bs, &vert_e, s, -1);
+  }
+  if (threadIdx.x == 0) {
+    a.v_cnt[h] = nv;
+    a.s_cnt[h] = ns;
+    if (a.active) a.active[h] = (long long)(slash_e + vert_e);
+  }
+}
+
+}  // namespace
+
+size_t select_smem_bytes(int nbs) { return align_up(nbs, 16) + (size_t)nbs * 4; }
+
+cudaError_t launch_select(const IndexArgs& a, cudaStream_t s) {
+  const size_t smem = select_smem_bytes(a.nbs);
+  cudaError_t e = cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  select_kernel<<<a.Hq, kThreads, smem, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace vs

@@ -1,0 +1,150 @@
+/*
+ * vs.h - C ABI of the GB300 (sm_103a) vertical-slash (VS) sparse attention library.
+ *
+ * The method (MTraining, arXiv 2510.18830; described in the paper review
+ * "MTraining: 分布式动态稀疏注意力高效超长上下文训练", section 三 "技术架构"):
+ *   1. online sparse-index approximation: the last `last_q` query rows are
+ *      scored against every key, the softmax mass is summed along vertical
+ *      lines (key token m) and slash bands (64x64 block diagonals), and the
+ *      smallest sets of verticals and slashes that recall `top_p` of the mass
+ *      are kept (section "分布式稀疏索引近似");
+ *   2. block-sparse causal attention, forward and backward, over only the
+ *      active entries, with an online softmax across key blocks (ring
+ *      attention page, section 2.1 "块级循环计算范式").
+ *
+ * Conventions shared by every entry point
+ *   - Tensors are token-major, batch 1: Q, O, dO, dQ are [L][Hq][d] and
+ *     K, V, dK, dV are [L][Hkv][d], all bf16, rows packed (stride Hq*d or
+ *     Hkv*d elements).  Every data pointer is a DEVICE pointer, 16-byte aligned.
+ *   - The caller owns all memory.  The library never allocates or frees; the
+ *     scratch an entry point needs is the caller's `ws` buffer of at least
+ *     vs_workspace_bytes(...) bytes (256-byte aligned).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = legacy default stream) and never synchronises.
+ *   - Argument errors are detected on the host before any launch and returned
+ *     as VS_ERR_INVALID_ARG / VS_ERR_UNSUPPORTED / VS_ERR_WORKSPACE; a failed
+ *     launch returns VS_ERR_CUDA.  Kernels that wait on an in-CTA barrier do
+ *     so for a bounded time; on timeout they record VS_ERR_TIMEOUT in the
+ *     workspace status word (first 16 bytes of `ws`) and return, which
+ *     vs_device_status() reports after the stream is synchronised.
+ *   - No global state: calls on different streams with different workspaces
+ *     are independent.
+ */
+#ifndef VS_H_
+#define VS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define VS_API __attribute__((visibility("default")))
+#else
+#define VS_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum vs_status {
+  VS_OK = 0,
+  VS_ERR_INVALID_ARG = 1, /* null pointer, out-of-range size or parameter */
+  VS_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d not in {64,128}) */
+  VS_ERR_WORKSPACE = 3,   /* ws too small or misaligned */
+  VS_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed */
+  VS_ERR_TIMEOUT = 5      /* a bounded in-kernel wait gave up (device-side) */
+} vs_status;
+
+/* Problem description.  Batch 1. */
+typedef struct vs_params {
+  int32_t L;             /* tokens; multiple of 64 * stripes                         */
+  int32_t Hq;            /* query heads                                              */
+  int32_t Hkv;           /* key/value heads; Hq % Hkv == 0 (GQA group G = Hq/Hkv)     */
+  int32_t d;             /* head dim: 64 or 128                                      */
+  int32_t last_q;        /* index rows: the last last_q queries, 1 <= last_q <= L    */
+  float top_p;           /* recall target per direction, 0 < top_p <= 1             */
+  int32_t block;         /* slash tile edge; must be 64                              */
+  int32_t stripes;       /* W >= 1: striped layout emulation (1 = contiguous)        */
+  float softmax_scale;   /* 0 -> 1/sqrt(d)                                           */
+  float density;         /* 0 -> top-p selection; in (0,1] -> budget fill to this    */
+                         /*      active density (fixed-sparsity operating point)     */
+  double rope_theta;     /* RoPE base (vs_rope only)                                 */
+  float yarn_factor;     /* YaRN scale s (1 = plain RoPE)       (vs_rope only)       */
+  int32_t yarn_orig_len; /* YaRN original context length        (vs_rope only)       */
+} vs_params;
+
+/*
+ * The sparse index, per query head h (all DEVICE pointers, caller-owned).
+ * Slash band B of entry (n, m) is n/bs - m/bs with bs = block * stripes;
+ * entry (n, m) is active iff m <= n and (band kept or m a kept vertical).
+ */
+typedef struct vs_index {
+  int32_t* v_idx;          /* [Hq][L]     row h: v_cnt[h] ascending kept vertical token ids  */
+  int32_t* v_cnt;          /* [Hq]                                                           */
+  int32_t* s_idx;          /* [Hq][L/bs]  row h: s_cnt[h] ascending kept bands; band 0 kept  */
+  int32_t* s_cnt;          /* [Hq]                                                           */
+  float* v_score;          /* optional [Hq][L]    vertical mass (sum over the last_q rows)   */
+  float* s_score;          /* optional [Hq][L/bs] slash-band mass                            */
+  int64_t* active_entries; /* optional [Hq] exact active (n, m) entries per head             */
+} vs_index;
+
+enum { VS_OP_INDEX = 0, VS_OP_FWD = 1, VS_OP_BWD = 2, VS_OP_ROPE = 3 };
+
+/* Bytes of scratch `op` needs for problem `p` (0 if p is invalid). */
+VS_API size_t vs_workspace_bytes(const vs_params* p, int op);
+
+/* Human-readable name of a status code (static string). */
+VS_API const char* vs_status_string(vs_status s);
+
+/*
+ * Rotate-half RoPE ("Vertical-Slash 稀疏模式" section: channel i pairs with
+ * i + d/2, theta_i = rope_theta^(-2i/d); YaRN NTK-by-parts frequencies and
+ * temperature when yarn_factor > 1).  x, y: [L][H][d] bf16, y may equal x.
+ * transpose != 0 applies the adjoint (rotation by -phi), which maps the
+ * gradient of a rotated tensor back to the un-rotated one.
+ */
+VS_API vs_status vs_rope(const vs_params* p, int32_t H, const void* x, void* y, int32_t transpose, void* stream);
+
+/*
+ * Sparse-index approximation ("分布式稀疏索引近似" section): scores the last
+ * last_q rows of Q against all of K (scale * q.k, causal, softmax per row),
+ * sums the probabilities per key (vertical) and per slash band, and keeps per
+ * head the smallest descending prefix (ties: lower index) reaching top_p of
+ * each direction's mass; band 0 is always kept.  With density > 0 the kept
+ * set is instead the largest-mass candidates (verticals and bands ranked
+ * together) whose active entries reach `density` of the causal entries.
+ * Fills every non-NULL field of *out.
+ */
+VS_API vs_status vs_index_build(const vs_params* p, const void* Q, const void* K, const vs_index* out, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/*
+ * Block-sparse causal attention forward over the active entries of `index`
+ * ("Ring Attention with sparse index" in the same section; online softmax
+ * across key blocks): O = softmax(scale Q K^T restricted to the mask) V,
+ * lse[h][n] = log sum_{m active} exp(scale q_n . k_m).
+ * O: [L][Hq][d] bf16; lse: [Hq][L] fp32.
+ */
+VS_API vs_status vs_sparse_attn_fwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,
+                             const void* V, void* O, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Backward of vs_sparse_attn_fwd with the mask held fixed:
+ * dV = P^T dO, dS = P * (dO V^T - rowsum(dO * O)), dQ = scale dS K,
+ * dK = scale dS^T Q; dK and dV sum over the Hq/Hkv query heads sharing a
+ * key/value head and are written (not accumulated).
+ */
+VS_API vs_status vs_sparse_attn_bwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,
+                             const void* V, const void* O, const float* lse, const void* dO, void* dQ,
+                             void* dK, void* dV, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Reads the device-side status word of workspace `ws` (synchronises
+ * `stream` first) and clears it.  Returns VS_OK or VS_ERR_TIMEOUT.
+ */
+VS_API vs_status vs_device_status(void* ws, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* VS_H_ */

@@ -1,0 +1,54 @@
+"""Test helpers: tensor conversion and index-set comparison (no method arithmetic)."""
+import numpy as np
+
+import synth
+
+
+def to_dev(bits, dev):
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+def f64(bits):
+    return synth.bf16_bits_to_f64(bits)
+
+
+def bf16_bits_of(t):
+    import torch
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def gpu_index_lists(ix, Hq):
+    out = []
+    vc, sc = ix.v_cnt.cpu().numpy(), ix.s_cnt.cpu().numpy()
+    vi, si = ix.v_idx.cpu().numpy(), ix.s_idx.cpu().numpy()
+    for h in range(Hq):
+        out.append((vi[h, :vc[h]].astype(np.int64), si[h, :sc[h]].astype(np.int64)))
+    return out
+
+
+def topp_sets_agree(x_or, sel_or, sel_gpu, p, tol=1e-6, forced=()):
+    """True if the GPU selection equals the oracle's, except for elements at
+    the top-p threshold: each element in the symmetric difference must have a
+    normalised mass within `tol` of the oracle's threshold element, or sit at
+    a cumulative normalised mass within `tol` of p."""
+    a, b = set(sel_or.tolist()), set(sel_gpu.tolist())
+    diff = (a ^ b) - set(forced)
+    if not diff:
+        return True, []
+    tot = x_or.sum()
+    xn = x_or / tot
+    kept = np.array(sorted(a - set(forced)), dtype=np.int64)
+    thr = xn[kept].min() if kept.size else 0.0
+    order = np.argsort(-x_or, kind="stable")
+    cum = np.cumsum(xn[order])
+    rank = np.empty_like(order)
+    rank[order] = np.arange(order.size)
+    bad = []
+    for e in diff:
+        near_thr = abs(xn[e] - thr) <= tol
+        c_before = cum[rank[e]] - xn[e]
+        near_p = abs(c_before - p) <= tol or abs(cum[rank[e]] - p) <= tol
+        if not (near_thr or near_p):
+            bad.append((e, xn[e], thr))
+    return not bad, bad

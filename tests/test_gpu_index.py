@@ -1,0 +1,109 @@
+"""Index build on the GPU vs the oracle.
+
+Three levels:
+  * scores: the vertical / slash masses match the fp64 oracle's to fp32
+    accuracy;
+  * decisions: the oracle's selection run on the GPU's own fp32 masses gives
+    exactly the GPU's kept sets (both decide in the same precision), and the
+    exact active-entry count matches;
+  * end to end: the GPU's sets equal the oracle's fp64 sets except for
+    elements at the top-p threshold (within 1e-6 normalised mass).
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from _util import f64, gpu_index_lists, to_dev, topp_sets_agree
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(w, density=0.0, stripes=1):
+    import torch
+    import dynamic_sparse_attention_index_gb300 as vs
+    dev = torch.device("cuda:0")
+    p = vs.make_params(w.L, w.Hq, w.Hkv, w.d, last_q=w.last_q, top_p=w.top_p, stripes=stripes,
+                       density=density)
+    Q, K = to_dev(w.q, dev), to_dev(w.k, dev)
+    ix = vs.IndexBuffers.allocate(p, dev)
+    ws = vs.workspace(p, vs.VS_OP_INDEX, dev)
+    vs.vs_index_build(p, Q, K, ix, ws)
+    torch.cuda.synchronize()
+    return p, ix
+
+
+CASES = [
+    # (workload recipe, L, Hq, Hkv, d, last_q, top_p, stripes)
+    (1, 4096, 1, 1, 64, 64, 0.9, 1),
+    (1, 256, 1, 1, 64, 64, 0.9, 1),
+    (3, 1024, 4, 2, 128, 64, 0.95, 1),
+    (3, 2048, 16, 2, 128, 64, 0.5, 1),
+    (3, 1024, 4, 1, 64, 16, 0.9, 1),
+    (3, 1024, 2, 2, 128, 100, 0.9, 1),
+    (3, 4096, 4, 2, 128, 64, 0.95, 4),
+    (2, 2048, 8, 8, 128, 64, 1.0, 1),
+    (3, 512, 2, 1, 64, 1, 0.9, 1),
+    (3, 768, 8, 1, 128, 200, 0.9, 2),
+]
+
+
+@pytest.mark.parametrize("wid,L,Hq,Hkv,d,lq,p_,W", CASES)
+def test_index_topp(wid, L, Hq, Hkv, d, lq, p_, W):
+    w = synth.make_workload(wid, L=L, Hq=Hq, Hkv=Hkv, d=d, last_q=lq, top_p=p_)
+    p, ix = _run(w, stripes=W)
+    v_or, S_or = oracle.index_scores(f64(w.q), f64(w.k), lq, stripes=W)
+    v_gpu = ix.v_score.double().cpu().numpy()
+    S_gpu = ix.s_score.double().cpu().numpy()
+    np.testing.assert_allclose(v_gpu, v_or, rtol=5e-5, atol=1e-7 * lq / L)
+    np.testing.assert_allclose(S_gpu, S_or, rtol=5e-5, atol=1e-7 * lq)
+    lists = gpu_index_lists(ix, Hq)
+    act = ix.active_entries.cpu().numpy()
+    bs = 64 * W
+    for h in range(Hq):
+        Vg, Sg = lists[h]
+        # same-precision decisions: oracle selection on the GPU's fp32 masses
+        v32 = ix.v_score[h].cpu().numpy().astype(np.float64)
+        S32 = ix.s_score[h].cpu().numpy().astype(np.float64)
+        np.testing.assert_array_equal(Vg, oracle.select_top_p(v32, np.float32(p_)))
+        np.testing.assert_array_equal(Sg, np.union1d(oracle.select_top_p(S32, np.float32(p_)), [0]))
+        assert act[h] == oracle.active_entries(L, Vg, Sg, bs)
+        # end to end against the fp64 oracle, ties at the threshold excepted
+        ok, bad = topp_sets_agree(v_or[h], oracle.select_top_p(v_or[h], p_), Vg, p_)
+        assert ok, bad[:5]
+        ok, bad = topp_sets_agree(S_or[h], oracle.select_top_p(S_or[h], p_), Sg, p_, forced=(0,))
+        assert ok, bad[:5]
+
+
+@pytest.mark.parametrize("density", [0.05, 0.2, 0.6])
+@pytest.mark.parametrize("wid,L,Hq,Hkv,d,W", [(3, 2048, 4, 2, 128, 1), (1, 4096, 1, 1, 64, 1),
+                                              (3, 4096, 2, 1, 128, 2)])
+def test_index_budget_fill(wid, L, Hq, Hkv, d, W, density):
+    w = synth.make_workload(wid, L=L, Hq=Hq, Hkv=Hkv, d=d)
+    p, ix = _run(w, density=density, stripes=W)
+    lists = gpu_index_lists(ix, Hq)
+    act = ix.active_entries.cpu().numpy()
+    dens32 = float(np.float32(density))
+    bs = 64 * W
+    for h in range(Hq):
+        v32 = ix.v_score[h].cpu().numpy().astype(np.float64)
+        S32 = ix.s_score[h].cpu().numpy().astype(np.float64)
+        Vo, So = oracle.select_budget(v32, S32, L, bs, dens32)
+        np.testing.assert_array_equal(lists[h][0], Vo)
+        np.testing.assert_array_equal(lists[h][1], So)
+        assert act[h] == oracle.active_entries(L, Vo, So, bs)
+        assert act[h] >= dens32 * oracle.total_causal_entries(L)
+
+
+def test_index_full_size_gqa_128k():
+    """The 128K GQA workload (16 query heads, 2 KV heads, d=128) at full size."""
+    w = synth.make_workload(3, backward=False)
+    p, ix = _run(w)
+    v_or, S_or = oracle.index_scores(f64(w.q), f64(w.k), w.last_q)
+    np.testing.assert_allclose(ix.v_score.double().cpu().numpy(), v_or, rtol=1e-4, atol=1e-10)
+    lists = gpu_index_lists(ix, w.Hq)
+    for h in range(w.Hq):
+        ok, bad = topp_sets_agree(v_or[h], oracle.select_top_p(v_or[h], w.top_p), lists[h][0], w.top_p)
+        assert ok, bad[:5]
+        # planted outliers carry most of the mass: all of them are verticals
+        assert set(w.outliers.tolist()) <= set(lists[h][0].tolist())

@@ -1,0 +1,103 @@
+"""Host-side checks of the C ABI: the library loads, exports every symbol the
+header declares, sizes workspaces, and rejects bad arguments before any
+launch (no GPU needed: validation returns before touching CUDA)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def vs():
+    from dynamic_sparse_attention_index_gb300 import build as b
+    b.build()
+    import dynamic_sparse_attention_index_gb300 as m
+    m.lib()
+    return m
+
+
+def test_exports_match_header(vs):
+    hdr = open(os.path.join(ROOT, "include", "vs.h")).read()
+    declared = set(re.findall(r"^\s*VS_API\s+(?:vs_status|size_t|const char\*)\s+(vs_\w+)\s*\(", hdr, re.M))
+    assert declared == set(vs.EXPORTED)
+    for name in declared:
+        assert hasattr(vs.lib(), name)
+
+
+def test_status_strings(vs):
+    for c in range(6):
+        assert vs.vs_status_string(c).startswith("VS_")
+
+
+def test_workspace_sizes(vs):
+    p = vs.make_params(131072, 16, 2, 128)
+    for op in (vs.VS_OP_INDEX, vs.VS_OP_FWD, vs.VS_OP_BWD):
+        assert vs.vs_workspace_bytes(p, op) >= 256
+    assert vs.vs_workspace_bytes(p, vs.VS_OP_ROPE) == 0
+    bad = vs.make_params(131072, 16, 3, 128)
+    assert vs.vs_workspace_bytes(bad, vs.VS_OP_INDEX) == 0
+
+
+FAKE = 1 << 20  # an aligned non-null address; never dereferenced on these paths
+
+
+def _call_index(vs, p, q=FAKE, k=FAKE, ws=FAKE, ws_bytes=1 << 40, ix=None):
+    if ix is None:
+        ix = vs.vs_index(FAKE, FAKE, FAKE, FAKE, None, None, None)
+    return vs.lib().vs_index_build(ctypes.byref(p), q, k, ctypes.byref(ix), ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(Hkv=3), "VS_ERR_INVALID_ARG"),
+    (dict(d=96), "VS_ERR_UNSUPPORTED"),
+    (dict(block=32), "VS_ERR_UNSUPPORTED"),
+    (dict(last_q=0), "VS_ERR_INVALID_ARG"),
+    (dict(last_q=4097), "VS_ERR_INVALID_ARG"),
+    (dict(top_p=0.0), "VS_ERR_INVALID_ARG"),
+    (dict(top_p=1.5), "VS_ERR_INVALID_ARG"),
+    (dict(L=4000), "VS_ERR_INVALID_ARG"),
+    (dict(stripes=3), "VS_ERR_INVALID_ARG"),
+    (dict(density=-0.1), "VS_ERR_INVALID_ARG"),
+])
+def test_index_rejects_bad_params(vs, kw, code):
+    args = dict(L=4096, Hq=4, Hkv=2, d=64, last_q=64, top_p=0.9)
+    args.update(kw)
+    p = vs.make_params(**args)
+    assert _call_index(vs, p) == getattr(vs, code)
+
+
+def test_index_rejects_bad_pointers_and_workspace(vs):
+    p = vs.make_params(4096, 4, 2, 64)
+    assert _call_index(vs, p, q=None) == vs.VS_ERR_INVALID_ARG
+    assert _call_index(vs, p, q=FAKE + 2) == vs.VS_ERR_INVALID_ARG       # misaligned
+    assert _call_index(vs, p, ix=vs.vs_index(None, FAKE, FAKE, FAKE, None, None, None)) == vs.VS_ERR_INVALID_ARG
+    assert _call_index(vs, p, ws=None) == vs.VS_ERR_WORKSPACE
+    assert _call_index(vs, p, ws=FAKE + 16) == vs.VS_ERR_WORKSPACE       # not 256-aligned
+    assert _call_index(vs, p, ws_bytes=16) == vs.VS_ERR_WORKSPACE
+
+
+def test_attention_rejects_bad_args(vs):
+    L = vs.lib()
+    p = vs.make_params(4096, 4, 2, 64)
+    ix = vs.vs_index(FAKE, FAKE, FAKE, FAKE, None, None, None)
+    r = L.vs_sparse_attn_fwd(ctypes.byref(p), ctypes.byref(ix), FAKE, FAKE, None, FAKE, FAKE, FAKE, 1 << 40, None)
+    assert r == vs.VS_ERR_INVALID_ARG
+    r = L.vs_sparse_attn_fwd(ctypes.byref(p), ctypes.byref(ix), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, None)
+    assert r == vs.VS_ERR_WORKSPACE
+    r = L.vs_sparse_attn_bwd(ctypes.byref(p), ctypes.byref(ix), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                             FAKE, None, FAKE, 1 << 40, None)
+    assert r == vs.VS_ERR_INVALID_ARG
+    bad = vs.make_params(4096, 4, 2, 80)
+    r = L.vs_sparse_attn_fwd(ctypes.byref(bad), ctypes.byref(ix), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
+    assert r == vs.VS_ERR_UNSUPPORTED
+
+
+def test_rope_rejects_bad_args(vs):
+    L = vs.lib()
+    p = vs.make_params(4096, 4, 2, 64, rope_theta=1.0)
+    assert L.vs_rope(ctypes.byref(p), 4, FAKE, FAKE, 0, None) == vs.VS_ERR_INVALID_ARG
+    p = vs.make_params(4096, 4, 2, 64, yarn_factor=32.0, yarn_orig_len=0)
+    assert L.vs_rope(ctypes.byref(p), 4, FAKE, FAKE, 0, None) == vs.VS_ERR_INVALID_ARG
