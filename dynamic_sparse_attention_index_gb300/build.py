@@ -61,6 +61,12 @@ def build(verbose: bool = False, force: bool = False) -> str:
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    # a shared library links with unresolved symbols; refuse any of our own
+    r = subprocess.run(["nm", "-u", "-C", tmp], capture_output=True, text=True)
+    missing = [l for l in r.stdout.splitlines() if "vs::" in l]
+    if missing:
+        os.remove(tmp)
+        raise RuntimeError("unresolved library symbols:\n" + "\n".join(missing))
     os.replace(tmp, LIB)
     return LIB
 

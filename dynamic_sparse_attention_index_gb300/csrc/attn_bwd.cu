@@ -1,0 +1,696 @@
+// Block-sparse causal attention backward: D = rowsum(dO * O) and the
+// key-stationary dK / dV kernel (tcgen05).  dQ runs in the query-major
+// kernel of attn_fwd.cu.
+//
+// Gradients of softmax attention with the mask held fixed (ring-attention
+// page, section 2.1 online softmax; MTraining review, section
+// "分布式稀疏索引近似" active regions):  P = exp(scale S - LSE) on active
+// entries, dV = P^T dO, dS = P (dO V^T - D), dK = scale dS^T Q.
+//
+// Key-stationary tiling.  A work unit keeps 64 keys (K and V rows) in shared
+// memory and streams "query sources" = 64 rows (head h, query block I) of
+// the GQA group that are active for those keys.  Two sources form a
+// 128-row tile (any two: no union waste):
+//   S  = Q_tile K^T, dP = dO_tile V^T            M = 128 rows, N = 64 keys
+//   P, dS per row (thread per TMEM lane) -> bf16 tiles in shared memory
+//   dV^T += dO_tile^T P,  dK^T += Q_tile^T dS    M = d, N = 64 keys, K = rows
+// so dK / dV of the 64 keys accumulate in TMEM across all sources and GQA
+// heads.  Slash units keep key block kb and stream (h, I) with band
+// I/W - kb/W kept (band 0 causal).  Vertical units keep 64 entries of a
+// head pair's packed vertical list and stream (h, I) over a slice of the
+// later query blocks with per-column masks (vertical m active for rows of
+// block I > m/64 whose band is not kept); their fp32 partials are summed,
+// in a fixed order, into the slash units' epilogue.
+#include "attn_common.cuh"
+#include "ptx.cuh"
+
+namespace vs {
+
+cudaError_t launch_attn_dq(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const void* Q, const void* K,
+                           const void* V, const void* dO, const float* lse, const float* Dsum, void* dQ,
+                           DevStatus* st, cudaStream_t s);
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kStages = 2;
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr int kMaxSplits = 32;
+
+// ---------------------------------------------------------------- D = rowsum(dO * O)
+__global__ void bwd_dsum_kernel(const __nv_bfloat16* __restrict__ O, const __nv_bfloat16* __restrict__ dO,
+                                float* __restrict__ Dsum, int L, int Hq, int d) {
+  // one 16-lane group per (token, head) row; 8 bf16 per lane
+  const long long gid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long row = gid >> 4;
+  const int sub = threadIdx.x & 15;
+  float acc = 0.f;
+  if (row < (long long)L * Hq) {
+    for (int c = sub * 8; c < d; c += 128) {
+      const uint4 a = *reinterpret_cast<const uint4*>(O + row * d + c);
+      const uint4 b = *reinterpret_cast<const uint4*>(dO + row * d + c);
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+      for (int k = 0; k < 4; ++k) {
+        const float2 fa = __bfloat1622float2(pa[k]), fb = __bfloat1622float2(pb[k]);
+        acc += fa.x * fb.x + fa.y * fb.y;
+      }
+    }
+  }
+  for (int o = 8; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if (sub == 0 && row < (long long)L * Hq) {
+    const int tok = (int)(row / Hq), h = (int)(row % Hq);
+    Dsum[(size_t)h * L + tok] = acc;
+  }
+}
+
+struct BwdParams {
+  AttnGeom g;
+  const uint32_t* inS;
+  const uint32_t* vlist;
+  const int32_t* vcnt;
+  const int32_t* s_idx;
+  const int32_t* s_cnt;
+  const float* lse;
+  const float* Dsum;
+  __nv_bfloat16* dK;
+  __nv_bfloat16* dV;
+  float* part_k;  // vertical partials [nvg][L][d] (fp32), split slots inside
+  float* part_v;
+  float scale;
+  float log2e;
+  DevStatus* status;
+  int vertical;   // 1: vertical units, 0: slash units
+};
+
+struct SrcMeta {
+  int32_t h[2];
+  int32_t I[2];
+  uint32_t mask[2][2];  // per source, 64 key columns
+  int32_t diag[2];      // 1 if the source's rows are the diagonal block of the keys
+  int32_t nsrc;
+  int32_t first, last;
+};
+
+// shared memory plan (bytes, 1024-aligned)
+constexpr int kHalfRows128 = 128 * 128;  // 128 rows x 128 B
+constexpr int kKVs = 0;                  // stationary K (2 x 8 KB) and V (2 x 8 KB): 64 keys
+constexpr int kKVsBytes = 4 * 8192;
+constexpr int kStage = kKVs + kKVsBytes;
+constexpr int kStageBytes = 4 * kHalfRows128;  // Q (2 halves) + dO (2 halves)
+constexpr int kPdS = kStage + kStages * kStageBytes;
+constexpr int kPdSBytes = 2 * 128 * 128;        // P and dS: 128 rows x 64 keys bf16 each
+constexpr int kMeta = kPdS + 2 * kPdSBytes;
+constexpr int kBars = kMeta + kStages * (int)sizeof(SrcMeta);
+// kvs_full, kvs_empty, st_full[S], st_empty[S], sdp_full[2], pds_ready[2], pds_free[2], acc_done, acc_free
+constexpr int kNumBars = 2 + 2 * kStages + 6 + 2;
+constexpr int kMisc = kBars + kNumBars * 8;
+constexpr int kSmemBytes = kMisc + 64;
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ bool band_kept(const uint32_t* bm, int B) { return (bm[B >> 5] >> (B & 31)) & 1u; }
+
+// number of row splits of a vertical group and the stride of its partial slots
+__device__ __forceinline__ void vsplit(const AttnGeom& g, int cnt, int* R, int* stride) {
+  const int r64 = (cnt + 63) & ~63;
+  int r = r64 > 0 ? g.L / r64 : 1;
+  if (r > kMaxSplits) r = kMaxSplits;
+  if (r < 1) r = 1;
+  *R = r;
+  *stride = r64;
+}
+
+// Vertical unit enumeration: units (vg, chunk, split), vg-major.
+struct VUnit {
+  int vg, chunk, split, R, stride, cnt;
+};
+__device__ bool decode_vunit(const AttnGeom& g, const int32_t* vcnt, int id, VUnit* u) {
+  for (int vg = 0; vg < g.nvg; ++vg) {
+    const int cnt = vcnt[(size_t)vg * (g.nb + 1) + g.nb];
+    int R, stride;
+    vsplit(g, cnt, &R, &stride);
+    const int nchunk = (cnt + 63) / 64;
+    const int n = nchunk * R;
+    if (id < n) {
+      u->vg = vg;
+      u->chunk = id / R;
+      u->split = id % R;
+      u->R = R;
+      u->stride = stride;
+      u->cnt = cnt;
+      return true;
+    }
+    id -= n;
+  }
+  return false;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
+                     const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
+                     const __grid_constant__ CUtensorMap mKp, const __grid_constant__ CUtensorMap mVp,
+                     const BwdParams P) {
+  constexpr int D = 128;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBars);
+  uint64_t* kvs_full = bars;
+  uint64_t* kvs_empty = bars + 1;
+  uint64_t* st_full = bars + 2;
+  uint64_t* st_empty = st_full + kStages;
+  uint64_t* sdp_full = st_empty + kStages;
+  uint64_t* pds_ready = sdp_full + 2;
+  uint64_t* pds_free = pds_ready + 2;
+  uint64_t* acc_done = pds_free + 2;
+  uint64_t* acc_free = acc_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc + 4);
+  SrcMeta* metas = reinterpret_cast<SrcMeta*>(sm + kMeta);
+  const AttnGeom& g = P.g;
+  const int W = g.bs / kBlock;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    mbar_init(kvs_full, 1);
+    mbar_init(kvs_empty, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&st_full[i], 1);
+      mbar_init(&st_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sdp_full[i], 1);
+      mbar_init(&pds_ready[i], 128);
+      mbar_init(&pds_free[i], 1);
+    }
+    mbar_init(acc_done, 1);
+    mbar_init(acc_free, 128);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+  // TMEM: S[2] at 0, 64; dP[2] at 128, 192; dV^T at 256; dK^T at 320 (64 columns each)
+  auto wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
+    if (*abort_flag) return false;
+    if (mbar_wait(bar, parity, kWaitLimitNs)) return true;
+    *abort_flag = 1;
+    report_timeout(P.status, where);
+    return false;
+  };
+  // the same, agreed across the warp (callers then issue warp-collective
+  // tcgen05 loads/stores, which every lane must execute together)
+  auto wait_warp = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
+    return __all_sync(0xffffffffu, wait(bar, parity, where));
+  };
+
+  // number of units of this launch
+  int nunits;
+  if (P.vertical) {
+    nunits = 0;
+    for (int vg = 0; vg < g.nvg; ++vg) {
+      const int cnt = P.vcnt[(size_t)vg * (g.nb + 1) + g.nb];
+      int R, stride;
+      vsplit(g, cnt, &R, &stride);
+      nunits += ((cnt + 63) / 64) * R;
+    }
+  } else {
+    nunits = g.Hkv * g.nb;
+  }
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    const uint32_t* bm0 = P.inS;
+    const uint32_t* bm1 = P.inS;
+    int t = 0, un = 0;
+    for (int uid = blockIdx.x; uid < nunits && !*abort_flag; uid += gridDim.x, ++un) {
+      int kvh, kb = 0, vg = 0, chunk = 0, split = 0, R = 1, nv = 0;
+      int hs[2] = {0, 0};
+      int nheads;
+      if (P.vertical) {
+        VUnit u;
+        decode_vunit(g, P.vcnt, uid, &u);
+        vg = u.vg;
+        chunk = u.chunk;
+        split = u.split;
+        R = u.R;
+        nv = u.cnt;
+        if (g.pair_heads) {
+          kvh = vg / (g.G / 2);
+          hs[0] = kvh * g.G + 2 * (vg % (g.G / 2));
+          hs[1] = hs[0] + 1;
+          nheads = 2;
+        } else {
+          kvh = vg / g.G;
+          hs[0] = hs[1] = vg;
+          nheads = 1;
+        }
+        bm0 = P.inS + (size_t)hs[0] * g.nw;
+        bm1 = P.inS + (size_t)hs[1] * g.nw;
+      } else {
+        // key blocks in ascending order (more causal rows first)
+        kvh = uid / g.nb;
+        kb = uid % g.nb;
+        nheads = g.G;
+      }
+      // stationary keys
+      if (lane == 0) {
+        if (wait(kvs_empty, (un & 1) ^ 1, 1)) {
+          mbar_arrive_expect_tx(kvs_full, kKVsBytes);
+          for (int hf = 0; hf < 2; ++hf) {
+            if (P.vertical) {
+              const int row = vg * g.L + chunk * 64;
+              tma_load_2d(sm + kKVs + hf * 8192, &mKp, kvs_full, hf * 64, row);
+              tma_load_2d(sm + kKVs + 16384 + hf * 8192, &mVp, kvs_full, hf * 64, row);
+            } else {
+              tma_load_3d(sm + kKVs + hf * 8192, &mK, kvs_full, hf * 64, kvh, kb * kBlock);
+              tma_load_3d(sm + kKVs + 16384 + hf * 8192, &mV, kvs_full, hf * 64, kvh, kb * kBlock);
+            }
+          }
+        }
+      }
+      __syncwarp();
+
+      // ---- the unit's sources, emitted two per tile
+      int nsrc = 0;
+      bool first = true;
+      SrcMeta pend;
+      auto emit = [&](bool last) {
+        const int st = t % kStages;
+        bool ok = true;
+        if (lane == 0) ok = wait(&st_empty[st], ((t / kStages) & 1) ^ 1, 2);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok && lane == 0) {
+          pend.nsrc = nsrc;
+          pend.first = first ? 1 : 0;
+          pend.last = last ? 1 : 0;
+          metas[st] = pend;
+          uint8_t* qd = sm + kStage + st * kStageBytes;
+          uint8_t* od = qd + 2 * kHalfRows128;
+          mbar_arrive_expect_tx(&st_full[st], nsrc * 4 * 8192);
+          for (int j = 0; j < nsrc; ++j)
+            for (int hf = 0; hf < 2; ++hf) {
+              tma_load_3d(qd + hf * kHalfRows128 + j * 8192, &mQ, &st_full[st], hf * 64, pend.h[j], pend.I[j] * kBlock);
+              tma_load_3d(od + hf * kHalfRows128 + j * 8192, &mdO, &st_full[st], hf * 64, pend.h[j],
+                          pend.I[j] * kBlock);
+            }
+        }
+        __syncwarp();
+        ++t;
+        nsrc = 0;
+        first = false;
+      };
+      // Sources are produced in batches of up to 32 candidates per warp step;
+      // to flag the last tile, a source is emitted only once the next one is
+      // known (one-source lookahead).
+      bool have_look = false;
+      int look_h = 0, look_I = 0;
+      uint32_t look_m0 = 0, look_m1 = 0;
+      int look_diag = 0;
+      auto push = [&](int h, int I, uint32_t m0, uint32_t m1, int diag) {
+        if (have_look) {
+          const int j = nsrc;
+          pend.h[j] = look_h;
+          pend.I[j] = look_I;
+          pend.mask[j][0] = look_m0;
+          pend.mask[j][1] = look_m1;
+          pend.diag[j] = look_diag;
+          if (++nsrc == 2) emit(false);
+        }
+        have_look = true;
+        look_h = h;
+        look_I = I;
+        look_m0 = m0;
+        look_m1 = m1;
+        look_diag = diag;
+      };
+
+      if (!P.vertical) {
+        for (int hl = 0; hl < nheads && !*abort_flag; ++hl) {
+          const int h = kvh * g.G + hl;
+          const int ns = P.s_cnt[h];
+          for (int j0 = 0; j0 < ns; j0 += 32) {
+            const int j = j0 + lane;
+            const int B = (j < ns) ? P.s_idx[(size_t)h * g.nbs + j] : -1;
+            // query blocks of band B for key block kb: I/W = kb/W + B, I >= kb
+            for (int k = 0; k < 32 && j0 + k < ns; ++k) {
+              const int Bk = __shfl_sync(0xffffffffu, B, k);
+              const int lo = max(kb, (kb / W + Bk) * W), hi = min(g.nb - 1, (kb / W + Bk) * W + W - 1);
+              for (int I = lo; I <= hi; ++I) push(h, I, 0xffffffffu, 0xffffffffu, I == kb ? 1 : 0);
+            }
+          }
+          // band 0 is always active even if the index omits it
+          bool has0 = ns > 0 && P.s_idx[(size_t)h * g.nbs] == 0;
+          if (!has0) {
+            const int lo = kb, hi = min(g.nb - 1, (kb / W) * W + W - 1);
+            for (int I = lo; I <= hi; ++I) push(h, I, 0xffffffffu, 0xffffffffu, I == kb ? 1 : 0);
+          }
+        }
+      } else {
+        // entries [chunk*64, chunk*64 + 64) of the union list; rows of later blocks
+        const size_t vbase = (size_t)vg * g.L + chunk * 64;
+        const int u0 = chunk * 64 + lane, u1 = u0 + 32;
+        const uint32_t e0 = u0 < nv ? P.vlist[vbase + lane] : 0xffffffffu;
+        const uint32_t e1 = u1 < nv ? P.vlist[vbase + 32 + lane] : 0xffffffffu;
+        const int m0 = u0 < nv ? (int)(e0 & kVTokenMask) : -1;
+        const int m1 = u1 < nv ? (int)(e1 & kVTokenMask) : -1;
+        const int kbmin = __shfl_sync(0xffffffffu, m0, 0) / kBlock;
+        const int Ilo = kbmin + 1;
+        const int nI = g.nb - Ilo;
+        const int per = (nI + R - 1) / R;
+        const int Ib = Ilo + split * per, Ie = min(g.nb, Ib + per);
+        for (int hi = 0; hi < nheads; ++hi) {
+          const uint32_t* bm = hi ? bm1 : bm0;
+          const int h = hs[hi];
+          for (int I = Ib; I < Ie && !*abort_flag; ++I) {
+            auto act = [&](int m, uint32_t e) -> bool {
+              if (m < 0 || !((e >> (kVFlagShift + hi)) & 1u)) return false;
+              const int kbm = m / kBlock;
+              if (kbm >= I) return false;
+              const int B = I / W - kbm / W;
+              return B != 0 && !band_kept(bm, B);
+            };
+            const uint32_t w0 = __ballot_sync(0xffffffffu, act(m0, e0));
+            const uint32_t w1 = __ballot_sync(0xffffffffu, act(m1, e1));
+            if (w0 | w1) push(h, I, w0, w1, 0);
+          }
+        }
+      }
+      // flush: the lookahead source is the unit's last
+      if (have_look) {
+        const int j = nsrc;
+        pend.h[j] = look_h;
+        pend.I[j] = look_I;
+        pend.mask[j][0] = look_m0;
+        pend.mask[j][1] = look_m1;
+        pend.diag[j] = look_diag;
+        ++nsrc;
+        emit(true);
+      } else {
+        // a vertical unit whose split has no active rows: one empty tile
+        pend.h[0] = P.vertical ? hs[0] : kvh * g.G;
+        pend.I[0] = P.vertical ? g.nb - 1 : kb;
+        pend.mask[0][0] = pend.mask[0][1] = 0u;
+        pend.diag[0] = 0;
+        nsrc = 1;
+        emit(true);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescSN64 = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t kIdescAcc = idesc_bf16(128, 64, true, true);  // M = d (A^T), N = 64 keys (B MN-major)
+      const uint32_t kvs = smem_u32(sm + kKVs);
+      int t = 0, un = 0;
+      bool have_prev = false;
+      int prev_t = 0, prev_nsrc = 0, prev_first = 0, prev_last = 0, prev_un = 0;
+      auto issue_acc = [&]() -> bool {
+        if (!wait(&pds_ready[prev_t & 1], (prev_t >> 1) & 1, 10)) return false;
+        if (prev_first && prev_un > 0)
+          if (!wait(acc_free, (prev_un - 1) & 1, 11)) return false;
+        tc_fence_after();
+        const int st = prev_t % kStages;
+        const uint32_t qa = smem_u32(sm + kStage + st * kStageBytes);
+        const uint32_t oa = qa + 2 * kHalfRows128;
+        const uint32_t pb = smem_u32(sm + kPdS + (prev_t & 1) * kPdSBytes);
+        const uint32_t db = pb + 128 * 128;
+        for (int kk = 0; kk < 4 * prev_nsrc; ++kk) {
+          // rows kk*16 .. kk*16+15: A = dO^T / Q^T (MN-major, two 64-d chunks 16 KB apart)
+          const uint32_t acc = (kk > 0 || !prev_first) ? 1u : 0u;
+          umma_ss(tbase + 256, sdesc_sw128(oa + kk * 2048, kHalfRows128, 1024), sdesc_sw128(pb + kk * 2048, 8192, 1024),
+                  kIdescAcc, acc);
+          umma_ss(tbase + 320, sdesc_sw128(qa + kk * 2048, kHalfRows128, 1024), sdesc_sw128(db + kk * 2048, 8192, 1024),
+                  kIdescAcc, acc);
+        }
+        umma_commit(&st_empty[st]);
+        umma_commit(&pds_free[prev_t & 1]);
+        if (prev_last) umma_commit(acc_done);
+        return true;
+      };
+      for (int uid = blockIdx.x; uid < nunits && !*abort_flag; uid += gridDim.x, ++un) {
+        bool last = false;
+        do {
+          const int st = t % kStages;
+          if (!wait(&st_full[st], (t / kStages) & 1, 12)) break;
+          const SrcMeta m = metas[st];
+          last = m.last != 0;
+          if (m.first)
+            if (!wait(kvs_full, un & 1, 13)) break;
+          tc_fence_after();
+          const uint32_t qa = smem_u32(sm + kStage + st * kStageBytes);
+          const uint32_t oa = qa + 2 * kHalfRows128;
+          const uint32_t buf = (uint32_t)(t & 1) * 64;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kHalfRows128 + (kk & 3) * 32;
+            const uint32_t koff = (kk >> 2) * 8192 + (kk & 3) * 32;
+            umma_ss(tbase + buf, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kvs + koff, 16, 1024), kIdescSN64,
+                    kk > 0 ? 1u : 0u);
+            umma_ss(tbase + 128 + buf, sdesc_sw128(oa + off, 16, 1024), sdesc_sw128(kvs + 16384 + koff, 16, 1024),
+                    kIdescSN64, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&sdp_full[t & 1]);
+          // the stationary keys are read only by S and dP: release them now
+          if (last) umma_commit(kvs_empty);
+          if (have_prev && !issue_acc()) break;
+          have_prev = true;
+          prev_t = t;
+          prev_nsrc = m.nsrc;
+          prev_first = m.first;
+          prev_last = m.last;
+          prev_un = un;
+          ++t;
+        } while (!last && !*abort_flag);
+      }
+      if (have_prev && !*abort_flag) issue_acc();
+    }
+    // lanes 1..31 wait here for the issuing lane: the block-wide barrier
+    // below is warp-aligned and must see the whole warp together
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ P / dS, epilogue
+    const int r = threadIdx.x - 128;
+    const int src = r >> 6, rr = r & 63;
+    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+    int t = 0, un = 0;
+    for (int uid = blockIdx.x; uid < nunits && !*abort_flag; uid += gridDim.x, ++un) {
+      bool last = false;
+      do {
+        const int st = t % kStages;
+        if (!wait_warp(&st_full[st], (t / kStages) & 1, 20)) break;
+        const SrcMeta& mref = metas[st];
+        const bool valid = src < mref.nsrc;
+        const uint32_t mw0 = valid ? mref.mask[src][0] : 0u, mw1 = valid ? mref.mask[src][1] : 0u;
+        const int diag = valid ? mref.diag[src] : 0;
+        const int h = mref.h[valid ? src : 0];
+        const int tok = mref.I[valid ? src : 0] * kBlock + rr;
+        last = mref.last != 0;
+        float lse2 = 0.f, Dr = 0.f;
+        if (valid) {
+          lse2 = P.lse[(size_t)h * g.L + tok] * P.log2e;
+          Dr = P.Dsum[(size_t)h * g.L + tok];
+        }
+        if (!wait_warp(&sdp_full[t & 1], (t >> 1) & 1, 21)) break;
+        if (t >= 2 && !wait_warp(&pds_free[t & 1], ((t >> 1) - 1) & 1, 22)) break;
+        tc_fence_after();
+        const float c = P.scale * P.log2e;
+        uint8_t* pbuf = sm + kPdS + (t & 1) * kPdSBytes;
+        uint8_t* dbuf = pbuf + 128 * 128;
+#pragma unroll
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t sv[32], dv[32];
+          tmem_ld32(tbase + (uint32_t)((t & 1) * 64) + lane_off + c0, sv);
+          tmem_ld32(tbase + 128 + (uint32_t)((t & 1) * 64) + lane_off + c0, dv);
+          tmem_ld_wait();
+          const uint32_t mw = c0 ? mw1 : mw0;
+          uint32_t pk[16], dk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            float pp[2], dd[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int col = 2 * k + e;
+              bool on = (mw >> col) & 1u;
+              if (diag && (c0 + col) > rr) on = false;
+              const float p = on ? fast_exp2(__uint_as_float(sv[col]) * c - lse2) : 0.f;
+              pp[e] = p;
+              dd[e] = p * (__uint_as_float(dv[col]) - Dr);
+            }
+            pk[k] = pack_bf16(pp[0], pp[1]);
+            dk[k] = pack_bf16(dd[0], dd[1]);
+          }
+          // row r of a 128-row x 64-key MN-major SW128 tile: 8 chunks of 16 B
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int chunk = (c0 / 8) + q;  // 16-byte chunk index within the 128-byte row
+            const int phys = chunk ^ (r & 7);
+            const int off = (r >> 3) * 1024 + (r & 7) * 128 + phys * 16;
+            *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            *reinterpret_cast<uint4*>(dbuf + off) = make_uint4(dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(&pds_ready[t & 1]);
+        if (last) {
+          // ---- epilogue: thread r holds dV^T[d = r][0..63] and dK^T[d = r][0..63]
+          if (!wait_warp(acc_done, un & 1, 23)) break;
+          tc_fence_after();
+          const int dcol = r;
+          uint32_t av[64], ak[64];
+          tmem_ld32(tbase + 256 + lane_off, av);
+          tmem_ld32(tbase + 256 + lane_off + 32, av + 32);
+          tmem_ld32(tbase + 320 + lane_off, ak);
+          tmem_ld32(tbase + 320 + lane_off + 32, ak + 32);
+          tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(acc_free);
+          if (P.vertical) {
+            VUnit u;
+            decode_vunit(g, P.vcnt, uid, &u);
+            for (int j = 0; j < 64; ++j) {
+              const int e = u.chunk * 64 + j;
+              if (e >= u.cnt) break;
+              const size_t o = ((size_t)u.vg * g.L + (size_t)u.split * u.stride + e) * D + dcol;
+              P.part_v[o] = __uint_as_float(av[j]);
+              P.part_k[o] = __uint_as_float(ak[j]);
+            }
+          } else {
+            const int kvh = uid / g.nb, kb = uid % g.nb;
+            // add the vertical partials of tokens in this key block (all union groups of kvh)
+            const int vg_per_kv = g.pair_heads ? g.G / 2 : g.G;
+            for (int q = 0; q < vg_per_kv; ++q) {
+              const int vg = kvh * vg_per_kv + q;
+              const int cnt = P.vcnt[(size_t)vg * (g.nb + 1) + g.nb];
+              int R, stride;
+              vsplit(g, cnt, &R, &stride);
+              const int e0 = P.vcnt[(size_t)vg * (g.nb + 1) + kb], e1 = P.vcnt[(size_t)vg * (g.nb + 1) + kb + 1];
+              for (int e = e0; e < e1; ++e) {
+                const int j = (int)(P.vlist[(size_t)vg * g.L + e] & kVTokenMask) - kb * kBlock;
+                float sk = 0.f, sv = 0.f;
+                for (int sp = 0; sp < R; ++sp) {
+                  const size_t o = ((size_t)vg * g.L + (size_t)sp * stride + e) * D + dcol;
+                  sk += P.part_k[o];
+                  sv += P.part_v[o];
+                }
+#pragma unroll 1
+                for (int jj = 0; jj < 64; ++jj)
+                  if (jj == j) {
+                    ak[jj] = __float_as_uint(__uint_as_float(ak[jj]) + sk);
+                    av[jj] = __float_as_uint(__uint_as_float(av[jj]) + sv);
+                  }
+              }
+            }
+            for (int j = 0; j < 64; ++j) {
+              const size_t o = ((size_t)(kb * kBlock + j) * g.Hkv + kvh) * D + dcol;
+              P.dV[o] = __float2bfloat16_rn(__uint_as_float(av[j]));
+              P.dK[o] = __float2bfloat16_rn(__uint_as_float(ak[j]) * P.scale);
+            }
+          }
+        }
+        ++t;
+      } while (!last && !*abort_flag);
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tbase, 512);
+}
+
+struct BwdWs {
+  size_t status, prep_end, dsum, part_k, part_v, total;
+  PrepWs prep;
+};
+
+BwdWs bwd_layout(const AttnGeom& g) {
+  WsLayout w;
+  BwdWs o;
+  o.status = w.take(sizeof(DevStatus));
+  o.prep = prep_layout(g, w);
+  o.dsum = w.take((size_t)g.Hq * g.L * 4);
+  o.part_k = w.take((size_t)g.nvg * g.L * g.d * 4);
+  o.part_v = w.take((size_t)g.nvg * g.L * g.d * 4);
+  o.total = w.off;
+  return o;
+}
+
+}  // namespace
+
+size_t attn_bwd_ws_bytes(const vs_params& p) { return bwd_layout(make_geom(p)).total; }
+
+cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
+                            const void* O, const float* lse, const void* dO, void* dQ, void* dK, void* dV, void* ws,
+                            cudaStream_t s) {
+  if (p.d != 128) return cudaErrorNotSupported;
+  const AttnGeom g = make_geom(p);
+  const BwdWs lay = bwd_layout(g);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  PrepPtrs pp;
+  pp.inS = reinterpret_cast<uint32_t*>(w + lay.prep.inS);
+  pp.vlist = reinterpret_cast<uint32_t*>(w + lay.prep.vlist);
+  pp.vcnt = reinterpret_cast<int32_t*>(w + lay.prep.vcnt);
+  pp.Kp = reinterpret_cast<__nv_bfloat16*>(w + lay.prep.Kp);
+  pp.Vp = reinterpret_cast<__nv_bfloat16*>(w + lay.prep.Vp);
+  float* dsum = reinterpret_cast<float*>(w + lay.dsum);
+  DevStatus* st = reinterpret_cast<DevStatus*>(w + lay.status);
+  cudaError_t e = launch_attn_prep(g, ix, K, V, pp, s);
+  if (e != cudaSuccess) return e;
+  {
+    const long long rows = (long long)g.L * g.Hq;
+    const long long threads = rows * 16;
+    bwd_dsum_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), dsum, g.L, g.Hq, g.d);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  CUtensorMap mQ, mdO, mK, mV, mKp, mVp;
+  if (!make_map_heads(&mQ, Q, g.L, g.Hq, 128) || !make_map_heads(&mdO, dO, g.L, g.Hq, 128) ||
+      !make_map_heads(&mK, K, g.L, g.Hkv, 128) || !make_map_heads(&mV, V, g.L, g.Hkv, 128) ||
+      !make_map_rows(&mKp, pp.Kp, (long long)g.nvg * g.L, 128) ||
+      !make_map_rows(&mVp, pp.Vp, (long long)g.nvg * g.L, 128))
+    return cudaErrorInvalidValue;
+  BwdParams P;
+  P.g = g;
+  P.inS = pp.inS;
+  P.vlist = pp.vlist;
+  P.vcnt = pp.vcnt;
+  P.s_idx = ix.s_idx;
+  P.s_cnt = ix.s_cnt;
+  P.lse = lse;
+  P.Dsum = dsum;
+  P.dK = static_cast<__nv_bfloat16*>(dK);
+  P.dV = static_cast<__nv_bfloat16*>(dV);
+  P.part_k = reinterpret_cast<float*>(w + lay.part_k);
+  P.part_v = reinterpret_cast<float*>(w + lay.part_v);
+  P.scale = default_scale(p);
+  P.log2e = 1.4426950408889634f;
+  P.status = st;
+  const size_t smem = kSmemBytes + 1024;
+  if ((e = cudaFuncSetAttribute(attn_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+      cudaSuccess)
+    return e;
+  int dev = 0, nsm = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  // vertical units first: their partials feed the slash units' epilogue
+  P.vertical = 1;
+  attn_dkdv_kernel<<<nsm, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, P);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  P.vertical = 0;
+  const int nunits = g.Hkv * g.nb;
+  attn_dkdv_kernel<<<nunits < nsm ? nunits : nsm, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, P);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_attn_dq(p, g, pp, Q, K, V, dO, lse, dsum, dQ, st, s);
+}
+
+}  // namespace vs

@@ -1,0 +1,138 @@
+// Work decomposition and preparation shared by the sparse attention forward
+// and backward kernels.
+//
+// A row tile is 128 query rows = two 64-row "segments" (h_s, I_s) that use
+// the same key/value head.  When the GQA group size G is even, a tile holds
+// query block I of two heads of one group (their kept lines overlap heavily,
+// so the union of their key sources wastes little); otherwise it holds
+// blocks I and I+1 of one head.  A segment's active entries are
+//   slash: key block kb with kb <= I_s and band I_s - kb kept for h_s
+//          (band 0 = the diagonal block, causal inside);
+//   vertical: kept token m of h_s with m/64 < I_s whose band I_s - m/64 is
+//          not kept (otherwise the slash block already covers it).
+// Key sources are 64-key units: one slash key block, or 64 consecutive
+// entries of the tile's vertical union list (verticals of both segments'
+// heads, ascending, with per-entry membership flags), whose K/V rows are
+// packed contiguously by the prep kernels so TMA can stage them.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace vs {
+
+constexpr uint32_t kVFlagShift = 30;  // union entry = token | (membership bits << 30)
+constexpr uint32_t kVTokenMask = (1u << kVFlagShift) - 1u;
+
+struct AttnGeom {
+  int L, Hq, Hkv, G, d;
+  int nb;           // L / 64 query / key blocks
+  int nbs;          // L / bs (bands)
+  int bs;           // 64 * stripes
+  int nw;           // 32-bit words per kept-band bitmap (covers nbs bands)
+  int pair_heads;   // 1: tiles pair two heads at the same block; 0: blocks I, I+1 of one head
+  int nvg;          // vertical union groups (head pairs, or heads)
+  int nitems;       // row tiles
+  int items_per_row;  // tiles per block index (pair_heads) or per block pair
+};
+
+inline AttnGeom make_geom(const vs_params& p) {
+  AttnGeom g;
+  g.L = p.L;
+  g.Hq = p.Hq;
+  g.Hkv = p.Hkv;
+  g.G = p.Hq / p.Hkv;
+  g.d = p.d;
+  g.nb = p.L / kBlock;
+  g.bs = kBlock * p.stripes;
+  g.nbs = p.L / g.bs;
+  g.nw = (g.nbs + 31) / 32;
+  g.pair_heads = (g.G % 2 == 0) ? 1 : 0;
+  if (g.pair_heads) {
+    g.nvg = p.Hq / 2;
+    g.items_per_row = p.Hq / 2;
+    g.nitems = g.nb * g.items_per_row;
+  } else {
+    g.nvg = p.Hq;
+    g.items_per_row = p.Hq;
+    g.nitems = ((g.nb + 1) / 2) * g.items_per_row;
+  }
+  return g;
+}
+
+struct Item {
+  int g;        // key/value head
+  int h[2];     // query heads of the two segments
+  int I[2];     // query blocks (64 rows each)
+  bool valid[2];
+  int vg;       // vertical union group
+};
+
+// Items are numbered heaviest-first: larger block index = more causal keys.
+__host__ __device__ inline Item decode_item(const AttnGeom& g, int id) {
+  Item it;
+  if (g.pair_heads) {
+    const int I = g.nb - 1 - id / g.items_per_row;
+    const int pr = id % g.items_per_row;
+    const int kv = pr / (g.G / 2), hp = pr % (g.G / 2);
+    it.g = kv;
+    it.h[0] = kv * g.G + 2 * hp;
+    it.h[1] = it.h[0] + 1;
+    it.I[0] = it.I[1] = I;
+    it.valid[0] = it.valid[1] = true;
+    it.vg = pr;
+  } else {
+    const int npair = (g.nb + 1) / 2;
+    const int u = npair - 1 - id / g.items_per_row;
+    const int h = id % g.items_per_row;
+    it.g = h / g.G;
+    it.h[0] = it.h[1] = h;
+    it.I[0] = 2 * u;
+    it.I[1] = 2 * u + 1;
+    it.valid[0] = true;
+    it.valid[1] = (2 * u + 1) < g.nb;
+    it.vg = h;
+  }
+  return it;
+}
+
+// Workspace regions written by the prep kernels (offsets from ws base).
+struct PrepWs {
+  size_t inS;     // [Hq][nw] uint32 kept-band bitmaps
+  size_t vlist;   // [nvg][L] uint32 union entries
+  size_t vcnt;    // [nvg][nb + 1] int32: entries with token < 64 * b
+  size_t Kp;      // [nvg][L][d] bf16 packed key rows of the union
+  size_t Vp;      // [nvg][L][d] bf16 packed value rows
+  size_t end;
+};
+
+inline PrepWs prep_layout(const AttnGeom& g, WsLayout& w) {
+  PrepWs o;
+  o.inS = w.take((size_t)g.Hq * g.nw * 4);
+  o.vlist = w.take((size_t)g.nvg * g.L * 4);
+  o.vcnt = w.take((size_t)g.nvg * (g.nb + 1) * 4);
+  o.Kp = w.take((size_t)g.nvg * g.L * g.d * 2);
+  o.Vp = w.take((size_t)g.nvg * g.L * g.d * 2);
+  o.end = w.off;
+  return o;
+}
+
+struct PrepPtrs {
+  uint32_t* inS;
+  uint32_t* vlist;
+  int32_t* vcnt;
+  __nv_bfloat16* Kp;
+  __nv_bfloat16* Vp;
+};
+
+cudaError_t launch_attn_prep(const AttnGeom& g, const vs_index& ix, const void* K, const void* V,
+                             const PrepPtrs& pp, cudaStream_t s);
+
+// Tensor-map helpers (host): 3-D view (d, heads, tokens) of a [L][H][d] bf16
+// tensor with a (64, 1, 64) box, and a 2-D view (d, rows) with a (64, 64) box,
+// both with 128-byte swizzle (the tcgen05 K-major / MN-major SW128 layouts).
+bool make_map_heads(CUtensorMap* m, const void* base, int L, int H, int d);
+bool make_map_rows(CUtensorMap* m, const void* base, long long rows, int d);
+
+}  // namespace vs

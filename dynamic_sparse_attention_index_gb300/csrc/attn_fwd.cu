@@ -1,0 +1,529 @@
+// Block-sparse causal attention forward on the active VS entries (tcgen05).
+//
+// MTraining review, section "分布式稀疏索引近似" (each worker computes only the
+// active regions of its sub-matrix derived from the vertical and slash
+// indices) with the online softmax across key blocks of the ring-attention
+// page (section 2.1): for each 128-row tile the kernel walks its active key
+// sources, S = Q K^T on the tensor cores into TMEM, masks, updates the row
+// max / sum, writes P (bf16) back into TMEM and accumulates O += P V with the
+// A operand read from TMEM.
+//
+// Persistent CTAs (one per SM), 8 warps:
+//   warp 0     producer: enumerates the tile's key sources, builds per-column
+//              masks, issues TMA loads of Q (per tile) and K/V (per source)
+//   warp 1     MMA issuer (one thread): S_t = Q K_t^T, then O += P_{t-1} V_{t-1}
+//   warp 2     owns the TMEM allocation
+//   warps 4-7  softmax + epilogue: thread r owns row r (TMEM lane r)
+// TMEM columns: S double buffer [0,128) and [128,256) (P aliases the first
+// 64 columns of its S buffer as packed bf16), O at [256, 256 + d).
+// O is rescaled lazily: only when a row maximum grows by more than 8 (log2
+// units) is the running O multiplied down; otherwise exponentials are taken
+// against the stale maximum, which is exact after the final 1/l.
+#include "attn_common.cuh"
+#include "ptx.cuh"
+
+namespace vs {
+namespace {
+
+constexpr int kStages = 2;
+constexpr int kThreads = 256;
+constexpr float kNegInf = -__builtin_huge_valf();
+constexpr float kRescaleThreshold = 8.0f;
+
+struct TileMeta {
+  uint32_t mask[2][4];  // per segment, columns 0..127 active (before the causal rule)
+  int32_t diag[2];      // per segment: column offset of the diagonal source, or -1
+  int32_t nsrc;         // 1 or 2 sources of 64 keys
+  int32_t first, last;  // first / last tile of the row tile
+  int32_t qslot;
+};
+
+struct FwdParams {
+  AttnGeom g;
+  const uint32_t* inS;
+  const uint32_t* vlist;
+  const int32_t* vcnt;
+  __nv_bfloat16* O;
+  float* lse;
+  float scale_log2;
+  DevStatus* status;
+};
+
+template <int D>
+struct Layout {
+  static constexpr int kHalves = D / 64;
+  static constexpr int kRowBytes = 128 * 128;            // 128 rows x 128 bytes (one 64-wide d half)
+  static constexpr int kQBytes = kHalves * kRowBytes;    // one Q slot
+  static constexpr int kKBytes = kHalves * kRowBytes;    // 128 keys of K
+  static constexpr int kQ = 0;
+  static constexpr int kStage = 2 * kQBytes;
+  static constexpr int kStageBytes = 2 * kKBytes;        // K then V
+  static constexpr int kMeta = kStage + kStages * kStageBytes;
+  static constexpr int kBars = kMeta + kStages * (int)sizeof(TileMeta);
+  // barriers: q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_ready[2], pv_done, o_free
+  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 1 + 1;
+  static constexpr int kMisc = kBars + kNumBars * 8;      // tmem slot, abort flag
+  static constexpr int kBitmaps = kMisc + 64;             // producer-private band bitmaps
+};
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ bool band_kept(const uint32_t* bm, int B) { return (bm[B >> 5] >> (B & 31)) & 1u; }
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1)
+    attn_fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
+                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mKp,
+                    const __grid_constant__ CUtensorMap mVp, const FwdParams P) {
+  using Ly = Layout<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::kBars);
+  uint64_t* q_full = bars;
+  uint64_t* q_empty = bars + 2;
+  uint64_t* kv_full = bars + 4;
+  uint64_t* kv_empty = kv_full + kStages;
+  uint64_t* s_full = kv_empty + kStages;
+  uint64_t* p_ready = s_full + 2;
+  uint64_t* pv_done = p_ready + 2;
+  uint64_t* o_free = pv_done + 1;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Ly::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Ly::kMisc + 4);
+  TileMeta* metas = reinterpret_cast<TileMeta*>(sm + Ly::kMeta);
+  const AttnGeom& g = P.g;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_ready[i], 128);
+    }
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    mbar_init(pv_done, 1);
+    mbar_init(o_free, 128);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = *tmem_slot;
+
+  auto wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
+    if (*abort_flag) return false;
+    if (mbar_wait(bar, parity, kWaitLimitNs)) return true;
+    *abort_flag = 1;
+    report_timeout(P.status, where);
+    return false;
+  };
+  // the same, agreed across the warp (callers then issue warp-collective
+  // tcgen05 loads/stores, which every lane must execute together)
+  auto wait_warp = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
+    return __all_sync(0xffffffffu, wait(bar, parity, where));
+  };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    uint32_t* bm0 = reinterpret_cast<uint32_t*>(sm + Ly::kBitmaps);
+    uint32_t* bm1 = bm0 + g.nw;
+    const int W = g.bs / kBlock;
+    int t = 0, it_local = 0;
+    if (lane == 0) {
+      tma_prefetch_desc(&mQ);
+      tma_prefetch_desc(&mK);
+      tma_prefetch_desc(&mV);
+      tma_prefetch_desc(&mKp);
+      tma_prefetch_desc(&mVp);
+    }
+    for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
+      const Item it = decode_item(g, id);
+      const int qslot = it_local & 1;
+      for (int w = lane; w < g.nw; w += 32) {
+        bm0[w] = P.inS[(size_t)it.h[0] * g.nw + w];
+        bm1[w] = P.inS[(size_t)it.h[1] * g.nw + w];
+      }
+      __syncwarp();
+      if (lane == 0) {
+        if (wait(&q_empty[qslot], ((it_local >> 1) & 1) ^ 1, 1)) {
+          mbar_arrive_expect_tx(&q_full[qslot], Ly::kQBytes);
+          uint8_t* q = sm + Ly::kQ + qslot * Ly::kQBytes;
+          for (int s = 0; s < 2; ++s)
+            for (int hf = 0; hf < Ly::kHalves; ++hf)
+              tma_load_3d(q + hf * Ly::kRowBytes + s * 8192, &mQ, &q_full[qslot], hf * 64, it.h[s],
+                          it.I[s] * kBlock);
+        }
+      }
+      __syncwarp();
+      const int Itop = it.valid[1] ? max(it.I[0], it.I[1]) : it.I[0];
+
+      // a segment's key block kb is an active slash source when kb <= I_s
+      // and its band is kept (band 0, the diagonal tile, always is)
+      auto slash_active = [&](int s, int kb) -> bool {
+        if (!it.valid[s] || kb < 0 || kb > it.I[s]) return false;
+        const int B = it.I[s] / W - kb / W;
+        return B == 0 || band_kept(s ? bm1 : bm0, B);
+      };
+      // ---- count the sources first so the final tile can be flagged
+      int nslash = 0;
+      for (int kb0 = Itop; kb0 >= 0; kb0 -= 32) {
+        const int kb = kb0 - lane;
+        const bool a = slash_active(0, kb) || slash_active(1, kb);
+        nslash += __popc(__ballot_sync(0xffffffffu, a));
+      }
+      const int nv = P.vcnt[(size_t)it.vg * (g.nb + 1) + Itop];
+      const int nchunks = (nv + 63) / 64;
+      const int total_src = nslash + nchunks;
+
+      // pending sources of the tile being assembled
+      int nsrc = 0, done_src = 0;
+      int src_kind[2] = {0, 0};  // 0 slash key block, 1 vertical chunk
+      int src_arg[2] = {0, 0};
+      uint32_t smask[2][4];
+      int sdiag[2];
+      bool first = true;
+      auto reset_masks = [&]() {
+        for (int s = 0; s < 2; ++s) {
+          for (int w = 0; w < 4; ++w) smask[s][w] = 0;
+          sdiag[s] = -1;
+        }
+      };
+      auto emit = [&]() {
+        done_src += nsrc;
+        const bool last = done_src == total_src;
+        const int st = t % kStages;
+        bool ok = true;
+        if (lane == 0) ok = wait(&kv_empty[st], ((t / kStages) & 1) ^ 1, 2);
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (ok && lane == 0) {
+          TileMeta& m = metas[st];
+          for (int s = 0; s < 2; ++s) {
+            for (int w = 0; w < 4; ++w) m.mask[s][w] = smask[s][w];
+            m.diag[s] = sdiag[s];
+          }
+          m.nsrc = nsrc;
+          m.first = first ? 1 : 0;
+          m.last = last ? 1 : 0;
+          m.qslot = qslot;
+          uint8_t* kst = sm + Ly::kStage + st * Ly::kStageBytes;
+          uint8_t* vst = kst + Ly::kKBytes;
+          mbar_arrive_expect_tx(&kv_full[st], nsrc * 2 * Ly::kHalves * 8192);
+          for (int j = 0; j < nsrc; ++j) {
+            for (int hf = 0; hf < Ly::kHalves; ++hf) {
+              uint8_t* kd = kst + hf * Ly::kRowBytes + j * 8192;
+              uint8_t* vd = vst + hf * Ly::kRowBytes + j * 8192;
+              if (src_kind[j] == 0) {
+                tma_load_3d(kd, &mK, &kv_full[st], hf * 64, it.g, src_arg[j] * kBlock);
+                tma_load_3d(vd, &mV, &kv_full[st], hf * 64, it.g, src_arg[j] * kBlock);
+              } else {
+                const int row = it.vg * g.L + src_arg[j] * 64;
+                tma_load_2d(kd, &mKp, &kv_full[st], hf * 64, row);
+                tma_load_2d(vd, &mVp, &kv_full[st], hf * 64, row);
+              }
+            }
+          }
+        }
+        __syncwarp();
+        ++t;
+        nsrc = 0;
+        first = false;
+        reset_masks();
+      };
+      reset_masks();
+
+      // ---- slash sources: key blocks kb = Itop, Itop-1, ..., 0 (32 per step)
+      for (int kb0 = Itop; kb0 >= 0 && !*abort_flag; kb0 -= 32) {
+        const int kb = kb0 - lane;
+        const uint32_t b0 = __ballot_sync(0xffffffffu, slash_active(0, kb));
+        const uint32_t b1 = __ballot_sync(0xffffffffu, slash_active(1, kb));
+        uint32_t u = b0 | b1;
+        while (u) {
+          const int bit = __ffs(u) - 1;
+          u &= u - 1;
+          const int kbs = kb0 - bit;
+          const int j = nsrc;
+          src_kind[j] = 0;
+          src_arg[j] = kbs;
+          for (int s = 0; s < 2; ++s) {
+            const bool on = (s ? (b1 >> bit) : (b0 >> bit)) & 1u;
+            smask[s][2 * j] = on ? 0xffffffffu : 0u;
+            smask[s][2 * j + 1] = on ? 0xffffffffu : 0u;
+            if (on && kbs == it.I[s]) sdiag[s] = 64 * j;
+          }
+          if (++nsrc == 2) emit();
+        }
+      }
+      // ---- vertical sources: 64-entry chunks of the union list below block Itop
+      for (int c = 0; c < nchunks && !*abort_flag; ++c) {
+        const int j = nsrc;
+        src_kind[j] = 1;
+        src_arg[j] = c;
+        for (int half = 0; half < 2; ++half) {
+          const int u = c * 64 + half * 32 + lane;
+          bool a[2] = {false, false};
+          if (u < nv) {
+            const uint32_t e = P.vlist[(size_t)it.vg * g.L + u];
+            const int m = (int)(e & kVTokenMask);
+            const uint32_t f = e >> kVFlagShift;
+            const int kbm = m / kBlock;
+            for (int s = 0; s < 2; ++s) {
+              if (!it.valid[s] || !((f >> s) & 1u) || kbm >= it.I[s]) continue;
+              const int B = it.I[s] / W - kbm / W;
+              a[s] = B != 0 && !band_kept(s ? bm1 : bm0, B);
+            }
+          }
+          smask[0][2 * j + half] = __ballot_sync(0xffffffffu, a[0]);
+          smask[1][2 * j + half] = __ballot_sync(0xffffffffu, a[1]);
+        }
+        if (++nsrc == 2) emit();
+      }
+      if (nsrc > 0) emit();
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdescS64 = idesc_bf16(128, 64, false, false);
+      constexpr uint32_t kIdescS128 = idesc_bf16(128, 128, false, false);
+      constexpr uint32_t kIdescPV = idesc_bf16(128, D, false, true);
+      const uint32_t tO = tbase + 256;
+      int t = 0, it_local = 0;
+      bool have_prev = false;
+      int prev_t = 0, prev_nsrc = 0, prev_first = 0, prev_item = 0;
+      auto issue_pv = [&]() -> bool {
+        if (!wait(&p_ready[prev_t & 1], (prev_t >> 1) & 1, 10)) return false;
+        if (prev_first && prev_item > 0)
+          if (!wait(o_free, (prev_item - 1) & 1, 11)) return false;
+        tc_fence_after();
+        const int st = prev_t % kStages;
+        const uint32_t vst = smem_u32(sm + Ly::kStage + st * Ly::kStageBytes + Ly::kKBytes);
+        const uint32_t pS = tbase + (uint32_t)((prev_t & 1) * 128);
+        for (int kk = 0; kk < 4 * prev_nsrc; ++kk) {
+          const uint64_t bd = sdesc_sw128(vst + kk * 2048, Ly::kRowBytes, 1024);
+          umma_ts(tO, pS + kk * 8, bd, kIdescPV, (kk > 0 || !prev_first) ? 1u : 0u);
+        }
+        umma_commit(&kv_empty[st]);
+        umma_commit(pv_done);
+        return true;
+      };
+      for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
+        bool last = false;
+        do {
+          const int st = t % kStages;
+          if (!wait(&kv_full[st], (t / kStages) & 1, 12)) break;
+          const TileMeta m = metas[st];
+          last = m.last != 0;
+          if (m.first)
+            if (!wait(&q_full[m.qslot], (it_local >> 1) & 1, 13)) break;
+          tc_fence_after();
+          const uint32_t qa = smem_u32(sm + Ly::kQ + m.qslot * Ly::kQBytes);
+          const uint32_t kb = smem_u32(sm + Ly::kStage + st * Ly::kStageBytes);
+          const uint32_t dS = tbase + (uint32_t)((t & 1) * 128);
+          const uint32_t idS = m.nsrc == 2 ? kIdescS128 : kIdescS64;
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * Ly::kRowBytes + (kk & 3) * 32;
+            umma_ss(dS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(&s_full[t & 1]);
+          if (last) umma_commit(&q_empty[m.qslot]);
+          if (have_prev && !issue_pv()) break;
+          have_prev = true;
+          prev_t = t;
+          prev_nsrc = m.nsrc;
+          prev_first = m.first;
+          prev_item = it_local;
+          ++t;
+        } while (!last && !*abort_flag);
+      }
+      if (have_prev && !*abort_flag) issue_pv();
+    }
+    // lanes 1..31 wait here for the issuing lane: the block-wide barrier
+    // below is warp-aligned and must see the whole warp together
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax + epilogue
+    const int r = threadIdx.x - 128;  // row of the tile == TMEM lane
+    const int seg = r >> 6, rr = r & 63;
+    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+    const uint32_t tO = tbase + 256 + lane_off;
+    int t = 0, it_local = 0;
+    for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
+      const Item it = decode_item(g, id);
+      float m_ref = kNegInf, l = 0.f;
+      bool last = false;
+      do {
+        const int st = t % kStages;
+        if (!wait_warp(&kv_full[st], (t / kStages) & 1, 20)) break;
+        uint32_t mw[4];
+        for (int w = 0; w < 4; ++w) mw[w] = metas[st].mask[seg][w];
+        const int diag = metas[st].diag[seg];
+        last = metas[st].last != 0;
+        if (!wait_warp(&s_full[t & 1], (t >> 1) & 1, 21)) break;
+        tc_fence_after();
+        const uint32_t tS = tbase + (uint32_t)((t & 1) * 128) + lane_off;
+        float x[128];
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32(tS + c0, reinterpret_cast<uint32_t*>(x + c0));
+        tmem_ld_wait();
+        float mt = kNegInf;
+#pragma unroll
+        for (int c = 0; c < 128; ++c) {
+          bool on = (mw[c >> 5] >> (c & 31)) & 1u;
+          if (diag >= 0 && c >= diag && c < diag + 64 && (c - diag) > rr) on = false;
+          x[c] = on ? x[c] * P.scale_log2 : kNegInf;
+          mt = fmaxf(mt, x[c]);
+        }
+        const float m_new = fmaxf(m_ref, mt);
+        // Rows whose maximum grew by more than the threshold rescale their
+        // running O after the previous PV landed.  The TMEM loads/stores are
+        // warp-collective, so the whole warp takes the branch when any row
+        // needs it (factor 1 for the others).
+        const bool need = m_ref != kNegInf && m_new > m_ref + kRescaleThreshold;
+        if (__any_sync(0xffffffffu, need)) {
+          if (!wait_warp(pv_done, (t - 1) & 1, 22)) break;
+          tc_fence_after();
+          const float f = need ? fast_exp2(m_ref - m_new) : 1.0f;
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t o[16];
+            tmem_ld16(tO + c0, o);
+            tmem_ld_wait();
+            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+            tmem_st16(tO + c0, o);
+          }
+          tmem_st_wait();
+          if (need) {
+            l *= f;
+            m_ref = m_new;
+          }
+        }
+        if (m_ref == kNegInf) m_ref = m_new;
+        // P = exp2(x - m_ref) as packed bf16 into the first 64 columns of the S buffer
+        const float mref_use = (m_ref == kNegInf) ? 0.f : m_ref;  // all x are -inf then
+#pragma unroll
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const float p0 = fast_exp2(x[c0 + 2 * k] - mref_use);
+            const float p1 = fast_exp2(x[c0 + 2 * k + 1] - mref_use);
+            l += p0 + p1;
+            pk[k] = pack_bf16(p0, p1);
+          }
+          tmem_st16(tS + c0 / 2, pk);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&p_ready[t & 1]);
+        if (last) {
+          if (!wait_warp(pv_done, t & 1, 23)) break;
+          tc_fence_after();
+          const bool valid = it.valid[seg];
+          const float inv = (l > 0.f) ? 1.0f / l : 0.f;
+          const int tok = it.I[seg] * kBlock + rr;
+          const int h = it.h[seg];
+          __nv_bfloat16* orow = P.O + ((size_t)tok * g.Hq + h) * D;
+          for (int c0 = 0; c0 < D; c0 += 16) {
+            uint32_t o[16];
+            tmem_ld16(tO + c0, o);
+            tmem_ld_wait();
+            uint32_t pk[8];
+            for (int k = 0; k < 8; ++k)
+              pk[k] = pack_bf16(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
+            if (valid) {
+              uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+          }
+          if (valid) P.lse[(size_t)h * g.L + tok] = (l > 0.f) ? (m_ref + __log2f(l)) * 0.69314718055994531f : kNegInf;
+          tc_fence_before();
+          mbar_arrive(o_free);
+        }
+        ++t;
+      } while (!last && !*abort_flag);
+    }
+  }
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 2) tmem_dealloc(tbase, 512);
+}
+
+}  // namespace
+
+size_t attn_fwd_ws_bytes(const vs_params& p) {
+  const AttnGeom g = make_geom(p);
+  WsLayout w;
+  w.take(sizeof(DevStatus));
+  prep_layout(g, w);
+  return w.off;
+}
+
+template <int D>
+static cudaError_t launch_fwd_d(const AttnGeom& g, const vs_params& p, const vs_index& ix, const void* Q,
+                                const void* K, const void* V, void* O, float* lse, void* ws, cudaStream_t s) {
+  using Ly = Layout<D>;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  WsLayout lay;
+  const size_t st_off = lay.take(sizeof(DevStatus));
+  const PrepWs pw = prep_layout(g, lay);
+  PrepPtrs pp;
+  pp.inS = reinterpret_cast<uint32_t*>(w + pw.inS);
+  pp.vlist = reinterpret_cast<uint32_t*>(w + pw.vlist);
+  pp.vcnt = reinterpret_cast<int32_t*>(w + pw.vcnt);
+  pp.Kp = reinterpret_cast<__nv_bfloat16*>(w + pw.Kp);
+  pp.Vp = reinterpret_cast<__nv_bfloat16*>(w + pw.Vp);
+  cudaError_t e = launch_attn_prep(g, ix, K, V, pp, s);
+  if (e != cudaSuccess) return e;
+  CUtensorMap mQ, mK, mV, mKp, mVp;
+  if (!make_map_heads(&mQ, Q, g.L, g.Hq, D) || !make_map_heads(&mK, K, g.L, g.Hkv, D) ||
+      !make_map_heads(&mV, V, g.L, g.Hkv, D) || !make_map_rows(&mKp, pp.Kp, (long long)g.nvg * g.L, D) ||
+      !make_map_rows(&mVp, pp.Vp, (long long)g.nvg * g.L, D))
+    return cudaErrorInvalidValue;
+  FwdParams P;
+  P.g = g;
+  P.inS = pp.inS;
+  P.vlist = pp.vlist;
+  P.vcnt = pp.vcnt;
+  P.O = static_cast<__nv_bfloat16*>(O);
+  P.lse = lse;
+  P.scale_log2 = default_scale(p) * 1.4426950408889634f;
+  P.status = reinterpret_cast<DevStatus*>(w + st_off);
+  const size_t smem = Ly::kBitmaps + 2 * g.nw * 4 + 1024;
+  e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, nsm = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = g.nitems < nsm ? g.nitems : nsm;
+  attn_fwd_kernel<D><<<grid, kThreads, smem, s>>>(mQ, mK, mV, mKp, mVp, P);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_fwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
+                            void* O, float* lse, void* ws, cudaStream_t s) {
+  const AttnGeom g = make_geom(p);
+  if (p.d == 128) return launch_fwd_d<128>(g, p, ix, Q, K, V, O, lse, ws, s);
+  return launch_fwd_d<64>(g, p, ix, Q, K, V, O, lse, ws, s);
+}
+
+}  // namespace vs
+
+namespace vs {
+cudaError_t launch_attn_dq(const vs_params&, const AttnGeom&, const PrepPtrs&, const void*, const void*, const void*,
+                           const void*, const float*, const float*, void*, DevStatus*, cudaStream_t) {
+  return cudaErrorNotSupported;
+}
+}  // namespace vs

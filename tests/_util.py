@@ -52,3 +52,27 @@ def topp_sets_agree(x_or, sel_or, sel_gpu, p, tol=1e-6, forced=()):
         if not (near_thr or near_p):
             bad.append((e, xn[e], thr))
     return not bad, bad
+
+
+def inject_index(vs, p, index, dev):
+    """Device IndexBuffers holding a given per-head (V_h, S_h) index."""
+    import torch
+    ix = vs.IndexBuffers.allocate(p, dev, scores=False)
+    nbs = p.L // (p.block * p.stripes)
+    vi = np.zeros((p.Hq, p.L), np.int32)
+    si = np.zeros((p.Hq, nbs), np.int32)
+    vc = np.zeros(p.Hq, np.int32)
+    sc = np.zeros(p.Hq, np.int32)
+    for h, (Vh, Sh) in enumerate(index):
+        vi[h, :len(Vh)] = Vh
+        si[h, :len(Sh)] = Sh
+        vc[h], sc[h] = len(Vh), len(Sh)
+    ix.v_idx.copy_(torch.from_numpy(vi))
+    ix.s_idx.copy_(torch.from_numpy(si))
+    ix.v_cnt.copy_(torch.from_numpy(vc))
+    ix.s_cnt.copy_(torch.from_numpy(sc))
+    return ix
+
+
+def rel_l2(a, b):
+    return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
