@@ -1,0 +1,368 @@
+"""Benchmark: one training step of the vertical-slash sparse attention hot path.
+
+Workload (default): the 128K GQA training shape, 16 query / 2 key-value heads,
+d = 128, L = 131072, batch 1, bf16, synthetic seeded inputs (N(0,1) queries,
+keys and values with 0.1 % outlier keys at 6x norm, dO ~ N(0,1)).
+
+One step = every stage of the path on one batch:
+  RoPE(Q), RoPE(K) -> sparse index (last 64 queries, budget fill to the
+  pages' 95 % sparsity operating point) -> sparse attention forward ->
+  backward (D, dK/dV, dQ) -> RoPE adjoint on dQ, dK.
+Metric: effective TFLOP/s of sparse attention fwd+bwd = 14 d A / step time,
+A = exact active (query, key) entries (fwd 4 d A + bwd 10 d A), with the
+index and RoPE time inside the step.
+
+Usage: python bench.py [--gpus N --steps K --warmup W] [--impl reference]
+For N > 1 (torchrun, one rank per GPU) every rank runs an independent
+replica of the step (the path has no cross-GPU exchange): value sums the
+ranks' FLOPs over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+WORKLOADS = {
+    # name -> (recipe id, overrides)
+    "gqa16x2_L131072_d128_fwdbwd": (3, {}),
+    "gqa16x2_L16384_d128_fwdbwd": (3, {"L": 16384}),   # small case for profiling
+}
+DENSITY = 0.05     # budget fill: 95 % sparsity (fixed in the pages' experiments)
+LAST_Q, TOP_P = 64, 0.95
+KERNELS_PER_STEP = {"rope": 4, "index": 5, "fwd": 4, "bwd": 8}
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return {"bf16_tflops": m["bf16_tflops"], "bf16_tflops_sustained": m["bf16_tflops_sustained"],
+                "hbm_gbs": m["hbm_gbs"], "src": "measured"}
+    except Exception:
+        return {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0, "src": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    if ws > 1:
+        import torch.distributed as dist
+        rank = int(os.environ["RANK"])
+        local = int(os.environ.get("LOCAL_RANK", rank))
+        dist.init_process_group("nccl")
+        return dist, rank, local, ws
+    return None, 0, 0, 1
+
+
+def run_gpu(args):
+    import torch
+
+    import dynamic_sparse_attention_index_gb300 as vs
+    from dynamic_sparse_attention_index_gb300 import build as vsbuild
+
+    dist, rank, local, world = _dist()
+    vsbuild.build()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wid, ov = WORKLOADS[args.workload]
+    w = synth.make_workload(wid, **ov)
+    L, Hq, Hkv, d = w.L, w.Hq, w.Hkv, w.d
+    p = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=DENSITY, rope_theta=w.rope_theta)
+    p_nat = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=0.0, rope_theta=w.rope_theta)
+
+    def pinned(bits):
+        t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
+        return t.pin_memory()
+
+    hQ, hK, hV, hdO = pinned(w.q), pinned(w.k), pinned(w.v), pinned(w.do)
+    Qr, Kr, V, dO = (t.to(dev) for t in (hQ, hK, hV, hdO))
+    Q, K = torch.empty_like(Qr), torch.empty_like(Kr)
+    O = torch.empty_like(Q)
+    lse = torch.empty((Hq, L), dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    ix = vs.IndexBuffers.allocate(p, dev)
+    ws_i = vs.workspace(p, vs.VS_OP_INDEX, dev)
+    ws_f = vs.workspace(p, vs.VS_OP_FWD, dev)
+    ws_b = vs.workspace(p, vs.VS_OP_BWD, dev)
+    hdQ = torch.empty(dQ.shape, dtype=dQ.dtype).pin_memory()
+    hdK = torch.empty(dK.shape, dtype=dK.dtype).pin_memory()
+    hdV = torch.empty(dV.shape, dtype=dV.dtype).pin_memory()
+    stream = torch.cuda.current_stream()
+    ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for k in ("rope", "index", "fwd", "bwd")}
+
+    def step(timed=False):
+        def rec(k, i):
+            if timed:
+                ev[k][i].record(stream)
+        rec("rope", 0)
+        vs.vs_rope(p, Hq, Qr, Q, False)
+        vs.vs_rope(p, Hkv, Kr, K, False)
+        rec("rope", 1)
+        rec("index", 0)
+        vs.vs_index_build(p, Q, K, ix, ws_i)
+        rec("index", 1)
+        rec("fwd", 0)
+        vs.vs_sparse_attn_fwd(p, ix, Q, K, V, O, lse, ws_f)
+        rec("fwd", 1)
+        rec("bwd", 0)
+        vs.vs_sparse_attn_bwd(p, ix, Q, K, V, O, lse, dO, dQ, dK, dV, ws_b)
+        rec("bwd", 1)
+        vs.vs_rope(p, Hq, dQ, dQ, True)
+        vs.vs_rope(p, Hkv, dK, dK, True)
+
+    # natural top-p sparsity (reported; not the timed operating point)
+    vs.vs_rope(p, Hq, Qr, Q, False)
+    vs.vs_rope(p, Hkv, Kr, K, False)
+    ix_nat = vs.IndexBuffers.allocate(p_nat, dev)
+    vs.vs_index_build(p_nat, Q, K, ix_nat, vs.workspace(p_nat, vs.VS_OP_INDEX, dev))
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    T = L * (L + 1) // 2
+    A = int(ix.active_entries.sum().item())
+    A_nat = int(ix_nat.active_entries.sum().item())
+    del ix_nat
+    assert vs.vs_device_status(ws_f) == vs.VS_OK and vs.vs_device_status(ws_b) == vs.VS_OK
+
+    sampler = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    phase = {k: 0.0 for k in ev}
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(timed=True)
+        # per-phase times are read after the loop; keep the last step's
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    for k in ev:
+        phase[k] = ev[k][0].elapsed_time(ev[k][1])
+    # per-phase averages over K extra steps (events on every step)
+    acc = {k: 0.0 for k in ev}
+    for _ in range(args.steps):
+        step(timed=True)
+        torch.cuda.synchronize()
+        for k in ev:
+            acc[k] += ev[k][0].elapsed_time(ev[k][1])
+    phase = {k: v / args.steps for k, v in acc.items()}
+    clocks = sampler.stop()
+
+    # end to end through the C ABI with host buffers: H2D of the step's
+    # inputs, the step, D2H of its results (dQ, dK, dV)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(args.steps):
+        Qr.copy_(hQ, non_blocking=True)
+        Kr.copy_(hK, non_blocking=True)
+        V.copy_(hV, non_blocking=True)
+        dO.copy_(hdO, non_blocking=True)
+        step()
+        hdQ.copy_(dQ, non_blocking=True)
+        hdK.copy_(dK, non_blocking=True)
+        hdV.copy_(dV, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / args.steps
+    h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hV, hdO))
+    d2h = sum(t.numel() * t.element_size() for t in (hdQ, hdK, hdV))
+
+    flops = 14.0 * d * A
+    ms_t = torch.tensor([ms, e2e_ms], device=dev)
+    if dist:
+        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
+    ms, e2e_ms = ms_t.tolist()
+    value = world * flops / (ms * 1e-3) / 1e12
+    e2e_val = world * flops / (e2e_ms * 1e-3) / 1e12
+    pk = _peaks()
+    # dominant kernel group: the backward call (dK/dV + dQ kernels), 10 d A per launch
+    bwd_tf = 10.0 * d * A / (phase["bwd"] * 1e-3) / 1e12
+    fwd_tf = 4.0 * d * A / (phase["fwd"] * 1e-3) / 1e12
+    peak = pk["bf16_tflops_sustained"]
+    out = {
+        "metric": "VS sparse attn fwd+bwd ms and effective TFLOP/s at 128K (% bf16 peak)",
+        "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "L": L, "Hq": Hq, "Hkv": Hkv, "d": d, "batch": 1,
+                   "last_q": LAST_Q, "index": f"budget fill to density {DENSITY}",
+                   "sparsity": round(1 - A / (Hq * T), 5),
+                   "natural_top_p_sparsity": round(1 - A_nat / (Hq * T), 5), "top_p": TOP_P,
+                   "active_entries": A, "l2": "inputs larger than L2 (no flush)",
+                   "parallelism": f"replicas x{world}"},
+        "breakdown_ms": {k: round(v, 4) for k, v in phase.items()},
+        "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
+        "index_overhead": round(phase["index"] / max(ms, 1e-9), 4),
+        "roofline": {"kernel": "vs_sparse_attn_bwd (dK/dV + dQ)", "bound": "tensor",
+                     "achieved": round(bwd_tf, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(bwd_tf / peak, 4), "traffic": None,
+                     "peak_src": pk["src"] + " bf16 sustained"},
+        "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": sum(KERNELS_PER_STEP.values()) * args.steps,
+        "clocks": clocks,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(w, index_lists(ix, Hq), d, args.cpu_rows)
+    if dist:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(out))
+
+
+def index_lists(ix, Hq):
+    vc, sc = ix.v_cnt.cpu().numpy(), ix.s_cnt.cpu().numpy()
+    vi, si = ix.v_idx.cpu().numpy(), ix.s_idx.cpu().numpy()
+    return [(vi[h, :vc[h]].astype(np.int64), si[h, :sc[h]].astype(np.int64)) for h in range(Hq)]
+
+
+def cpu_baseline(w, index, d, nrows):
+    """The fp64 oracle, as it stands, on a bounded sample of the step: the
+    forward and dQ of `nrows` query rows spread over the sequence, every
+    head.  Reported as effective TFLOP/s of the same 14 d (active entries)
+    convention over the sampled rows."""
+    import oracle
+    f = synth.bf16_bits_to_f64
+    Q, K, V, dO = f(w.q), f(w.k), f(w.v), f(w.do)
+    rows = np.linspace(0, w.L - 1, nrows).astype(np.int64)
+    bs = 64
+    act = 0
+    for (Vh, Sh) in index:
+        inS = np.zeros(w.L // bs, bool)
+        inS[Sh] = True
+        isV = np.zeros(w.L, bool)
+        isV[Vh] = True
+        for n in rows:
+            m = np.arange(n + 1)
+            act += int((inS[n // bs - m // bs] | isV[m]).sum())
+    t0 = time.perf_counter()
+    oracle.attention_forward_rows(Q, K, V, index, rows)
+    oracle.attention_backward_dq_rows(Q, K, V, dO, index, rows)
+    dt = time.perf_counter() - t0
+    try:
+        cores = len(os.sched_getaffinity(0))
+    except Exception:
+        cores = os.cpu_count()
+    return {"value": round(14.0 * d * act / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 forward + dQ of {nrows} query rows x {w.Hq} heads ({act} active entries), "
+                      f"{dt:.1f} s"}
+
+
+def run_reference(args):
+    """Reference arm: the fp64 CPU oracle timed on this machine's host cores."""
+    dist, rank, local, world = (None, 0, 0, 1)
+    if int(os.environ.get("WORLD_SIZE", "1")) > 1 and int(os.environ.get("RANK", "0")) != 0:
+        return
+    import oracle
+    wid, ov = WORKLOADS[args.workload]
+    w = synth.make_workload(wid, **ov)
+    f = synth.bf16_bits_to_f64
+    Q, K = f(w.q), f(w.k)
+    index, _, _ = oracle.build_index(Q, K, LAST_Q, TOP_P, density=DENSITY)
+    vals = []
+    base = None
+    for i in range(args.warmup + args.steps):
+        r = cpu_baseline(w, index, w.d, max(4, args.cpu_rows // 8))
+        if i >= args.warmup:
+            vals.append(r["value"])
+            base = r
+    v = float(np.mean(vals))
+    out = {"metric": "VS sparse attn fwd+bwd ms and effective TFLOP/s at 128K (% bf16 peak)",
+           "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+           "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+           "config": {"workload": args.workload, "index": f"budget fill to density {DENSITY}"},
+           "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": base["cores"], "kind": "oracle",
+                            "sample": base["sample"]},
+           "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="gqa16x2_L131072_d128_fwdbwd", choices=sorted(WORKLOADS))
+    ap.add_argument("--cpu-rows", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,24 +1,30 @@
-// Block-sparse causal attention forward on the active VS entries (tcgen05).
+// Query-major block-sparse causal attention on the active VS entries
+// (tcgen05): the forward pass, and the dQ part of the backward pass.
 //
 // MTraining review, section "分布式稀疏索引近似" (each worker computes only the
 // active regions of its sub-matrix derived from the vertical and slash
 // indices) with the online softmax across key blocks of the ring-attention
-// page (section 2.1): for each 128-row tile the kernel walks its active key
-// sources, S = Q K^T on the tensor cores into TMEM, masks, updates the row
-// max / sum, writes P (bf16) back into TMEM and accumulates O += P V with the
-// A operand read from TMEM.
+// page (section 2.1).  For each 128-row tile the kernel walks the tile's
+// active key sources (64-key slash blocks and 64-entry vertical chunks, two
+// per step):
+//   forward:  S = Q K^T into TMEM, mask, online max / sum, P (bf16) written
+//             back into TMEM, O += P V with the A operand read from TMEM;
+//   dQ:       S = Q K^T and dP = dO V^T into TMEM, P = exp(scale S - LSE),
+//             dS = P (dP - D) (bf16) into TMEM, dQ += dS K.
 //
 // Persistent CTAs (one per SM), 8 warps:
 //   warp 0     producer: enumerates the tile's key sources, builds per-column
-//              masks, issues TMA loads of Q (per tile) and K/V (per source)
-//   warp 1     MMA issuer (one thread): S_t = Q K_t^T, then O += P_{t-1} V_{t-1}
+//              masks, issues TMA loads of Q (and dO) per tile and K/V per source
+//   warp 1     MMA issuer (one thread)
 //   warp 2     owns the TMEM allocation
-//   warps 4-7  softmax + epilogue: thread r owns row r (TMEM lane r)
-// TMEM columns: S double buffer [0,128) and [128,256) (P aliases the first
-// 64 columns of its S buffer as packed bf16), O at [256, 256 + d).
-// O is rescaled lazily: only when a row maximum grows by more than 8 (log2
-// units) is the running O multiplied down; otherwise exponentials are taken
-// against the stale maximum, which is exact after the final 1/l.
+//   warps 4-7  softmax / dS + epilogue: thread r owns row r (TMEM lane r)
+// TMEM columns: S double buffer [0,128) and [128,256) (P or dS alias the first
+// 64 columns of their S buffer as packed bf16); forward: O at [256, 256+d);
+// dQ: dP at [256, 384), dQ at [384, 384+d).
+// The forward rescales O lazily: only when a row maximum grows by more than
+// 8 (log2 units) is the running O multiplied down; otherwise exponentials are
+// taken against the stale maximum, which is exact after the final 1/l.
+// tcgen05.ld/st are warp-collective: every branch around them is warp-uniform.
 #include "attn_common.cuh"
 #include "ptx.cuh"
 
@@ -38,30 +44,34 @@ struct TileMeta {
   int32_t qslot;
 };
 
-struct FwdParams {
+struct QmParams {
   AttnGeom g;
   const uint32_t* inS;
   const uint32_t* vlist;
   const int32_t* vcnt;
-  __nv_bfloat16* O;
-  float* lse;
+  __nv_bfloat16* out;  // O (forward) or dQ
+  float* lse;          // forward: written; dQ: read
+  const float* Dsum;   // dQ: rowsum(dO * O)
   float scale_log2;
+  float scale;
   DevStatus* status;
 };
 
-template <int D>
+template <int D, bool kDQ>
 struct Layout {
   static constexpr int kHalves = D / 64;
   static constexpr int kRowBytes = 128 * 128;            // 128 rows x 128 bytes (one 64-wide d half)
-  static constexpr int kQBytes = kHalves * kRowBytes;    // one Q slot
-  static constexpr int kKBytes = kHalves * kRowBytes;    // 128 keys of K
+  static constexpr int kQBytes = kHalves * kRowBytes;    // 128 rows of Q (or dO)
+  static constexpr int kKBytes = kHalves * kRowBytes;    // 128 keys of K (or V)
+  static constexpr int kQSlots = kDQ ? 1 : 2;            // dQ: one slot holding Q then dO
+  static constexpr int kSlotBytes = kDQ ? 2 * kQBytes : kQBytes;
   static constexpr int kQ = 0;
   static constexpr int kStage = 2 * kQBytes;
   static constexpr int kStageBytes = 2 * kKBytes;        // K then V
   static constexpr int kMeta = kStage + kStages * kStageBytes;
   static constexpr int kBars = kMeta + kStages * (int)sizeof(TileMeta);
-  // barriers: q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_ready[2], pv_done, o_free
-  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 1 + 1;
+  // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_ready[2], pv_done, o_free, dp_full, dp_free
+  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 1 + 1 + 1 + 1;
   static constexpr int kMisc = kBars + kNumBars * 8;      // tmem slot, abort flag
   static constexpr int kBitmaps = kMisc + 64;             // producer-private band bitmaps
 };
@@ -74,12 +84,13 @@ __device__ __forceinline__ float fast_exp2(float x) {
 
 __device__ __forceinline__ bool band_kept(const uint32_t* bm, int B) { return (bm[B >> 5] >> (B & 31)) & 1u; }
 
-template <int D>
+template <int D, bool kDQ>
 __global__ void __launch_bounds__(kThreads, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
-                    const __grid_constant__ CUtensorMap mV, const __grid_constant__ CUtensorMap mKp,
-                    const __grid_constant__ CUtensorMap mVp, const FwdParams P) {
-  using Ly = Layout<D>;
+    attn_qmajor_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
+                       const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
+                       const __grid_constant__ CUtensorMap mKp, const __grid_constant__ CUtensorMap mVp,
+                       const QmParams P) {
+  using Ly = Layout<D, kDQ>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::kBars);
@@ -88,13 +99,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* kv_full = bars + 4;
   uint64_t* kv_empty = kv_full + kStages;
   uint64_t* s_full = kv_empty + kStages;
-  uint64_t* p_ready = s_full + 2;
-  uint64_t* pv_done = p_ready + 2;
-  uint64_t* o_free = pv_done + 1;
+  uint64_t* p_ready = s_full + 2;     // P (forward) or dS (dQ) written to TMEM
+  uint64_t* pv_done = p_ready + 2;    // O += P V (forward) or dQ += dS K landed
+  uint64_t* o_free = pv_done + 1;     // epilogue finished reading the accumulator
+  uint64_t* dp_full = o_free + 1;     // dQ: dP landed
+  uint64_t* dp_free = dp_full + 1;    // dQ: dP read by every row
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Ly::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Ly::kMisc + 4);
   TileMeta* metas = reinterpret_cast<TileMeta*>(sm + Ly::kMeta);
   const AttnGeom& g = P.g;
+  constexpr uint32_t kAccCol = kDQ ? 384 : 256;  // O or dQ
+  constexpr uint32_t kDPCol = 256;               // dQ: dP
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
@@ -110,6 +125,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(pv_done, 1);
     mbar_init(o_free, 128);
+    mbar_init(dp_full, 1);
+    mbar_init(dp_free, 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -147,23 +164,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&mV);
       tma_prefetch_desc(&mKp);
       tma_prefetch_desc(&mVp);
+      if (kDQ) tma_prefetch_desc(&mdO);
     }
     for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
       const Item it = decode_item(g, id);
-      const int qslot = it_local & 1;
+      const int qslot = it_local % Ly::kQSlots;
       for (int w = lane; w < g.nw; w += 32) {
         bm0[w] = P.inS[(size_t)it.h[0] * g.nw + w];
         bm1[w] = P.inS[(size_t)it.h[1] * g.nw + w];
       }
       __syncwarp();
       if (lane == 0) {
-        if (wait(&q_empty[qslot], ((it_local >> 1) & 1) ^ 1, 1)) {
-          mbar_arrive_expect_tx(&q_full[qslot], Ly::kQBytes);
-          uint8_t* q = sm + Ly::kQ + qslot * Ly::kQBytes;
+        if (wait(&q_empty[qslot], ((it_local / Ly::kQSlots) & 1) ^ 1, 1)) {
+          mbar_arrive_expect_tx(&q_full[qslot], Ly::kSlotBytes);
+          uint8_t* q = sm + Ly::kQ + qslot * Ly::kSlotBytes;
           for (int s = 0; s < 2; ++s)
-            for (int hf = 0; hf < Ly::kHalves; ++hf)
+            for (int hf = 0; hf < Ly::kHalves; ++hf) {
               tma_load_3d(q + hf * Ly::kRowBytes + s * 8192, &mQ, &q_full[qslot], hf * 64, it.h[s],
                           it.I[s] * kBlock);
+              if (kDQ)
+                tma_load_3d(q + Ly::kQBytes + hf * Ly::kRowBytes + s * 8192, &mdO, &q_full[qslot], hf * 64,
+                            it.h[s], it.I[s] * kBlock);
+            }
         }
       }
       __syncwarp();
@@ -296,22 +318,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdescS64 = idesc_bf16(128, 64, false, false);
       constexpr uint32_t kIdescS128 = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t kIdescPV = idesc_bf16(128, D, false, true);
-      const uint32_t tO = tbase + 256;
+      constexpr uint32_t kIdescAcc = idesc_bf16(128, D, false, true);  // B (V or K) MN-major
+      const uint32_t tAcc = tbase + kAccCol;
       int t = 0, it_local = 0;
       bool have_prev = false;
       int prev_t = 0, prev_nsrc = 0, prev_first = 0, prev_item = 0;
-      auto issue_pv = [&]() -> bool {
+      // O += P V (forward) or dQ += dS K (dQ) for the previous tile
+      auto issue_acc = [&]() -> bool {
         if (!wait(&p_ready[prev_t & 1], (prev_t >> 1) & 1, 10)) return false;
         if (prev_first && prev_item > 0)
           if (!wait(o_free, (prev_item - 1) & 1, 11)) return false;
         tc_fence_after();
         const int st = prev_t % kStages;
-        const uint32_t vst = smem_u32(sm + Ly::kStage + st * Ly::kStageBytes + Ly::kKBytes);
+        const uint32_t bst = smem_u32(sm + Ly::kStage + st * Ly::kStageBytes + (kDQ ? 0 : Ly::kKBytes));
         const uint32_t pS = tbase + (uint32_t)((prev_t & 1) * 128);
         for (int kk = 0; kk < 4 * prev_nsrc; ++kk) {
-          const uint64_t bd = sdesc_sw128(vst + kk * 2048, Ly::kRowBytes, 1024);
-          umma_ts(tO, pS + kk * 8, bd, kIdescPV, (kk > 0 || !prev_first) ? 1u : 0u);
+          const uint64_t bd = sdesc_sw128(bst + kk * 2048, Ly::kRowBytes, 1024);
+          umma_ts(tAcc, pS + kk * 8, bd, kIdescAcc, (kk > 0 || !prev_first) ? 1u : 0u);
         }
         umma_commit(&kv_empty[st]);
         umma_commit(pv_done);
@@ -325,9 +348,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const TileMeta m = metas[st];
           last = m.last != 0;
           if (m.first)
-            if (!wait(&q_full[m.qslot], (it_local >> 1) & 1, 13)) break;
+            if (!wait(&q_full[m.qslot], (it_local / Ly::kQSlots) & 1, 13)) break;
           tc_fence_after();
-          const uint32_t qa = smem_u32(sm + Ly::kQ + m.qslot * Ly::kQBytes);
+          const uint32_t qa = smem_u32(sm + Ly::kQ + m.qslot * Ly::kSlotBytes);
           const uint32_t kb = smem_u32(sm + Ly::kStage + st * Ly::kStageBytes);
           const uint32_t dS = tbase + (uint32_t)((t & 1) * 128);
           const uint32_t idS = m.nsrc == 2 ? kIdescS128 : kIdescS64;
@@ -336,8 +359,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_ss(dS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
           }
           umma_commit(&s_full[t & 1]);
+          if (kDQ) {
+            // dP = dO V^T into the single dP buffer, once every row read the previous one
+            if (t > 0 && !wait(dp_free, (t - 1) & 1, 14)) break;
+            tc_fence_after();
+            const uint32_t oa = qa + Ly::kQBytes;
+            const uint32_t vb = kb + Ly::kKBytes;
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t off = (kk >> 2) * Ly::kRowBytes + (kk & 3) * 32;
+              umma_ss(tbase + kDPCol, sdesc_sw128(oa + off, 16, 1024), sdesc_sw128(vb + off, 16, 1024), idS,
+                      kk > 0 ? 1u : 0u);
+            }
+            umma_commit(dp_full);
+          }
           if (last) umma_commit(&q_empty[m.qslot]);
-          if (have_prev && !issue_pv()) break;
+          if (have_prev && !issue_acc()) break;
           have_prev = true;
           prev_t = t;
           prev_nsrc = m.nsrc;
@@ -346,21 +382,29 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++t;
         } while (!last && !*abort_flag);
       }
-      if (have_prev && !*abort_flag) issue_pv();
+      if (have_prev && !*abort_flag) issue_acc();
     }
     // lanes 1..31 wait here for the issuing lane: the block-wide barrier
     // below is warp-aligned and must see the whole warp together
     __syncwarp();
   } else if (warp >= 4) {
-    // ------------------------------------------------------------ softmax + epilogue
+    // ------------------------------------------------------------ softmax / dS + epilogue
     const int r = threadIdx.x - 128;  // row of the tile == TMEM lane
     const int seg = r >> 6, rr = r & 63;
     const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-    const uint32_t tO = tbase + 256 + lane_off;
+    const uint32_t tAcc = tbase + kAccCol + lane_off;
     int t = 0, it_local = 0;
     for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
       const Item it = decode_item(g, id);
+      const int tok = it.I[seg] * kBlock + rr;
+      const int h = it.h[seg];
+      const bool valid = it.valid[seg];
       float m_ref = kNegInf, l = 0.f;
+      float lse2 = 0.f, Dr = 0.f;
+      if (kDQ && valid) {
+        lse2 = P.lse[(size_t)h * g.L + tok] * 1.4426950408889634f;
+        Dr = P.Dsum[(size_t)h * g.L + tok];
+      }
       bool last = false;
       do {
         const int st = t % kStages;
@@ -372,55 +416,85 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_warp(&s_full[t & 1], (t >> 1) & 1, 21)) break;
         tc_fence_after();
         const uint32_t tS = tbase + (uint32_t)((t & 1) * 128) + lane_off;
-        float x[128];
-#pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32(tS + c0, reinterpret_cast<uint32_t*>(x + c0));
-        tmem_ld_wait();
-        float mt = kNegInf;
-#pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          bool on = (mw[c >> 5] >> (c & 31)) & 1u;
-          if (diag >= 0 && c >= diag && c < diag + 64 && (c - diag) > rr) on = false;
-          x[c] = on ? x[c] * P.scale_log2 : kNegInf;
-          mt = fmaxf(mt, x[c]);
-        }
-        const float m_new = fmaxf(m_ref, mt);
-        // Rows whose maximum grew by more than the threshold rescale their
-        // running O after the previous PV landed.  The TMEM loads/stores are
-        // warp-collective, so the whole warp takes the branch when any row
-        // needs it (factor 1 for the others).
-        const bool need = m_ref != kNegInf && m_new > m_ref + kRescaleThreshold;
-        if (__any_sync(0xffffffffu, need)) {
-          if (!wait_warp(pv_done, (t - 1) & 1, 22)) break;
+        if (kDQ) {
+          // ---- dS = P (dP - D), P = exp2(scale_log2 S - lse2) on active entries
+          if (!wait_warp(dp_full, t & 1, 24)) break;
           tc_fence_after();
-          const float f = need ? fast_exp2(m_ref - m_new) : 1.0f;
-          for (int c0 = 0; c0 < D; c0 += 16) {
-            uint32_t o[16];
-            tmem_ld16(tO + c0, o);
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t sv[32], dv[32];
+            tmem_ld32(tS + c0, sv);
+            tmem_ld32(tbase + kDPCol + lane_off + c0, dv);
             tmem_ld_wait();
-            for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-            tmem_st16(tO + c0, o);
-          }
-          tmem_st_wait();
-          if (need) {
-            l *= f;
-            m_ref = m_new;
-          }
-        }
-        if (m_ref == kNegInf) m_ref = m_new;
-        // P = exp2(x - m_ref) as packed bf16 into the first 64 columns of the S buffer
-        const float mref_use = (m_ref == kNegInf) ? 0.f : m_ref;  // all x are -inf then
+            uint32_t pk[16];
 #pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) {
-          uint32_t pk[16];
+            for (int k = 0; k < 16; ++k) {
+              float ds[2];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            const float p0 = fast_exp2(x[c0 + 2 * k] - mref_use);
-            const float p1 = fast_exp2(x[c0 + 2 * k + 1] - mref_use);
-            l += p0 + p1;
-            pk[k] = pack_bf16(p0, p1);
+              for (int e = 0; e < 2; ++e) {
+                const int c = c0 + 2 * k + e;
+                bool on = (mw[c >> 5] >> (c & 31)) & 1u;
+                if (diag >= 0 && c >= diag && c < diag + 64 && (c - diag) > rr) on = false;
+                const float p = on ? fast_exp2(__uint_as_float(sv[2 * k + e]) * P.scale_log2 - lse2) : 0.f;
+                ds[e] = p * (__uint_as_float(dv[2 * k + e]) - Dr);
+              }
+              pk[k] = pack_bf16(ds[0], ds[1]);
+            }
+            tmem_st16(tS + c0 / 2, pk);
           }
-          tmem_st16(tS + c0 / 2, pk);
+          tc_fence_before();
+          mbar_arrive(dp_free);
+        } else {
+          float x[128];
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32(tS + c0, reinterpret_cast<uint32_t*>(x + c0));
+          tmem_ld_wait();
+          float mt = kNegInf;
+#pragma unroll
+          for (int c = 0; c < 128; ++c) {
+            bool on = (mw[c >> 5] >> (c & 31)) & 1u;
+            if (diag >= 0 && c >= diag && c < diag + 64 && (c - diag) > rr) on = false;
+            x[c] = on ? x[c] * P.scale_log2 : kNegInf;
+            mt = fmaxf(mt, x[c]);
+          }
+          const float m_new = fmaxf(m_ref, mt);
+          // Rows whose maximum grew by more than the threshold rescale their
+          // running O after the previous PV landed.  The TMEM loads/stores are
+          // warp-collective, so the whole warp takes the branch when any row
+          // needs it (factor 1 for the others).
+          const bool need = m_ref != kNegInf && m_new > m_ref + kRescaleThreshold;
+          if (__any_sync(0xffffffffu, need)) {
+            if (!wait_warp(pv_done, (t - 1) & 1, 22)) break;
+            tc_fence_after();
+            const float f = need ? fast_exp2(m_ref - m_new) : 1.0f;
+            for (int c0 = 0; c0 < D; c0 += 16) {
+              uint32_t o[16];
+              tmem_ld16(tAcc + c0, o);
+              tmem_ld_wait();
+              for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+              tmem_st16(tAcc + c0, o);
+            }
+            tmem_st_wait();
+            if (need) {
+              l *= f;
+              m_ref = m_new;
+            }
+          }
+          if (m_ref == kNegInf) m_ref = m_new;
+          // P = exp2(x - m_ref) as packed bf16 into the first 64 columns of the S buffer
+          const float mref_use = (m_ref == kNegInf) ? 0.f : m_ref;  // all x are -inf then
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const float p0 = fast_exp2(x[c0 + 2 * k] - mref_use);
+              const float p1 = fast_exp2(x[c0 + 2 * k + 1] - mref_use);
+              l += p0 + p1;
+              pk[k] = pack_bf16(p0, p1);
+            }
+            tmem_st16(tS + c0 / 2, pk);
+          }
         }
         tmem_st_wait();
         tc_fence_before();
@@ -428,25 +502,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (last) {
           if (!wait_warp(pv_done, t & 1, 23)) break;
           tc_fence_after();
-          const bool valid = it.valid[seg];
-          const float inv = (l > 0.f) ? 1.0f / l : 0.f;
-          const int tok = it.I[seg] * kBlock + rr;
-          const int h = it.h[seg];
-          __nv_bfloat16* orow = P.O + ((size_t)tok * g.Hq + h) * D;
+          const float mult = kDQ ? P.scale : ((l > 0.f) ? 1.0f / l : 0.f);
+          __nv_bfloat16* orow = P.out + ((size_t)tok * g.Hq + h) * D;
           for (int c0 = 0; c0 < D; c0 += 16) {
             uint32_t o[16];
-            tmem_ld16(tO + c0, o);
+            tmem_ld16(tAcc + c0, o);
             tmem_ld_wait();
             uint32_t pk[8];
             for (int k = 0; k < 8; ++k)
-              pk[k] = pack_bf16(__uint_as_float(o[2 * k]) * inv, __uint_as_float(o[2 * k + 1]) * inv);
+              pk[k] = pack_bf16(__uint_as_float(o[2 * k]) * mult, __uint_as_float(o[2 * k + 1]) * mult);
             if (valid) {
               uint4* dst = reinterpret_cast<uint4*>(orow + c0);
               dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
               dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
             }
           }
-          if (valid) P.lse[(size_t)h * g.L + tok] = (l > 0.f) ? (m_ref + __log2f(l)) * 0.69314718055994531f : kNegInf;
+          if (!kDQ && valid)
+            P.lse[(size_t)h * g.L + tok] = (l > 0.f) ? (m_ref + __log2f(l)) * 0.69314718055994531f : kNegInf;
           tc_fence_before();
           mbar_arrive(o_free);
         }
@@ -461,6 +533,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) tmem_dealloc(tbase, 512);
 }
 
+template <int D, bool kDQ>
+cudaError_t launch_qmajor(const AttnGeom& g, const PrepPtrs& pp, const void* Q, const void* dO, const void* K,
+                          const void* V, const QmParams& P, cudaStream_t s) {
+  using Ly = Layout<D, kDQ>;
+  CUtensorMap mQ, mdO, mK, mV, mKp, mVp;
+  if (!make_map_heads(&mQ, Q, g.L, g.Hq, D) || !make_map_heads(&mdO, kDQ ? dO : Q, g.L, g.Hq, D) ||
+      !make_map_heads(&mK, K, g.L, g.Hkv, D) || !make_map_heads(&mV, V, g.L, g.Hkv, D) ||
+      !make_map_rows(&mKp, pp.Kp, (long long)g.nvg * g.L, D) ||
+      !make_map_rows(&mVp, pp.Vp, (long long)g.nvg * g.L, D))
+    return cudaErrorInvalidValue;
+  const size_t smem = Ly::kBitmaps + 2 * g.nw * 4 + 1024;
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_qmajor_kernel<D, kDQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, nsm = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const int grid = g.nitems < nsm ? g.nitems : nsm;
+  attn_qmajor_kernel<D, kDQ><<<grid, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, P);
+  return cudaGetLastError();
+}
+
 }  // namespace
 
 size_t attn_fwd_ws_bytes(const vs_params& p) {
@@ -471,10 +565,9 @@ size_t attn_fwd_ws_bytes(const vs_params& p) {
   return w.off;
 }
 
-template <int D>
-static cudaError_t launch_fwd_d(const AttnGeom& g, const vs_params& p, const vs_index& ix, const void* Q,
-                                const void* K, const void* V, void* O, float* lse, void* ws, cudaStream_t s) {
-  using Ly = Layout<D>;
+cudaError_t launch_attn_fwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
+                            void* O, float* lse, void* ws, cudaStream_t s) {
+  const AttnGeom g = make_geom(p);
   uint8_t* w = static_cast<uint8_t*>(ws);
   WsLayout lay;
   const size_t st_off = lay.take(sizeof(DevStatus));
@@ -487,43 +580,37 @@ static cudaError_t launch_fwd_d(const AttnGeom& g, const vs_params& p, const vs_
   pp.Vp = reinterpret_cast<__nv_bfloat16*>(w + pw.Vp);
   cudaError_t e = launch_attn_prep(g, ix, K, V, pp, s);
   if (e != cudaSuccess) return e;
-  CUtensorMap mQ, mK, mV, mKp, mVp;
-  if (!make_map_heads(&mQ, Q, g.L, g.Hq, D) || !make_map_heads(&mK, K, g.L, g.Hkv, D) ||
-      !make_map_heads(&mV, V, g.L, g.Hkv, D) || !make_map_rows(&mKp, pp.Kp, (long long)g.nvg * g.L, D) ||
-      !make_map_rows(&mVp, pp.Vp, (long long)g.nvg * g.L, D))
-    return cudaErrorInvalidValue;
-  FwdParams P;
+  QmParams P;
   P.g = g;
   P.inS = pp.inS;
   P.vlist = pp.vlist;
   P.vcnt = pp.vcnt;
-  P.O = static_cast<__nv_bfloat16*>(O);
+  P.out = static_cast<__nv_bfloat16*>(O);
   P.lse = lse;
-  P.scale_log2 = default_scale(p) * 1.4426950408889634f;
+  P.Dsum = nullptr;
+  P.scale = default_scale(p);
+  P.scale_log2 = P.scale * 1.4426950408889634f;
   P.status = reinterpret_cast<DevStatus*>(w + st_off);
-  const size_t smem = Ly::kBitmaps + 2 * g.nw * 4 + 1024;
-  e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
-  int dev = 0, nsm = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = g.nitems < nsm ? g.nitems : nsm;
-  attn_fwd_kernel<D><<<grid, kThreads, smem, s>>>(mQ, mK, mV, mKp, mVp, P);
-  return cudaGetLastError();
+  if (p.d == 128) return launch_qmajor<128, false>(g, pp, Q, nullptr, K, V, P, s);
+  return launch_qmajor<64, false>(g, pp, Q, nullptr, K, V, P, s);
 }
 
-cudaError_t launch_attn_fwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
-                            void* O, float* lse, void* ws, cudaStream_t s) {
-  const AttnGeom g = make_geom(p);
-  if (p.d == 128) return launch_fwd_d<128>(g, p, ix, Q, K, V, O, lse, ws, s);
-  return launch_fwd_d<64>(g, p, ix, Q, K, V, O, lse, ws, s);
+cudaError_t launch_attn_dq(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const void* Q, const void* K,
+                           const void* V, const void* dO, const float* lse, const float* Dsum, void* dQ,
+                           DevStatus* st, cudaStream_t s) {
+  QmParams P;
+  P.g = g;
+  P.inS = pp.inS;
+  P.vlist = pp.vlist;
+  P.vcnt = pp.vcnt;
+  P.out = static_cast<__nv_bfloat16*>(dQ);
+  P.lse = const_cast<float*>(lse);
+  P.Dsum = Dsum;
+  P.scale = default_scale(p);
+  P.scale_log2 = P.scale * 1.4426950408889634f;
+  P.status = st;
+  if (p.d == 128) return launch_qmajor<128, true>(g, pp, Q, dO, K, V, P, s);
+  return launch_qmajor<64, true>(g, pp, Q, dO, K, V, P, s);
 }
 
-}  // namespace vs
-
-namespace vs {
-cudaError_t launch_attn_dq(const vs_params&, const AttnGeom&, const PrepPtrs&, const void*, const void*, const void*,
-                           const void*, const float*, const float*, void*, DevStatus*, cudaStream_t) {
-  return cudaErrorNotSupported;
-}
 }  // namespace vs

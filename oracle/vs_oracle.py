@@ -47,7 +47,7 @@ __all__ = [
     "bf16_round", "rope_inv_freq", "rope_mscale", "rope", "index_scores",
     "select_top_p", "select_budget", "build_index", "active_entries",
     "sparsity_ratio", "explicit_mask", "attention_forward", "attention_backward",
-    "attention_forward_rows", "total_causal_entries",
+    "attention_forward_rows", "attention_backward_dq_rows", "total_causal_entries",
 ]
 
 
@@ -359,3 +359,34 @@ def attention_backward(Q, K, V, dO, index, scale=None, stripes=1, block=64):
             dQ[r, h, :] = scale * (dS @ kh)
             dK[:, g, :] += scale * (dS.T @ Q[r, h, :])
     return dQ, dK, dV
+
+
+def attention_backward_dq_rows(Q, K, V, dO, index, rows, scale=None, stripes=1, block=64):
+    """dQ of the listed query rows only (same definitions as
+    ``attention_backward``): per row n, P_n = masked softmax,
+    dP_n = dO_n V^T, dS_n = P_n * (dP_n - P_n . dP_n), dQ_n = scale dS_n K."""
+    Q = np.asarray(Q, np.float64)
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    dO = np.asarray(dO, np.float64)
+    L, Hq, d = Q.shape
+    G = Hq // K.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    bs = block * stripes
+    rows = np.asarray(rows, np.int64)
+    dQ = np.zeros((rows.size, Hq, d))
+    for h in range(Hq):
+        Vh, Sh = index[h]
+        kh, vh = K[:, h // G, :], V[:, h // G, :]
+        off = 0
+        for r in _chunks(L, rows):
+            msk = _row_mask(r, L, Vh, Sh, bs)
+            s = np.where(msk, scale * (Q[r, h, :] @ kh.T), -np.inf)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            p /= p.sum(axis=1, keepdims=True)
+            dP = dO[r, h, :] @ vh.T
+            dS = p * (dP - (p * dP).sum(axis=1, keepdims=True))
+            dQ[off:off + r.size, h, :] = scale * (dS @ kh)
+            off += r.size
+    return dQ

@@ -126,3 +126,29 @@ def test_rows_subset_matches_full():
     Or, LSEr = attention_forward_rows(Q, K, V, index, rows)
     np.testing.assert_allclose(Or, O[rows], atol=1e-14)
     np.testing.assert_allclose(LSEr, LSE[:, rows], atol=1e-14)
+
+
+def test_dq_rows_matches_full_backward():
+    from oracle import attention_backward_dq_rows
+    L, Hq, Hkv, d = 256, 4, 2, 8
+    Q, K, V, dO = _inputs(L, Hq, Hkv, d, 31)
+    rng = np.random.default_rng(4)
+    index = [(np.sort(rng.choice(L, 7, replace=False)), np.union1d(rng.choice(4, 2, replace=False), [0]))
+             for _ in range(Hq)]
+    dQ, _, _ = attention_backward(Q, K, V, dO, index)
+    rows = np.array([0, 5, 64, 200, 255])
+    np.testing.assert_allclose(attention_backward_dq_rows(Q, K, V, dO, index, rows), dQ[rows], atol=1e-13)
+
+
+def test_gradient_column_identities():
+    """Identities used for full-size checks: summed over keys, dV equals the
+    sum of dO over the rows of the group's heads (softmax rows sum to 1), and
+    dK sums to zero (each row of dS sums to zero)."""
+    L, Hq, Hkv, d = 128, 4, 2, 8
+    Q, K, V, dO = _inputs(L, Hq, Hkv, d, 32)
+    rng = np.random.default_rng(5)
+    index = [(np.sort(rng.choice(L, 5, replace=False)), np.array([0, 1])) for _ in range(Hq)]
+    _, dK, dV = attention_backward(Q, K, V, dO, index)
+    for g in range(Hkv):
+        np.testing.assert_allclose(dV[:, g].sum(0), dO[:, g * 2:(g + 1) * 2].sum((0, 1)), atol=1e-10)
+        np.testing.assert_allclose(dK[:, g].sum(0), 0.0, atol=1e-10)
