@@ -37,7 +37,7 @@ import synth  # noqa: E402
 WORKLOADS = {
     # name -> (recipe id, overrides)
     "gqa16x2_L131072_d128_fwdbwd": (3, {}),
-    "gqa16x2_L16384_d128_fwdbwd": (3, {"L": 16384}),   # small case for profiling
+    "gqa16x2_L32768_d128_fwdbwd": (3, {"L": 32768}),   # small case for profiling
 }
 DENSITY = 0.05     # budget fill: 95 % sparsity (fixed in the pages' experiments)
 LAST_Q, TOP_P = 64, 0.95

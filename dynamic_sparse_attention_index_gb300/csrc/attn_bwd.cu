@@ -105,7 +105,8 @@ constexpr int kBars = kMeta + kStages * (int)sizeof(SrcMeta);
 // kvs_full, kvs_empty, st_full[S], st_empty[S], sdp_full[2], pds_ready[2], pds_free[2], acc_done, acc_free
 constexpr int kNumBars = 2 + 2 * kStages + 6 + 2;
 constexpr int kMisc = kBars + kNumBars * 8;
-constexpr int kSmemBytes = kMisc + 64;
+constexpr int kWaitCyc = kMisc + 64;
+constexpr int kSmemBytes = kWaitCyc + kWaitSites * 8;
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -113,6 +114,27 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 __device__ __forceinline__ bool band_kept(const uint32_t* bm, int B) { return (bm[B >> 5] >> (B & 31)) & 1u; }
+
+// Masking mode of one 64-key block for one source's rows (warp-uniform):
+// inactive, fully active, the causal diagonal block, or per-column bits.
+enum : int { kSrcOff = 0, kSrcFull = 1, kSrcDiag = 2, kSrcBits = 3 };
+__device__ __forceinline__ int src_mode(uint32_t w0, uint32_t w1, bool is_diag) {
+  if ((w0 | w1) == 0u) return kSrcOff;
+  if (is_diag) return kSrcDiag;
+  if ((w0 & w1) == 0xffffffffu) return kSrcFull;
+  return kSrcBits;
+}
+__device__ __forceinline__ void mask_source(float* x, int mode, uint32_t w0, uint32_t w1, int rr) {
+  if (mode == kSrcDiag) {
+#pragma unroll
+    for (int c = 0; c < 64; ++c)
+      if (c > rr) x[c] = -__builtin_huge_valf();
+  } else if (mode == kSrcBits) {
+#pragma unroll
+    for (int c = 0; c < 64; ++c)
+      if (!(((c < 32 ? w0 : w1) >> (c & 31)) & 1u)) x[c] = -__builtin_huge_valf();
+  }
+}
 
 // number of row splits of a vertical group and the stride of its partial slots
 __device__ __forceinline__ void vsplit(const AttnGeom& g, int cnt, int* R, int* stride) {
@@ -170,6 +192,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc + 4);
   SrcMeta* metas = reinterpret_cast<SrcMeta*>(sm + kMeta);
+  unsigned long long* wcyc = reinterpret_cast<unsigned long long*>(sm + kWaitCyc);
+  const long long kernel_t0 = clock64();
   const AttnGeom& g = P.g;
   const int W = g.bs / kBlock;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -191,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (threadIdx.x < kWaitSites) wcyc[threadIdx.x] = 0;
   if (warp == 2) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
@@ -202,7 +227,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // TMEM: S[2] at 0, 64; dP[2] at 128, 192; dV^T at 256; dK^T at 320 (64 columns each)
   auto wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
     if (*abort_flag) return false;
-    if (mbar_wait(bar, parity, kWaitLimitNs)) return true;
+    const long long w0 = clock64();
+    const bool ok = mbar_wait(bar, parity, kWaitLimitNs);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&wcyc[where & (kWaitSites - 1)], (unsigned long long)(clock64() - w0));
+    if (ok) return true;
     *abort_flag = 1;
     report_timeout(P.status, where);
     return false;
@@ -505,38 +533,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c = P.scale * P.log2e;
         uint8_t* pbuf = sm + kPdS + (t & 1) * kPdSBytes;
         uint8_t* dbuf = pbuf + 128 * 128;
+        // warp-uniform masking mode of this row's source for the 64 keys
+        const int mode = src_mode(mw0, mw1, diag != 0);
+        uint32_t pk[32], dk[32];
+        if (mode == kSrcOff) {
 #pragma unroll
-        for (int c0 = 0; c0 < 64; c0 += 32) {
-          uint32_t sv[32], dv[32];
-          tmem_ld32(tbase + (uint32_t)((t & 1) * 64) + lane_off + c0, sv);
-          tmem_ld32(tbase + 128 + (uint32_t)((t & 1) * 64) + lane_off + c0, dv);
+          for (int k = 0; k < 32; ++k) pk[k] = dk[k] = 0u;
+        } else {
+          uint32_t sv[64], dv[64];
+          const uint32_t tb = tbase + (uint32_t)((t & 1) * 64) + lane_off;
+          tmem_ld32(tb, sv);
+          tmem_ld32(tb + 32, sv + 32);
+          tmem_ld32(tb + 128, dv);
+          tmem_ld32(tb + 128 + 32, dv + 32);
           tmem_ld_wait();
-          const uint32_t mw = c0 ? mw1 : mw0;
-          uint32_t pk[16], dk[16];
+          float x[64];
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            float pp[2], dd[2];
+          for (int k = 0; k < 64; ++k) x[k] = __uint_as_float(sv[k]);
+          mask_source(x, mode, mw0, mw1, rr);
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int col = 2 * k + e;
-              bool on = (mw >> col) & 1u;
-              if (diag && (c0 + col) > rr) on = false;
-              const float p = on ? fast_exp2(__uint_as_float(sv[col]) * c - lse2) : 0.f;
-              pp[e] = p;
-              dd[e] = p * (__uint_as_float(dv[col]) - Dr);
-            }
-            pk[k] = pack_bf16(pp[0], pp[1]);
-            dk[k] = pack_bf16(dd[0], dd[1]);
+          for (int k = 0; k < 32; ++k) {
+            const float p0 = fast_exp2(fmaf(x[2 * k], c, -lse2));
+            const float p1 = fast_exp2(fmaf(x[2 * k + 1], c, -lse2));
+            pk[k] = pack_bf16(p0, p1);
+            dk[k] = pack_bf16(p0 * (__uint_as_float(dv[2 * k]) - Dr), p1 * (__uint_as_float(dv[2 * k + 1]) - Dr));
           }
-          // row r of a 128-row x 64-key MN-major SW128 tile: 8 chunks of 16 B
+        }
+        // row r of a 128-row x 64-key MN-major SW128 tile: 8 chunks of 16 B
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int chunk = (c0 / 8) + q;  // 16-byte chunk index within the 128-byte row
-            const int phys = chunk ^ (r & 7);
-            const int off = (r >> 3) * 1024 + (r & 7) * 128 + phys * 16;
-            *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-            *reinterpret_cast<uint4*>(dbuf + off) = make_uint4(dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
-          }
+        for (int q = 0; q < 8; ++q) {
+          const int off = (r >> 3) * 1024 + (r & 7) * 128 + ((q ^ (r & 7)) * 16);
+          *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+          *reinterpret_cast<uint4*>(dbuf + off) = make_uint4(dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -557,12 +585,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (P.vertical) {
             VUnit u;
             decode_vunit(g, P.vcnt, uid, &u);
+#pragma unroll
             for (int j = 0; j < 64; ++j) {
               const int e = u.chunk * 64 + j;
-              if (e >= u.cnt) break;
-              const size_t o = ((size_t)u.vg * g.L + (size_t)u.split * u.stride + e) * D + dcol;
-              P.part_v[o] = __uint_as_float(av[j]);
-              P.part_k[o] = __uint_as_float(ak[j]);
+              if (e < u.cnt) {
+                const size_t o = ((size_t)u.vg * g.L + (size_t)u.split * u.stride + e) * D + dcol;
+                P.part_v[o] = __uint_as_float(av[j]);
+                P.part_k[o] = __uint_as_float(ak[j]);
+              }
             }
           } else {
             const int kvh = uid / g.nb, kb = uid % g.nb;
@@ -582,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   sk += P.part_k[o];
                   sv += P.part_v[o];
                 }
-#pragma unroll 1
+#pragma unroll
                 for (int jj = 0; jj < 64; ++jj)
                   if (jj == j) {
                     ak[jj] = __float_as_uint(__uint_as_float(ak[jj]) + sk);
@@ -590,6 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   }
               }
             }
+#pragma unroll
             for (int j = 0; j < 64; ++j) {
               const size_t o = ((size_t)(kb * kBlock + j) * g.Hkv + kvh) * D + dcol;
               P.dV[o] = __float2bfloat16_rn(__uint_as_float(av[j]));
@@ -606,6 +637,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tbase, 512);
+  if (threadIdx.x < kWaitSites - 1 && wcyc[threadIdx.x]) atomicAdd(&P.status->wait_cycles[threadIdx.x], wcyc[threadIdx.x]);
+  if (threadIdx.x == kWaitSites - 1)
+    atomicAdd(&P.status->wait_cycles[kWaitSites - 1], (unsigned long long)(clock64() - kernel_t0));
 }
 
 struct BwdWs {

@@ -73,7 +73,8 @@ struct Layout {
   // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_ready[2], pv_done, o_free, dp_full, dp_free
   static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 1 + 1 + 1 + 1;
   static constexpr int kMisc = kBars + kNumBars * 8;      // tmem slot, abort flag
-  static constexpr int kBitmaps = kMisc + 64;             // producer-private band bitmaps
+  static constexpr int kWaitCyc = kMisc + 64;             // per-site wait cycle counters
+  static constexpr int kBitmaps = kWaitCyc + kWaitSites * 8;  // producer-private band bitmaps
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -83,6 +84,28 @@ __device__ __forceinline__ float fast_exp2(float x) {
 }
 
 __device__ __forceinline__ bool band_kept(const uint32_t* bm, int B) { return (bm[B >> 5] >> (B & 31)) & 1u; }
+
+// Masking mode of one 64-key source for one segment's rows (warp-uniform):
+// inactive, fully active, the causal diagonal block, or per-column bits.
+enum : int { kSrcOff = 0, kSrcFull = 1, kSrcDiag = 2, kSrcBits = 3 };
+__device__ __forceinline__ int src_mode(uint32_t w0, uint32_t w1, bool is_diag) {
+  if ((w0 | w1) == 0u) return kSrcOff;
+  if (is_diag) return kSrcDiag;
+  if ((w0 & w1) == 0xffffffffu) return kSrcFull;
+  return kSrcBits;
+}
+// Set masked entries of a 64-key source to -inf (row rr of its 64-row block).
+__device__ __forceinline__ void mask_source(float* x, int mode, uint32_t w0, uint32_t w1, int rr) {
+  if (mode == kSrcDiag) {
+#pragma unroll
+    for (int c = 0; c < 64; ++c)
+      if (c > rr) x[c] = -__builtin_huge_valf();
+  } else if (mode == kSrcBits) {
+#pragma unroll
+    for (int c = 0; c < 64; ++c)
+      if (!(((c < 32 ? w0 : w1) >> (c & 31)) & 1u)) x[c] = -__builtin_huge_valf();
+  }
+}
 
 template <int D, bool kDQ>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -106,6 +129,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dp_free = dp_full + 1;    // dQ: dP read by every row
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Ly::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Ly::kMisc + 4);
+  unsigned long long* wcyc = reinterpret_cast<unsigned long long*>(sm + Ly::kWaitCyc);
+  const long long kernel_t0 = clock64();
   TileMeta* metas = reinterpret_cast<TileMeta*>(sm + Ly::kMeta);
   const AttnGeom& g = P.g;
   constexpr uint32_t kAccCol = kDQ ? 384 : 256;  // O or dQ
@@ -130,6 +155,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (threadIdx.x < kWaitSites) wcyc[threadIdx.x] = 0;
   if (warp == 2) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
@@ -141,7 +167,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   auto wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
     if (*abort_flag) return false;
-    if (mbar_wait(bar, parity, kWaitLimitNs)) return true;
+    const long long w0 = clock64();
+    const bool ok = mbar_wait(bar, parity, kWaitLimitNs);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&wcyc[where & (kWaitSites - 1)], (unsigned long long)(clock64() - w0));
+    if (ok) return true;
     *abort_flag = 1;
     report_timeout(P.status, where);
     return false;
@@ -409,55 +438,79 @@ __global__ void __launch_bounds__(kThreads, 1)
       do {
         const int st = t % kStages;
         if (!wait_warp(&kv_full[st], (t / kStages) & 1, 20)) break;
+        // per 64-key source: warp-uniform masking mode (rows of a warp share a segment)
+        int mode[2];
         uint32_t mw[4];
+#pragma unroll
         for (int w = 0; w < 4; ++w) mw[w] = metas[st].mask[seg][w];
-        const int diag = metas[st].diag[seg];
+        {
+          const int diag = metas[st].diag[seg];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) mode[j] = src_mode(mw[2 * j], mw[2 * j + 1], diag == 64 * j);
+        }
         last = metas[st].last != 0;
         if (!wait_warp(&s_full[t & 1], (t >> 1) & 1, 21)) break;
         tc_fence_after();
         const uint32_t tS = tbase + (uint32_t)((t & 1) * 128) + lane_off;
+        const float c2 = P.scale_log2;
         if (kDQ) {
           // ---- dS = P (dP - D), P = exp2(scale_log2 S - lse2) on active entries
           if (!wait_warp(dp_full, t & 1, 24)) break;
           tc_fence_after();
 #pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) {
-            uint32_t sv[32], dv[32];
-            tmem_ld32(tS + c0, sv);
-            tmem_ld32(tbase + kDPCol + lane_off + c0, dv);
-            tmem_ld_wait();
-            uint32_t pk[16];
+          for (int j = 0; j < 2; ++j) {
+            if (mode[j] == kSrcOff) {
+              uint32_t z[16];
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              float ds[2];
-#pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const int c = c0 + 2 * k + e;
-                bool on = (mw[c >> 5] >> (c & 31)) & 1u;
-                if (diag >= 0 && c >= diag && c < diag + 64 && (c - diag) > rr) on = false;
-                const float p = on ? fast_exp2(__uint_as_float(sv[2 * k + e]) * P.scale_log2 - lse2) : 0.f;
-                ds[e] = p * (__uint_as_float(dv[2 * k + e]) - Dr);
-              }
-              pk[k] = pack_bf16(ds[0], ds[1]);
+              for (int k = 0; k < 16; ++k) z[k] = 0u;
+              tmem_st16(tS + 32 * j, z);
+              tmem_st16(tS + 32 * j + 16, z);
+              continue;
             }
-            tmem_st16(tS + c0 / 2, pk);
+            uint32_t sv[64], dv[64];
+            tmem_ld32(tS + 64 * j, sv);
+            tmem_ld32(tS + 64 * j + 32, sv + 32);
+            tmem_ld32(tbase + kDPCol + lane_off + 64 * j, dv);
+            tmem_ld32(tbase + kDPCol + lane_off + 64 * j + 32, dv + 32);
+            tmem_ld_wait();
+            float x[64];
+#pragma unroll
+            for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sv[c]);
+            mask_source(x, mode[j], mw[2 * j], mw[2 * j + 1], rr);
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint32_t pk[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k) {
+                const int c = 32 * h2 + 2 * k;
+                const float p0 = fast_exp2(fmaf(x[c], c2, -lse2));
+                const float p1 = fast_exp2(fmaf(x[c + 1], c2, -lse2));
+                pk[k] = pack_bf16(p0 * (__uint_as_float(dv[c]) - Dr), p1 * (__uint_as_float(dv[c + 1]) - Dr));
+              }
+              tmem_st16(tS + 32 * j + 16 * h2, pk);
+            }
           }
           tc_fence_before();
           mbar_arrive(dp_free);
         } else {
+          uint32_t sraw[128];
+#pragma unroll
+          for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32(tS + c0, sraw + c0);
+          tmem_ld_wait();
           float x[128];
 #pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32(tS + c0, reinterpret_cast<uint32_t*>(x + c0));
-          tmem_ld_wait();
-          float mt = kNegInf;
+          for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sraw[c]);
+          // row maximum of the raw scores (scale > 0 keeps the order), 4 chains
+          float mx[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
 #pragma unroll
-          for (int c = 0; c < 128; ++c) {
-            bool on = (mw[c >> 5] >> (c & 31)) & 1u;
-            if (diag >= 0 && c >= diag && c < diag + 64 && (c - diag) > rr) on = false;
-            x[c] = on ? x[c] * P.scale_log2 : kNegInf;
-            mt = fmaxf(mt, x[c]);
+          for (int j = 0; j < 2; ++j) {
+            if (mode[j] == kSrcOff) continue;
+            mask_source(x + 64 * j, mode[j], mw[2 * j], mw[2 * j + 1], rr);
+#pragma unroll
+            for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], x[64 * j + c]);
           }
-          const float m_new = fmaxf(m_ref, mt);
+          const float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          const float m_new = (mraw == kNegInf) ? m_ref : fmaxf(m_ref, mraw * c2);
           // Rows whose maximum grew by more than the threshold rescale their
           // running O after the previous PV landed.  The TMEM loads/stores are
           // warp-collective, so the whole warp takes the branch when any row
@@ -481,25 +534,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (m_ref == kNegInf) m_ref = m_new;
-          // P = exp2(x - m_ref) as packed bf16 into the first 64 columns of the S buffer
-          const float mref_use = (m_ref == kNegInf) ? 0.f : m_ref;  // all x are -inf then
+          // P = exp2(c2 x - m_ref) as packed bf16 into the first 64 columns of the S buffer
+          const float neg_m = (m_ref == kNegInf) ? 0.f : -m_ref;  // all x are -inf then
+          float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) {
-            uint32_t pk[16];
+          for (int j = 0; j < 2; ++j) {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const float p0 = fast_exp2(x[c0 + 2 * k] - mref_use);
-              const float p1 = fast_exp2(x[c0 + 2 * k + 1] - mref_use);
-              l += p0 + p1;
-              pk[k] = pack_bf16(p0, p1);
+            for (int h2 = 0; h2 < 2; ++h2) {
+              uint32_t pk[16];
+              if (mode[j] == kSrcOff) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) pk[k] = 0u;
+              } else {
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                  const int c = 64 * j + 32 * h2 + 2 * k;
+                  const float p0 = fast_exp2(fmaf(x[c], c2, neg_m));
+                  const float p1 = fast_exp2(fmaf(x[c + 1], c2, neg_m));
+                  ls[k & 3] += p0 + p1;
+                  pk[k] = pack_bf16(p0, p1);
+                }
+              }
+              tmem_st16(tS + 32 * j + 16 * h2, pk);
             }
-            tmem_st16(tS + c0 / 2, pk);
           }
+          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(&p_ready[t & 1]);
         if (last) {
+          // pv_done completes once per tile and a parity wait only tells the
+          // open phase from the one before it: the PV of tile t-1 may still be
+          // running here, so wait for its phase first, then for tile t's.
+          if (!wait_warp(pv_done, (t - 1) & 1, 25)) break;
           if (!wait_warp(pv_done, t & 1, 23)) break;
           tc_fence_after();
           const float mult = kDQ ? P.scale : ((l > 0.f) ? 1.0f / l : 0.f);
@@ -531,6 +599,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tbase, 512);
+  if (threadIdx.x < kWaitSites - 1 && wcyc[threadIdx.x]) atomicAdd(&P.status->wait_cycles[threadIdx.x], wcyc[threadIdx.x]);
+  if (threadIdx.x == kWaitSites - 1)
+    atomicAdd(&P.status->wait_cycles[kWaitSites - 1], (unsigned long long)(clock64() - kernel_t0));
 }
 
 template <int D, bool kDQ>

@@ -12,11 +12,16 @@ constexpr int kBlock = 64;                       // slash tile edge (keys and qu
 constexpr uint64_t kWaitLimitNs = 2000000000ull; // bounded in-kernel waits: 2 s
 constexpr int kMaxL = 1 << 20;                   // supported sequence length ceiling
 
-// Device-side status word (first bytes of every workspace).
+// Device-side status block (first bytes of every workspace).
+constexpr int kWaitSites = 32;
 struct DevStatus {
   int32_t code;   // VS_OK or VS_ERR_TIMEOUT
   int32_t where;  // which wait gave up (kernel-specific tag)
   int32_t pad[2];
+  // Cycles spent blocked at each wait site of the attention kernels, summed
+  // over CTAs (lane 0 of each waiting warp), and the kernels' total cycles
+  // per CTA in slot 31: a pipeline-balance diagnostic read by profiling tools.
+  unsigned long long wait_cycles[kWaitSites];
 };
 
 __device__ __forceinline__ void report_timeout(DevStatus* st, int where) {
