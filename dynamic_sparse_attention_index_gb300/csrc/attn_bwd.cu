@@ -34,7 +34,6 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kStages = 2;
-constexpr float kNegInf = -__builtin_huge_valf();
 constexpr int kMaxSplits = 32;
 
 // ---------------------------------------------------------------- D = rowsum(dO * O)
@@ -124,16 +123,12 @@ __device__ __forceinline__ int src_mode(uint32_t w0, uint32_t w1, bool is_diag) 
   if ((w0 & w1) == 0xffffffffu) return kSrcFull;
   return kSrcBits;
 }
-__device__ __forceinline__ void mask_source(float* x, int mode, uint32_t w0, uint32_t w1, int rr) {
-  if (mode == kSrcDiag) {
-#pragma unroll
-    for (int c = 0; c < 64; ++c)
-      if (c > rr) x[c] = -__builtin_huge_valf();
-  } else if (mode == kSrcBits) {
-#pragma unroll
-    for (int c = 0; c < 64; ++c)
-      if (!(((c < 32 ? w0 : w1) >> (c & 31)) & 1u)) x[c] = -__builtin_huge_valf();
-  }
+// Active keys of the 64-key block for row rr of its source, as a 64-bit mask.
+__device__ __forceinline__ uint64_t active_bits(int mode, uint32_t w0, uint32_t w1, int rr) {
+  if (mode == kSrcOff) return 0ull;
+  if (mode == kSrcFull) return ~0ull;
+  if (mode == kSrcDiag) return rr >= 63 ? ~0ull : ((2ull << rr) - 1ull);
+  return (uint64_t)w0 | ((uint64_t)w1 << 32);
 }
 
 // number of row splits of a vertical group and the stride of its partial slots
@@ -547,14 +542,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tb + 128, dv);
           tmem_ld32(tb + 128 + 32, dv + 32);
           tmem_ld_wait();
-          float x[64];
-#pragma unroll
-          for (int k = 0; k < 64; ++k) x[k] = __uint_as_float(sv[k]);
-          mask_source(x, mode, mw0, mw1, rr);
+          const uint64_t act = active_bits(mode, mw0, mw1, rr);
 #pragma unroll
           for (int k = 0; k < 32; ++k) {
-            const float p0 = fast_exp2(fmaf(x[2 * k], c, -lse2));
-            const float p1 = fast_exp2(fmaf(x[2 * k + 1], c, -lse2));
+            const float p0 = ((act >> (2 * k)) & 1ull) ? fast_exp2(fmaf(__uint_as_float(sv[2 * k]), c, -lse2)) : 0.f;
+            const float p1 =
+                ((act >> (2 * k + 1)) & 1ull) ? fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), c, -lse2)) : 0.f;
             pk[k] = pack_bf16(p0, p1);
             dk[k] = pack_bf16(p0 * (__uint_as_float(dv[2 * k]) - Dr), p1 * (__uint_as_float(dv[2 * k + 1]) - Dr));
           }

@@ -14,10 +14,15 @@
 //
 // Persistent CTAs (one per SM), 8 warps:
 //   warp 0     producer: enumerates the tile's key sources, builds per-column
-//              masks, issues TMA loads of Q (and dO) per tile and K/V per source
+//              masks, issues TMA loads of Q (and dO) per row tile and of K
+//   warp 3     second producer: the same enumeration, TMA loads of V
 //   warp 1     MMA issuer (one thread)
 //   warp 2     owns the TMEM allocation
 //   warps 4-7  softmax / dS + epilogue: thread r owns row r (TMEM lane r)
+// K and V sit in separate rings so each is released as soon as its last
+// reader is done: forward K after S (3 deep), V after O += P V (2 deep); dQ
+// V after dP (2 deep), K after dQ += dS K (3 deep).  Per-tile metadata has
+// its own ring, released by the softmax warps once they copied it.
 // TMEM columns: S double buffer [0,128) and [128,256) (P or dS alias the first
 // 64 columns of their S buffer as packed bf16); forward: O at [256, 256+d);
 // dQ: dP at [256, 384), dQ at [384, 384+d).
@@ -31,7 +36,6 @@
 namespace vs {
 namespace {
 
-constexpr int kStages = 2;
 constexpr int kThreads = 256;
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleThreshold = 8.0f;
@@ -65,16 +69,19 @@ struct Layout {
   static constexpr int kKBytes = kHalves * kRowBytes;    // 128 keys of K (or V)
   static constexpr int kQSlots = kDQ ? 1 : 2;            // dQ: one slot holding Q then dO
   static constexpr int kSlotBytes = kDQ ? 2 * kQBytes : kQBytes;
+  static constexpr int kRK = 3;                          // K ring depth
+  static constexpr int kRV = 2;                          // V ring depth
   static constexpr int kQ = 0;
-  static constexpr int kStage = 2 * kQBytes;
-  static constexpr int kStageBytes = 2 * kKBytes;        // K then V
-  static constexpr int kMeta = kStage + kStages * kStageBytes;
-  static constexpr int kBars = kMeta + kStages * (int)sizeof(TileMeta);
-  // q_full[2], q_empty[2], kv_full[S], kv_empty[S], s_full[2], p_ready[2], pv_done, o_free, dp_full, dp_free
-  static constexpr int kNumBars = 2 + 2 + kStages + kStages + 2 + 2 + 1 + 1 + 1 + 1;
+  static constexpr int kKRing = 2 * kQBytes;
+  static constexpr int kVRing = kKRing + kRK * kKBytes;
+  static constexpr int kMeta = kVRing + kRV * kKBytes;
+  static constexpr int kBars = kMeta + kRK * (int)sizeof(TileMeta);
+  // q_full[2], q_empty[2], k_full[RK], k_empty[RK], v_full[RV], v_empty[RV], meta_free[RK],
+  // s_full[2], p_ready[2], pv_done, o_free, dp_full, dp_free
+  static constexpr int kNumBars = 2 + 2 + 3 * kRK + 2 * kRV + 2 + 2 + 1 + 1 + 1 + 1;
   static constexpr int kMisc = kBars + kNumBars * 8;      // tmem slot, abort flag
   static constexpr int kWaitCyc = kMisc + 64;             // per-site wait cycle counters
-  static constexpr int kBitmaps = kWaitCyc + kWaitSites * 8;  // producer-private band bitmaps
+  static constexpr int kSmemEnd = kWaitCyc + kWaitSites * 8;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -94,17 +101,26 @@ __device__ __forceinline__ int src_mode(uint32_t w0, uint32_t w1, bool is_diag) 
   if ((w0 & w1) == 0xffffffffu) return kSrcFull;
   return kSrcBits;
 }
-// Set masked entries of a 64-key source to -inf (row rr of its 64-row block).
-__device__ __forceinline__ void mask_source(float* x, int mode, uint32_t w0, uint32_t w1, int rr) {
-  if (mode == kSrcDiag) {
+// Active columns of a 64-key source for row rr of the segment, as a 64-bit mask.
+__device__ __forceinline__ uint64_t active_bits(int mode, uint32_t w0, uint32_t w1, int rr) {
+  if (mode == kSrcOff) return 0ull;
+  if (mode == kSrcFull) return ~0ull;
+  if (mode == kSrcDiag) return rr >= 63 ? ~0ull : ((2ull << rr) - 1ull);
+  return (uint64_t)w0 | ((uint64_t)w1 << 32);
+}
+// Multiply one row of the TMEM accumulator by f (warp-collective; kept out of
+// line because it runs rarely and would otherwise bloat the softmax loop).
+template <int D>
+__device__ __noinline__ void rescale_acc_row(uint32_t taddr, float f) {
+  for (int c0 = 0; c0 < D; c0 += 16) {
+    uint32_t o[16];
+    tmem_ld16(taddr + c0, o);
+    tmem_ld_wait();
 #pragma unroll
-    for (int c = 0; c < 64; ++c)
-      if (c > rr) x[c] = -__builtin_huge_valf();
-  } else if (mode == kSrcBits) {
-#pragma unroll
-    for (int c = 0; c < 64; ++c)
-      if (!(((c < 32 ? w0 : w1) >> (c & 31)) & 1u)) x[c] = -__builtin_huge_valf();
+    for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+    tmem_st16(taddr + c0, o);
   }
+  tmem_st_wait();
 }
 
 template <int D, bool kDQ>
@@ -119,9 +135,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::kBars);
   uint64_t* q_full = bars;
   uint64_t* q_empty = bars + 2;
-  uint64_t* kv_full = bars + 4;
-  uint64_t* kv_empty = kv_full + kStages;
-  uint64_t* s_full = kv_empty + kStages;
+  uint64_t* k_full = bars + 4;
+  uint64_t* k_empty = k_full + Ly::kRK;
+  uint64_t* v_full = k_empty + Ly::kRK;
+  uint64_t* v_empty = v_full + Ly::kRV;
+  uint64_t* meta_free = v_empty + Ly::kRV;
+  uint64_t* s_full = meta_free + Ly::kRK;
   uint64_t* p_ready = s_full + 2;     // P (forward) or dS (dQ) written to TMEM
   uint64_t* pv_done = p_ready + 2;    // O += P V (forward) or dQ += dS K landed
   uint64_t* o_free = pv_done + 1;     // epilogue finished reading the accumulator
@@ -144,9 +163,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&s_full[i], 1);
       mbar_init(&p_ready[i], 128);
     }
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+    for (int i = 0; i < Ly::kRK; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&meta_free[i], 128);
+    }
+    for (int i = 0; i < Ly::kRV; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
     }
     mbar_init(pv_done, 1);
     mbar_init(o_free, 128);
@@ -181,29 +205,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     return __all_sync(0xffffffffu, wait(bar, parity, where));
   };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    uint32_t* bm0 = reinterpret_cast<uint32_t*>(sm + Ly::kBitmaps);
-    uint32_t* bm1 = bm0 + g.nw;
+  // ------------------------------------------------------------ producers
+  // warp 0 (kprod): Q (+ dO) per row tile, per-tile metadata, K per source;
+  // warp 3: V per source.  Both walk the same source enumeration.
+  auto produce = [&](const bool kprod) {
     const int W = g.bs / kBlock;
     int t = 0, it_local = 0;
     if (lane == 0) {
-      tma_prefetch_desc(&mQ);
-      tma_prefetch_desc(&mK);
-      tma_prefetch_desc(&mV);
-      tma_prefetch_desc(&mKp);
-      tma_prefetch_desc(&mVp);
-      if (kDQ) tma_prefetch_desc(&mdO);
+      if (kprod) {
+        tma_prefetch_desc(&mQ);
+        tma_prefetch_desc(&mK);
+        tma_prefetch_desc(&mKp);
+        if (kDQ) tma_prefetch_desc(&mdO);
+      } else {
+        tma_prefetch_desc(&mV);
+        tma_prefetch_desc(&mVp);
+      }
     }
     for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
       const Item it = decode_item(g, id);
       const int qslot = it_local % Ly::kQSlots;
-      for (int w = lane; w < g.nw; w += 32) {
-        bm0[w] = P.inS[(size_t)it.h[0] * g.nw + w];
-        bm1[w] = P.inS[(size_t)it.h[1] * g.nw + w];
-      }
-      __syncwarp();
-      if (lane == 0) {
+      const uint32_t* bm0 = P.inS + (size_t)it.h[0] * g.nw;
+      const uint32_t* bm1 = P.inS + (size_t)it.h[1] * g.nw;
+      if (kprod && lane == 0) {
         if (wait(&q_empty[qslot], ((it_local / Ly::kQSlots) & 1) ^ 1, 1)) {
           mbar_arrive_expect_tx(&q_full[qslot], Ly::kSlotBytes);
           uint8_t* q = sm + Ly::kQ + qslot * Ly::kSlotBytes;
@@ -254,36 +278,48 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto emit = [&]() {
         done_src += nsrc;
         const bool last = done_src == total_src;
-        const int st = t % kStages;
         bool ok = true;
-        if (lane == 0) ok = wait(&kv_empty[st], ((t / kStages) & 1) ^ 1, 2);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (ok && lane == 0) {
-          TileMeta& m = metas[st];
-          for (int s = 0; s < 2; ++s) {
-            for (int w = 0; w < 4; ++w) m.mask[s][w] = smask[s][w];
-            m.diag[s] = sdiag[s];
-          }
-          m.nsrc = nsrc;
-          m.first = first ? 1 : 0;
-          m.last = last ? 1 : 0;
-          m.qslot = qslot;
-          uint8_t* kst = sm + Ly::kStage + st * Ly::kStageBytes;
-          uint8_t* vst = kst + Ly::kKBytes;
-          mbar_arrive_expect_tx(&kv_full[st], nsrc * 2 * Ly::kHalves * 8192);
-          for (int j = 0; j < nsrc; ++j) {
-            for (int hf = 0; hf < Ly::kHalves; ++hf) {
-              uint8_t* kd = kst + hf * Ly::kRowBytes + j * 8192;
-              uint8_t* vd = vst + hf * Ly::kRowBytes + j * 8192;
-              if (src_kind[j] == 0) {
-                tma_load_3d(kd, &mK, &kv_full[st], hf * 64, it.g, src_arg[j] * kBlock);
-                tma_load_3d(vd, &mV, &kv_full[st], hf * 64, it.g, src_arg[j] * kBlock);
-              } else {
-                const int row = it.vg * g.L + src_arg[j] * 64;
-                tma_load_2d(kd, &mKp, &kv_full[st], hf * 64, row);
-                tma_load_2d(vd, &mVp, &kv_full[st], hf * 64, row);
-              }
+        if (kprod) {
+          const int sk = t % Ly::kRK;
+          if (lane == 0)
+            ok = wait(&k_empty[sk], ((t / Ly::kRK) & 1) ^ 1, 2) && wait(&meta_free[sk], ((t / Ly::kRK) & 1) ^ 1, 3);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (ok && lane == 0) {
+            TileMeta& m = metas[sk];
+            for (int s = 0; s < 2; ++s) {
+              for (int w = 0; w < 4; ++w) m.mask[s][w] = smask[s][w];
+              m.diag[s] = sdiag[s];
             }
+            m.nsrc = nsrc;
+            m.first = first ? 1 : 0;
+            m.last = last ? 1 : 0;
+            m.qslot = qslot;
+            uint8_t* kst = sm + Ly::kKRing + sk * Ly::kKBytes;
+            mbar_arrive_expect_tx(&k_full[sk], nsrc * Ly::kHalves * 8192);
+            for (int j = 0; j < nsrc; ++j)
+              for (int hf = 0; hf < Ly::kHalves; ++hf) {
+                uint8_t* kd = kst + hf * Ly::kRowBytes + j * 8192;
+                if (src_kind[j] == 0)
+                  tma_load_3d(kd, &mK, &k_full[sk], hf * 64, it.g, src_arg[j] * kBlock);
+                else
+                  tma_load_2d(kd, &mKp, &k_full[sk], hf * 64, it.vg * g.L + src_arg[j] * 64);
+              }
+          }
+        } else {
+          const int sv = t % Ly::kRV;
+          if (lane == 0) ok = wait(&v_empty[sv], ((t / Ly::kRV) & 1) ^ 1, 4);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (ok && lane == 0) {
+            uint8_t* vst = sm + Ly::kVRing + sv * Ly::kKBytes;
+            mbar_arrive_expect_tx(&v_full[sv], nsrc * Ly::kHalves * 8192);
+            for (int j = 0; j < nsrc; ++j)
+              for (int hf = 0; hf < Ly::kHalves; ++hf) {
+                uint8_t* vd = vst + hf * Ly::kRowBytes + j * 8192;
+                if (src_kind[j] == 0)
+                  tma_load_3d(vd, &mV, &v_full[sv], hf * 64, it.g, src_arg[j] * kBlock);
+                else
+                  tma_load_2d(vd, &mVp, &v_full[sv], hf * 64, it.vg * g.L + src_arg[j] * 64);
+              }
           }
         }
         __syncwarp();
@@ -321,27 +357,33 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int j = nsrc;
         src_kind[j] = 1;
         src_arg[j] = c;
-        for (int half = 0; half < 2; ++half) {
-          const int u = c * 64 + half * 32 + lane;
-          bool a[2] = {false, false};
-          if (u < nv) {
-            const uint32_t e = P.vlist[(size_t)it.vg * g.L + u];
-            const int m = (int)(e & kVTokenMask);
-            const uint32_t f = e >> kVFlagShift;
-            const int kbm = m / kBlock;
-            for (int s = 0; s < 2; ++s) {
-              if (!it.valid[s] || !((f >> s) & 1u) || kbm >= it.I[s]) continue;
-              const int B = it.I[s] / W - kbm / W;
-              a[s] = B != 0 && !band_kept(s ? bm1 : bm0, B);
+        if (kprod) {
+          for (int half = 0; half < 2; ++half) {
+            const int u = c * 64 + half * 32 + lane;
+            bool a[2] = {false, false};
+            if (u < nv) {
+              const uint32_t e = P.vlist[(size_t)it.vg * g.L + u];
+              const int m = (int)(e & kVTokenMask);
+              const uint32_t f = e >> kVFlagShift;
+              const int kbm = m / kBlock;
+              for (int s = 0; s < 2; ++s) {
+                if (!it.valid[s] || !((f >> s) & 1u) || kbm >= it.I[s]) continue;
+                const int B = it.I[s] / W - kbm / W;
+                a[s] = B != 0 && !band_kept(s ? bm1 : bm0, B);
+              }
             }
+            smask[0][2 * j + half] = __ballot_sync(0xffffffffu, a[0]);
+            smask[1][2 * j + half] = __ballot_sync(0xffffffffu, a[1]);
           }
-          smask[0][2 * j + half] = __ballot_sync(0xffffffffu, a[0]);
-          smask[1][2 * j + half] = __ballot_sync(0xffffffffu, a[1]);
         }
         if (++nsrc == 2) emit();
       }
       if (nsrc > 0) emit();
     }
+  };
+
+  if (warp == 0 || warp == 3) {
+    produce(warp == 0);
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -357,30 +399,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait(&p_ready[prev_t & 1], (prev_t >> 1) & 1, 10)) return false;
         if (prev_first && prev_item > 0)
           if (!wait(o_free, (prev_item - 1) & 1, 11)) return false;
+        const int pk = prev_t % Ly::kRK, pv = prev_t % Ly::kRV;
+        if (!kDQ && !wait(&v_full[pv], (prev_t / Ly::kRV) & 1, 15)) return false;
         tc_fence_after();
-        const int st = prev_t % kStages;
-        const uint32_t bst = smem_u32(sm + Ly::kStage + st * Ly::kStageBytes + (kDQ ? 0 : Ly::kKBytes));
+        // B operand: V of the tile (forward) or K of the tile (dQ), MN-major
+        const uint32_t bst = kDQ ? smem_u32(sm + Ly::kKRing + pk * Ly::kKBytes)
+                                 : smem_u32(sm + Ly::kVRing + pv * Ly::kKBytes);
         const uint32_t pS = tbase + (uint32_t)((prev_t & 1) * 128);
         for (int kk = 0; kk < 4 * prev_nsrc; ++kk) {
           const uint64_t bd = sdesc_sw128(bst + kk * 2048, Ly::kRowBytes, 1024);
           umma_ts(tAcc, pS + kk * 8, bd, kIdescAcc, (kk > 0 || !prev_first) ? 1u : 0u);
         }
-        umma_commit(&kv_empty[st]);
         umma_commit(pv_done);
+        if (kDQ)
+          umma_commit(&k_empty[pk]);
+        else
+          umma_commit(&v_empty[pv]);
         return true;
       };
       for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
         bool last = false;
         do {
-          const int st = t % kStages;
-          if (!wait(&kv_full[st], (t / kStages) & 1, 12)) break;
-          const TileMeta m = metas[st];
+          const int sk = t % Ly::kRK, sv = t % Ly::kRV;
+          if (!wait(&k_full[sk], (t / Ly::kRK) & 1, 12)) break;
+          const TileMeta m = metas[sk];
           last = m.last != 0;
           if (m.first)
             if (!wait(&q_full[m.qslot], (it_local / Ly::kQSlots) & 1, 13)) break;
           tc_fence_after();
           const uint32_t qa = smem_u32(sm + Ly::kQ + m.qslot * Ly::kSlotBytes);
-          const uint32_t kb = smem_u32(sm + Ly::kStage + st * Ly::kStageBytes);
+          const uint32_t kb = smem_u32(sm + Ly::kKRing + sk * Ly::kKBytes);
           const uint32_t dS = tbase + (uint32_t)((t & 1) * 128);
           const uint32_t idS = m.nsrc == 2 ? kIdescS128 : kIdescS64;
           for (int kk = 0; kk < D / 16; ++kk) {
@@ -388,18 +436,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_ss(dS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
           }
           umma_commit(&s_full[t & 1]);
+          if (!kDQ) umma_commit(&k_empty[sk]);  // forward: K is read only by S
           if (kDQ) {
             // dP = dO V^T into the single dP buffer, once every row read the previous one
             if (t > 0 && !wait(dp_free, (t - 1) & 1, 14)) break;
+            if (!wait(&v_full[sv], (t / Ly::kRV) & 1, 15)) break;
             tc_fence_after();
             const uint32_t oa = qa + Ly::kQBytes;
-            const uint32_t vb = kb + Ly::kKBytes;
+            const uint32_t vb = smem_u32(sm + Ly::kVRing + sv * Ly::kKBytes);
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * Ly::kRowBytes + (kk & 3) * 32;
               umma_ss(tbase + kDPCol, sdesc_sw128(oa + off, 16, 1024), sdesc_sw128(vb + off, 16, 1024), idS,
                       kk > 0 ? 1u : 0u);
             }
             umma_commit(dp_full);
+            umma_commit(&v_empty[sv]);  // dQ: V is read only by dP
           }
           if (last) umma_commit(&q_empty[m.qslot]);
           if (have_prev && !issue_acc()) break;
@@ -436,79 +487,76 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bool last = false;
       do {
-        const int st = t % kStages;
-        if (!wait_warp(&kv_full[st], (t / kStages) & 1, 20)) break;
+        const int sk = t % Ly::kRK;
+        if (!wait_warp(&k_full[sk], (t / Ly::kRK) & 1, 20)) break;
         // per 64-key source: warp-uniform masking mode (rows of a warp share a segment)
         int mode[2];
         uint32_t mw[4];
 #pragma unroll
-        for (int w = 0; w < 4; ++w) mw[w] = metas[st].mask[seg][w];
+        for (int w = 0; w < 4; ++w) mw[w] = metas[sk].mask[seg][w];
         {
-          const int diag = metas[st].diag[seg];
+          const int diag = metas[sk].diag[seg];
 #pragma unroll
           for (int j = 0; j < 2; ++j) mode[j] = src_mode(mw[2 * j], mw[2 * j + 1], diag == 64 * j);
         }
-        last = metas[st].last != 0;
+        last = metas[sk].last != 0;
+        mbar_arrive(&meta_free[sk]);
         if (!wait_warp(&s_full[t & 1], (t >> 1) & 1, 21)) break;
         tc_fence_after();
         const uint32_t tS = tbase + (uint32_t)((t & 1) * 128) + lane_off;
         const float c2 = P.scale_log2;
+        const long long ph0 = clock64();
+        long long ph_rescale = 0;
         if (kDQ) {
           // ---- dS = P (dP - D), P = exp2(scale_log2 S - lse2) on active entries
           if (!wait_warp(dp_full, t & 1, 24)) break;
           tc_fence_after();
-#pragma unroll
+#pragma unroll 1
           for (int j = 0; j < 2; ++j) {
-            if (mode[j] == kSrcOff) {
-              uint32_t z[16];
+            const int md = j ? mode[1] : mode[0];
+            uint32_t pk[32];
+            if (md == kSrcOff) {
 #pragma unroll
-              for (int k = 0; k < 16; ++k) z[k] = 0u;
-              tmem_st16(tS + 32 * j, z);
-              tmem_st16(tS + 32 * j + 16, z);
-              continue;
-            }
-            uint32_t sv[64], dv[64];
-            tmem_ld32(tS + 64 * j, sv);
-            tmem_ld32(tS + 64 * j + 32, sv + 32);
-            tmem_ld32(tbase + kDPCol + lane_off + 64 * j, dv);
-            tmem_ld32(tbase + kDPCol + lane_off + 64 * j + 32, dv + 32);
-            tmem_ld_wait();
-            float x[64];
+              for (int k = 0; k < 32; ++k) pk[k] = 0u;
+            } else {
+              uint32_t sv[64], dv[64];
+              tmem_ld32(tS + 64 * j, sv);
+              tmem_ld32(tS + 64 * j + 32, sv + 32);
+              tmem_ld32(tbase + kDPCol + lane_off + 64 * j, dv);
+              tmem_ld32(tbase + kDPCol + lane_off + 64 * j + 32, dv + 32);
+              tmem_ld_wait();
+              const uint64_t act = active_bits(md, j ? mw[2] : mw[0], j ? mw[3] : mw[1], rr);
 #pragma unroll
-            for (int c = 0; c < 64; ++c) x[c] = __uint_as_float(sv[c]);
-            mask_source(x, mode[j], mw[2 * j], mw[2 * j + 1], rr);
-#pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              uint32_t pk[16];
-#pragma unroll
-              for (int k = 0; k < 16; ++k) {
-                const int c = 32 * h2 + 2 * k;
-                const float p0 = fast_exp2(fmaf(x[c], c2, -lse2));
-                const float p1 = fast_exp2(fmaf(x[c + 1], c2, -lse2));
+              for (int k = 0; k < 32; ++k) {
+                const int c = 2 * k;
+                const float p0 = ((act >> c) & 1ull) ? fast_exp2(fmaf(__uint_as_float(sv[c]), c2, -lse2)) : 0.f;
+                const float p1 =
+                    ((act >> (c + 1)) & 1ull) ? fast_exp2(fmaf(__uint_as_float(sv[c + 1]), c2, -lse2)) : 0.f;
                 pk[k] = pack_bf16(p0 * (__uint_as_float(dv[c]) - Dr), p1 * (__uint_as_float(dv[c + 1]) - Dr));
               }
-              tmem_st16(tS + 32 * j + 16 * h2, pk);
             }
+            tmem_st16(tS + 32 * j, pk);
+            tmem_st16(tS + 32 * j + 16, pk + 16);
           }
           tc_fence_before();
           mbar_arrive(dp_free);
         } else {
-          uint32_t sraw[128];
-#pragma unroll
-          for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32(tS + c0, sraw + c0);
-          tmem_ld_wait();
-          float x[128];
-#pragma unroll
-          for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sraw[c]);
-          // row maximum of the raw scores (scale > 0 keeps the order), 4 chains
+          // pass 1: row maximum of the raw scores (scale > 0 keeps the order)
           float mx[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
-#pragma unroll
+#pragma unroll 1
           for (int j = 0; j < 2; ++j) {
-            if (mode[j] == kSrcOff) continue;
-            mask_source(x + 64 * j, mode[j], mw[2 * j], mw[2 * j + 1], rr);
+            const int md = j ? mode[1] : mode[0];
+            if (md == kSrcOff) continue;
+            uint32_t v[64];
+            tmem_ld32(tS + 64 * j, v);
+            tmem_ld32(tS + 64 * j + 32, v + 32);
+            tmem_ld_wait();
+            const uint64_t act = active_bits(md, j ? mw[2] : mw[0], j ? mw[3] : mw[1], rr);
 #pragma unroll
-            for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], x[64 * j + c]);
+            for (int c = 0; c < 64; ++c)
+              mx[c & 3] = fmaxf(mx[c & 3], ((act >> c) & 1ull) ? __uint_as_float(v[c]) : kNegInf);
           }
+          if (lane == 0) atomicAdd(&wcyc[26], (unsigned long long)(clock64() - ph0));
           const float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
           const float m_new = (mraw == kNegInf) ? m_ref : fmaxf(m_ref, mraw * c2);
           // Rows whose maximum grew by more than the threshold rescale their
@@ -517,53 +565,65 @@ __global__ void __launch_bounds__(kThreads, 1)
           // needs it (factor 1 for the others).
           const bool need = m_ref != kNegInf && m_new > m_ref + kRescaleThreshold;
           if (__any_sync(0xffffffffu, need)) {
+            ph_rescale = clock64();
+            if (lane == 0) atomicAdd(&wcyc[29], 1ull << 40);  // count in the high bits
             if (!wait_warp(pv_done, (t - 1) & 1, 22)) break;
             tc_fence_after();
-            const float f = need ? fast_exp2(m_ref - m_new) : 1.0f;
-            for (int c0 = 0; c0 < D; c0 += 16) {
-              uint32_t o[16];
-              tmem_ld16(tAcc + c0, o);
-              tmem_ld_wait();
-              for (int k = 0; k < 16; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-              tmem_st16(tAcc + c0, o);
-            }
-            tmem_st_wait();
+            rescale_acc_row<D>(tAcc, need ? fast_exp2(m_ref - m_new) : 1.0f);
             if (need) {
-              l *= f;
+              l *= fast_exp2(m_ref - m_new);
               m_ref = m_new;
             }
+            ph_rescale = clock64() - ph_rescale;
+            if (lane == 0) atomicAdd(&wcyc[29], (unsigned long long)ph_rescale);
           }
           if (m_ref == kNegInf) m_ref = m_new;
-          // P = exp2(c2 x - m_ref) as packed bf16 into the first 64 columns of the S buffer
+          // pass 2: P = exp2(c2 x - m_ref) as packed bf16 into the first 64
+          // columns of the S buffer (each source's scores re-read from TMEM)
           const float neg_m = (m_ref == kNegInf) ? 0.f : -m_ref;  // all x are -inf then
           float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
+#pragma unroll 1
           for (int j = 0; j < 2; ++j) {
+            const int md = j ? mode[1] : mode[0];
+            uint32_t pk[32];
+            if (md == kSrcOff) {
 #pragma unroll
-            for (int h2 = 0; h2 < 2; ++h2) {
-              uint32_t pk[16];
-              if (mode[j] == kSrcOff) {
+              for (int k = 0; k < 32; ++k) pk[k] = 0u;
+            } else {
+              uint32_t v[64];
+              tmem_ld32(tS + 64 * j, v);
+              tmem_ld32(tS + 64 * j + 32, v + 32);
+              tmem_ld_wait();
+              const uint64_t act = active_bits(md, j ? mw[2] : mw[0], j ? mw[3] : mw[1], rr);
 #pragma unroll
-                for (int k = 0; k < 16; ++k) pk[k] = 0u;
-              } else {
-#pragma unroll
-                for (int k = 0; k < 16; ++k) {
-                  const int c = 64 * j + 32 * h2 + 2 * k;
-                  const float p0 = fast_exp2(fmaf(x[c], c2, neg_m));
-                  const float p1 = fast_exp2(fmaf(x[c + 1], c2, neg_m));
-                  ls[k & 3] += p0 + p1;
-                  pk[k] = pack_bf16(p0, p1);
-                }
+              for (int k = 0; k < 32; ++k) {
+                const int c = 2 * k;
+                const float x0 = ((act >> c) & 1ull) ? __uint_as_float(v[c]) : kNegInf;
+                const float x1 = ((act >> (c + 1)) & 1ull) ? __uint_as_float(v[c + 1]) : kNegInf;
+                const float p0 = fast_exp2(fmaf(x0, c2, neg_m));
+                const float p1 = fast_exp2(fmaf(x1, c2, neg_m));
+                ls[k & 3] += p0 + p1;
+                pk[k] = pack_bf16(p0, p1);
               }
-              tmem_st16(tS + 32 * j + 16 * h2, pk);
             }
+            // P of source j goes to packed columns [32 j, 32 j + 32): the raw
+            // scores there (columns of source 0) were consumed in pass 2 for
+            // j = 0 before this store of j = 1, and in pass 1 otherwise
+            tmem_st16(tS + 32 * j, pk);
+            tmem_st16(tS + 32 * j + 16, pk + 16);
           }
           l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
+        const long long ph1 = clock64();
         tmem_st_wait();
+        if (lane == 0) {
+          atomicAdd(&wcyc[27], (unsigned long long)(ph1 - ph0 - ph_rescale));
+          atomicAdd(&wcyc[28], (unsigned long long)(clock64() - ph1));
+        }
         tc_fence_before();
         mbar_arrive(&p_ready[t & 1]);
         if (last) {
+          const long long pe0 = clock64();
           // pv_done completes once per tile and a parity wait only tells the
           // open phase from the one before it: the PV of tile t-1 may still be
           // running here, so wait for its phase first, then for tile t's.
@@ -589,6 +649,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             P.lse[(size_t)h * g.L + tok] = (l > 0.f) ? (m_ref + __log2f(l)) * 0.69314718055994531f : kNegInf;
           tc_fence_before();
           mbar_arrive(o_free);
+          if (lane == 0) atomicAdd(&wcyc[30], (unsigned long long)(clock64() - pe0));
         }
         ++t;
       } while (!last && !*abort_flag);
@@ -614,7 +675,7 @@ cudaError_t launch_qmajor(const AttnGeom& g, const PrepPtrs& pp, const void* Q, 
       !make_map_rows(&mKp, pp.Kp, (long long)g.nvg * g.L, D) ||
       !make_map_rows(&mVp, pp.Vp, (long long)g.nvg * g.L, D))
     return cudaErrorInvalidValue;
-  const size_t smem = Ly::kBitmaps + 2 * g.nw * 4 + 1024;
+  const size_t smem = Ly::kSmemEnd + 1024;
   cudaError_t e =
       cudaFuncSetAttribute(attn_qmajor_kernel<D, kDQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
