@@ -542,14 +542,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tb + 128, dv);
           tmem_ld32(tb + 128 + 32, dv + 32);
           tmem_ld_wait();
-          const uint64_t act = active_bits(mode, mw0, mw1, rr);
+          if (mode == kSrcFull) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) {
-            const float p0 = ((act >> (2 * k)) & 1ull) ? fast_exp2(fmaf(__uint_as_float(sv[2 * k]), c, -lse2)) : 0.f;
-            const float p1 =
-                ((act >> (2 * k + 1)) & 1ull) ? fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), c, -lse2)) : 0.f;
-            pk[k] = pack_bf16(p0, p1);
-            dk[k] = pack_bf16(p0 * (__uint_as_float(dv[2 * k]) - Dr), p1 * (__uint_as_float(dv[2 * k + 1]) - Dr));
+            for (int k = 0; k < 32; ++k) {
+              const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * k]), c, -lse2));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), c, -lse2));
+              pk[k] = pack_bf16(p0, p1);
+              dk[k] = pack_bf16(p0 * (__uint_as_float(dv[2 * k]) - Dr), p1 * (__uint_as_float(dv[2 * k + 1]) - Dr));
+            }
+          } else {
+            const uint64_t act = active_bits(mode, mw0, mw1, rr);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+              const float p0 = ((act >> (2 * k)) & 1ull) ? fast_exp2(fmaf(__uint_as_float(sv[2 * k]), c, -lse2)) : 0.f;
+              const float p1 =
+                  ((act >> (2 * k + 1)) & 1ull) ? fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), c, -lse2)) : 0.f;
+              pk[k] = pack_bf16(p0, p1);
+              dk[k] = pack_bf16(p0 * (__uint_as_float(dv[2 * k]) - Dr), p1 * (__uint_as_float(dv[2 * k + 1]) - Dr));
+            }
           }
         }
         // row r of a 128-row x 64-key MN-major SW128 tile: 8 chunks of 16 B

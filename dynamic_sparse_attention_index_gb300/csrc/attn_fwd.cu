@@ -18,17 +18,23 @@
 //   warp 3     second producer: the same enumeration, TMA loads of V
 //   warp 1     MMA issuer (one thread)
 //   warp 2     owns the TMEM allocation
-//   warps 4-7  softmax / dS + epilogue: thread r owns row r (TMEM lane r)
+//   warps 4-11 two softmax / dS warpgroups: group g handles the key columns
+//              of source slot g (64 keys) for all 128 rows; thread r of a
+//              group owns row r (TMEM lane r)
 // K and V sit in separate rings so each is released as soon as its last
 // reader is done: forward K after S (3 deep), V after O += P V (2 deep); dQ
 // V after dP (2 deep), K after dQ += dS K (3 deep).  Per-tile metadata has
 // its own ring, released by the softmax warps once they copied it.
-// TMEM columns: S double buffer [0,128) and [128,256) (P or dS alias the first
-// 64 columns of their S buffer as packed bf16); forward: O at [256, 256+d);
-// dQ: dP at [256, 384), dQ at [384, 384+d).
-// The forward rescales O lazily: only when a row maximum grows by more than
-// 8 (log2 units) is the running O multiplied down; otherwise exponentials are
-// taken against the stale maximum, which is exact after the final 1/l.
+// TMEM columns: S double buffer [0,128) and [128,256); P or dS of source
+// slot g are written packed (bf16) over the first 32 columns of that slot's
+// scores ([64 g, 64 g + 32) of the S buffer).  Forward: two accumulators,
+// O_A at [256, 256+d) for slot 0 and O_B at [384, 384+d) for slot 1, each
+// with its own running max and sum (independent online softmax per group),
+// combined per row in the epilogue.  dQ: dP at [256, 384), dQ at [384, 384+d).
+// The forward rescales lazily: only when a group's row maximum grows by more
+// than 8 (log2 units) is its accumulator multiplied down; otherwise
+// exponentials are taken against the stale maximum, which is exact after the
+// final normalisation.
 // tcgen05.ld/st are warp-collective: every branch around them is warp-uniform.
 #include "attn_common.cuh"
 #include "ptx.cuh"
@@ -36,7 +42,7 @@
 namespace vs {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr float kNegInf = -__builtin_huge_valf();
 constexpr float kRescaleThreshold = 8.0f;
 
@@ -77,11 +83,12 @@ struct Layout {
   static constexpr int kMeta = kVRing + kRV * kKBytes;
   static constexpr int kBars = kMeta + kRK * (int)sizeof(TileMeta);
   // q_full[2], q_empty[2], k_full[RK], k_empty[RK], v_full[RV], v_empty[RV], meta_free[RK],
-  // s_full[2], p_ready[2], pv_done, o_free, dp_full, dp_free
-  static constexpr int kNumBars = 2 + 2 + 3 * kRK + 2 * kRV + 2 + 2 + 1 + 1 + 1 + 1;
+  // s_full[2], p_ready[2], pv_done, o_free, dp_full, dp_free, ep_a, ep_b
+  static constexpr int kNumBars = 2 + 2 + 3 * kRK + 2 * kRV + 2 + 2 + 1 + 1 + 1 + 1 + 2;
   static constexpr int kMisc = kBars + kNumBars * 8;      // tmem slot, abort flag
   static constexpr int kWaitCyc = kMisc + 64;             // per-site wait cycle counters
-  static constexpr int kSmemEnd = kWaitCyc + kWaitSites * 8;
+  static constexpr int kXchg = kWaitCyc + kWaitSites * 8; // epilogue row exchange: 128 x 2 floats
+  static constexpr int kSmemEnd = kXchg + 128 * 2 * 4;
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -146,13 +153,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* o_free = pv_done + 1;     // epilogue finished reading the accumulator
   uint64_t* dp_full = o_free + 1;     // dQ: dP landed
   uint64_t* dp_free = dp_full + 1;    // dQ: dP read by every row
+  uint64_t* ep_a = dp_free + 1;       // forward epilogue: group 1 posted (m, l) of its rows
+  uint64_t* ep_b = ep_a + 1;          // forward epilogue: group 0 posted the combination factors
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Ly::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Ly::kMisc + 4);
   unsigned long long* wcyc = reinterpret_cast<unsigned long long*>(sm + Ly::kWaitCyc);
   const long long kernel_t0 = clock64();
   TileMeta* metas = reinterpret_cast<TileMeta*>(sm + Ly::kMeta);
   const AttnGeom& g = P.g;
-  constexpr uint32_t kAccCol = kDQ ? 384 : 256;  // O or dQ
+  constexpr uint32_t kAccCol = kDQ ? 384 : 256;  // O_A or dQ (O_B at 384)
   constexpr uint32_t kDPCol = 256;               // dQ: dP
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -161,21 +170,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_ready[i], 128);
+      mbar_init(&p_ready[i], 256);
     }
     for (int i = 0; i < Ly::kRK; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
-      mbar_init(&meta_free[i], 128);
+      mbar_init(&meta_free[i], 256);
     }
     for (int i = 0; i < Ly::kRV; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
     mbar_init(pv_done, 1);
-    mbar_init(o_free, 128);
+    mbar_init(o_free, 256);
+    mbar_init(ep_a, 128);
+    mbar_init(ep_b, 128);
     mbar_init(dp_full, 1);
-    mbar_init(dp_free, 128);
+    mbar_init(dp_free, 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -392,7 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescAcc = idesc_bf16(128, D, false, true);  // B (V or K) MN-major
       const uint32_t tAcc = tbase + kAccCol;
       int t = 0, it_local = 0;
-      bool have_prev = false;
+      bool have_prev = false, ob_init = false;
       int prev_t = 0, prev_nsrc = 0, prev_first = 0, prev_item = 0;
       // O += P V (forward) or dQ += dS K (dQ) for the previous tile
       auto issue_acc = [&]() -> bool {
@@ -406,9 +417,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bst = kDQ ? smem_u32(sm + Ly::kKRing + pk * Ly::kKBytes)
                                  : smem_u32(sm + Ly::kVRing + pv * Ly::kKBytes);
         const uint32_t pS = tbase + (uint32_t)((prev_t & 1) * 128);
-        for (int kk = 0; kk < 4 * prev_nsrc; ++kk) {
-          const uint64_t bd = sdesc_sw128(bst + kk * 2048, Ly::kRowBytes, 1024);
-          umma_ts(tAcc, pS + kk * 8, bd, kIdescAcc, (kk > 0 || !prev_first) ? 1u : 0u);
+        if (kDQ) {
+          // dS of slot g sits at S-buffer columns [64 g, 64 g + 32)
+          for (int kk = 0; kk < 4 * prev_nsrc; ++kk) {
+            const uint64_t bd = sdesc_sw128(bst + kk * 2048, Ly::kRowBytes, 1024);
+            umma_ts(tAcc, pS + (kk >> 2) * 64 + (kk & 3) * 8, bd, kIdescAcc, (kk > 0 || !prev_first) ? 1u : 0u);
+          }
+        } else {
+          // O_A += P_0 V_0 and O_B += P_1 V_1: two independent chains, interleaved
+          if (prev_first) ob_init = false;
+          for (int kk = 0; kk < 4; ++kk) {
+            umma_ts(tbase + 256, pS + kk * 8, sdesc_sw128(bst + kk * 2048, Ly::kRowBytes, 1024), kIdescAcc,
+                    (kk > 0 || !prev_first) ? 1u : 0u);
+            if (prev_nsrc == 2)
+              umma_ts(tbase + 384, pS + 64 + kk * 8, sdesc_sw128(bst + (kk + 4) * 2048, Ly::kRowBytes, 1024),
+                      kIdescAcc, (kk > 0 || ob_init) ? 1u : 0u);
+          }
+          if (prev_nsrc == 2) ob_init = true;
         }
         umma_commit(pv_done);
         if (kDQ)
@@ -469,10 +494,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ softmax / dS + epilogue
-    const int r = threadIdx.x - 128;  // row of the tile == TMEM lane
+    const int grp = (threadIdx.x - 128) >> 7;  // source slot handled by this warpgroup
+    const int r = (threadIdx.x - 128) & 127;   // row of the tile == TMEM lane
     const int seg = r >> 6, rr = r & 63;
-    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
-    const uint32_t tAcc = tbase + kAccCol + lane_off;
+    const uint32_t lane_off = (uint32_t)(((warp - 4) & 3) * 32) << 16;
+    // forward: this group's accumulator (O_A or O_B); dQ: its half of the dQ columns
+    const uint32_t tAcc = kDQ ? tbase + kAccCol + lane_off + grp * (D / 2) : tbase + 256 + 128 * grp + lane_off;
+    float* xch = reinterpret_cast<float*>(sm + Ly::kXchg);
     int t = 0, it_local = 0;
     for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
       const Item it = decode_item(g, id);
@@ -489,43 +517,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       do {
         const int sk = t % Ly::kRK;
         if (!wait_warp(&k_full[sk], (t / Ly::kRK) & 1, 20)) break;
-        // per 64-key source: warp-uniform masking mode (rows of a warp share a segment)
-        int mode[2];
-        uint32_t mw[4];
-#pragma unroll
-        for (int w = 0; w < 4; ++w) mw[w] = metas[sk].mask[seg][w];
-        {
-          const int diag = metas[sk].diag[seg];
-#pragma unroll
-          for (int j = 0; j < 2; ++j) mode[j] = src_mode(mw[2 * j], mw[2 * j + 1], diag == 64 * j);
-        }
+        // masking mode of this group's source for this row's segment (warp-uniform)
+        const uint32_t mw0 = metas[sk].mask[seg][2 * grp], mw1 = metas[sk].mask[seg][2 * grp + 1];
+        const int md = src_mode(mw0, mw1, metas[sk].diag[seg] == 64 * grp);
         last = metas[sk].last != 0;
         mbar_arrive(&meta_free[sk]);
         if (!wait_warp(&s_full[t & 1], (t >> 1) & 1, 21)) break;
         tc_fence_after();
-        const uint32_t tS = tbase + (uint32_t)((t & 1) * 128) + lane_off;
+        const uint32_t tS = tbase + (uint32_t)((t & 1) * 128) + lane_off + 64 * grp;  // this slot's scores
         const float c2 = P.scale_log2;
         const long long ph0 = clock64();
         long long ph_rescale = 0;
+        uint32_t pk[32];
         if (kDQ) {
           // ---- dS = P (dP - D), P = exp2(scale_log2 S - lse2) on active entries
           if (!wait_warp(dp_full, t & 1, 24)) break;
           tc_fence_after();
-#pragma unroll 1
-          for (int j = 0; j < 2; ++j) {
-            const int md = j ? mode[1] : mode[0];
-            uint32_t pk[32];
-            if (md == kSrcOff) {
+          if (md == kSrcOff) {
 #pragma unroll
-              for (int k = 0; k < 32; ++k) pk[k] = 0u;
+            for (int k = 0; k < 32; ++k) pk[k] = 0u;
+          } else {
+            uint32_t sv[64], dv[64];
+            tmem_ld32(tS, sv);
+            tmem_ld32(tS + 32, sv + 32);
+            tmem_ld32(tbase + kDPCol + lane_off + 64 * grp, dv);
+            tmem_ld32(tbase + kDPCol + lane_off + 64 * grp + 32, dv + 32);
+            tmem_ld_wait();
+            if (md == kSrcFull) {
+#pragma unroll
+              for (int k = 0; k < 32; ++k) {
+                const int c = 2 * k;
+                const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), c2, -lse2));
+                const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), c2, -lse2));
+                pk[k] = pack_bf16(p0 * (__uint_as_float(dv[c]) - Dr), p1 * (__uint_as_float(dv[c + 1]) - Dr));
+              }
             } else {
-              uint32_t sv[64], dv[64];
-              tmem_ld32(tS + 64 * j, sv);
-              tmem_ld32(tS + 64 * j + 32, sv + 32);
-              tmem_ld32(tbase + kDPCol + lane_off + 64 * j, dv);
-              tmem_ld32(tbase + kDPCol + lane_off + 64 * j + 32, dv + 32);
-              tmem_ld_wait();
-              const uint64_t act = active_bits(md, j ? mw[2] : mw[0], j ? mw[3] : mw[1], rr);
+              const uint64_t act = active_bits(md, mw0, mw1, rr);
 #pragma unroll
               for (int k = 0; k < 32; ++k) {
                 const int c = 2 * k;
@@ -535,85 +562,74 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[k] = pack_bf16(p0 * (__uint_as_float(dv[c]) - Dr), p1 * (__uint_as_float(dv[c + 1]) - Dr));
               }
             }
-            tmem_st16(tS + 32 * j, pk);
-            tmem_st16(tS + 32 * j + 16, pk + 16);
           }
           tc_fence_before();
           mbar_arrive(dp_free);
         } else {
-          // pass 1: row maximum of the raw scores (scale > 0 keeps the order)
-          float mx[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
-#pragma unroll 1
-          for (int j = 0; j < 2; ++j) {
-            const int md = j ? mode[1] : mode[0];
-            if (md == kSrcOff) continue;
-            uint32_t v[64];
-            tmem_ld32(tS + 64 * j, v);
-            tmem_ld32(tS + 64 * j + 32, v + 32);
+          uint32_t v[64];
+          uint64_t act;
+          float mraw = kNegInf;
+          if (md != kSrcOff) {
+            tmem_ld32(tS, v);
+            tmem_ld32(tS + 32, v + 32);
             tmem_ld_wait();
-            const uint64_t act = active_bits(md, j ? mw[2] : mw[0], j ? mw[3] : mw[1], rr);
+            act = active_bits(md, mw0, mw1, rr);
+            float mx[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
+            if (md == kSrcFull) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c)
-              mx[c & 3] = fmaxf(mx[c & 3], ((act >> c) & 1ull) ? __uint_as_float(v[c]) : kNegInf);
+              for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
+            } else {
+              // masked entries become -inf in place, so the exp pass needs no mask
+#pragma unroll
+              for (int c = 0; c < 64; ++c) {
+                if (!((act >> c) & 1ull)) v[c] = __float_as_uint(kNegInf);
+                mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
+              }
+            }
+            mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
           }
           if (lane == 0) atomicAdd(&wcyc[26], (unsigned long long)(clock64() - ph0));
-          const float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
           const float m_new = (mraw == kNegInf) ? m_ref : fmaxf(m_ref, mraw * c2);
-          // Rows whose maximum grew by more than the threshold rescale their
-          // running O after the previous PV landed.  The TMEM loads/stores are
-          // warp-collective, so the whole warp takes the branch when any row
-          // needs it (factor 1 for the others).
+          // Rows whose maximum grew by more than the threshold rescale this
+          // group's accumulator after the previous PV landed.  The TMEM
+          // loads/stores are warp-collective, so the whole warp takes the
+          // branch when any row needs it (factor 1 for the others).
           const bool need = m_ref != kNegInf && m_new > m_ref + kRescaleThreshold;
           if (__any_sync(0xffffffffu, need)) {
             ph_rescale = clock64();
             if (lane == 0) atomicAdd(&wcyc[29], 1ull << 40);  // count in the high bits
             if (!wait_warp(pv_done, (t - 1) & 1, 22)) break;
             tc_fence_after();
-            rescale_acc_row<D>(tAcc, need ? fast_exp2(m_ref - m_new) : 1.0f);
+            const float f = need ? fast_exp2(m_ref - m_new) : 1.0f;
+            rescale_acc_row<D>(tAcc, f);
             if (need) {
-              l *= fast_exp2(m_ref - m_new);
+              l *= f;
               m_ref = m_new;
             }
             ph_rescale = clock64() - ph_rescale;
             if (lane == 0) atomicAdd(&wcyc[29], (unsigned long long)ph_rescale);
           }
           if (m_ref == kNegInf) m_ref = m_new;
-          // pass 2: P = exp2(c2 x - m_ref) as packed bf16 into the first 64
-          // columns of the S buffer (each source's scores re-read from TMEM)
-          const float neg_m = (m_ref == kNegInf) ? 0.f : -m_ref;  // all x are -inf then
-          float ls[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-          for (int j = 0; j < 2; ++j) {
-            const int md = j ? mode[1] : mode[0];
-            uint32_t pk[32];
-            if (md == kSrcOff) {
+          if (md == kSrcOff) {
 #pragma unroll
-              for (int k = 0; k < 32; ++k) pk[k] = 0u;
-            } else {
-              uint32_t v[64];
-              tmem_ld32(tS + 64 * j, v);
-              tmem_ld32(tS + 64 * j + 32, v + 32);
-              tmem_ld_wait();
-              const uint64_t act = active_bits(md, j ? mw[2] : mw[0], j ? mw[3] : mw[1], rr);
+            for (int k = 0; k < 32; ++k) pk[k] = 0u;
+          } else {
+            const float neg_m = -m_ref;
+            float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-              for (int k = 0; k < 32; ++k) {
-                const int c = 2 * k;
-                const float x0 = ((act >> c) & 1ull) ? __uint_as_float(v[c]) : kNegInf;
-                const float x1 = ((act >> (c + 1)) & 1ull) ? __uint_as_float(v[c + 1]) : kNegInf;
-                const float p0 = fast_exp2(fmaf(x0, c2, neg_m));
-                const float p1 = fast_exp2(fmaf(x1, c2, neg_m));
-                ls[k & 3] += p0 + p1;
-                pk[k] = pack_bf16(p0, p1);
-              }
+            for (int k = 0; k < 32; ++k) {
+              const int c = 2 * k;
+              const float p0 = fast_exp2(fmaf(__uint_as_float(v[c]), c2, neg_m));
+              const float p1 = fast_exp2(fmaf(__uint_as_float(v[c + 1]), c2, neg_m));
+              ls[k & 3] += p0 + p1;
+              pk[k] = pack_bf16(p0, p1);
             }
-            // P of source j goes to packed columns [32 j, 32 j + 32): the raw
-            // scores there (columns of source 0) were consumed in pass 2 for
-            // j = 0 before this store of j = 1, and in pass 1 otherwise
-            tmem_st16(tS + 32 * j, pk);
-            tmem_st16(tS + 32 * j + 16, pk + 16);
+            l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
           }
-          l += (ls[0] + ls[1]) + (ls[2] + ls[3]);
         }
+        // P (or dS) of this slot over the first 32 columns of its scores
+        tmem_st16(tS, pk);
+        tmem_st16(tS + 16, pk + 16);
         const long long ph1 = clock64();
         tmem_st_wait();
         if (lane == 0) {
@@ -630,23 +646,71 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_warp(pv_done, (t - 1) & 1, 25)) break;
           if (!wait_warp(pv_done, t & 1, 23)) break;
           tc_fence_after();
-          const float mult = kDQ ? P.scale : ((l > 0.f) ? 1.0f / l : 0.f);
           __nv_bfloat16* orow = P.out + ((size_t)tok * g.Hq + h) * D;
-          for (int c0 = 0; c0 < D; c0 += 16) {
-            uint32_t o[16];
-            tmem_ld16(tAcc + c0, o);
-            tmem_ld_wait();
-            uint32_t pk[8];
-            for (int k = 0; k < 8; ++k)
-              pk[k] = pack_bf16(__uint_as_float(o[2 * k]) * mult, __uint_as_float(o[2 * k + 1]) * mult);
-            if (valid) {
-              uint4* dst = reinterpret_cast<uint4*>(orow + c0);
-              dst[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              dst[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+          if (kDQ) {
+            // this group's half of the dQ columns
+            for (int c0 = 0; c0 < D / 2; c0 += 16) {
+              uint32_t o[16];
+              tmem_ld16(tAcc + c0, o);
+              tmem_ld_wait();
+              uint32_t q8[8];
+              for (int k = 0; k < 8; ++k)
+                q8[k] = pack_bf16(__uint_as_float(o[2 * k]) * P.scale, __uint_as_float(o[2 * k + 1]) * P.scale);
+              if (valid) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + grp * (D / 2) + c0);
+                dst[0] = make_uint4(q8[0], q8[1], q8[2], q8[3]);
+                dst[1] = make_uint4(q8[4], q8[5], q8[6], q8[7]);
+              }
+            }
+          } else {
+            // combine the two groups' partial softmax states of this row:
+            // group 1 posts (m, l); group 0 forms the normalised factors and LSE
+            float ca, cb;
+            if (grp == 1) {
+              xch[2 * r] = m_ref;
+              xch[2 * r + 1] = l;
+              mbar_arrive(ep_a);
+              if (!wait_warp(ep_b, it_local & 1, 5)) break;
+              ca = xch[2 * r];
+              cb = xch[2 * r + 1];
+            } else {
+              if (!wait_warp(ep_a, it_local & 1, 6)) break;
+              const float mb = xch[2 * r], lb = xch[2 * r + 1];
+              const float m = fmaxf(m_ref, mb);
+              const float fa = (l > 0.f) ? fast_exp2(m_ref - m) : 0.f;
+              const float fb = (lb > 0.f) ? fast_exp2(mb - m) : 0.f;
+              const float ltot = l * fa + lb * fb;
+              const float inv = ltot > 0.f ? 1.0f / ltot : 0.f;
+              ca = fa * inv;
+              cb = fb * inv;
+              if (valid)
+                P.lse[(size_t)h * g.L + tok] = ltot > 0.f ? (m + __log2f(ltot)) * 0.69314718055994531f : kNegInf;
+              xch[2 * r] = ca;
+              xch[2 * r + 1] = cb;
+              mbar_arrive(ep_b);
+            }
+            // this group's half of the output columns from both accumulators
+            const uint32_t tA = tbase + 256 + lane_off + grp * (D / 2), tB = tA + 128;
+            for (int c0 = 0; c0 < D / 2; c0 += 16) {
+              uint32_t oa[16], ob[16];
+              tmem_ld16(tA + c0, oa);
+              tmem_ld16(tB + c0, ob);
+              tmem_ld_wait();
+              uint32_t q8[8];
+              for (int k = 0; k < 8; ++k) {
+                // an accumulator with no contribution (factor 0) may hold stale data
+                const float a0 = ca * __uint_as_float(oa[2 * k]) + (cb != 0.f ? cb * __uint_as_float(ob[2 * k]) : 0.f);
+                const float a1 =
+                    ca * __uint_as_float(oa[2 * k + 1]) + (cb != 0.f ? cb * __uint_as_float(ob[2 * k + 1]) : 0.f);
+                q8[k] = pack_bf16(a0, a1);
+              }
+              if (valid) {
+                uint4* dst = reinterpret_cast<uint4*>(orow + grp * (D / 2) + c0);
+                dst[0] = make_uint4(q8[0], q8[1], q8[2], q8[3]);
+                dst[1] = make_uint4(q8[4], q8[5], q8[6], q8[7]);
+              }
             }
           }
-          if (!kDQ && valid)
-            P.lse[(size_t)h * g.L + tok] = (l > 0.f) ? (m_ref + __log2f(l)) * 0.69314718055994531f : kNegInf;
           tc_fence_before();
           mbar_arrive(o_free);
           if (lane == 0) atomicAdd(&wcyc[30], (unsigned long long)(clock64() - pe0));
