@@ -6,7 +6,7 @@ device memory and the current stream.  There is no fallback: if the shared
 library is missing or fails to load, every call raises.
 
 Entry points mirror the C names: ``vs_workspace_bytes``, ``vs_rope``,
-``vs_index_build``, ``vs_sparse_attn_fwd``, ``vs_sparse_attn_bwd``,
+``vs_index_build``, ``vs_index_build_noalloc``, ``vs_sparse_attn_fwd``, ``vs_sparse_attn_bwd``,
 ``vs_device_status``, ``vs_status_string``.
 """
 from __future__ import annotations
@@ -23,7 +23,10 @@ VS_OP_INDEX, VS_OP_FWD, VS_OP_BWD, VS_OP_ROPE = range(4)
 
 #: every symbol the header declares
 EXPORTED = ("vs_workspace_bytes", "vs_status_string", "vs_rope", "vs_index_build",
-            "vs_sparse_attn_fwd", "vs_sparse_attn_bwd", "vs_device_status")
+            "vs_index_build_noalloc", "vs_sparse_attn_fwd", "vs_sparse_attn_bwd", "vs_device_status")
+
+#: size of the static scratch behind vs_index_build_noalloc (VS_INDEX_NOALLOC_SCRATCH_BYTES)
+INDEX_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class VSError(RuntimeError):
@@ -67,10 +70,12 @@ def lib() -> ctypes.CDLL:
         L.vs_status_string.restype = ctypes.c_char_p
         L.vs_rope.argtypes = [P, i32, VP, VP, i32, VP]
         L.vs_index_build.argtypes = [P, VP, VP, I, VP, SZ, VP]
+        L.vs_index_build_noalloc.argtypes = [P, VP, VP, I, VP]
         L.vs_sparse_attn_fwd.argtypes = [P, I, VP, VP, VP, VP, VP, VP, SZ, VP]
         L.vs_sparse_attn_bwd.argtypes = [P, I, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]
         L.vs_device_status.argtypes = [VP, VP]
-        for f in ("vs_rope", "vs_index_build", "vs_sparse_attn_fwd", "vs_sparse_attn_bwd", "vs_device_status"):
+        for f in ("vs_rope", "vs_index_build", "vs_index_build_noalloc", "vs_sparse_attn_fwd",
+                  "vs_sparse_attn_bwd", "vs_device_status"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -150,6 +155,14 @@ def vs_index_build(p: vs_params, Q, K, index: IndexBuffers, ws, stream=None):
     ix = index.c()
     _check(lib().vs_index_build(ctypes.byref(p), _ptr(Q), _ptr(K), ctypes.byref(ix), _ptr(ws),
                                 ws.numel(), _stream(stream)), "vs_index_build")
+
+
+def vs_index_build_noalloc(p: vs_params, Q, K, index: IndexBuffers, stream=None):
+    """vs_index_build on the library's static scratch: for callers that cannot
+    hand over a workspace (see ``vs_index_build_noalloc`` in include/vs.h)."""
+    ix = index.c()
+    _check(lib().vs_index_build_noalloc(ctypes.byref(p), _ptr(Q), _ptr(K), ctypes.byref(ix), _stream(stream)),
+           "vs_index_build_noalloc")
 
 
 def vs_sparse_attn_fwd(p: vs_params, index: IndexBuffers, Q, K, V, O, lse, ws, stream=None):

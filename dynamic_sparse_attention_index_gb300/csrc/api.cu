@@ -2,6 +2,7 @@
 // validation (host, before any launch), workspace layout, and launches.
 #include <cmath>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -187,6 +188,65 @@ vs_status vs_index_build(const vs_params* p, const void* Q, const void* K, const
   if (launch_index_scores(a, s) != cudaSuccess) return VS_ERR_CUDA;
   if (launch_select(a, s) != cudaSuccess) return VS_ERR_CUDA;
   return VS_OK;
+}
+
+// ---------------------------------------------------------------------------
+// vs_index_build_noalloc: vs_index_build with library-owned scratch.
+//
+// Every other entry point takes its scratch from the caller.  This one is for
+// callers that cannot provide it: code running where a device allocation is
+// not allowed or not affordable at call time, e.g. a service whose caching
+// allocator is already at its memory cap, a host program whose device
+// footprint is planned once when the library loads, or a pipeline that must
+// not stall (cudaMalloc and cudaFree synchronise the whole device).  Its
+// scratch is a fixed-size array in the library's own device image, so no call
+// allocates or frees anything.
+}  // extern "C"
+
+namespace {
+
+// Holds the same layout as vs_index_build's caller workspace; problems whose
+// workspace is larger are rejected.  Only the status block at its head must
+// start at zero, and each call clears it on its stream first (inside
+// vs_index_build); every other byte is written before it is read, so what an
+// earlier call left behind does not matter.
+static __device__ __align__(256) unsigned char g_index_scratch[VS_INDEX_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kMaxDevices];  // device address of g_index_scratch, per device
+
+// Host code sees g_index_scratch only as a host-side shadow symbol, never as
+// a device address: the address is resolved with cudaGetSymbolAddress, once
+// per device with that device current (on its first use there), and cached.
+vs_status noalloc_scratch(void** out) {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return VS_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return VS_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_addr[dev]) {
+    void* a = nullptr;
+    if (cudaGetSymbolAddress(&a, g_index_scratch) != cudaSuccess || !a) return VS_ERR_CUDA;
+    g_scratch_addr[dev] = a;
+  }
+  *out = g_scratch_addr[dev];
+  return VS_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+vs_status vs_index_build_noalloc(const vs_params* p, const void* Q, const void* K, const vs_index* out,
+                                 void* stream) {
+  vs_status st = check_index_params(p);
+  if (st != VS_OK) return st;
+  if (!Q || !K || !aligned16(Q) || !aligned16(K)) return VS_ERR_INVALID_ARG;
+  if ((st = check_index_ptrs(out)) != VS_OK) return st;
+  if (index_ws(*p).total > (size_t)VS_INDEX_NOALLOC_SCRATCH_BYTES) return VS_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if ((st = noalloc_scratch(&scratch)) != VS_OK) return st;
+  return vs_index_build(p, Q, K, out, scratch, (size_t)VS_INDEX_NOALLOC_SCRATCH_BYTES, stream);
 }
 
 vs_status vs_sparse_attn_fwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,

@@ -27,8 +27,9 @@
  *     so for a bounded time; on timeout they record VS_ERR_TIMEOUT in the
  *     workspace status word (first 16 bytes of `ws`) and return, which
  *     vs_device_status() reports after the stream is synchronised.
- *   - No global state: calls on different streams with different workspaces
- *     are independent.
+ *   - No global state, except the static scratch of vs_index_build_noalloc
+ *     (see there): other calls on different streams with different
+ *     workspaces are independent.
  */
 #ifndef VS_H_
 #define VS_H_
@@ -117,6 +118,38 @@ VS_API vs_status vs_rope(const vs_params* p, int32_t H, const void* x, void* y, 
  */
 VS_API vs_status vs_index_build(const vs_params* p, const void* Q, const void* K, const vs_index* out, void* ws,
                          size_t ws_bytes, void* stream);
+
+/*
+ * Variant of vs_index_build that allocates nothing and takes no workspace.
+ * The paper has no counterpart: this call exists for callers that cannot
+ * give the library scratch memory at call time (e.g. code under an allocator
+ * that is at its cap, code whose device footprint is fixed when the library
+ * loads, or a pipeline that must not stall on cudaMalloc / cudaFree, which
+ * synchronise the device).  Its scratch is one static device array of
+ * VS_INDEX_NOALLOC_SCRATCH_BYTES (8 MiB) inside the library image, held by
+ * every GPU that loads the library until the process exits; the call never
+ * allocates or frees device memory.
+ *   - Size limit: problems with vs_workspace_bytes(p, VS_OP_INDEX) above
+ *     VS_INDEX_NOALLOC_SCRATCH_BYTES are rejected with VS_ERR_WORKSPACE
+ *     before anything is launched (e.g. L = 32768, Hq = 16, last_q = 64
+ *     needs 5 MiB and fits; L = 131072 with 16 heads does not).
+ *   - Set-up: the first call on a device resolves the array's address on
+ *     that device (which must be current) and caches it; make that first
+ *     call before any stream capture begins.
+ *   - Zeroing: the array keeps what the last call left in it.  Only the
+ *     status block at its head must start at zero, and every call clears it
+ *     on `stream` before its kernels run.
+ *   - Concurrency: all calls on one device share the one array.  Calls whose
+ *     executions overlap on the GPU (different streams without an ordering
+ *     between them, e.g. from several host threads) race on it and corrupt
+ *     each other's results: issue them on one stream or order them with
+ *     events.
+ * Results, other arguments and other errors are exactly those of
+ * vs_index_build.
+ */
+#define VS_INDEX_NOALLOC_SCRATCH_BYTES (8u << 20)
+VS_API vs_status vs_index_build_noalloc(const vs_params* p, const void* Q, const void* K, const vs_index* out,
+                                        void* stream);
 
 /*
  * Block-sparse causal attention forward over the active entries of `index`

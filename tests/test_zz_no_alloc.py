@@ -1,0 +1,83 @@
+"""vs_index_build_noalloc against vs_index_build.
+
+vs_index_build_noalloc serves callers that cannot hand the library a
+workspace (an allocator at its cap, a device footprint fixed at load time, a
+pipeline that must not stall on cudaMalloc): it runs the same kernels on a
+static scratch array inside the library.  Two calls are issued back to back on
+one stream with no synchronisation between them (different problems; the
+second without score outputs, so the scratch's own score arrays are used) and
+each result is compared with vs_index_build on the same inputs.  Index work is
+compared bit for bit, as everywhere in these tests.  The file sorts last, so
+a run that stops at the first failure has run every other test before it.
+"""
+import numpy as np
+import pytest
+
+import synth
+from _util import to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(vs, dev, wid, L, Hq, Hkv, density, scores):
+    w = synth.make_workload(wid, L=L, Hq=Hq, Hkv=Hkv, d=128)
+    p = vs.make_params(L, Hq, Hkv, 128, last_q=w.last_q, top_p=w.top_p, density=density)
+    Q, K = to_dev(w.q, dev), to_dev(w.k, dev)
+    return p, Q, K, vs.IndexBuffers.allocate(p, dev, scores=scores)
+
+
+def _host(ix):
+    names = ("v_idx", "v_cnt", "s_idx", "s_cnt", "v_score", "s_score", "active_entries")
+    return {k: getattr(ix, k).cpu().numpy() for k in names if getattr(ix, k) is not None}
+
+
+def _same(a, b):
+    assert set(a) == set(b)
+    assert np.array_equal(a["v_cnt"], b["v_cnt"]) and np.array_equal(a["s_cnt"], b["s_cnt"])
+    for h in range(len(a["v_cnt"])):
+        assert np.array_equal(a["v_idx"][h, :a["v_cnt"][h]], b["v_idx"][h, :b["v_cnt"][h]])
+        assert np.array_equal(a["s_idx"][h, :a["s_cnt"][h]], b["s_idx"][h, :b["s_cnt"][h]])
+    for k in ("v_score", "s_score", "active_entries"):
+        if k in a:
+            assert np.array_equal(a[k], b[k]), k
+
+
+def test_noalloc_two_calls_match_index_build():
+    import torch
+    import dynamic_sparse_attention_index_gb300 as vs
+    dev = torch.device("cuda:0")
+    problems = [
+        dict(wid=3, L=4096, Hq=8, Hkv=2, density=0.0, scores=True),      # top-p selection
+        dict(wid=1, L=32768, Hq=16, Hkv=2, density=0.05, scores=False),  # budget fill, near the size limit
+    ]
+    cases = [_inputs(vs, dev, **c) for c in problems]
+    for p, _, _, _ in cases:
+        assert vs.vs_workspace_bytes(p, vs.VS_OP_INDEX) <= vs.INDEX_NOALLOC_SCRATCH_BYTES
+    for p, Q, K, ix in cases:
+        vs.vs_index_build_noalloc(p, Q, K, ix)
+    torch.cuda.synchronize()
+    got = [_host(ix) for _, _, _, ix in cases]
+    for (p, Q, K, _), g in zip(cases, got):
+        ref = vs.IndexBuffers.allocate(p, dev, scores="v_score" in g)
+        ws = vs.workspace(p, vs.VS_OP_INDEX, dev)
+        vs.vs_index_build(p, Q, K, ref, ws)
+        torch.cuda.synchronize()
+        assert vs.vs_device_status(ws) == vs.VS_OK
+        _same(g, _host(ref))
+        assert (g["v_cnt"] > 0).any() and (g["s_cnt"] >= 1).all()
+
+
+def test_noalloc_rejects_problem_beyond_scratch():
+    import torch
+    import dynamic_sparse_attention_index_gb300 as vs
+    dev = torch.device("cuda:0")
+    p = vs.make_params(131072, 16, 2, 128, last_q=64)
+    assert vs.vs_workspace_bytes(p, vs.VS_OP_INDEX) > vs.INDEX_NOALLOC_SCRATCH_BYTES
+    # the size check comes before any launch: small placeholders stand in for Q, K and the outputs
+    Q = torch.zeros(64, dtype=torch.int32, device=dev)
+    ix = vs.IndexBuffers(*[torch.full((16,), -7, dtype=torch.int32, device=dev) for _ in range(4)])
+    with pytest.raises(vs.VSError) as e:
+        vs.vs_index_build_noalloc(p, Q, Q, ix)
+    assert e.value.code == vs.VS_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert all((t.cpu() == -7).all() for t in (ix.v_idx, ix.v_cnt, ix.s_idx, ix.s_cnt))
