@@ -29,8 +29,22 @@ def _nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
+STAMP = os.path.join(BUILD, "flags.txt")
+
+
+def _flags() -> list:
+    # VS_WAIT_PROFILE=1 compiles in the attention kernels' wait-cycle counters
+    return FLAGS + (["-DVS_WAIT_PROFILE=1"] if os.environ.get("VS_WAIT_PROFILE") == "1" else [])
+
+
 def _stale() -> bool:
     if not os.path.exists(LIB):
+        return True
+    try:
+        with open(STAMP) as f:
+            if f.read() != " ".join(_flags()):
+                return True
+    except OSError:
         return True
     t = os.path.getmtime(LIB)
     deps = glob.glob(os.path.join(CSRC, "*")) + glob.glob(os.path.join(ROOT, "include", "*.h"))
@@ -46,7 +60,7 @@ def build(verbose: bool = False, force: bool = False) -> str:
 
     def compile_one(src):
         obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *_flags(), "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
@@ -68,6 +82,8 @@ def build(verbose: bool = False, force: bool = False) -> str:
         os.remove(tmp)
         raise RuntimeError("unresolved library symbols:\n" + "\n".join(missing))
     os.replace(tmp, LIB)
+    with open(STAMP, "w") as f:
+        f.write(" ".join(_flags()))
     return LIB
 
 

@@ -222,9 +222,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   // TMEM: S[2] at 0, 64; dP[2] at 128, 192; dV^T at 256; dK^T at 320 (64 columns each)
   auto wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
     if (*abort_flag) return false;
-    const long long w0 = clock64();
+    const long long w0 = kWaitProfile ? clock64() : 0;
     const bool ok = mbar_wait(bar, parity, kWaitLimitNs);
-    if ((threadIdx.x & 31) == 0) atomicAdd(&wcyc[where & (kWaitSites - 1)], (unsigned long long)(clock64() - w0));
+    if (kWaitProfile && (threadIdx.x & 31) == 0)
+      atomicAdd(&wcyc[where & (kWaitSites - 1)], (unsigned long long)(clock64() - w0));
     if (ok) return true;
     *abort_flag = 1;
     report_timeout(P.status, where);
@@ -482,6 +483,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     kIdescSN64, kk > 0 ? 1u : 0u);
           }
           umma_commit(&sdp_full[t & 1]);
+          if (kWaitProfile) {
+            atomicAdd(&wcyc[16], 1ull);
+            atomicAdd(&wcyc[17], (unsigned long long)m.nsrc);
+            if (last) atomicAdd(&wcyc[18], 1ull);
+          }
           // the stationary keys are read only by S and dP: release them now
           if (last) umma_commit(kvs_empty);
           if (have_prev && !issue_acc()) break;
@@ -640,8 +646,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tbase, 512);
-  if (threadIdx.x < kWaitSites - 1 && wcyc[threadIdx.x]) atomicAdd(&P.status->wait_cycles[threadIdx.x], wcyc[threadIdx.x]);
-  if (threadIdx.x == kWaitSites - 1)
+  if (kWaitProfile && threadIdx.x < kWaitSites - 1 && wcyc[threadIdx.x])
+    atomicAdd(&P.status->wait_cycles[threadIdx.x], wcyc[threadIdx.x]);
+  if (kWaitProfile && threadIdx.x == kWaitSites - 1)
     atomicAdd(&P.status->wait_cycles[kWaitSites - 1], (unsigned long long)(clock64() - kernel_t0));
 }
 
