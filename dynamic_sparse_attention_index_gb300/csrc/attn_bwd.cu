@@ -549,12 +549,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tb + 128 + 32, dv + 32);
           tmem_ld_wait();
           if (mode == kSrcFull) {
+            const uint64_t cc = f2pack(c, c), ll = f2pack(-lse2, -lse2);
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-              const float p0 = fast_exp2(fmaf(__uint_as_float(sv[2 * k]), c, -lse2));
-              const float p1 = fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), c, -lse2));
+              float x0, x1, t0, t1;
+              ffma2(x0, x1, __uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1]), cc, ll);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
               pk[k] = pack_bf16(p0, p1);
-              dk[k] = pack_bf16(p0 * (__uint_as_float(dv[2 * k]) - Dr), p1 * (__uint_as_float(dv[2 * k + 1]) - Dr));
+              fadd2(t0, t1, __uint_as_float(dv[2 * k]), __uint_as_float(dv[2 * k + 1]), -Dr, -Dr);
+              fmul2(t0, t1, t0, t1, p0, p1);
+              dk[k] = pack_bf16(t0, t1);
             }
           } else {
             const uint64_t act = active_bits(mode, mw0, mw1, rr);

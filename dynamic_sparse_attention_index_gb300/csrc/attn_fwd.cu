@@ -263,12 +263,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int B = it.I[s] / W - kb / W;
         return B == 0 || band_kept(s ? bm1 : bm0, B);
       };
+      // Kept-band words of the two segments for bands 32 w .. 32 w + 31 up to
+      // the diagonal band Iw (band 0 forced); head-paired tiles only, where
+      // both segments share the query block.
+      const int Iw = it.I[0] / W;
+      auto band_words = [&](int w, uint32_t* u0, uint32_t* u1) {
+        *u0 = *u1 = 0u;
+        if (w * 32 > Iw) return;
+        uint32_t a = bm0[w], b = bm1[w];
+        const int top = Iw - w * 32;
+        if (top < 31) {
+          a &= (2u << top) - 1u;
+          b &= (2u << top) - 1u;
+        }
+        if (w == 0) {
+          a |= 1u;
+          b |= 1u;
+        }
+        *u0 = a;
+        *u1 = b;
+      };
       // ---- count the sources first so the final tile can be flagged
       int nslash = 0;
-      for (int kb0 = Itop; kb0 >= 0; kb0 -= 32) {
-        const int kb = kb0 - lane;
-        const bool a = slash_active(0, kb) || slash_active(1, kb);
-        nslash += __popc(__ballot_sync(0xffffffffu, a));
+      if (g.pair_heads) {
+        // band B >= 1 covers W key blocks, band 0 the blocks Iw W .. I
+        int cnt = 0;
+        for (int w0 = 0; w0 * 32 <= Iw; w0 += 32) {
+          uint32_t u0, u1;
+          band_words(w0 + lane, &u0, &u1);
+          cnt += __popc((u0 | u1) & (w0 + lane == 0 ? ~1u : ~0u));
+        }
+        nslash = __reduce_add_sync(0xffffffffu, cnt) * W + (it.I[0] - Iw * W + 1);
+      } else {
+        for (int kb0 = Itop; kb0 >= 0; kb0 -= 32) {
+          const int kb = kb0 - lane;
+          const bool a = slash_active(0, kb) || slash_active(1, kb);
+          nslash += __popc(__ballot_sync(0xffffffffu, a));
+        }
       }
       const int nv = P.vcnt[(size_t)it.vg * (g.nb + 1) + Itop];
       const int nchunks = (nv + 63) / 64;
@@ -342,8 +373,42 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       reset_masks();
 
-      // ---- slash sources: key blocks kb = Itop, Itop-1, ..., 0 (32 per step)
-      for (int kb0 = Itop; kb0 >= 0 && !*abort_flag; kb0 -= 32) {
+      // ---- slash sources: key blocks kb = Itop, Itop-1, ..., 0
+      auto push_slash = [&](int kbs, bool on0, bool on1) {
+        const int j = nsrc;
+        src_kind[j] = 0;
+        src_arg[j] = kbs;
+        const bool on[2] = {on0, on1};
+        for (int s = 0; s < 2; ++s) {
+          smask[s][2 * j] = on[s] ? 0xffffffffu : 0u;
+          smask[s][2 * j + 1] = on[s] ? 0xffffffffu : 0u;
+          if (on[s] && kbs == it.I[s]) sdiag[s] = 64 * j;
+        }
+        if (++nsrc == 2) emit();
+      };
+      if (g.pair_heads) {
+        // walk the kept bands in ascending order (key blocks descending),
+        // skipping empty bitmap words 32 at a time
+        for (int w0 = 0; w0 * 32 <= Iw && !*abort_flag; w0 += 32) {
+          uint32_t u0, u1;
+          band_words(w0 + lane, &u0, &u1);
+          uint32_t nz = __ballot_sync(0xffffffffu, (u0 | u1) != 0u);
+          while (nz) {
+            const int jw = __ffs(nz) - 1;
+            nz &= nz - 1;
+            const uint32_t a0 = __shfl_sync(0xffffffffu, u0, jw), a1 = __shfl_sync(0xffffffffu, u1, jw);
+            uint32_t u = a0 | a1;
+            while (u) {
+              const int bit = __ffs(u) - 1;
+              u &= u - 1;
+              const int B = (w0 + jw) * 32 + bit;
+              const int lo = (Iw - B) * W, hi = min(it.I[0], lo + W - 1);
+              for (int kbs = hi; kbs >= lo; --kbs) push_slash(kbs, (a0 >> bit) & 1u, (a1 >> bit) & 1u);
+            }
+          }
+        }
+      }
+      for (int kb0 = Itop; kb0 >= 0 && !*abort_flag && !g.pair_heads; kb0 -= 32) {
         const int kb = kb0 - lane;
         const uint32_t b0 = __ballot_sync(0xffffffffu, slash_active(0, kb));
         const uint32_t b1 = __ballot_sync(0xffffffffu, slash_active(1, kb));
@@ -351,17 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (u) {
           const int bit = __ffs(u) - 1;
           u &= u - 1;
-          const int kbs = kb0 - bit;
-          const int j = nsrc;
-          src_kind[j] = 0;
-          src_arg[j] = kbs;
-          for (int s = 0; s < 2; ++s) {
-            const bool on = (s ? (b1 >> bit) : (b0 >> bit)) & 1u;
-            smask[s][2 * j] = on ? 0xffffffffu : 0u;
-            smask[s][2 * j + 1] = on ? 0xffffffffu : 0u;
-            if (on && kbs == it.I[s]) sdiag[s] = 64 * j;
-          }
-          if (++nsrc == 2) emit();
+          push_slash(kb0 - bit, (b0 >> bit) & 1u, (b1 >> bit) & 1u);
         }
       }
       // ---- vertical sources: 64-entry chunks of the union list below block Itop
@@ -490,6 +545,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           prev_nsrc = m.nsrc;
           prev_first = m.first;
           prev_item = it_local;
+          // the row tile's epilogue waits for its last accumulate: issue it
+          // now rather than behind the next row tile's first S
+          if (last) {
+            if (!issue_acc()) break;
+            have_prev = false;
+          }
           ++t;
         } while (!last && !*abort_flag);
       }
@@ -550,12 +611,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tbase + kDPCol + lane_off + 64 * grp + 32, dv + 32);
             tmem_ld_wait();
             if (md == kSrcFull) {
+              const uint64_t cc = f2pack(c2, c2), ll = f2pack(-lse2, -lse2);
 #pragma unroll
               for (int k = 0; k < 32; ++k) {
-                const int c = 2 * k;
-                const float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), c2, -lse2));
-                const float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), c2, -lse2));
-                pk[k] = pack_bf16(p0 * (__uint_as_float(dv[c]) - Dr), p1 * (__uint_as_float(dv[c + 1]) - Dr));
+                float x0, x1, t0, t1;
+                ffma2(x0, x1, __uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1]), cc, ll);
+                const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+                fadd2(t0, t1, __uint_as_float(dv[2 * k]), __uint_as_float(dv[2 * k + 1]), -Dr, -Dr);
+                fmul2(t0, t1, t0, t1, p0, p1);
+                pk[k] = pack_bf16(t0, t1);
               }
             } else {
               const uint64_t act = active_bits(md, mw0, mw1, rr);
@@ -579,20 +643,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tS, v);
             tmem_ld32(tS + 32, v + 32);
             tmem_ld_wait();
-            act = active_bits(md, mw0, mw1, rr);
-            float mx[4] = {kNegInf, kNegInf, kNegInf, kNegInf};
-            if (md == kSrcFull) {
+            if (md != kSrcFull) {
+              // masked entries become -inf in place, so neither pass needs the mask
+              act = active_bits(md, mw0, mw1, rr);
 #pragma unroll
-              for (int c = 0; c < 64; ++c) mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
-            } else {
-              // masked entries become -inf in place, so the exp pass needs no mask
-#pragma unroll
-              for (int c = 0; c < 64; ++c) {
+              for (int c = 0; c < 64; ++c)
                 if (!((act >> c) & 1ull)) v[c] = __float_as_uint(kNegInf);
-                mx[c & 3] = fmaxf(mx[c & 3], __uint_as_float(v[c]));
-              }
             }
-            mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            mraw = row_max64(v);
           }
           if (kWaitProfile && lane == 0) atomicAdd(&wcyc[26], (unsigned long long)(clock64() - ph0));
           const float m_new = (mraw == kNegInf) ? m_ref : fmaxf(m_ref, mraw * c2);
@@ -620,14 +678,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < 32; ++k) pk[k] = 0u;
           } else {
-            const float neg_m = -m_ref;
+            const uint64_t cc = f2pack(c2, c2), mm = f2pack(-m_ref, -m_ref);
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
-              const int c = 2 * k;
-              const float p0 = fast_exp2(fmaf(__uint_as_float(v[c]), c2, neg_m));
-              const float p1 = fast_exp2(fmaf(__uint_as_float(v[c + 1]), c2, neg_m));
-              ls[k & 3] += p0 + p1;
+              float x0, x1;
+              ffma2(x0, x1, __uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]), cc, mm);
+              const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+              if (k & 1)
+                fadd2(ls[2], ls[3], ls[2], ls[3], p0, p1);
+              else
+                fadd2(ls[0], ls[1], ls[0], ls[1], p0, p1);
               pk[k] = pack_bf16(p0, p1);
             }
             l += (ls[0] + ls[1]) + (ls[2] + ls[3]);

@@ -181,6 +181,57 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// Packed fp32 pairs: sm_100's fp32 pipe executes fma / add / mul on two
+// lanes per instruction, halving the issue slots of elementwise softmax math.
+__device__ __forceinline__ uint64_t f2pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+// (d0, d1) = (a0, a1) * b + c, b and c packed pairs
+__device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, uint64_t b, uint64_t c) {
+  asm("{\n\t.reg .b64 t, u;\n\tmov.b64 t, {%2, %3};\n\tfma.rn.f32x2 u, t, %4, %5;\n\tmov.b64 {%0, %1}, u;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "l"(b), "l"(c));
+}
+// (d0, d1) = (a0, a1) + (b0, b1)
+__device__ __forceinline__ void fadd2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 t, u, v;\n\tmov.b64 t, {%2, %3};\n\tmov.b64 u, {%4, %5};\n\tadd.rn.f32x2 v, t, u;\n\t"
+      "mov.b64 {%0, %1}, v;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// (d0, d1) = (a0, a1) * (b0, b1)
+__device__ __forceinline__ void fmul2(float& d0, float& d1, float a0, float a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 t, u, v;\n\tmov.b64 t, {%2, %3};\n\tmov.b64 u, {%4, %5};\n\tmul.rn.f32x2 v, t, u;\n\t"
+      "mov.b64 {%0, %1}, v;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+// max of three (one instruction on sm_100)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// row maximum of 64 scores held as fp32 bit patterns
+__device__ __forceinline__ float row_max64(const uint32_t* v) {
+  float m0 = fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]), __uint_as_float(v[2]));
+  float m1 = fmax3(__uint_as_float(v[3]), __uint_as_float(v[4]), __uint_as_float(v[5]));
+  float m2 = fmax3(__uint_as_float(v[6]), __uint_as_float(v[7]), __uint_as_float(v[8]));
+  float m3 = fmax3(__uint_as_float(v[9]), __uint_as_float(v[10]), __uint_as_float(v[11]));
+#pragma unroll
+  for (int c = 12; c < 60; c += 8) {
+    m0 = fmax3(m0, __uint_as_float(v[c]), __uint_as_float(v[c + 1]));
+    m1 = fmax3(m1, __uint_as_float(v[c + 2]), __uint_as_float(v[c + 3]));
+    m2 = fmax3(m2, __uint_as_float(v[c + 4]), __uint_as_float(v[c + 5]));
+    m3 = fmax3(m3, __uint_as_float(v[c + 6]), __uint_as_float(v[c + 7]));
+  }
+  m0 = fmax3(m0, __uint_as_float(v[60]), __uint_as_float(v[61]));
+  m1 = fmax3(m1, __uint_as_float(v[62]), __uint_as_float(v[63]));
+  return fmax3(m0, m1, fmaxf(m2, m3));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
