@@ -435,45 +435,53 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kIdescSN64 = idesc_bf16(128, 64, false, false);
       constexpr uint32_t kIdescAcc = idesc_bf16(128, 64, true, true);  // M = d (A^T), N = 64 keys (B MN-major)
       const uint32_t kvs = smem_u32(sm + kKVs);
-      int t = 0, un = 0;
-      bool have_prev = false;
-      int prev_t = 0, prev_nsrc = 0, prev_first = 0, prev_last = 0, prev_un = 0;
-      auto issue_acc = [&]() -> bool {
-        if (!wait(&pds_ready[prev_t & 1], (prev_t >> 1) & 1, 10)) return false;
-        if (prev_first && prev_un > 0)
-          if (!wait(acc_free, (prev_un - 1) & 1, 11)) return false;
-        tc_fence_after();
-        const int st = prev_t % kStages;
-        const uint32_t qa = smem_u32(sm + kStage + st * kStageBytes);
-        const uint32_t oa = qa + 2 * kHalfRows128;
-        const uint32_t pb = smem_u32(sm + kPdS + (prev_t & 1) * kPdSBytes);
-        const uint32_t db = pb + 128 * 128;
-        for (int kk = 0; kk < 4 * prev_nsrc; ++kk) {
-          // rows kk*16 .. kk*16+15: A = dO^T / Q^T (MN-major, two 64-d chunks 16 KB apart)
-          const uint32_t acc = (kk > 0 || !prev_first) ? 1u : 0u;
-          umma_ss(tbase + 256, sdesc_sw128(oa + kk * 2048, kHalfRows128, 1024), sdesc_sw128(pb + kk * 2048, 8192, 1024),
-                  kIdescAcc, acc);
-          umma_ss(tbase + 320, sdesc_sw128(qa + kk * 2048, kHalfRows128, 1024), sdesc_sw128(db + kk * 2048, 8192, 1024),
-                  kIdescAcc, acc);
-        }
-        umma_commit(&st_empty[st]);
-        umma_commit(&pds_free[prev_t & 1]);
-        if (prev_last) umma_commit(acc_done);
-        return true;
+      // Two kinds of work, issued in whichever order they become ready:
+      // S / dP of tile ts (its Q / dO stage landed, fewer than two tiles in
+      // flight) and dV / dK of tile ta (its P / dS are in shared memory).
+      // Accumulating as soon as P / dS exist frees the tile's stage early, so
+      // the next load overlaps the wait for the following tile's data.
+      struct Pend {
+        int nsrc, first, last, un;
       };
-      for (int uid = blockIdx.x; uid < nunits && !*abort_flag; uid += gridDim.x, ++un) {
-        bool last = false;
-        do {
-          const int st = t % kStages;
-          if (!wait(&st_full[st], (t / kStages) & 1, 12)) break;
+      Pend pend[2] = {};
+      int ts = 0, ta = 0;
+      int uid = blockIdx.x, un = 0;
+      long long idle0 = clock64();
+      const long long idle_limit = (long long)(kWaitLimitNs * 21 / 10);
+      while (!*abort_flag) {
+        const bool more = uid < nunits;
+        if (!more && ta == ts) break;
+        bool progressed = false;
+        if (ta < ts && mbar_test_wait(&pds_ready[ta & 1], (ta >> 1) & 1)) {
+          const Pend q = pend[ta & 1];
+          if (q.first && q.un > 0 && !wait(acc_free, (q.un - 1) & 1, 11)) break;
+          tc_fence_after();
+          const int st = ta % kStages;
+          const uint32_t qa = smem_u32(sm + kStage + st * kStageBytes);
+          const uint32_t oa = qa + 2 * kHalfRows128;
+          const uint32_t pb = smem_u32(sm + kPdS + (ta & 1) * kPdSBytes);
+          const uint32_t db = pb + 128 * 128;
+          for (int kk = 0; kk < 4 * q.nsrc; ++kk) {
+            // rows kk*16 .. kk*16+15: A = dO^T / Q^T (MN-major, two 64-d chunks 16 KB apart)
+            const uint32_t acc = (kk > 0 || !q.first) ? 1u : 0u;
+            umma_ss(tbase + 256, sdesc_sw128(oa + kk * 2048, kHalfRows128, 1024),
+                    sdesc_sw128(pb + kk * 2048, 8192, 1024), kIdescAcc, acc);
+            umma_ss(tbase + 320, sdesc_sw128(qa + kk * 2048, kHalfRows128, 1024),
+                    sdesc_sw128(db + kk * 2048, 8192, 1024), kIdescAcc, acc);
+          }
+          umma_commit(&st_empty[st]);
+          umma_commit(&pds_free[ta & 1]);
+          if (q.last) umma_commit(acc_done);
+          ++ta;
+          progressed = true;
+        } else if (more && ts - ta < 2 && mbar_test_wait(&st_full[ts % kStages], (ts / kStages) & 1)) {
+          const int st = ts % kStages;
           const SrcMeta m = metas[st];
-          last = m.last != 0;
-          if (m.first)
-            if (!wait(kvs_full, un & 1, 13)) break;
+          if (m.first && !wait(kvs_full, un & 1, 13)) break;
           tc_fence_after();
           const uint32_t qa = smem_u32(sm + kStage + st * kStageBytes);
           const uint32_t oa = qa + 2 * kHalfRows128;
-          const uint32_t buf = (uint32_t)(t & 1) * 64;
+          const uint32_t buf = (uint32_t)(ts & 1) * 64;
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * kHalfRows128 + (kk & 3) * 32;
             const uint32_t koff = (kk >> 2) * 8192 + (kk & 3) * 32;
@@ -482,25 +490,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_ss(tbase + 128 + buf, sdesc_sw128(oa + off, 16, 1024), sdesc_sw128(kvs + 16384 + koff, 16, 1024),
                     kIdescSN64, kk > 0 ? 1u : 0u);
           }
-          umma_commit(&sdp_full[t & 1]);
+          umma_commit(&sdp_full[ts & 1]);
           if (kWaitProfile) {
             atomicAdd(&wcyc[16], 1ull);
             atomicAdd(&wcyc[17], (unsigned long long)m.nsrc);
-            if (last) atomicAdd(&wcyc[18], 1ull);
+            if (m.last) atomicAdd(&wcyc[18], 1ull);
           }
           // the stationary keys are read only by S and dP: release them now
-          if (last) umma_commit(kvs_empty);
-          if (have_prev && !issue_acc()) break;
-          have_prev = true;
-          prev_t = t;
-          prev_nsrc = m.nsrc;
-          prev_first = m.first;
-          prev_last = m.last;
-          prev_un = un;
-          ++t;
-        } while (!last && !*abort_flag);
+          if (m.last) umma_commit(kvs_empty);
+          pend[ts & 1] = Pend{m.nsrc, m.first, m.last, un};
+          ++ts;
+          if (m.last) {
+            uid += gridDim.x;
+            ++un;
+          }
+          progressed = true;
+        }
+        if (progressed) {
+          idle0 = clock64();
+        } else if (clock64() - idle0 > idle_limit) {
+          *abort_flag = 1;
+          report_timeout(P.status, 12);
+          break;
+        }
       }
-      if (have_prev && !*abort_flag) issue_acc();
     }
     // lanes 1..31 wait here for the issuing lane: the block-wide barrier
     // below is warp-aligned and must see the whole warp together
