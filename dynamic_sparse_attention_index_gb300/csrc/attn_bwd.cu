@@ -89,6 +89,9 @@ struct SrcMeta {
   int32_t diag[2];      // 1 if the source's rows are the diagonal block of the keys
   int32_t nsrc;
   int32_t first, last;
+  int32_t kv0, kv1;     // the unit's stationary keys: packed row (vertical) or (kv head, first key) (slash)
+  int32_t pad;
+  long long t_issue;    // wait profiling: clock when the stage's loads were issued
 };
 
 // shared memory plan (bytes, 1024-aligned)
@@ -99,10 +102,12 @@ constexpr int kStage = kKVs + kKVsBytes;
 constexpr int kStageBytes = 4 * kHalfRows128;  // Q (2 halves) + dO (2 halves)
 constexpr int kPdS = kStage + kStages * kStageBytes;
 constexpr int kPdSBytes = 2 * 128 * 128;        // P and dS: 128 rows x 64 keys bf16 each
+constexpr int kMQ = 8;  // tile metadata ring (planner -> loader, MMA, P / dS warps)
 constexpr int kMeta = kPdS + 2 * kPdSBytes;
-constexpr int kBars = kMeta + kStages * (int)sizeof(SrcMeta);
-// kvs_full, kvs_empty, st_full[S], st_empty[S], sdp_full[2], pds_ready[2], pds_free[2], acc_done, acc_free
-constexpr int kNumBars = 2 + 2 * kStages + 6 + 2;
+constexpr int kBars = kMeta + kMQ * (int)sizeof(SrcMeta);
+// kvs_full, kvs_empty, st_full[S], st_empty[S], sdp_full[2], pds_ready[2], pds_free[2], acc_done, acc_free,
+// mq_full[MQ], mq_empty[MQ]
+constexpr int kNumBars = 2 + 2 * kStages + 6 + 2 + 2 * kMQ;
 constexpr int kMisc = kBars + kNumBars * 8;
 constexpr int kWaitCyc = kMisc + 64;
 constexpr int kSmemBytes = kWaitCyc + kWaitSites * 8;
@@ -184,9 +189,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* pds_free = pds_ready + 2;
   uint64_t* acc_done = pds_free + 2;
   uint64_t* acc_free = acc_done + 1;
+  uint64_t* mq_full = acc_free + 1;
+  uint64_t* mq_empty = mq_full + kMQ;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc + 4);
-  SrcMeta* metas = reinterpret_cast<SrcMeta*>(sm + kMeta);
+  SrcMeta* mq = reinterpret_cast<SrcMeta*>(sm + kMeta);
   unsigned long long* wcyc = reinterpret_cast<unsigned long long*>(sm + kWaitCyc);
   const long long kernel_t0 = clock64();
   const AttnGeom& g = P.g;
@@ -207,6 +214,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     mbar_init(acc_done, 1);
     mbar_init(acc_free, 128);
+    for (int i = 0; i < kMQ; ++i) {
+      mbar_init(&mq_full[i], 1);
+      mbar_init(&mq_empty[i], 6);  // loader, MMA thread, four P / dS warps
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -222,9 +233,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // TMEM: S[2] at 0, 64; dP[2] at 128, 192; dV^T at 256; dK^T at 320 (64 columns each)
   auto wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
     if (*abort_flag) return false;
-    const long long w0 = kWaitProfile ? clock64() : 0;
+    const long long w0 = kWaitProfileKv ? clock64() : 0;
     const bool ok = mbar_wait(bar, parity, kWaitLimitNs);
-    if (kWaitProfile && (threadIdx.x & 31) == 0)
+    if (kWaitProfileKv && (threadIdx.x & 31) == 0)
       atomicAdd(&wcyc[where & (kWaitSites - 1)], (unsigned long long)(clock64() - w0));
     if (ok) return true;
     *abort_flag = 1;
@@ -252,14 +263,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (warp == 0) {
-    // ------------------------------------------------------------ producer
+    // ------------------------------------------------------------ planner
+    // Enumerates each unit's sources, two per tile, into the metadata ring;
+    // the loader warp issues the loads, so neither waits on the other's latency.
+    const long long prod0 = kWaitProfileKv ? clock64() : 0;
     const uint32_t* bm0 = P.inS;
     const uint32_t* bm1 = P.inS;
-    int t = 0, un = 0;
-    for (int uid = blockIdx.x; uid < nunits && !*abort_flag; uid += gridDim.x, ++un) {
+    int t = 0;
+    for (int uid = blockIdx.x; uid < nunits && !*abort_flag; uid += gridDim.x) {
       int kvh, kb = 0, vg = 0, chunk = 0, split = 0, R = 1, nv = 0;
       int hs[2] = {0, 0};
-      int nheads;
+      int nheads, kv0, kv1 = 0;
       if (P.vertical) {
         VUnit u;
         decode_vunit(g, P.vcnt, uid, &u);
@@ -280,75 +294,75 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         bm0 = P.inS + (size_t)hs[0] * g.nw;
         bm1 = P.inS + (size_t)hs[1] * g.nw;
+        kv0 = vg * g.L + chunk * 64;
       } else {
         // key blocks in ascending order (more causal rows first)
         kvh = uid / g.nb;
         kb = uid % g.nb;
         nheads = g.G;
+        kv0 = kvh;
+        kv1 = kb * kBlock;
       }
-      // stationary keys
-      if (lane == 0) {
-        if (wait(kvs_empty, (un & 1) ^ 1, 1)) {
-          mbar_arrive_expect_tx(kvs_full, kKVsBytes);
-          for (int hf = 0; hf < 2; ++hf) {
-            if (P.vertical) {
-              const int row = vg * g.L + chunk * 64;
-              tma_load_2d(sm + kKVs + hf * 8192, &mKp, kvs_full, hf * 64, row);
-              tma_load_2d(sm + kKVs + 16384 + hf * 8192, &mVp, kvs_full, hf * 64, row);
-            } else {
-              tma_load_3d(sm + kKVs + hf * 8192, &mK, kvs_full, hf * 64, kvh, kb * kBlock);
-              tma_load_3d(sm + kKVs + 16384 + hf * 8192, &mV, kvs_full, hf * 64, kvh, kb * kBlock);
-            }
-          }
-        }
-      }
-      __syncwarp();
 
-      // ---- the unit's sources, emitted two per tile
+      // ---- the unit's sources, two per tile (warp-uniform registers)
       int nsrc = 0;
       bool first = true;
-      SrcMeta pend;
+      int th[2] = {0, 0}, tI[2] = {0, 0}, tdg[2] = {0, 0};
+      uint32_t tm[2][2] = {{0u, 0u}, {0u, 0u}};
       auto emit = [&](bool last) {
-        const int st = t % kStages;
+        const int q = t % kMQ;
         bool ok = true;
-        if (lane == 0) ok = wait(&st_empty[st], ((t / kStages) & 1) ^ 1, 2);
+        if (lane == 0) ok = wait(&mq_empty[q], ((t / kMQ) & 1) ^ 1, 2);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (ok && lane == 0) {
-          pend.nsrc = nsrc;
-          pend.first = first ? 1 : 0;
-          pend.last = last ? 1 : 0;
-          metas[st] = pend;
-          uint8_t* qd = sm + kStage + st * kStageBytes;
-          uint8_t* od = qd + 2 * kHalfRows128;
-          mbar_arrive_expect_tx(&st_full[st], nsrc * 4 * 8192);
-          for (int j = 0; j < nsrc; ++j)
-            for (int hf = 0; hf < 2; ++hf) {
-              tma_load_3d(qd + hf * kHalfRows128 + j * 8192, &mQ, &st_full[st], hf * 64, pend.h[j], pend.I[j] * kBlock);
-              tma_load_3d(od + hf * kHalfRows128 + j * 8192, &mdO, &st_full[st], hf * 64, pend.h[j],
-                          pend.I[j] * kBlock);
-            }
+          SrcMeta& m = mq[q];
+          m.h[0] = th[0];
+          m.h[1] = th[1];
+          m.I[0] = tI[0];
+          m.I[1] = tI[1];
+          m.mask[0][0] = tm[0][0];
+          m.mask[0][1] = tm[0][1];
+          m.mask[1][0] = tm[1][0];
+          m.mask[1][1] = tm[1][1];
+          m.diag[0] = tdg[0];
+          m.diag[1] = tdg[1];
+          m.nsrc = nsrc;
+          m.first = first ? 1 : 0;
+          m.last = last ? 1 : 0;
+          m.kv0 = kv0;
+          m.kv1 = kv1;
+          mbar_arrive(&mq_full[q]);
         }
         __syncwarp();
         ++t;
         nsrc = 0;
         first = false;
       };
-      // Sources are produced in batches of up to 32 candidates per warp step;
-      // to flag the last tile, a source is emitted only once the next one is
-      // known (one-source lookahead).
+      auto put = [&](int h, int I, uint32_t m0, uint32_t m1, int diag) {
+        if (nsrc == 0) {
+          th[0] = h;
+          tI[0] = I;
+          tm[0][0] = m0;
+          tm[0][1] = m1;
+          tdg[0] = diag;
+        } else {
+          th[1] = h;
+          tI[1] = I;
+          tm[1][0] = m0;
+          tm[1][1] = m1;
+          tdg[1] = diag;
+        }
+        ++nsrc;
+      };
+      // to flag the last tile, a source is placed only once the next one is
+      // known (one-source lookahead)
       bool have_look = false;
-      int look_h = 0, look_I = 0;
+      int look_h = 0, look_I = 0, look_diag = 0;
       uint32_t look_m0 = 0, look_m1 = 0;
-      int look_diag = 0;
       auto push = [&](int h, int I, uint32_t m0, uint32_t m1, int diag) {
         if (have_look) {
-          const int j = nsrc;
-          pend.h[j] = look_h;
-          pend.I[j] = look_I;
-          pend.mask[j][0] = look_m0;
-          pend.mask[j][1] = look_m1;
-          pend.diag[j] = look_diag;
-          if (++nsrc == 2) emit(false);
+          put(look_h, look_I, look_m0, look_m1, look_diag);
+          if (nsrc == 2) emit(false);
         }
         have_look = true;
         look_h = h;
@@ -362,18 +376,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hl = 0; hl < nheads && !*abort_flag; ++hl) {
           const int h = kvh * g.G + hl;
           const int ns = P.s_cnt[h];
+          bool has0 = false;
           for (int j0 = 0; j0 < ns; j0 += 32) {
             const int j = j0 + lane;
             const int B = (j < ns) ? P.s_idx[(size_t)h * g.nbs + j] : -1;
+            if (j0 == 0) has0 = __shfl_sync(0xffffffffu, B, 0) == 0;
             // query blocks of band B for key block kb: I/W = kb/W + B, I >= kb
-            for (int k = 0; k < 32 && j0 + k < ns; ++k) {
-              const int Bk = __shfl_sync(0xffffffffu, B, k);
-              const int lo = max(kb, (kb / W + Bk) * W), hi = min(g.nb - 1, (kb / W + Bk) * W + W - 1);
-              for (int I = lo; I <= hi; ++I) push(h, I, 0xffffffffu, 0xffffffffu, I == kb ? 1 : 0);
+            const int lo = max(kb, (kb / W + B) * W), hi = min(g.nb - 1, (kb / W + B) * W + W - 1);
+            uint32_t live = __ballot_sync(0xffffffffu, B >= 0 && lo <= hi);
+            while (live) {
+              const int k = __ffs(live) - 1;
+              live &= live - 1;
+              const int lk = __shfl_sync(0xffffffffu, lo, k), hk = __shfl_sync(0xffffffffu, hi, k);
+              for (int I = lk; I <= hk; ++I) push(h, I, 0xffffffffu, 0xffffffffu, I == kb ? 1 : 0);
             }
           }
           // band 0 is always active even if the index omits it
-          bool has0 = ns > 0 && P.s_idx[(size_t)h * g.nbs] == 0;
           if (!has0) {
             const int lo = kb, hi = min(g.nb - 1, (kb / W) * W + W - 1);
             for (int I = lo; I <= hi; ++I) push(h, I, 0xffffffffu, 0xffffffffu, I == kb ? 1 : 0);
@@ -411,24 +429,63 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // flush: the lookahead source is the unit's last
       if (have_look) {
-        const int j = nsrc;
-        pend.h[j] = look_h;
-        pend.I[j] = look_I;
-        pend.mask[j][0] = look_m0;
-        pend.mask[j][1] = look_m1;
-        pend.diag[j] = look_diag;
-        ++nsrc;
+        put(look_h, look_I, look_m0, look_m1, look_diag);
         emit(true);
       } else {
         // a vertical unit whose split has no active rows: one empty tile
-        pend.h[0] = P.vertical ? hs[0] : kvh * g.G;
-        pend.I[0] = P.vertical ? g.nb - 1 : kb;
-        pend.mask[0][0] = pend.mask[0][1] = 0u;
-        pend.diag[0] = 0;
-        nsrc = 1;
+        put(P.vertical ? hs[0] : kvh * g.G, P.vertical ? g.nb - 1 : kb, 0u, 0u, 0);
         emit(true);
       }
     }
+    if (kWaitProfileKv && lane == 0) atomicAdd(&wcyc[28], (unsigned long long)(clock64() - prod0));
+  } else if (warp == 3) {
+    // ------------------------------------------------------------ loader
+    if (lane == 0) {
+      int t = 0, un = 0;
+      for (int uid = blockIdx.x; uid < nunits && !*abort_flag; uid += gridDim.x, ++un) {
+        bool last = false;
+        do {
+          const int q = t % kMQ;
+          if (!wait(&mq_full[q], (t / kMQ) & 1, 3)) break;
+          const int nsrc = mq[q].nsrc, kv0 = mq[q].kv0, kv1 = mq[q].kv1;
+          const int h0 = mq[q].h[0], h1 = mq[q].h[1], I0 = mq[q].I[0], I1 = mq[q].I[1];
+          const bool first = mq[q].first != 0;
+          last = mq[q].last != 0;
+          if (kWaitProfileKv) mq[q].t_issue = clock64();
+          mbar_arrive(&mq_empty[q]);
+          if (first) {
+            // stationary keys of the unit
+            if (!wait(kvs_empty, (un & 1) ^ 1, 1)) break;
+            mbar_arrive_expect_tx(kvs_full, kKVsBytes);
+            for (int hf = 0; hf < 2; ++hf) {
+              if (P.vertical) {
+                tma_load_2d(sm + kKVs + hf * 8192, &mKp, kvs_full, hf * 64, kv0);
+                tma_load_2d(sm + kKVs + 16384 + hf * 8192, &mVp, kvs_full, hf * 64, kv0);
+              } else {
+                tma_load_3d(sm + kKVs + hf * 8192, &mK, kvs_full, hf * 64, kv0, kv1);
+                tma_load_3d(sm + kKVs + 16384 + hf * 8192, &mV, kvs_full, hf * 64, kv0, kv1);
+              }
+            }
+          }
+          const int st = t % kStages;
+          if (!wait(&st_empty[st], ((t / kStages) & 1) ^ 1, 4)) break;
+          const long long e0 = kWaitProfileKv ? clock64() : 0;
+          uint8_t* qd = sm + kStage + st * kStageBytes;
+          uint8_t* od = qd + 2 * kHalfRows128;
+          mbar_arrive_expect_tx(&st_full[st], nsrc * 4 * 8192);
+          for (int j = 0; j < nsrc; ++j) {
+            const int h = j ? h1 : h0, row = (j ? I1 : I0) * kBlock;
+            for (int hf = 0; hf < 2; ++hf) {
+              tma_load_3d(qd + hf * kHalfRows128 + j * 8192, &mQ, &st_full[st], hf * 64, h, row);
+              tma_load_3d(od + hf * kHalfRows128 + j * 8192, &mdO, &st_full[st], hf * 64, h, row);
+            }
+          }
+          if (kWaitProfileKv) atomicAdd(&wcyc[27], (unsigned long long)(clock64() - e0));
+          ++t;
+        } while (!last && !*abort_flag);
+      }
+    }
+    __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
@@ -476,7 +533,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           progressed = true;
         } else if (more && ts - ta < 2 && mbar_test_wait(&st_full[ts % kStages], (ts / kStages) & 1)) {
           const int st = ts % kStages;
-          const SrcMeta m = metas[st];
+          const SrcMeta m = mq[ts % kMQ];
+          mbar_arrive(&mq_empty[ts % kMQ]);
+          if (kWaitProfileKv) atomicAdd(&wcyc[19], (unsigned long long)(clock64() - m.t_issue));
           if (m.first && !wait(kvs_full, un & 1, 13)) break;
           tc_fence_after();
           const uint32_t qa = smem_u32(sm + kStage + st * kStageBytes);
@@ -491,7 +550,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     kIdescSN64, kk > 0 ? 1u : 0u);
           }
           umma_commit(&sdp_full[ts & 1]);
-          if (kWaitProfile) {
+          if (kWaitProfileKv) {
             atomicAdd(&wcyc[16], 1ull);
             atomicAdd(&wcyc[17], (unsigned long long)m.nsrc);
             if (m.last) atomicAdd(&wcyc[18], 1ull);
@@ -527,21 +586,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int uid = blockIdx.x; uid < nunits && !*abort_flag; uid += gridDim.x, ++un) {
       bool last = false;
       do {
-        const int st = t % kStages;
-        if (!wait_warp(&st_full[st], (t / kStages) & 1, 20)) break;
-        const SrcMeta& mref = metas[st];
+        if (!wait_warp(&mq_full[t % kMQ], (t / kMQ) & 1, 20)) break;
+        const SrcMeta& mref = mq[t % kMQ];
         const bool valid = src < mref.nsrc;
         const uint32_t mw0 = valid ? mref.mask[src][0] : 0u, mw1 = valid ? mref.mask[src][1] : 0u;
         const int diag = valid ? mref.diag[src] : 0;
         const int h = mref.h[valid ? src : 0];
         const int tok = mref.I[valid ? src : 0] * kBlock + rr;
         last = mref.last != 0;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mq_empty[t % kMQ]);
         float lse2 = 0.f, Dr = 0.f;
         if (valid) {
           lse2 = P.lse[(size_t)h * g.L + tok] * P.log2e;
           Dr = P.Dsum[(size_t)h * g.L + tok];
         }
         if (!wait_warp(&sdp_full[t & 1], (t >> 1) & 1, 21)) break;
+        const long long ph0 = kWaitProfileKv ? clock64() : 0;
         if (t >= 2 && !wait_warp(&pds_free[t & 1], ((t >> 1) - 1) & 1, 22)) break;
         tc_fence_after();
         const float c = P.scale * P.log2e;
@@ -595,6 +656,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&pds_ready[t & 1]);
+        if (kWaitProfileKv && lane == 0) atomicAdd(&wcyc[26], (unsigned long long)(clock64() - ph0));
         if (last) {
           // ---- epilogue: thread r holds dV^T[d = r][0..63] and dK^T[d = r][0..63]
           if (!wait_warp(acc_done, un & 1, 23)) break;
@@ -663,9 +725,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tbase, 512);
-  if (kWaitProfile && threadIdx.x < kWaitSites - 1 && wcyc[threadIdx.x])
+  if (kWaitProfileKv && threadIdx.x < kWaitSites - 1 && wcyc[threadIdx.x])
     atomicAdd(&P.status->wait_cycles[threadIdx.x], wcyc[threadIdx.x]);
-  if (kWaitProfile && threadIdx.x == kWaitSites - 1)
+  if (kWaitProfileKv && threadIdx.x == kWaitSites - 1)
     atomicAdd(&P.status->wait_cycles[kWaitSites - 1], (unsigned long long)(clock64() - kernel_t0));
 }
 

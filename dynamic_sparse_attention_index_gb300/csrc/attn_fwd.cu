@@ -202,9 +202,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   auto wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
     if (*abort_flag) return false;
-    const long long w0 = kWaitProfile ? clock64() : 0;
+    const long long w0 = kWaitProfileQm ? clock64() : 0;
     const bool ok = mbar_wait(bar, parity, kWaitLimitNs);
-    if (kWaitProfile && (threadIdx.x & 31) == 0)
+    if (kWaitProfileQm && (threadIdx.x & 31) == 0)
       atomicAdd(&wcyc[where & (kWaitSites - 1)], (unsigned long long)(clock64() - w0));
     if (ok) return true;
     *abort_flag = 1;
@@ -534,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_commit(&v_empty[sv]);  // dQ: V is read only by dP
           }
           if (last) umma_commit(&q_empty[m.qslot]);
-          if (kWaitProfile) {
+          if (kWaitProfileQm) {
             atomicAdd(&wcyc[16], 1ull);
             atomicAdd(&wcyc[17], (unsigned long long)m.nsrc);
             if (last) atomicAdd(&wcyc[18], 1ull);
@@ -652,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mraw = row_max64(v);
           }
-          if (kWaitProfile && lane == 0) atomicAdd(&wcyc[26], (unsigned long long)(clock64() - ph0));
+          if (kWaitProfileQm && lane == 0) atomicAdd(&wcyc[26], (unsigned long long)(clock64() - ph0));
           const float m_new = (mraw == kNegInf) ? m_ref : fmaxf(m_ref, mraw * c2);
           // Rows whose maximum grew by more than the threshold rescale this
           // group's accumulator after the previous PV landed.  The TMEM
@@ -661,7 +661,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const bool need = m_ref != kNegInf && m_new > m_ref + kRescaleThreshold;
           if (__any_sync(0xffffffffu, need)) {
             ph_rescale = clock64();
-            if (kWaitProfile && lane == 0) atomicAdd(&wcyc[29], 1ull << 40);  // count in the high bits
+            if (kWaitProfileQm && lane == 0) atomicAdd(&wcyc[29], 1ull << 40);  // count in the high bits
             if (!wait_warp(pv_done, (t - 1) & 1, 22)) break;
             tc_fence_after();
             const float f = need ? fast_exp2(m_ref - m_new) : 1.0f;
@@ -671,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               m_ref = m_new;
             }
             ph_rescale = clock64() - ph_rescale;
-            if (kWaitProfile && lane == 0) atomicAdd(&wcyc[29], (unsigned long long)ph_rescale);
+            if (kWaitProfileQm && lane == 0) atomicAdd(&wcyc[29], (unsigned long long)ph_rescale);
           }
           if (m_ref == kNegInf) m_ref = m_new;
           if (md == kSrcOff) {
@@ -699,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(tS + 16, pk + 16);
         const long long ph1 = clock64();
         tmem_st_wait();
-        if (kWaitProfile && lane == 0) {
+        if (kWaitProfileQm && lane == 0) {
           atomicAdd(&wcyc[27], (unsigned long long)(ph1 - ph0 - ph_rescale));
           atomicAdd(&wcyc[28], (unsigned long long)(clock64() - ph1));
         }
@@ -780,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_fence_before();
           mbar_arrive(o_free);
-          if (kWaitProfile && lane == 0) atomicAdd(&wcyc[30], (unsigned long long)(clock64() - pe0));
+          if (kWaitProfileQm && lane == 0) atomicAdd(&wcyc[30], (unsigned long long)(clock64() - pe0));
         }
         ++t;
       } while (!last && !*abort_flag);
@@ -791,9 +791,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tbase, 512);
-  if (kWaitProfile && threadIdx.x < kWaitSites - 1 && wcyc[threadIdx.x])
+  if (kWaitProfileQm && threadIdx.x < kWaitSites - 1 && wcyc[threadIdx.x])
     atomicAdd(&P.status->wait_cycles[threadIdx.x], wcyc[threadIdx.x]);
-  if (kWaitProfile && threadIdx.x == kWaitSites - 1)
+  if (kWaitProfileQm && threadIdx.x == kWaitSites - 1)
     atomicAdd(&P.status->wait_cycles[kWaitSites - 1], (unsigned long long)(clock64() - kernel_t0));
 }
 

@@ -13,12 +13,14 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull; // bounded in-kernel waits: 2 s
 constexpr int kMaxL = 1 << 20;                   // supported sequence length ceiling
 
 // Per-site wait-cycle and phase counters of the attention kernels are built
-// only with -DVS_WAIT_PROFILE=1 (a pipeline-balance diagnostic); the default
-// build leaves the wait_cycles array of the status block at zero.
+// only with -DVS_WAIT_PROFILE=n (a pipeline-balance diagnostic: 1 all
+// attention kernels, 2 the dK/dV kernel, 3 the query-major kernel); the
+// default build leaves the wait_cycles array of the status block at zero.
 #ifndef VS_WAIT_PROFILE
 #define VS_WAIT_PROFILE 0
 #endif
-constexpr bool kWaitProfile = VS_WAIT_PROFILE != 0;
+constexpr bool kWaitProfileKv = VS_WAIT_PROFILE == 1 || VS_WAIT_PROFILE == 2;
+constexpr bool kWaitProfileQm = VS_WAIT_PROFILE == 1 || VS_WAIT_PROFILE == 3;
 
 // Device-side status block (first bytes of every workspace).
 constexpr int kWaitSites = 32;
