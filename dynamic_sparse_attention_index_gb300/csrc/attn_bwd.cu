@@ -32,7 +32,7 @@ cudaError_t launch_attn_dq(const vs_params& p, const AttnGeom& g, const PrepPtrs
 
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kStages = 2;
 constexpr int kMaxSplits = 32;
 
@@ -209,14 +209,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sdp_full[i], 1);
-      mbar_init(&pds_ready[i], 128);
+      mbar_init(&pds_ready[i], 256);
       mbar_init(&pds_free[i], 1);
     }
     mbar_init(acc_done, 1);
-    mbar_init(acc_free, 128);
+    mbar_init(acc_free, 256);
     for (int i = 0; i < kMQ; ++i) {
       mbar_init(&mq_full[i], 1);
-      mbar_init(&mq_empty[i], 6);  // loader, MMA thread, four P / dS warps
+      mbar_init(&mq_empty[i], 10);  // loader, MMA thread, eight P / dS warps
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -509,6 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool more = uid < nunits;
         if (!more && ta == ts) break;
         bool progressed = false;
+        const long long i0 = kWaitProfileKv ? clock64() : 0;
         if (ta < ts && mbar_test_wait(&pds_ready[ta & 1], (ta >> 1) & 1)) {
           const Pend q = pend[ta & 1];
           if (q.first && q.un > 0 && !wait(acc_free, (q.un - 1) & 1, 11)) break;
@@ -531,6 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (q.last) umma_commit(acc_done);
           ++ta;
           progressed = true;
+          if (kWaitProfileKv) atomicAdd(&wcyc[25], (unsigned long long)(clock64() - i0));
         } else if (more && ts - ta < 2 && mbar_test_wait(&st_full[ts % kStages], (ts / kStages) & 1)) {
           const int st = ts % kStages;
           const SrcMeta m = mq[ts % kMQ];
@@ -564,6 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++un;
           }
           progressed = true;
+          if (kWaitProfileKv) atomicAdd(&wcyc[24], (unsigned long long)(clock64() - i0));
         }
         if (progressed) {
           idle0 = clock64();
@@ -579,9 +582,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ P / dS, epilogue
-    const int r = threadIdx.x - 128;
+    // Two warpgroups: group grp owns key columns [32 grp, 32 grp + 32) of every
+    // row; thread r of a group owns row r (TMEM lane r).
+    const int grp = (threadIdx.x - 128) >> 7;
+    const int r = (threadIdx.x - 128) & 127;
     const int src = r >> 6, rr = r & 63;
-    const uint32_t lane_off = (uint32_t)((warp - 4) * 32) << 16;
+    const uint32_t lane_off = (uint32_t)(((warp - 4) & 3) * 32) << 16;
+    const uint32_t col0 = (uint32_t)(32 * grp);
     int t = 0, un = 0;
     for (int uid = blockIdx.x; uid < nunits && !*abort_flag; uid += gridDim.x, ++un) {
       bool last = false;
@@ -608,24 +615,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c = P.scale * P.log2e;
         uint8_t* pbuf = sm + kPdS + (t & 1) * kPdSBytes;
         uint8_t* dbuf = pbuf + 128 * 128;
-        // warp-uniform masking mode of this row's source for the 64 keys
+        // warp-uniform masking mode of this row's source for the 64 keys,
+        // then this group's 32 of them
         const int mode = src_mode(mw0, mw1, diag != 0);
-        uint32_t pk[32], dk[32];
+        const uint32_t act = (uint32_t)(active_bits(mode, mw0, mw1, rr) >> col0);
+        uint32_t pk[16], dk[16];
         if (mode == kSrcOff) {
 #pragma unroll
-          for (int k = 0; k < 32; ++k) pk[k] = dk[k] = 0u;
+          for (int k = 0; k < 16; ++k) pk[k] = dk[k] = 0u;
         } else {
-          uint32_t sv[64], dv[64];
-          const uint32_t tb = tbase + (uint32_t)((t & 1) * 64) + lane_off;
+          uint32_t sv[32], dv[32];
+          const uint32_t tb = tbase + (uint32_t)((t & 1) * 64) + lane_off + col0;
           tmem_ld32(tb, sv);
-          tmem_ld32(tb + 32, sv + 32);
           tmem_ld32(tb + 128, dv);
-          tmem_ld32(tb + 128 + 32, dv + 32);
           tmem_ld_wait();
-          if (mode == kSrcFull) {
-            const uint64_t cc = f2pack(c, c), ll = f2pack(-lse2, -lse2);
+          const uint64_t cc = f2pack(c, c), ll = f2pack(-lse2, -lse2);
+          if (mode == kSrcFull || act == 0xffffffffu) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
+            for (int k = 0; k < 16; ++k) {
               float x0, x1, t0, t1;
               ffma2(x0, x1, __uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1]), cc, ll);
               const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
@@ -635,38 +642,39 @@ __global__ void __launch_bounds__(kThreads, 1)
               dk[k] = pack_bf16(t0, t1);
             }
           } else {
-            const uint64_t act = active_bits(mode, mw0, mw1, rr);
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-              const float p0 = ((act >> (2 * k)) & 1ull) ? fast_exp2(fmaf(__uint_as_float(sv[2 * k]), c, -lse2)) : 0.f;
-              const float p1 =
-                  ((act >> (2 * k + 1)) & 1ull) ? fast_exp2(fmaf(__uint_as_float(sv[2 * k + 1]), c, -lse2)) : 0.f;
+            for (int k = 0; k < 16; ++k) {
+              float x0, x1, t0, t1;
+              ffma2(x0, x1, __uint_as_float(sv[2 * k]), __uint_as_float(sv[2 * k + 1]), cc, ll);
+              const float p0 = ((act >> (2 * k)) & 1u) ? fast_exp2(x0) : 0.f;
+              const float p1 = ((act >> (2 * k + 1)) & 1u) ? fast_exp2(x1) : 0.f;
               pk[k] = pack_bf16(p0, p1);
-              dk[k] = pack_bf16(p0 * (__uint_as_float(dv[2 * k]) - Dr), p1 * (__uint_as_float(dv[2 * k + 1]) - Dr));
+              fadd2(t0, t1, __uint_as_float(dv[2 * k]), __uint_as_float(dv[2 * k + 1]), -Dr, -Dr);
+              fmul2(t0, t1, t0, t1, p0, p1);
+              dk[k] = pack_bf16(t0, t1);
             }
           }
         }
-        // row r of a 128-row x 64-key MN-major SW128 tile: 8 chunks of 16 B
+        // row r of a 128-row x 64-key MN-major SW128 tile: this group's 4 of its 8 chunks of 16 B
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
+        for (int qq = 0; qq < 4; ++qq) {
+          const int q = 4 * grp + qq;
           const int off = (r >> 3) * 1024 + (r & 7) * 128 + ((q ^ (r & 7)) * 16);
-          *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-          *reinterpret_cast<uint4*>(dbuf + off) = make_uint4(dk[4 * q], dk[4 * q + 1], dk[4 * q + 2], dk[4 * q + 3]);
+          *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pk[4 * qq], pk[4 * qq + 1], pk[4 * qq + 2], pk[4 * qq + 3]);
+          *reinterpret_cast<uint4*>(dbuf + off) = make_uint4(dk[4 * qq], dk[4 * qq + 1], dk[4 * qq + 2], dk[4 * qq + 3]);
         }
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(&pds_ready[t & 1]);
         if (kWaitProfileKv && lane == 0) atomicAdd(&wcyc[26], (unsigned long long)(clock64() - ph0));
         if (last) {
-          // ---- epilogue: thread r holds dV^T[d = r][0..63] and dK^T[d = r][0..63]
+          // ---- epilogue: thread r holds dV^T[d = r][keys of this group] and dK^T likewise
           if (!wait_warp(acc_done, un & 1, 23)) break;
           tc_fence_after();
           const int dcol = r;
-          uint32_t av[64], ak[64];
-          tmem_ld32(tbase + 256 + lane_off, av);
-          tmem_ld32(tbase + 256 + lane_off + 32, av + 32);
-          tmem_ld32(tbase + 320 + lane_off, ak);
-          tmem_ld32(tbase + 320 + lane_off + 32, ak + 32);
+          uint32_t av[32], ak[32];
+          tmem_ld32(tbase + 256 + lane_off + col0, av);
+          tmem_ld32(tbase + 320 + lane_off + col0, ak);
           tmem_ld_wait();
           tc_fence_before();
           mbar_arrive(acc_free);
@@ -674,12 +682,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             VUnit u;
             decode_vunit(g, P.vcnt, uid, &u);
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-              const int e = u.chunk * 64 + j;
+            for (int jj = 0; jj < 32; ++jj) {
+              const int e = u.chunk * 64 + (int)col0 + jj;
               if (e < u.cnt) {
                 const size_t o = ((size_t)u.vg * g.L + (size_t)u.split * u.stride + e) * D + dcol;
-                P.part_v[o] = __uint_as_float(av[j]);
-                P.part_k[o] = __uint_as_float(ak[j]);
+                P.part_v[o] = __uint_as_float(av[jj]);
+                P.part_k[o] = __uint_as_float(ak[jj]);
               }
             }
           } else {
@@ -693,7 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1)
               vsplit(g, cnt, &R, &stride);
               const int e0 = P.vcnt[(size_t)vg * (g.nb + 1) + kb], e1 = P.vcnt[(size_t)vg * (g.nb + 1) + kb + 1];
               for (int e = e0; e < e1; ++e) {
-                const int j = (int)(P.vlist[(size_t)vg * g.L + e] & kVTokenMask) - kb * kBlock;
+                const int j = (int)(P.vlist[(size_t)vg * g.L + e] & kVTokenMask) - kb * kBlock - (int)col0;
+                if (j < 0 || j >= 32) continue;  // the other group's key
                 float sk = 0.f, sv = 0.f;
                 for (int sp = 0; sp < R; ++sp) {
                   const size_t o = ((size_t)vg * g.L + (size_t)sp * stride + e) * D + dcol;
@@ -701,7 +710,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   sv += P.part_v[o];
                 }
 #pragma unroll
-                for (int jj = 0; jj < 64; ++jj)
+                for (int jj = 0; jj < 32; ++jj)
                   if (jj == j) {
                     ak[jj] = __float_as_uint(__uint_as_float(ak[jj]) + sk);
                     av[jj] = __float_as_uint(__uint_as_float(av[jj]) + sv);
@@ -709,10 +718,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-              const size_t o = ((size_t)(kb * kBlock + j) * g.Hkv + kvh) * D + dcol;
-              P.dV[o] = __float2bfloat16_rn(__uint_as_float(av[j]));
-              P.dK[o] = __float2bfloat16_rn(__uint_as_float(ak[j]) * P.scale);
+            for (int jj = 0; jj < 32; ++jj) {
+              const size_t o = ((size_t)(kb * kBlock + (int)col0 + jj) * g.Hkv + kvh) * D + dcol;
+              P.dV[o] = __float2bfloat16_rn(__uint_as_float(av[jj]));
+              P.dK[o] = __float2bfloat16_rn(__uint_as_float(ak[jj]) * P.scale);
             }
           }
         }

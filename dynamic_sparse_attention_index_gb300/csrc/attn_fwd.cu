@@ -221,6 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // warp 0 (kprod): Q (+ dO) per row tile, per-tile metadata, K per source;
   // warp 3: V per source.  Both walk the same source enumeration.
   auto produce = [&](const bool kprod) {
+    const long long prod0 = kWaitProfileQm ? clock64() : 0;
     const int W = g.bs / kBlock;
     int t = 0, it_local = 0;
     if (lane == 0) {
@@ -447,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (nsrc > 0) emit();
     }
+    if (kWaitProfileQm && lane == 0) atomicAdd(&wcyc[kprod ? 7 : 8], (unsigned long long)(clock64() - prod0));
   };
 
   if (warp == 0 || warp == 3) {
