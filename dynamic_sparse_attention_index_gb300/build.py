@@ -33,10 +33,10 @@ STAMP = os.path.join(BUILD, "flags.txt")
 
 
 def _flags() -> list:
-    # VS_WAIT_PROFILE=1|2|3 compiles in the attention kernels' wait-cycle
-    # counters (all, dK/dV only, query-major only)
+    # VS_WAIT_PROFILE=1|2|3|4 compiles in the attention kernels' wait-cycle
+    # counters (all, dK/dV only, query-major only, dK/dV MMA issue only)
     mode = os.environ.get("VS_WAIT_PROFILE", "")
-    return FLAGS + ([f"-DVS_WAIT_PROFILE={mode}"] if mode in ("1", "2", "3") else [])
+    return FLAGS + ([f"-DVS_WAIT_PROFILE={mode}"] if mode in ("1", "2", "3", "4") else [])
 
 
 def _stale() -> bool:

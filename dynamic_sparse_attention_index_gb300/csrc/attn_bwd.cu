@@ -509,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool more = uid < nunits;
         if (!more && ta == ts) break;
         bool progressed = false;
-        const long long i0 = kWaitProfileKv ? clock64() : 0;
+        const long long i0 = kMmaProfileKv ? clock64() : 0;
         if (ta < ts && mbar_test_wait(&pds_ready[ta & 1], (ta >> 1) & 1)) {
           const Pend q = pend[ta & 1];
           if (q.first && q.un > 0 && !wait(acc_free, (q.un - 1) & 1, 11)) break;
@@ -532,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (q.last) umma_commit(acc_done);
           ++ta;
           progressed = true;
-          if (kWaitProfileKv) atomicAdd(&wcyc[25], (unsigned long long)(clock64() - i0));
+          if (kMmaProfileKv) atomicAdd(&wcyc[25], (unsigned long long)(clock64() - i0));
         } else if (more && ts - ta < 2 && mbar_test_wait(&st_full[ts % kStages], (ts / kStages) & 1)) {
           const int st = ts % kStages;
           const SrcMeta m = mq[ts % kMQ];
@@ -552,7 +552,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     kIdescSN64, kk > 0 ? 1u : 0u);
           }
           umma_commit(&sdp_full[ts & 1]);
-          if (kWaitProfileKv) {
+          if (kMmaProfileKv) {
             atomicAdd(&wcyc[16], 1ull);
             atomicAdd(&wcyc[17], (unsigned long long)m.nsrc);
             if (m.last) atomicAdd(&wcyc[18], 1ull);
@@ -566,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ++un;
           }
           progressed = true;
-          if (kWaitProfileKv) atomicAdd(&wcyc[24], (unsigned long long)(clock64() - i0));
+          if (kMmaProfileKv) atomicAdd(&wcyc[24], (unsigned long long)(clock64() - i0));
         }
         if (progressed) {
           idle0 = clock64();
@@ -734,9 +734,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tbase, 512);
-  if (kWaitProfileKv && threadIdx.x < kWaitSites - 1 && wcyc[threadIdx.x])
+  if (kMmaProfileKv && threadIdx.x < kWaitSites - 1 && wcyc[threadIdx.x])
     atomicAdd(&P.status->wait_cycles[threadIdx.x], wcyc[threadIdx.x]);
-  if (kWaitProfileKv && threadIdx.x == kWaitSites - 1)
+  if (kMmaProfileKv && threadIdx.x == kWaitSites - 1)
     atomicAdd(&P.status->wait_cycles[kWaitSites - 1], (unsigned long long)(clock64() - kernel_t0));
 }
 

@@ -603,6 +603,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_warp(dp_full, t & 1, 24)) break;
           tc_fence_after();
           if (md == kSrcOff) {
+            // dP is released as soon as it has been read: the next tile's
+            // dP = dO V^T then overlaps this tile's arithmetic
+            tc_fence_before();
+            mbar_arrive(dp_free);
 #pragma unroll
             for (int k = 0; k < 32; ++k) pk[k] = 0u;
           } else {
@@ -612,6 +616,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld32(tbase + kDPCol + lane_off + 64 * grp, dv);
             tmem_ld32(tbase + kDPCol + lane_off + 64 * grp + 32, dv + 32);
             tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(dp_free);
             if (md == kSrcFull) {
               const uint64_t cc = f2pack(c2, c2), ll = f2pack(-lse2, -lse2);
 #pragma unroll
@@ -635,8 +641,6 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-          tc_fence_before();
-          mbar_arrive(dp_free);
         } else {
           uint32_t v[64];
           uint64_t act;
