@@ -38,6 +38,9 @@ WORKLOADS = {
     # name -> (recipe id, overrides)
     "gqa16x2_L131072_d128_fwdbwd": (3, {}),
     "gqa16x2_L32768_d128_fwdbwd": (3, {"L": 32768}),   # small case for profiling
+    # striped layout emulation: 32 round-robin shards (slash tiles of 64 x 32 tokens)
+    "gqa16x2_L262144_d128_striped32_fwdbwd": (4, {}),
+    "gqa16x2_L65536_d128_striped32_fwdbwd": (4, {"L": 65536}),
 }
 DENSITY = 0.05     # budget fill: 95 % sparsity (fixed in the pages' experiments)
 LAST_Q, TOP_P = 64, 0.95
@@ -129,8 +132,11 @@ def run_gpu(args):
     wid, ov = WORKLOADS[args.workload]
     w = synth.make_workload(wid, **ov)
     L, Hq, Hkv, d = w.L, w.Hq, w.Hkv, w.d
-    p = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=DENSITY, rope_theta=w.rope_theta)
-    p_nat = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=0.0, rope_theta=w.rope_theta)
+    W = w.stripes
+    p = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=DENSITY, rope_theta=w.rope_theta,
+                       stripes=W)
+    p_nat = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=0.0, rope_theta=w.rope_theta,
+                           stripes=W)
 
     def pinned(bits):
         t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
@@ -185,6 +191,18 @@ def run_gpu(args):
     A = int(ix.active_entries.sum().item())
     A_nat = int(ix_nat.active_entries.sum().item())
     del ix_nat
+    balance = None
+    if W > 1:
+        # per-shard work of the striped layout against contiguous and ZigZag
+        # splits of the contiguous (W = 1) index built on the same inputs
+        p1 = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=DENSITY, rope_theta=w.rope_theta)
+        ix1 = vs.IndexBuffers.allocate(p1, dev)
+        vs.vs_index_build(p1, Q, K, ix1, vs.workspace(p1, vs.VS_OP_INDEX, dev))
+        ix_w = vs.IndexBuffers.allocate(p, dev)
+        vs.vs_index_build(p, Q, K, ix_w, vs.workspace(p, vs.VS_OP_INDEX, dev))
+        torch.cuda.synchronize()
+        balance = shard_balance(L, W, index_lists(ix_w, Hq), index_lists(ix1, Hq))
+        del ix1, ix_w
     assert vs.vs_device_status(ws_f) == vs.VS_OK and vs.vs_device_status(ws_b) == vs.VS_OK
 
     sampler = ClockSampler(local)
@@ -258,9 +276,10 @@ def run_gpu(args):
                    "last_q": LAST_Q, "index": f"budget fill to density {DENSITY}",
                    "sparsity": round(1 - A / (Hq * T), 5),
                    "natural_top_p_sparsity": round(1 - A_nat / (Hq * T), 5), "top_p": TOP_P,
-                   "active_entries": A, "l2": "inputs larger than L2 (no flush)",
+                   "active_entries": A, "l2": "inputs larger than L2 (no flush)", "stripes": W,
                    "parallelism": f"replicas x{world}"},
         "breakdown_ms": {k: round(v, 4) for k, v in phase.items()},
+        **({"shard_balance": balance} if balance else {}),
         "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
         "index_overhead": round(phase["index"] / max(ms, 1e-9), 4),
         "roofline": {"kernel": "vs_sparse_attn_bwd (dK/dV + dQ)", "bound": "tensor",
@@ -284,6 +303,42 @@ def index_lists(ix, Hq):
     vc, sc = ix.v_cnt.cpu().numpy(), ix.s_cnt.cpu().numpy()
     vi, si = ix.v_idx.cpu().numpy(), ix.s_idx.cpu().numpy()
     return [(vi[h, :vc[h]].astype(np.int64), si[h, :sc[h]].astype(np.int64)) for h in range(Hq)]
+
+
+def row_active_counts(L, V, S, bs):
+    """Active causal entries of every query row of one head under a VS index:
+    kept slash bands S (band n//bs - m//bs, band 0 always kept) plus kept
+    verticals V outside kept bands (the mask the kernels compute)."""
+    nbs = L // bs
+    kept = np.zeros(nbs, bool)
+    kept[np.asarray(S, np.int64)] = True
+    kept[0] = True
+    n = np.arange(L, dtype=np.int64)
+    qb = n // bs
+    kc = np.cumsum(kept) - 1                      # kept bands 1..b
+    slash = kc[qb] * bs + (n - qb * bs + 1)
+    cnt_v = np.bincount(np.asarray(V, np.int64) // bs, minlength=nbs)
+    before = np.concatenate([[0], np.cumsum(cnt_v)[:-1]])   # verticals in earlier blocks
+    inband = np.zeros(nbs, np.int64)                        # ... of those, in kept bands
+    for B in np.flatnonzero(kept[1:]) + 1:
+        inband[B:] += cnt_v[:nbs - B]
+    return slash + (before - inband)[qb]
+
+
+def shard_balance(L, W, index_striped, index_contig):
+    """Work (active entries) per worker for W workers: the striped layout
+    (worker r holds tokens r, r + W, ...; index with 64 W-token slash tiles)
+    and the contiguous and ZigZag splits (2 W chunks, worker k holds chunks k
+    and 2 W - 1 - k) of the contiguous index.  Returns max / mean of each."""
+    striped = sum(row_active_counts(L, V, S, 64 * W) for V, S in index_striped).reshape(L // W, W).sum(0)
+    rows = sum(row_active_counts(L, V, S, 64) for V, S in index_contig)
+    contig = rows.reshape(W, L // W).sum(1)
+    chunks = rows.reshape(2 * W, L // (2 * W)).sum(1)
+    zigzag = chunks[:W] + chunks[::-1][:W]
+    r = lambda a: round(float(a.max() / a.mean()), 4)
+    return {"workers": W, "unit": "active entries per worker", "striped_max_over_mean": r(striped),
+            "contiguous_max_over_mean": r(contig), "zigzag_max_over_mean": r(zigzag),
+            "striped_total": int(striped.sum()), "contiguous_index_total": int(rows.sum())}
 
 
 def cpu_baseline(w, index, d, nrows):

@@ -113,6 +113,12 @@ def test_bwd_striped_bands():
     _check(w, index, stripes=4)
 
 
+def test_bwd_striped_32_shards():
+    w = synth.make_workload(4, L=4096, Hq=2, Hkv=1, d=128, backward=True)
+    index, _, _ = oracle.build_index(f64(w.q), f64(w.k), 64, 0.9, stripes=32)
+    _check(w, index, stripes=32)
+
+
 def test_bwd_full_size_gqa_128k():
     """The 128K GQA training workload at full size with the GPU budget-fill
     index: dQ on sampled rows against the oracle, dK / dV through identities

@@ -101,6 +101,14 @@ def test_fwd_striped_bands():
     _check(w, index, stripes=4)
 
 
+def test_fwd_striped_32_shards():
+    """The striped-layout workload's 32 round-robin shards: slash tiles of
+    64 x 32 tokens (two bands at L = 4096)."""
+    w = synth.make_workload(4, L=4096, Hq=2, Hkv=1, d=128)
+    index, _, _ = oracle.build_index(f64(w.q), f64(w.k), 64, 0.9, stripes=32)
+    _check(w, index, stripes=32)
+
+
 def test_fwd_full_size_gqa_128k_sampled():
     """The 128K GQA workload at full size, budget-fill index built on the GPU,
     checked on sampled rows (first, middle, last blocks; every head)."""
