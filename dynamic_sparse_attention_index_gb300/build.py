@@ -33,10 +33,11 @@ STAMP = os.path.join(BUILD, "flags.txt")
 
 
 def _flags() -> list:
-    # VS_WAIT_PROFILE=1|2|3|4 compiles in the attention kernels' wait-cycle
-    # counters (all, dK/dV only, query-major only, dK/dV MMA issue only)
+    # VS_WAIT_PROFILE=1..6 compiles in the attention kernels' wait-cycle
+    # counters (all, dK/dV only, query-major only, MMA issue of dK/dV or
+    # query-major only)
     mode = os.environ.get("VS_WAIT_PROFILE", "")
-    return FLAGS + ([f"-DVS_WAIT_PROFILE={mode}"] if mode in ("1", "2", "3", "4") else [])
+    return FLAGS + ([f"-DVS_WAIT_PROFILE={mode}"] if mode in ("1", "2", "3", "4", "5", "6") else [])
 
 
 def _stale() -> bool:

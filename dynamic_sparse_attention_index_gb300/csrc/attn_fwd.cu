@@ -200,12 +200,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
+  long long wl[20] = {};  // profiling (light mode): this thread's wait cycles of sites < 20
   auto wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
     if (*abort_flag) return false;
-    const long long w0 = kWaitProfileQm ? clock64() : 0;
+    const long long w0 = (kWaitProfileQm || kSmProfileQm) ? clock64() : 0;
     const bool ok = mbar_wait(bar, parity, kWaitLimitNs);
     if (kWaitProfileQm && (threadIdx.x & 31) == 0)
       atomicAdd(&wcyc[where & (kWaitSites - 1)], (unsigned long long)(clock64() - w0));
+    if (kSmProfileQm && where < 20) wl[where] += clock64() - w0;
     if (ok) return true;
     *abort_flag = 1;
     report_timeout(P.status, where);
@@ -221,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // warp 0 (kprod): Q (+ dO) per row tile, per-tile metadata, K per source;
   // warp 3: V per source.  Both walk the same source enumeration.
   auto produce = [&](const bool kprod) {
-    const long long prod0 = kWaitProfileQm ? clock64() : 0;
+    const long long prod0 = (kWaitProfileQm || kSmProfileQm) ? clock64() : 0;
     const int W = g.bs / kBlock;
     int t = 0, it_local = 0;
     if (lane == 0) {
@@ -448,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (nsrc > 0) emit();
     }
-    if (kWaitProfileQm && lane == 0) atomicAdd(&wcyc[kprod ? 7 : 8], (unsigned long long)(clock64() - prod0));
+    if ((kWaitProfileQm || kSmProfileQm) && lane == 0) atomicAdd(&wcyc[kprod ? 7 : 8], (unsigned long long)(clock64() - prod0));
   };
 
   if (warp == 0 || warp == 3) {
@@ -471,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int pk = prev_t % Ly::kRK, pv = prev_t % Ly::kRV;
         if (!kDQ && !wait(&v_full[pv], (prev_t / Ly::kRV) & 1, 15)) return false;
         tc_fence_after();
+        const long long a0 = kMmaProfileQm ? clock64() : 0;
         // B operand: V of the tile (forward) or K of the tile (dQ), MN-major
         const uint32_t bst = kDQ ? smem_u32(sm + Ly::kKRing + pk * Ly::kKBytes)
                                  : smem_u32(sm + Ly::kVRing + pv * Ly::kKBytes);
@@ -498,6 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           umma_commit(&k_empty[pk]);
         else
           umma_commit(&v_empty[pv]);
+        if (kMmaProfileQm) atomicAdd(&wcyc[19], (unsigned long long)(clock64() - a0));
         return true;
       };
       for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
@@ -514,17 +518,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t kb = smem_u32(sm + Ly::kKRing + sk * Ly::kKBytes);
           const uint32_t dS = tbase + (uint32_t)((t & 1) * 128);
           const uint32_t idS = m.nsrc == 2 ? kIdescS128 : kIdescS64;
+          const long long s0 = kMmaProfileQm ? clock64() : 0;
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * Ly::kRowBytes + (kk & 3) * 32;
             umma_ss(dS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
           }
           umma_commit(&s_full[t & 1]);
+          if (kMmaProfileQm) atomicAdd(&wcyc[0], (unsigned long long)(clock64() - s0));
           if (!kDQ) umma_commit(&k_empty[sk]);  // forward: K is read only by S
           if (kDQ) {
             // dP = dO V^T into the single dP buffer, once every row read the previous one
             if (t > 0 && !wait(dp_free, (t - 1) & 1, 14)) break;
             if (!wait(&v_full[sv], (t / Ly::kRV) & 1, 15)) break;
             tc_fence_after();
+            const long long d0 = kMmaProfileQm ? clock64() : 0;
             const uint32_t oa = qa + Ly::kQBytes;
             const uint32_t vb = smem_u32(sm + Ly::kVRing + sv * Ly::kKBytes);
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -534,9 +541,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             umma_commit(dp_full);
             umma_commit(&v_empty[sv]);  // dQ: V is read only by dP
+            if (kMmaProfileQm) atomicAdd(&wcyc[9], (unsigned long long)(clock64() - d0));
           }
           if (last) umma_commit(&q_empty[m.qslot]);
-          if (kWaitProfileQm) {
+          if (kMmaProfileQm) {
             atomicAdd(&wcyc[16], 1ull);
             atomicAdd(&wcyc[17], (unsigned long long)m.nsrc);
             if (last) atomicAdd(&wcyc[18], 1ull);
@@ -570,6 +578,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // forward: this group's accumulator (O_A or O_B); dQ: its half of the dQ columns
     const uint32_t tAcc = kDQ ? tbase + kAccCol + lane_off + grp * (D / 2) : tbase + 256 + 128 * grp + lane_off;
     float* xch = reinterpret_cast<float*>(sm + Ly::kXchg);
+    long long pw = 0, pk_ = 0, pe = 0;  // profiling: wait / work / epilogue cycles of this warp
     int t = 0, it_local = 0;
     for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
       const Item it = decode_item(g, id);
@@ -584,6 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       bool last = false;
       do {
+        const long long q0 = kSmProfileQm ? clock64() : 0;
         const int sk = t % Ly::kRK;
         if (!wait_warp(&k_full[sk], (t / Ly::kRK) & 1, 20)) break;
         // masking mode of this group's source for this row's segment (warp-uniform)
@@ -592,6 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         last = metas[sk].last != 0;
         mbar_arrive(&meta_free[sk]);
         if (!wait_warp(&s_full[t & 1], (t >> 1) & 1, 21)) break;
+        const long long q1 = kSmProfileQm ? clock64() : 0;
+        if (kSmProfileQm) pw += q1 - q0;
         tc_fence_after();
         const uint32_t tS = tbase + (uint32_t)((t & 1) * 128) + lane_off + 64 * grp;  // this slot's scores
         const float c2 = P.scale_log2;
@@ -711,6 +723,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(&p_ready[t & 1]);
+        if (kSmProfileQm) pk_ += clock64() - q1;
         if (last) {
           const long long pe0 = clock64();
           // pv_done completes once per tile and a parity wait only tells the
@@ -787,19 +800,28 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_before();
           mbar_arrive(o_free);
           if (kWaitProfileQm && lane == 0) atomicAdd(&wcyc[30], (unsigned long long)(clock64() - pe0));
+          if (kSmProfileQm) pe += clock64() - pe0;
         }
         ++t;
       } while (!last && !*abort_flag);
     }
+    if (kSmProfileQm && lane == 0) {
+      atomicAdd(&wcyc[21], (unsigned long long)pw);
+      atomicAdd(&wcyc[27], (unsigned long long)pk_);
+      atomicAdd(&wcyc[30], (unsigned long long)pe);
+    }
   }
   __syncwarp();
+  if (kSmProfileQm && lane == 0 && warp < 4)
+    for (int k = 1; k < 20; ++k)
+      if (k != 9 && wl[k]) atomicAdd(&wcyc[k], (unsigned long long)wl[k]);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tbase, 512);
-  if (kWaitProfileQm && threadIdx.x < kWaitSites - 1 && wcyc[threadIdx.x])
+  if (kMmaProfileQm && threadIdx.x < kWaitSites - 1 && wcyc[threadIdx.x])
     atomicAdd(&P.status->wait_cycles[threadIdx.x], wcyc[threadIdx.x]);
-  if (kWaitProfileQm && threadIdx.x == kWaitSites - 1)
+  if (kMmaProfileQm && threadIdx.x == kWaitSites - 1)
     atomicAdd(&P.status->wait_cycles[kWaitSites - 1], (unsigned long long)(clock64() - kernel_t0));
 }
 

@@ -15,7 +15,8 @@ constexpr int kMaxL = 1 << 20;                   // supported sequence length ce
 // Per-site wait-cycle and phase counters of the attention kernels are built
 // only with -DVS_WAIT_PROFILE=n (a pipeline-balance diagnostic: 1 all
 // attention kernels, 2 the dK/dV kernel, 3 the query-major kernel, 4 the
-// dK/dV kernel's MMA issue only); the
+// dK/dV kernel's MMA issue only, 5 the query-major kernel's MMA issue
+// only); the
 // default build leaves the wait_cycles array of the status block at zero.
 #ifndef VS_WAIT_PROFILE
 #define VS_WAIT_PROFILE 0
@@ -24,6 +25,10 @@ constexpr bool kWaitProfileKv = VS_WAIT_PROFILE == 1 || VS_WAIT_PROFILE == 2;
 // 4: only the dK/dV kernel's MMA-issue timers and total cycles (least intrusive)
 constexpr bool kMmaProfileKv = kWaitProfileKv || VS_WAIT_PROFILE == 4;
 constexpr bool kWaitProfileQm = VS_WAIT_PROFILE == 1 || VS_WAIT_PROFILE == 3;
+// 5: only the query-major kernel's MMA-issue timers and total cycles
+constexpr bool kMmaProfileQm = kWaitProfileQm || VS_WAIT_PROFILE == 5 || VS_WAIT_PROFILE == 6;
+// 6: additionally the softmax warps' per-tile wait / work split, kept in registers
+constexpr bool kSmProfileQm = VS_WAIT_PROFILE == 6;
 
 // Device-side status block (first bytes of every workspace).
 constexpr int kWaitSites = 32;
