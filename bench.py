@@ -108,15 +108,30 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def _dist():
+def _dist(backend: str = "nccl"):
+    """Process group of a torchrun launch (one rank per GPU), or none."""
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     if ws > 1:
         import torch.distributed as dist
         rank = int(os.environ["RANK"])
         local = int(os.environ.get("LOCAL_RANK", rank))
-        dist.init_process_group("nccl")
+        dist.init_process_group(backend)
         return dist, rank, local, ws
     return None, 0, 0, 1
+
+
+def replica_throughput(dist, world, flops_per_rank, ms, e2e_ms, device):
+    """Whole-job throughput of independent replicas: every rank did the same
+    work, the job takes as long as the slowest rank (max over ranks), and
+    the value is world x work / that time (TFLOP/s).  Returns (value, e2e
+    value, ms, e2e ms) with the times taken over all ranks."""
+    import torch
+    t = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=device)
+    if dist:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    ms, e2e_ms = t.tolist()
+    return (world * flops_per_rank / (ms * 1e-3) / 1e12, world * flops_per_rank / (e2e_ms * 1e-3) / 1e12, ms,
+            e2e_ms)
 
 
 def run_gpu(args):
@@ -256,12 +271,7 @@ def run_gpu(args):
     d2h = sum(t.numel() * t.element_size() for t in (hdQ, hdK, hdV))
 
     flops = 14.0 * d * A
-    ms_t = torch.tensor([ms, e2e_ms], device=dev)
-    if dist:
-        dist.all_reduce(ms_t, op=dist.ReduceOp.MAX)
-    ms, e2e_ms = ms_t.tolist()
-    value = world * flops / (ms * 1e-3) / 1e12
-    e2e_val = world * flops / (e2e_ms * 1e-3) / 1e12
+    value, e2e_val, ms, e2e_ms = replica_throughput(dist, world, flops, ms, e2e_ms, dev)
     pk = _peaks()
     # dominant kernel group: the backward call (dK/dV + dQ kernels), 10 d A per launch
     bwd_tf = 10.0 * d * A / (phase["bwd"] * 1e-3) / 1e12
@@ -344,8 +354,9 @@ def shard_balance(L, W, index_striped, index_contig):
 def cpu_baseline(w, index, d, nrows):
     """The fp64 oracle, as it stands, on a bounded sample of the step: the
     forward and dQ of `nrows` query rows spread over the sequence, every
-    head.  Reported as effective TFLOP/s of the same 14 d (active entries)
-    convention over the sampled rows."""
+    head.  Reported in TFLOP/s counting the work those calls do on the
+    sampled rows' active entries: 4 d for the forward and 6 d for dQ (S and
+    dP recomputed, dS K); the rows' dK / dV contributions are not run."""
     import oracle
     f = synth.bf16_bits_to_f64
     Q, K, V, dO = f(w.q), f(w.k), f(w.v), f(w.do)
@@ -368,9 +379,9 @@ def cpu_baseline(w, index, d, nrows):
         cores = len(os.sched_getaffinity(0))
     except Exception:
         cores = os.cpu_count()
-    return {"value": round(14.0 * d * act / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"fp64 forward + dQ of {nrows} query rows x {w.Hq} heads ({act} active entries), "
-                      f"{dt:.1f} s"}
+    return {"value": round(10.0 * d * act / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 forward + dQ of {nrows} query rows x {w.Hq} heads ({act} active entries, "
+                      f"10 d flop each), {dt:.1f} s"}
 
 
 def run_reference(args):
