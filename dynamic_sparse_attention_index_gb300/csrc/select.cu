@@ -267,6 +267,10 @@ __device__ unsigned long long slash_entries(const uint8_t* inS, int nbs, int bs,
 }
 
 // Vertical entries for threshold key tau (keep m iff key(v[m]) >= tau).
+// Budget fill: verticals whose key reached the running threshold, gathered in
+// shared memory once they fit, so later threshold probes skip the full list.
+constexpr int kCandCap = 8192;
+
 __device__ unsigned long long vert_entries_at(const float* v, int L, uint32_t tau, const int32_t* notS, int nbs,
                                               int bs, SelShared& s) {
   unsigned long long e = 0;
@@ -282,6 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) 
   const int nbs = a.nbs, L = a.L, bs = a.bs;
   uint8_t* inS = dyn;                                               // [nbs]
   int32_t* notS = reinterpret_cast<int32_t*>(dyn + align_up(nbs, 16));  // [nbs]
+  uint32_t* ckey = reinterpret_cast<uint32_t*>(dyn + align_up(nbs, 16) + align_up((size_t)nbs * 4, 16));
+  int32_t* cblk = reinterpret_cast<int32_t*>(ckey + kCandCap);  // candidate list: key, key block
   const float* v = a.v + (size_t)h * L;
   const float* S = a.S + (size_t)h * nbs;
   int32_t* vout = a.v_idx + (size_t)h * L;
@@ -360,13 +366,49 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) 
     // ---------------- budget fill
     const double T = (double)L * (double)(L + 1) * 0.5;
     const unsigned long long target = (unsigned long long)ceil((double)a.density * T);
+    // Verticals with key >= the accepted threshold, once there are at most
+    // kCandCap of them: the threshold only rises, so later probes need no
+    // other vertical (ncand < 0: not gathered yet, probe the full list).
+    int ncand = -1;
+    unsigned long long nabove = 0;  // verticals with key >= the last probed threshold
     auto entries_at = [&](uint32_t tau) -> unsigned long long {
       for (int B = threadIdx.x; B < nbs; B += kThreads) inS[B] = (B == 0) || (key_of(S[B]) >= tau);
       __syncthreads();
       build_notS(inS, notS, nbs, s);
       const unsigned long long se = slash_entries(inS, nbs, bs, s);
-      const unsigned long long ve = vert_entries_at(v, L, tau, notS, nbs, bs, s);
+      unsigned long long ve = 0, c = 0;
+      if (ncand < 0) {
+        for (int m = threadIdx.x; m < L; m += kThreads)
+          if (key_of(v[m]) >= tau) {
+            ve += (unsigned long long)notS[nbs - 1 - m / bs];
+            ++c;
+          }
+      } else {
+        for (int i = threadIdx.x; i < ncand; i += kThreads)
+          if (ckey[i] >= tau) {
+            ve += (unsigned long long)notS[nbs - 1 - cblk[i]];
+            ++c;
+          }
+      }
+      ve = block_sum_u64(ve, s) * (unsigned long long)bs;
+      nabove = block_sum_u64(c, s);
       return se + ve;
+    };
+    auto gather = [&](uint32_t tau) {
+      if (ncand >= 0 || nabove > (unsigned long long)kCandCap) return;
+      if (threadIdx.x == 0) s.bcast_u32[0] = 0u;
+      __syncthreads();
+      for (int m = threadIdx.x; m < L; m += kThreads) {
+        const uint32_t k = key_of(v[m]);
+        if (k >= tau) {
+          const unsigned i = atomicAdd(&s.bcast_u32[0], 1u);
+          ckey[i] = k;
+          cblk[i] = m / bs;
+        }
+      }
+      __syncthreads();
+      ncand = (int)s.bcast_u32[0];
+      __syncthreads();
     };
     uint32_t tau;
     if (entries_at(0x7f800001u) >= target) {
@@ -378,7 +420,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) 
       for (int bit = 30; bit >= 0; --bit) {
         const uint32_t cand = tau | (1u << bit);
         if (cand > 0x7f800000u) continue;
-        if (entries_at(cand) >= target) tau = cand;
+        if (entries_at(cand) >= target) {
+          tau = cand;
+          gather(tau);
+        }
       }
     }
     // final sets at tau: slash list (band 0 forced) and verticals
@@ -406,7 +451,8 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) 
 
 }  // namespace
 
-size_t select_smem_bytes(int nbs) { return align_up(nbs, 16) + (size_t)nbs * 4; }
+// kept-band flags, band prefix table, budget-fill candidate list (key, block)
+size_t select_smem_bytes(int nbs) { return align_up(nbs, 16) + align_up((size_t)nbs * 4, 16) + (size_t)kCandCap * 8; }
 
 cudaError_t launch_select(const IndexArgs& a, cudaStream_t s) {
   const size_t smem = select_smem_bytes(a.nbs);
