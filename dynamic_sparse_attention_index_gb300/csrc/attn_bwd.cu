@@ -186,8 +186,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* st_empty = st_full + kStages;
   uint64_t* sdp_full = st_empty + kStages;
   uint64_t* pds_ready = sdp_full + 2;
-  uint64_t* pds_free = pds_ready + 2;
-  uint64_t* acc_done = pds_free + 2;
+  // a tile's dV / dK completing frees both its Q / dO stage and its P / dS
+  // buffer (both indexed by tile parity), so one commit serves both waiters
+  static_assert(kStages == 2, "P / dS buffers and Q / dO stages share the release barrier");
+  uint64_t* pds_free = st_empty;
+  uint64_t* acc_done = pds_ready + 4;  // (the two slots after pds_ready are unused)
   uint64_t* acc_free = acc_done + 1;
   uint64_t* mq_full = acc_free + 1;
   uint64_t* mq_empty = mq_full + kMQ;
@@ -210,7 +213,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sdp_full[i], 1);
       mbar_init(&pds_ready[i], 256);
-      mbar_init(&pds_free[i], 1);
     }
     mbar_init(acc_done, 1);
     mbar_init(acc_free, 256);
@@ -527,8 +529,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_ss(tbase + 320, sdesc_sw128(qa + kk * 2048, kHalfRows128, 1024),
                     sdesc_sw128(db + kk * 2048, 8192, 1024), kIdescAcc, acc);
           }
-          umma_commit(&st_empty[st]);
-          umma_commit(&pds_free[ta & 1]);
+          umma_commit(&st_empty[st]);  // also the P / dS buffer's release
           if (q.last) umma_commit(acc_done);
           ++ta;
           progressed = true;
