@@ -45,6 +45,10 @@ WORKLOADS = {
 DENSITY = 0.05     # budget fill: 95 % sparsity (fixed in the pages' experiments)
 LAST_Q, TOP_P = 64, 0.95
 KERNELS_PER_STEP = {"rope": 4, "index": 5, "fwd": 4, "bwd": 8}
+# DRAM bytes of one backward call (dram__bytes_read.sum + dram__bytes_write.sum
+# over its kernels, one-pass ncu capture of this workload); measured for the
+# current backward kernels and to be taken again whenever they change
+BWD_TRAFFIC_BYTES = {"gqa16x2_L131072_d128_fwdbwd": 38279813888}
 
 
 def _peaks():
@@ -294,7 +298,7 @@ def run_gpu(args):
         "index_overhead": round(phase["index"] / max(ms, 1e-9), 4),
         "roofline": {"kernel": "vs_sparse_attn_bwd (dK/dV + dQ)", "bound": "tensor",
                      "achieved": round(bwd_tf, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(bwd_tf / peak, 4), "traffic": None,
+                     "frac": round(bwd_tf / peak, 4), "traffic": BWD_TRAFFIC_BYTES.get(args.workload),
                      "peak_src": pk["src"] + " bf16 sustained"},
         "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
