@@ -478,20 +478,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t bst = kDQ ? smem_u32(sm + Ly::kKRing + pk * Ly::kKBytes)
                                  : smem_u32(sm + Ly::kVRing + pv * Ly::kKBytes);
         const uint32_t pS = tbase + (uint32_t)((prev_t & 1) * 128);
+        const uint64_t bd0 = sdesc_sw128(bst, Ly::kRowBytes, 1024);
         if (kDQ) {
           // dS of slot g sits at S-buffer columns [64 g, 64 g + 32)
           for (int kk = 0; kk < 4 * prev_nsrc; ++kk) {
-            const uint64_t bd = sdesc_sw128(bst + kk * 2048, Ly::kRowBytes, 1024);
+            const uint64_t bd = sdesc_add(bd0, kk * 2048);
             umma_ts(tAcc, pS + (kk >> 2) * 64 + (kk & 3) * 8, bd, kIdescAcc, (kk > 0 || !prev_first) ? 1u : 0u);
           }
         } else {
           // O_A += P_0 V_0 and O_B += P_1 V_1: two independent chains, interleaved
           if (prev_first) ob_init = false;
           for (int kk = 0; kk < 4; ++kk) {
-            umma_ts(tbase + 256, pS + kk * 8, sdesc_sw128(bst + kk * 2048, Ly::kRowBytes, 1024), kIdescAcc,
+            umma_ts(tbase + 256, pS + kk * 8, sdesc_add(bd0, kk * 2048), kIdescAcc,
                     (kk > 0 || !prev_first) ? 1u : 0u);
             if (prev_nsrc == 2)
-              umma_ts(tbase + 384, pS + 64 + kk * 8, sdesc_sw128(bst + (kk + 4) * 2048, Ly::kRowBytes, 1024),
+              umma_ts(tbase + 384, pS + 64 + kk * 8, sdesc_add(bd0, (kk + 4) * 2048),
                       kIdescAcc, (kk > 0 || ob_init) ? 1u : 0u);
           }
           if (prev_nsrc == 2) ob_init = true;
@@ -509,23 +510,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         do {
           const int sk = t % Ly::kRK, sv = t % Ly::kRV;
           if (!wait(&k_full[sk], (t / Ly::kRK) & 1, 12)) break;
+          const long long mc0 = kSmProfileQm ? clock64() : 0;
           const TileMeta m = metas[sk];
           last = m.last != 0;
           if (m.first)
             if (!wait(&q_full[m.qslot], (it_local / Ly::kQSlots) & 1, 13)) break;
           tc_fence_after();
+          if (kSmProfileQm) wl[5] += clock64() - mc0;  // metadata copy + fence (and q_full)
           const uint32_t qa = smem_u32(sm + Ly::kQ + m.qslot * Ly::kSlotBytes);
           const uint32_t kb = smem_u32(sm + Ly::kKRing + sk * Ly::kKBytes);
           const uint32_t dS = tbase + (uint32_t)((t & 1) * 128);
           const uint32_t idS = m.nsrc == 2 ? kIdescS128 : kIdescS64;
           const long long s0 = kMmaProfileQm ? clock64() : 0;
+          const uint64_t qd0 = sdesc_sw128(qa, 16, 1024), kd0 = sdesc_sw128(kb, 16, 1024);
+#pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t off = (kk >> 2) * Ly::kRowBytes + (kk & 3) * 32;
-            umma_ss(dS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), idS, kk > 0 ? 1u : 0u);
+            umma_ss(dS, sdesc_add(qd0, off), sdesc_add(kd0, off), idS, kk > 0 ? 1u : 0u);
           }
           umma_commit(&s_full[t & 1]);
           if (kMmaProfileQm) atomicAdd(&wcyc[0], (unsigned long long)(clock64() - s0));
+          const long long kc0 = kSmProfileQm ? clock64() : 0;
           if (!kDQ) umma_commit(&k_empty[sk]);  // forward: K is read only by S
+          if (kSmProfileQm) wl[6] += clock64() - kc0;
           if (kDQ) {
             // dP = dO V^T into the single dP buffer, once every row read the previous one
             if (t > 0 && !wait(dp_free, (t - 1) & 1, 14)) break;
@@ -534,10 +541,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             const long long d0 = kMmaProfileQm ? clock64() : 0;
             const uint32_t oa = qa + Ly::kQBytes;
             const uint32_t vb = smem_u32(sm + Ly::kVRing + sv * Ly::kKBytes);
+            const uint64_t od0 = sdesc_sw128(oa, 16, 1024), vd0 = sdesc_sw128(vb, 16, 1024);
+#pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t off = (kk >> 2) * Ly::kRowBytes + (kk & 3) * 32;
-              umma_ss(tbase + kDPCol, sdesc_sw128(oa + off, 16, 1024), sdesc_sw128(vb + off, 16, 1024), idS,
-                      kk > 0 ? 1u : 0u);
+              umma_ss(tbase + kDPCol, sdesc_add(od0, off), sdesc_add(vd0, off), idS, kk > 0 ? 1u : 0u);
             }
             umma_commit(dp_full);
             umma_commit(&v_empty[sv]);  // dQ: V is read only by dP

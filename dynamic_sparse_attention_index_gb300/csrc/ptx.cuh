@@ -201,6 +201,10 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
 // D format bits [4,6) = 1 (f32), A format [7,10) = 1 (bf16), B format
 // [10,13) = 1 (bf16), A major bit 15, B major bit 16 (1 = MN-major),
 // N >> 3 in [17,23), M >> 4 in [24,29).
+// The descriptor of a tile `byte_off` bytes further on: the start address
+// field holds (address >> 4) in its low 14 bits and shared addresses stay
+// below 256 KB, so the offset adds without a carry into the other fields.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t byte_off) { return d + (byte_off >> 4); }
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major, bool b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);

@@ -30,7 +30,8 @@ SLOTS = {
           1: "K producer waits q_empty", 2: "K producer waits k_empty", 3: "K producer waits meta_free",
           4: "V producer waits v_empty", 7: "K producer total", 8: "V producer total",
           10: "MMA waits p_ready", 11: "MMA waits o_free", 12: "MMA waits k_full", 13: "MMA waits q_full",
-          14: "MMA waits dp_free", 15: "MMA waits v_full",
+          14: "MMA waits dp_free", 15: "MMA waits v_full", 5: "MMA metadata copy (+ q_full)",
+          6: "MMA K release commit",
           21: "softmax warp: waits for metadata and S", 27: "softmax warp: S -> P / dS written",
           30: "softmax warp: epilogue"},
 }
