@@ -511,7 +511,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int sk = t % Ly::kRK, sv = t % Ly::kRV;
           if (!wait(&k_full[sk], (t / Ly::kRK) & 1, 12)) break;
           const long long mc0 = kSmProfileQm ? clock64() : 0;
-          const TileMeta m = metas[sk];
+          // only the fields the MMA thread uses
+          const struct {
+            int nsrc, first, last, qslot;
+          } m = {metas[sk].nsrc, metas[sk].first, metas[sk].last, metas[sk].qslot};
           last = m.last != 0;
           if (m.first)
             if (!wait(&q_full[m.qslot], (it_local / Ly::kQSlots) & 1, 13)) break;
