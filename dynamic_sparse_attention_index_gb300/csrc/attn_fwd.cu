@@ -634,10 +634,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int k = 0; k < 32; ++k) pk[k] = 0u;
           } else {
             uint32_t sv[64], dv[64];
-            tmem_ld32(tS, sv);
-            tmem_ld32(tS + 32, sv + 32);
-            tmem_ld32(tbase + kDPCol + lane_off + 64 * grp, dv);
-            tmem_ld32(tbase + kDPCol + lane_off + 64 * grp + 32, dv + 32);
+            tmem_ld64(tS, sv);
+            tmem_ld64(tbase + kDPCol + lane_off + 64 * grp, dv);
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(dp_free);
@@ -669,8 +667,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           uint64_t act;
           float mraw = kNegInf;
           if (md != kSrcOff) {
-            tmem_ld32(tS, v);
-            tmem_ld32(tS + 32, v + 32);
+            tmem_ld64(tS, v);
             tmem_ld_wait();
             if (md != kSrcFull) {
               // masked entries become -inf in place, so neither pass needs the mask
@@ -724,8 +721,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         // P (or dS) of this slot over the first 32 columns of its scores
-        tmem_st16(tS, pk);
-        tmem_st16(tS + 16, pk + 16);
+        tmem_st32(tS, pk);
         const long long ph1 = clock64();
         tmem_st_wait();
         if (kWaitProfileQm && lane == 0) {
