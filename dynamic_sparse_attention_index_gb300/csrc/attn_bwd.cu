@@ -775,6 +775,7 @@ cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* 
   pp.vcnt = reinterpret_cast<int32_t*>(w + lay.prep.vcnt);
   pp.Kp = reinterpret_cast<__nv_bfloat16*>(w + lay.prep.Kp);
   pp.Vp = reinterpret_cast<__nv_bfloat16*>(w + lay.prep.Vp);
+  pp.vbits = lay.prep.vbits != lay.prep.end ? reinterpret_cast<uint32_t*>(w + lay.prep.vbits) : nullptr;
   float* dsum = reinterpret_cast<float*>(w + lay.dsum);
   DevStatus* st = reinterpret_cast<DevStatus*>(w + lay.status);
   cudaError_t e = launch_attn_prep(g, ix, K, V, pp, s);

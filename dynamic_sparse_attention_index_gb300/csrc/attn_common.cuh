@@ -104,8 +104,12 @@ struct PrepWs {
   size_t vcnt;    // [nvg][nb + 1] int32: entries with token < 64 * b
   size_t Kp;      // [nvg][L][d] bf16 packed key rows of the union
   size_t Vp;      // [nvg][L][d] bf16 packed value rows
+  size_t vbits;   // [nvg][2][L/32] uint32 per-head vertical bitmaps (when they exceed shared memory)
   size_t end;
 };
+// The vertical-union pass keeps two L-bit bitmaps per head pair; up to this
+// many bytes they live in shared memory, beyond it in the workspace.
+constexpr size_t kVunionSmemMax = 160 * 1024;
 
 inline PrepWs prep_layout(const AttnGeom& g, WsLayout& w) {
   PrepWs o;
@@ -114,6 +118,7 @@ inline PrepWs prep_layout(const AttnGeom& g, WsLayout& w) {
   o.vcnt = w.take((size_t)g.nvg * (g.nb + 1) * 4);
   o.Kp = w.take((size_t)g.nvg * g.L * g.d * 2);
   o.Vp = w.take((size_t)g.nvg * g.L * g.d * 2);
+  o.vbits = w.take((size_t)2 * (g.L / 32) * 4 > kVunionSmemMax ? (size_t)g.nvg * 2 * (g.L / 32) * 4 : 0);
   o.end = w.off;
   return o;
 }
@@ -124,6 +129,7 @@ struct PrepPtrs {
   int32_t* vcnt;
   __nv_bfloat16* Kp;
   __nv_bfloat16* Vp;
+  uint32_t* vbits;  // null when the bitmaps fit in shared memory
 };
 
 cudaError_t launch_attn_prep(const AttnGeom& g, const vs_index& ix, const void* K, const void* V,

@@ -877,6 +877,7 @@ cudaError_t launch_attn_fwd(const vs_params& p, const vs_index& ix, const void* 
   pp.vcnt = reinterpret_cast<int32_t*>(w + pw.vcnt);
   pp.Kp = reinterpret_cast<__nv_bfloat16*>(w + pw.Kp);
   pp.Vp = reinterpret_cast<__nv_bfloat16*>(w + pw.Vp);
+  pp.vbits = pw.vbits != pw.end ? reinterpret_cast<uint32_t*>(w + pw.vbits) : nullptr;
   cudaError_t e = launch_attn_prep(g, ix, K, V, pp, s);
   if (e != cudaSuccess) return e;
   QmParams P;

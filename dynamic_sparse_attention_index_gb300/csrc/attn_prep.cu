@@ -28,11 +28,14 @@ __global__ void prep_bands_kernel(AttnGeom g, const int32_t* __restrict__ s_idx,
 // then an in-order compaction into the union list.
 __global__ void __launch_bounds__(1024) prep_vunion_kernel(AttnGeom g, const int32_t* __restrict__ v_idx,
                                                            const int32_t* __restrict__ v_cnt,
-                                                           uint32_t* __restrict__ vlist, int32_t* __restrict__ vcnt) {
+                                                           uint32_t* __restrict__ vlist, int32_t* __restrict__ vcnt,
+                                                           uint32_t* __restrict__ gbits) {
   extern __shared__ uint32_t sm[];
   const int nwl = g.L / 32;
-  uint32_t* b0 = sm;
-  uint32_t* b1 = sm + nwl;
+  // the two heads' bitmaps: shared memory, or this pair's workspace slice
+  uint32_t* bits = gbits ? gbits + (size_t)blockIdx.x * 2 * nwl : sm;
+  uint32_t* b0 = bits;
+  uint32_t* b1 = bits + nwl;
   __shared__ int wsum[32];
   __shared__ int carry_s;
   const int vg = blockIdx.x;
@@ -44,7 +47,7 @@ __global__ void __launch_bounds__(1024) prep_vunion_kernel(AttnGeom g, const int
   } else {
     hs[0] = hs[1] = vg;
   }
-  for (int w = threadIdx.x; w < 2 * nwl; w += blockDim.x) sm[w] = 0;
+  for (int w = threadIdx.x; w < 2 * nwl; w += blockDim.x) bits[w] = 0;
   __syncthreads();
   for (int s = 0; s < 2; ++s) {
     uint32_t* b = s ? b1 : b0;
@@ -174,10 +177,11 @@ cudaError_t launch_attn_prep(const AttnGeom& g, const vs_index& ix, const void* 
   prep_bands_kernel<<<g.Hq, 256, g.nw * 4, s>>>(g, ix.s_idx, ix.s_cnt, pp.inS);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  const size_t sm = (size_t)2 * (g.L / 32) * 4;
+  const size_t bits = (size_t)2 * (g.L / 32) * 4;
+  const size_t sm = pp.vbits ? 0 : bits;
   e = cudaFuncSetAttribute(prep_vunion_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
   if (e != cudaSuccess) return e;
-  prep_vunion_kernel<<<g.nvg, 1024, sm, s>>>(g, ix.v_idx, ix.v_cnt, pp.vlist, pp.vcnt);
+  prep_vunion_kernel<<<g.nvg, 1024, sm, s>>>(g, ix.v_idx, ix.v_cnt, pp.vlist, pp.vcnt, pp.vbits);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   prep_pack_kernel<<<152 * 8, 256, 0, s>>>(g, static_cast<const __nv_bfloat16*>(K),
