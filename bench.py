@@ -270,30 +270,39 @@ def run_gpu(args):
     out_done = [torch.cuda.Event() for _ in range(2)]
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+
+    def e2e_steps(n):
+        s_in.wait_event(e0)
+        for i in range(n):
+            b = i & 1
+            slot = io[b]
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(comp_done[b])  # step i - 2 no longer reads these inputs
+                for dst, src in zip(slot[:4], (hQ, hK, hV, hdO)):
+                    dst.copy_(src, non_blocking=True)
+                in_done[b].record(s_in)
+            stream.wait_event(in_done[b])
+            if i >= 2:
+                stream.wait_event(out_done[b])  # step i - 2's results were copied out
+            step(io=slot)
+            comp_done[b].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(comp_done[b])
+                for dst, src in zip(hout[b], slot[4:]):
+                    dst.copy_(src, non_blocking=True)
+                out_done[b].record(s_out)
+        for b in range(min(2, n)):
+            stream.wait_event(out_done[b])
+
+    # one untimed pass over both buffer sets first (first use of the copy
+    # streams and of the second set of pinned host buffers)
     torch.cuda.synchronize()
     e0.record(stream)
-    s_in.wait_event(e0)
-    for i in range(args.steps):
-        b = i & 1
-        slot = io[b]
-        with torch.cuda.stream(s_in):
-            if i >= 2:
-                s_in.wait_event(comp_done[b])  # step i - 2 no longer reads these inputs
-            for dst, src in zip(slot[:4], (hQ, hK, hV, hdO)):
-                dst.copy_(src, non_blocking=True)
-            in_done[b].record(s_in)
-        stream.wait_event(in_done[b])
-        if i >= 2:
-            stream.wait_event(out_done[b])  # step i - 2's results were copied out
-        step(io=slot)
-        comp_done[b].record(stream)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(comp_done[b])
-            for dst, src in zip(hout[b], slot[4:]):
-                dst.copy_(src, non_blocking=True)
-            out_done[b].record(s_out)
-    for b in range(min(2, args.steps)):
-        stream.wait_event(out_done[b])
+    e2e_steps(min(2, args.steps))
+    torch.cuda.synchronize()
+    e0.record(stream)
+    e2e_steps(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps

@@ -91,7 +91,7 @@ struct SrcMeta {
   int32_t first, last;
   int32_t kv0, kv1;     // the unit's stationary keys: packed row (vertical) or (kv head, first key) (slash)
   int32_t pad;
-  long long t_issue;    // wait profiling: clock when the stage's loads were issued
+  long long t_issue;    // unused (kept for the 16-byte multiple size)
 };
 
 // shared memory plan (bytes, 1024-aligned)
@@ -111,6 +111,7 @@ constexpr int kNumBars = 2 + 2 * kStages + 6 + 2 + 2 * kMQ;
 constexpr int kMisc = kBars + kNumBars * 8;
 constexpr int kWaitCyc = kMisc + 64;
 constexpr int kSmemBytes = kWaitCyc + kWaitSites * 8;
+static_assert(kBars % 8 == 0 && kMisc % 8 == 0 && kWaitCyc % 8 == 0, "mbarriers and counters need 8-byte alignment");
 
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
@@ -196,6 +197,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* mq_empty = mq_full + kMQ;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc + 4);
+  // per Q / dO stage, written by the loader before it arms the stage's
+  // barrier: nsrc | first << 2 | last << 3 of the stage's tile (the MMA
+  // thread's one shared memory load per tile) and the issue clock (profiling)
+  volatile uint32_t* stage_word = reinterpret_cast<volatile uint32_t*>(sm + kMisc + 16);
+  long long* stage_t = reinterpret_cast<long long*>(sm + kMisc + 32);
   SrcMeta* mq = reinterpret_cast<SrcMeta*>(sm + kMeta);
   unsigned long long* wcyc = reinterpret_cast<unsigned long long*>(sm + kWaitCyc);
   const long long kernel_t0 = clock64();
@@ -212,13 +218,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sdp_full[i], 1);
-      mbar_init(&pds_ready[i], 256);
+      mbar_init(&pds_ready[i], 8);  // one arrival per P / dS warp
     }
     mbar_init(acc_done, 1);
-    mbar_init(acc_free, 256);
+    mbar_init(acc_free, 8);
     for (int i = 0; i < kMQ; ++i) {
       mbar_init(&mq_full[i], 1);
-      mbar_init(&mq_empty[i], 10);  // loader, MMA thread, eight P / dS warps
+      mbar_init(&mq_empty[i], 9);  // loader, eight P / dS warps
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -233,10 +239,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
   // TMEM: S[2] at 0, 64; dP[2] at 128, 192; dV^T at 256; dK^T at 320 (64 columns each)
+  // a phase that is already complete costs one probe; the abort flag is read
+  // only once that probe has failed
   auto wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
-    if (*abort_flag) return false;
     const long long w0 = kWaitProfileKv ? clock64() : 0;
-    const bool ok = mbar_wait(bar, parity, kWaitLimitNs);
+    bool ok = mbar_try_wait(bar, parity);
+    if (!ok) {
+      if (*abort_flag) return false;
+      ok = mbar_wait(bar, parity, kWaitLimitNs);
+    }
     if (kWaitProfileKv && (threadIdx.x & 31) == 0)
       atomicAdd(&wcyc[where & (kWaitSites - 1)], (unsigned long long)(clock64() - w0));
     if (ok) return true;
@@ -453,7 +464,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int h0 = mq[q].h[0], h1 = mq[q].h[1], I0 = mq[q].I[0], I1 = mq[q].I[1];
           const bool first = mq[q].first != 0;
           last = mq[q].last != 0;
-          if (kWaitProfileKv) mq[q].t_issue = clock64();
           mbar_arrive(&mq_empty[q]);
           if (first) {
             // stationary keys of the unit
@@ -474,6 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const long long e0 = kWaitProfileKv ? clock64() : 0;
           uint8_t* qd = sm + kStage + st * kStageBytes;
           uint8_t* od = qd + 2 * kHalfRows128;
+          stage_word[st] = (uint32_t)nsrc | (first ? 4u : 0u) | (last ? 8u : 0u);
+          if (kWaitProfileKv) stage_t[st] = clock64();
           mbar_arrive_expect_tx(&st_full[st], nsrc * 4 * 8192);
           for (int j = 0; j < nsrc; ++j) {
             const int h = j ? h1 : h0, row = (j ? I1 : I0) * kBlock;
@@ -502,18 +514,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       struct Pend {
         int nsrc, first, last, un;
       };
-      Pend pend[2] = {};
+      // Shared memory accesses of this thread wait behind its tcgen05.mma in
+      // flight, so the loop keeps its state in registers: the two pending
+      // tiles as named variables, the abort flag read only when idle.
+      Pend pend0 = {}, pend1 = {};
       int ts = 0, ta = 0;
       int uid = blockIdx.x, un = 0;
       long long idle0 = clock64();
       const long long idle_limit = (long long)(kWaitLimitNs * 21 / 10);
-      while (!*abort_flag) {
+      while (true) {
         const bool more = uid < nunits;
         if (!more && ta == ts) break;
         bool progressed = false;
         const long long i0 = kMmaProfileKv ? clock64() : 0;
         if (ta < ts && mbar_test_wait(&pds_ready[ta & 1], (ta >> 1) & 1)) {
-          const Pend q = pend[ta & 1];
+          const Pend q = (ta & 1) ? pend1 : pend0;
           if (q.first && q.un > 0 && !wait(acc_free, (q.un - 1) & 1, 11)) break;
           tc_fence_after();
           const int st = ta % kStages;
@@ -536,9 +551,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kMmaProfileKv) atomicAdd(&wcyc[25], (unsigned long long)(clock64() - i0));
         } else if (more && ts - ta < 2 && mbar_test_wait(&st_full[ts % kStages], (ts / kStages) & 1)) {
           const int st = ts % kStages;
-          const SrcMeta m = mq[ts % kMQ];
-          mbar_arrive(&mq_empty[ts % kMQ]);
-          if (kWaitProfileKv) atomicAdd(&wcyc[19], (unsigned long long)(clock64() - m.t_issue));
+          const uint32_t sw = stage_word[st];
+          const struct {
+            int nsrc, first, last;
+          } m = {(int)(sw & 3u), (int)((sw >> 2) & 1u), (int)((sw >> 3) & 1u)};
+          if (kWaitProfileKv) atomicAdd(&wcyc[19], (unsigned long long)(clock64() - stage_t[st]));
           if (m.first && !wait(kvs_full, un & 1, 13)) break;
           tc_fence_after();
           const uint32_t qa = smem_u32(sm + kStage + st * kStageBytes);
@@ -560,7 +577,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           // the stationary keys are read only by S and dP: release them now
           if (m.last) umma_commit(kvs_empty);
-          pend[ts & 1] = Pend{m.nsrc, m.first, m.last, un};
+          if (ts & 1)
+            pend1 = Pend{m.nsrc, m.first, m.last, un};
+          else
+            pend0 = Pend{m.nsrc, m.first, m.last, un};
           ++ts;
           if (m.last) {
             uid += gridDim.x;
@@ -571,6 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (progressed) {
           idle0 = clock64();
+        } else if (*abort_flag) {
+          break;
         } else if (clock64() - idle0 > idle_limit) {
           *abort_flag = 1;
           report_timeout(P.status, 12);
@@ -666,7 +688,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         fence_proxy_async_smem();
         tc_fence_before();
-        mbar_arrive(&pds_ready[t & 1]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pds_ready[t & 1]);
         if (kWaitProfileKv && lane == 0) atomicAdd(&wcyc[26], (unsigned long long)(clock64() - ph0));
         if (last) {
           // ---- epilogue: thread r holds dV^T[d = r][keys of this group] and dK^T likewise
@@ -678,7 +701,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_ld32(tbase + 320 + lane_off + col0, ak);
           tmem_ld_wait();
           tc_fence_before();
-          mbar_arrive(acc_free);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(acc_free);
           if (P.vertical) {
             VUnit u;
             decode_vunit(g, P.vcnt, uid, &u);

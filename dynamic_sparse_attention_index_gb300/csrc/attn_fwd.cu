@@ -52,6 +52,7 @@ struct TileMeta {
   int32_t nsrc;         // 1 or 2 sources of 64 keys
   int32_t first, last;  // first / last tile of the row tile
   int32_t qslot;
+  uint32_t mma;         // the MMA thread's copy: nsrc | first << 2 | last << 3 | qslot << 4
 };
 
 struct QmParams {
@@ -81,7 +82,7 @@ struct Layout {
   static constexpr int kKRing = 2 * kQBytes;
   static constexpr int kVRing = kKRing + kRK * kKBytes;
   static constexpr int kMeta = kVRing + kRV * kKBytes;
-  static constexpr int kBars = kMeta + kRK * (int)sizeof(TileMeta);
+  static constexpr int kBars = (kMeta + kRK * (int)sizeof(TileMeta) + 15) / 16 * 16;  // mbarriers: 8-byte aligned
   // q_full[2], q_empty[2], k_full[RK], k_empty[RK], v_full[RV], v_empty[RV], meta_free[RK],
   // s_full[2], p_ready[2], pv_done, o_free, dp_full, dp_free, ep_a, ep_b
   static constexpr int kNumBars = 2 + 2 + 3 * kRK + 2 * kRV + 2 + 2 + 1 + 1 + 1 + 1 + 2;
@@ -89,6 +90,7 @@ struct Layout {
   static constexpr int kWaitCyc = kMisc + 64;             // per-site wait cycle counters
   static constexpr int kXchg = kWaitCyc + kWaitSites * 8; // epilogue row exchange: 128 x 2 floats
   static constexpr int kSmemEnd = kXchg + 128 * 2 * 4;
+  static_assert(kBars % 8 == 0 && kMisc % 8 == 0 && kWaitCyc % 8 == 0, "mbarriers and counters need 8-byte alignment");
 };
 
 __device__ __forceinline__ float fast_exp2(float x) {
@@ -170,23 +172,23 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&q_full[i], 1);
       mbar_init(&q_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_ready[i], 256);
+      mbar_init(&p_ready[i], 8);  // one arrival per softmax warp
     }
     for (int i = 0; i < Ly::kRK; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
-      mbar_init(&meta_free[i], 256);
+      mbar_init(&meta_free[i], 8);
     }
     for (int i = 0; i < Ly::kRV; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
     }
     mbar_init(pv_done, 1);
-    mbar_init(o_free, 256);
-    mbar_init(ep_a, 128);
-    mbar_init(ep_b, 128);
+    mbar_init(o_free, 8);
+    mbar_init(ep_a, 4);
+    mbar_init(ep_b, 4);
     mbar_init(dp_full, 1);
-    mbar_init(dp_free, 256);
+    mbar_init(dp_free, 8);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -201,10 +203,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tbase = *tmem_slot;
 
   long long wl[20] = {};  // profiling (light mode): this thread's wait cycles of sites < 20
+  // A phase that is already complete costs one probe and no other shared
+  // memory access: each shared memory access of the MMA thread waits behind
+  // its tcgen05.mma in flight, so the abort flag is read only once the first
+  // probe has failed.
   auto wait = [&](uint64_t* bar, uint32_t parity, int where) -> bool {
-    if (*abort_flag) return false;
     const long long w0 = (kWaitProfileQm || kSmProfileQm) ? clock64() : 0;
-    const bool ok = mbar_wait(bar, parity, kWaitLimitNs);
+    bool ok = mbar_try_wait(bar, parity);
+    if (!ok) {
+      if (*abort_flag) return false;
+      ok = mbar_wait(bar, parity, kWaitLimitNs);
+    }
     if (kWaitProfileQm && (threadIdx.x & 31) == 0)
       atomicAdd(&wcyc[where & (kWaitSites - 1)], (unsigned long long)(clock64() - w0));
     if (kSmProfileQm && where < 20) wl[where] += clock64() - w0;
@@ -340,6 +349,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             m.first = first ? 1 : 0;
             m.last = last ? 1 : 0;
             m.qslot = qslot;
+            m.mma = (uint32_t)nsrc | (first ? 4u : 0u) | (last ? 8u : 0u) | ((uint32_t)qslot << 4);
             uint8_t* kst = sm + Ly::kKRing + sk * Ly::kKBytes;
             mbar_arrive_expect_tx(&k_full[sk], nsrc * Ly::kHalves * 8192);
             for (int j = 0; j < nsrc; ++j)
@@ -511,10 +521,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int sk = t % Ly::kRK, sv = t % Ly::kRV;
           if (!wait(&k_full[sk], (t / Ly::kRK) & 1, 12)) break;
           const long long mc0 = kSmProfileQm ? clock64() : 0;
-          // only the fields the MMA thread uses
+          // one shared memory load for the fields the MMA thread uses
+          const uint32_t mw = metas[sk].mma;
           const struct {
             int nsrc, first, last, qslot;
-          } m = {metas[sk].nsrc, metas[sk].first, metas[sk].last, metas[sk].qslot};
+          } m = {(int)(mw & 3u), (int)((mw >> 2) & 1u), (int)((mw >> 3) & 1u), (int)(mw >> 4)};
           last = m.last != 0;
           if (m.first)
             if (!wait(&q_full[m.qslot], (it_local / Ly::kQSlots) & 1, 13)) break;
@@ -573,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             have_prev = false;
           }
           ++t;
-        } while (!last && !*abort_flag);
+        } while (!last);  // a failed wait (timeout or abort) leaves by break
       }
       if (have_prev && !*abort_flag) issue_acc();
     }
@@ -611,7 +622,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t mw0 = metas[sk].mask[seg][2 * grp], mw1 = metas[sk].mask[seg][2 * grp + 1];
         const int md = src_mode(mw0, mw1, metas[sk].diag[seg] == 64 * grp);
         last = metas[sk].last != 0;
-        mbar_arrive(&meta_free[sk]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&meta_free[sk]);
         if (!wait_warp(&s_full[t & 1], (t >> 1) & 1, 21)) break;
         const long long q1 = kSmProfileQm ? clock64() : 0;
         if (kSmProfileQm) pw += q1 - q0;
@@ -629,7 +641,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // dP is released as soon as it has been read: the next tile's
             // dP = dO V^T then overlaps this tile's arithmetic
             tc_fence_before();
-            mbar_arrive(dp_free);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dp_free);
 #pragma unroll
             for (int k = 0; k < 32; ++k) pk[k] = 0u;
           } else {
@@ -638,7 +651,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld64(tbase + kDPCol + lane_off + 64 * grp, dv);
             tmem_ld_wait();
             tc_fence_before();
-            mbar_arrive(dp_free);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(dp_free);
             if (md == kSrcFull) {
               const uint64_t cc = f2pack(c2, c2), ll = f2pack(-lse2, -lse2);
 #pragma unroll
@@ -729,7 +743,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           atomicAdd(&wcyc[28], (unsigned long long)(clock64() - ph1));
         }
         tc_fence_before();
-        mbar_arrive(&p_ready[t & 1]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_ready[t & 1]);
         if (kSmProfileQm) pk_ += clock64() - q1;
         if (last) {
           const long long pe0 = clock64();
@@ -762,7 +777,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (grp == 1) {
               xch[2 * r] = m_ref;
               xch[2 * r + 1] = l;
-              mbar_arrive(ep_a);
+              __syncwarp();
+              if (lane == 0) mbar_arrive(ep_a);
               if (!wait_warp(ep_b, it_local & 1, 5)) break;
               ca = xch[2 * r];
               cb = xch[2 * r + 1];
@@ -780,7 +796,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 P.lse[(size_t)h * g.L + tok] = ltot > 0.f ? (m + __log2f(ltot)) * 0.69314718055994531f : kNegInf;
               xch[2 * r] = ca;
               xch[2 * r + 1] = cb;
-              mbar_arrive(ep_b);
+              __syncwarp();
+              if (lane == 0) mbar_arrive(ep_b);
             }
             // this group's half of the output columns from both accumulators
             const uint32_t tA = tbase + 256 + lane_off + grp * (D / 2), tB = tA + 128;
@@ -805,7 +822,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           tc_fence_before();
-          mbar_arrive(o_free);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(o_free);
           if (kWaitProfileQm && lane == 0) atomicAdd(&wcyc[30], (unsigned long long)(clock64() - pe0));
           if (kSmProfileQm) pe += clock64() - pe0;
         }

@@ -53,10 +53,6 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for phase `parity` of `bar` to complete, for at most about `limit_ns`
-// nanoseconds (measured in SM cycles at up to 2.1 GHz) and at most 2^24 polls.
-// Returns false on timeout (the caller records an error and unwinds instead
-// of spinning forever).
 // The same probe with a suspend-time hint: a thread whose phase is not yet
 // complete sleeps (issuing nothing) until the phase completes or about
 // `hint_ns` pass, instead of spinning and taking issue slots from the warps
@@ -71,6 +67,10 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
       : "memory");
   return ok != 0;
 }
+// Wait for phase `parity` of `bar` to complete, for at most about `limit_ns`
+// nanoseconds (measured in SM cycles at up to 2.1 GHz) and at most 2^24 polls.
+// Returns false on timeout (the caller records an error and unwinds instead
+// of spinning forever).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long c0 = clock64();
