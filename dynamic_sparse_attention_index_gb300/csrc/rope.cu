@@ -5,9 +5,10 @@
 // and phi = t * theta_i:  y_i = c (x_i cos phi - x_{i+d/2} sin phi),
 // y_{i+d/2} = c (x_{i+d/2} cos phi + x_i sin phi), c the YaRN temperature.
 //
-// One thread owns (token t, channel pair i) and walks all H heads, so the
-// angle is formed once per (t, i): the product t * theta_i and its reduction
-// to [-pi, pi] are done in fp64 (t reaches 2^20, where an fp32 product would
+// One thread owns (token t, 8 consecutive channel pairs) and walks all H
+// heads, so each angle is formed once per (t, i) and every access is a
+// 16-byte vector (8 bf16): the product t * theta_i and its reduction to
+// [-pi, pi] are done in fp64 (t reaches 2^20, where an fp32 product would
 // lose whole radians), the sine and cosine of the reduced angle in fp32.
 #include <cuda_bf16.h>
 
@@ -18,31 +19,47 @@ namespace vs {
 __global__ void __launch_bounds__(256) rope_kernel(const __nv_bfloat16* x, __nv_bfloat16* y,
                                                    int L, int H, int d, int transpose, float mscale,
                                                    RopeArgs freqs) {
-  const int half = d >> 1;
+  const int half = d >> 1, ng = half >> 3;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (long long)L * half) return;
-  const int t = (int)(idx / half);
-  const int i = (int)(idx - (long long)t * half);
+  if (idx >= (long long)L * ng) return;
+  const int t = (int)(idx / ng);
+  const int g = (int)(idx - (long long)t * ng);
   const double kTwoPi = 6.283185307179586476925286766559;
-  double phi = (double)t * freqs.inv_freq[i];
-  phi -= kTwoPi * rint(phi / kTwoPi);
-  float sn, cs;
-  sincosf((float)phi, &sn, &cs);
-  if (transpose) sn = -sn;
-  cs *= mscale;
-  sn *= mscale;
-  const size_t row = (size_t)t * H * d;
+  float cs[8], sn[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    double phi = (double)t * freqs.inv_freq[8 * g + k];
+    phi -= kTwoPi * rint(phi / kTwoPi);
+    float s1, c1;
+    sincosf((float)phi, &s1, &c1);
+    if (transpose) s1 = -s1;
+    cs[k] = c1 * mscale;
+    sn[k] = s1 * mscale;
+  }
+  const size_t row = (size_t)t * H * d + 8 * g;
   for (int h = 0; h < H; ++h) {
-    const size_t o = row + (size_t)h * d + i;
-    const float a = __bfloat162float(x[o]);
-    const float b = __bfloat162float(x[o + half]);
-    y[o] = __float2bfloat16_rn(a * cs - b * sn);
-    y[o + half] = __float2bfloat16_rn(b * cs + a * sn);
+    const size_t o = row + (size_t)h * d;
+    const uint4 va = *reinterpret_cast<const uint4*>(x + o);
+    const uint4 vb = *reinterpret_cast<const uint4*>(x + o + half);
+    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&va);
+    const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&vb);
+    uint4 ya, yb;
+    __nv_bfloat162* qa = reinterpret_cast<__nv_bfloat162*>(&ya);
+    __nv_bfloat162* qb = reinterpret_cast<__nv_bfloat162*>(&yb);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float2 a = __bfloat1622float2(pa[k]), b = __bfloat1622float2(pb[k]);
+      const int k0 = 2 * k, k1 = 2 * k + 1;
+      qa[k] = __floats2bfloat162_rn(a.x * cs[k0] - b.x * sn[k0], a.y * cs[k1] - b.y * sn[k1]);
+      qb[k] = __floats2bfloat162_rn(b.x * cs[k0] + a.x * sn[k0], b.y * cs[k1] + a.y * sn[k1]);
+    }
+    *reinterpret_cast<uint4*>(y + o) = ya;
+    *reinterpret_cast<uint4*>(y + o + half) = yb;
   }
 }
 
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s) {
-  const long long n = (long long)a.L * (a.d / 2);
+  const long long n = (long long)a.L * (a.d / 16);
   const int threads = 256;
   const long long blocks = (n + threads - 1) / threads;
   rope_kernel<<<(unsigned)blocks, threads, 0, s>>>(static_cast<const __nv_bfloat16*>(a.x),
