@@ -78,6 +78,10 @@ vs_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
 
 vs_status check_index_ptrs(const vs_index* ix) {
   if (!ix || !ix->v_idx || !ix->v_cnt || !ix->s_idx || !ix->s_cnt) return VS_ERR_INVALID_ARG;
+  // every data pointer 16-byte aligned (the selection reads v_score as 16-byte vectors)
+  const void* ptrs[] = {ix->v_idx, ix->v_cnt, ix->s_idx, ix->s_cnt, ix->v_score, ix->s_score, ix->active_entries};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return VS_ERR_INVALID_ARG;
   return VS_OK;
 }
 

@@ -236,21 +236,40 @@ __device__ int compact_select(const float* x, int n, uint32_t tau, unsigned n_ti
 }
 
 // notS[x] = #{B in [1, x] : B not kept}; kept given by inS (0/1 per band).
+// Block-wide scan: each thread counts a run of consecutive bands, the warps
+// scan their threads' counts, warp 0 the warps' totals.
 __device__ void build_notS(const uint8_t* inS, int32_t* notS, int nbs, SelShared& s) {
-  // single-warp scan is plenty for nbs <= 16384
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    int carry = 0;
-    for (int base = 0; base < nbs; base += 32) {
-      const int b = base + lane;
-      const int v = (b >= 1 && b < nbs && !inS[b]) ? 1 : 0;
-      int incl = v;
-      for (int o = 1; o < 32; o <<= 1) {
-        const int t = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += t;
-      }
-      if (b < nbs) notS[b] = carry + incl;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int per = (nbs + kThreads - 1) / kThreads;
+  const int b0 = threadIdx.x * per;
+  int cnt = 0;
+  for (int j = 0; j < per; ++j) {
+    const int b = b0 + j;
+    if (b >= 1 && b < nbs && !inS[b]) ++cnt;
+  }
+  int incl = cnt;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) s.wcnt[warp] = (unsigned)incl;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = (int)s.wcnt[lane];
+    int wi = w;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += t;
+    }
+    s.wcnt2[lane] = (unsigned)(wi - w);  // bands counted by the warps before this one
+  }
+  __syncthreads();
+  int run = (int)s.wcnt2[warp] + incl - cnt;  // not-kept bands before this thread's run
+  for (int j = 0; j < per; ++j) {
+    const int b = b0 + j;
+    if (b < nbs) {
+      if (b >= 1 && !inS[b]) ++run;
+      notS[b] = run;
     }
   }
   __syncthreads();
@@ -266,18 +285,9 @@ __device__ unsigned long long slash_entries(const uint8_t* inS, int nbs, int bs,
   return block_sum_u64(e, s);
 }
 
-// Vertical entries for threshold key tau (keep m iff key(v[m]) >= tau).
 // Budget fill: verticals whose key reached the running threshold, gathered in
 // shared memory once they fit, so later threshold probes skip the full list.
 constexpr int kCandCap = 8192;
-
-__device__ unsigned long long vert_entries_at(const float* v, int L, uint32_t tau, const int32_t* notS, int nbs,
-                                              int bs, SelShared& s) {
-  unsigned long long e = 0;
-  for (int m = threadIdx.x; m < L; m += kThreads)
-    if (key_of(v[m]) >= tau) e += (unsigned long long)notS[nbs - 1 - m / bs];
-  return block_sum_u64(e, s) * (unsigned long long)bs;
-}
 
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) {
   extern __shared__ __align__(16) uint8_t dyn[];
@@ -378,11 +388,19 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) 
       const unsigned long long se = slash_entries(inS, nbs, bs, s);
       unsigned long long ve = 0, c = 0;
       if (ncand < 0) {
-        for (int m = threadIdx.x; m < L; m += kThreads)
-          if (key_of(v[m]) >= tau) {
-            ve += (unsigned long long)notS[nbs - 1 - m / bs];
-            ++c;
+        // four verticals per 16-byte load (L and bs are multiples of 64, so
+        // the four share a key block)
+        const float4* v4 = reinterpret_cast<const float4*>(v);
+#pragma unroll 4
+        for (int q = threadIdx.x; q < L / 4; q += kThreads) {
+          const float4 x = v4[q];
+          const unsigned n4 = (key_of(x.x) >= tau) + (key_of(x.y) >= tau) + (key_of(x.z) >= tau) +
+                              (key_of(x.w) >= tau);
+          if (n4) {
+            ve += (unsigned long long)n4 * (unsigned long long)notS[nbs - 1 - (4 * q) / bs];
+            c += n4;
           }
+        }
       } else {
         for (int i = threadIdx.x; i < ncand; i += kThreads)
           if (ckey[i] >= tau) {

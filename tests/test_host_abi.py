@@ -74,6 +74,7 @@ def test_index_rejects_bad_pointers_and_workspace(vs):
     assert _call_index(vs, p, q=None) == vs.VS_ERR_INVALID_ARG
     assert _call_index(vs, p, q=FAKE + 2) == vs.VS_ERR_INVALID_ARG       # misaligned
     assert _call_index(vs, p, ix=vs.vs_index(None, FAKE, FAKE, FAKE, None, None, None)) == vs.VS_ERR_INVALID_ARG
+    assert _call_index(vs, p, ix=vs.vs_index(FAKE, FAKE, FAKE, FAKE, FAKE + 4, None, None)) == vs.VS_ERR_INVALID_ARG
     assert _call_index(vs, p, ws=None) == vs.VS_ERR_WORKSPACE
     assert _call_index(vs, p, ws=FAKE + 16) == vs.VS_ERR_WORKSPACE       # not 256-aligned
     assert _call_index(vs, p, ws_bytes=16) == vs.VS_ERR_WORKSPACE
