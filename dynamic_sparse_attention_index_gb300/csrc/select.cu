@@ -235,6 +235,60 @@ __device__ int compact_select(const float* x, int n, uint32_t tau, unsigned n_ti
   return base;
 }
 
+// The same compaction for {i : key_i > tau} alone (no ties) over a 16-byte
+// aligned x with n a multiple of 4: each thread takes four consecutive
+// elements per pass, a warp scan and one scan of the warp totals place them.
+__device__ int compact_above(const float* x, int n, uint32_t tau, int32_t* out, const int32_t* notS, int nbs,
+                             int bs, unsigned long long* vert_entries, SelShared& s) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float4* x4 = reinterpret_cast<const float4*>(x);
+  int base = 0;
+  unsigned long long ve = 0;
+  for (int start = 0; start < n / 4; start += kThreads) {
+    const int q = start + threadIdx.x;
+    bool k0 = false, k1 = false, k2 = false, k3 = false;
+    if (q < n / 4) {
+      const float4 v = x4[q];
+      k0 = key_of(v.x) > tau;
+      k1 = key_of(v.y) > tau;
+      k2 = key_of(v.z) > tau;
+      k3 = key_of(v.w) > tau;
+    }
+    const int cnt = (int)k0 + (int)k1 + (int)k2 + (int)k3;
+    int incl = cnt;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int t = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += t;
+    }
+    if (lane == 31) s.wcnt[warp] = (unsigned)incl;
+    __syncthreads();
+    if (warp == 0) {
+      const int w = (int)s.wcnt[lane];
+      int wi = w;
+      for (int o = 1; o < 32; o <<= 1) {
+        const int t = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) wi += t;
+      }
+      s.wcnt2[lane] = (unsigned)(wi - w);
+      if (lane == 31) s.bcast_u32[3] = (unsigned)wi;
+    }
+    __syncthreads();
+    int o = base + (int)s.wcnt2[warp] + incl - cnt;
+    const int total = (int)s.bcast_u32[3];
+    if (cnt) {
+      const int i0 = 4 * q;
+      if (notS) ve += (unsigned long long)bs * (unsigned long long)cnt * (unsigned long long)notS[nbs - 1 - i0 / bs];
+      if (k0) out[o++] = i0;
+      if (k1) out[o++] = i0 + 1;
+      if (k2) out[o++] = i0 + 2;
+      if (k3) out[o++] = i0 + 3;
+    }
+    base += total;
+  }
+  if (vert_entries) *vert_entries = block_sum_u64(ve, s);
+  return base;
+}
+
 // notS[x] = #{B in [1, x] : B not kept}; kept given by inS (0/1 per band).
 // Block-wide scan: each thread counts a run of consecutive bands, the warps
 // scan their threads' counts, warp 0 the warps' totals.
@@ -408,9 +462,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) 
             ++c;
           }
       }
-      ve = block_sum_u64(ve, s) * (unsigned long long)bs;
-      nabove = block_sum_u64(c, s);
-      return se + ve;
+      // the block totals stay below 2^34 (ve) and 2^21 (c): one block sum carries both
+      const unsigned long long both = block_sum_u64((ve << 21) | c, s);
+      nabove = both & ((1ull << 21) - 1ull);
+      return se + (both >> 21) * (unsigned long long)bs;
     };
     auto gather = [&](uint32_t tau) {
       if (ncand >= 0 || nabove > (unsigned long long)kCandCap) return;
@@ -458,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) 
     }
     __syncthreads();
     ++ns;
-    nv = compact_select(v, L, tau - 1u, 0u, vout, notS, nbs, bs, &vert_e, s, -1);
+    nv = compact_above(v, L, tau - 1u, vout, notS, nbs, bs, &vert_e, s);
   }
   if (threadIdx.x == 0) {
     a.v_cnt[h] = nv;
