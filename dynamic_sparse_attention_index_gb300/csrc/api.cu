@@ -141,7 +141,9 @@ vs_status vs_rope(const vs_params* p, int32_t H, const void* x, void* y, int32_t
       g = g < 0.0 ? 0.0 : (g > 1.0 ? 1.0 : g);
       f = f * (g + (1.0 - g) / s);
     }
-    a.inv_freq[i] = f;
+    // f / (2 pi) < 1; its double value scaled by 2^64 converts to uint64 exactly
+    const double turns = f / (2.0 * 3.14159265358979323846);
+    a.turn[i] = turns < 1.0 ? (uint64_t)(turns * 18446744073709551616.0) : ~0ull;
   }
   a.mscale = s > 1.0 ? (float)(0.1 * std::log(s) + 1.0) : 1.0f;
   return launch_rope(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? VS_OK : VS_ERR_CUDA;

@@ -74,7 +74,7 @@ struct RopeArgs {
   int32_t L, H, d;
   int32_t transpose;
   float mscale;
-  double inv_freq[64];  // d/2 <= 64 frequencies, host-computed in fp64
+  uint64_t turn[64];  // theta_i / (2 pi) as a 0.64 fixed-point fraction, d/2 <= 64 (host-computed in fp64)
 };
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s);
 

@@ -7,9 +7,13 @@
 //
 // One thread owns (token t, 8 consecutive channel pairs) and walks all H
 // heads, so each angle is formed once per (t, i) and every access is a
-// 16-byte vector (8 bf16): the product t * theta_i and its reduction to
-// [-pi, pi] are done in fp64 (t reaches 2^20, where an fp32 product would
-// lose whole radians), the sine and cosine of the reduced angle in fp32.
+// 16-byte vector (8 bf16).  The angle t * theta_i is reduced modulo 2 pi in
+// 64-bit fixed point: with theta_i / (2 pi) held as a 0.64 fraction, the
+// wrapping integer product t * frac_i is the angle's fraction of a turn,
+// exact up to the fraction's rounding (t reaches 2^20, where an fp32 product
+// would lose whole radians; fp64 arithmetic is slow on this GPU).  Its top
+// 32 bits read as a signed integer give the angle in [-pi, pi); the sine and
+// cosine are taken in fp32.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -24,14 +28,14 @@ __global__ void __launch_bounds__(256) rope_kernel(const __nv_bfloat16* x, __nv_
   if (idx >= (long long)L * ng) return;
   const int t = (int)(idx / ng);
   const int g = (int)(idx - (long long)t * ng);
-  const double kTwoPi = 6.283185307179586476925286766559;
+  const float kTurnToRad = 1.4629180792671596e-09f;  // 2 pi / 2^32
   float cs[8], sn[8];
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
-    double phi = (double)t * freqs.inv_freq[8 * g + k];
-    phi -= kTwoPi * rint(phi / kTwoPi);
+    const uint64_t frac = (uint64_t)t * freqs.turn[8 * g + k];  // modulo 2^64: the fraction of a turn
+    const float phi = (float)(int32_t)(uint32_t)(frac >> 32) * kTurnToRad;
     float s1, c1;
-    sincosf((float)phi, &s1, &c1);
+    sincosf(phi, &s1, &c1);
     if (transpose) s1 = -s1;
     cs[k] = c1 * mscale;
     sn[k] = s1 * mscale;
