@@ -2,7 +2,6 @@
 // validation (host, before any launch), workspace layout, and launches.
 #include <cmath>
 #include <cstring>
-#include <mutex>
 
 #include "common.cuh"
 
@@ -112,7 +111,7 @@ size_t vs_workspace_bytes(const vs_params* p, int op) {
   }
   if (check_params(p) != VS_OK) return 0;
   if (op == VS_OP_FWD) return attn_fwd_ws_bytes(*p);
-  if (op == VS_OP_BWD) return attn_bwd_ws_bytes(*p);
+  if (op == VS_OP_BWD) return p->d == 128 ? attn_bwd_ws_bytes(*p) : 0;
   return 0;
 }
 
@@ -157,6 +156,10 @@ vs_status vs_index_build(const vs_params* p, const void* Q, const void* K, const
   if ((st = check_index_ptrs(out)) != VS_OK) return st;
   const IndexWs lay = index_ws(*p);
   if ((st = check_ws(ws, ws_bytes, lay.total)) != VS_OK) return st;
+  // every host-side check comes before the first enqueue: a rejected call
+  // leaves the stream and the workspace untouched
+  const int nbs_check = p->L / (kBlock * p->stripes);
+  if (select_smem_bytes(nbs_check) + 26 * 1024 > 227 * 1024) return VS_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   if (cudaMemsetAsync(w + lay.status, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
@@ -190,7 +193,6 @@ vs_status vs_index_build(const vs_params* p, const void* Q, const void* K, const
   a.s_cnt = out->s_cnt;
   a.active = out->active_entries;
   a.status = reinterpret_cast<DevStatus*>(w + lay.status);
-  if (select_smem_bytes(a.nbs) + 26 * 1024 > 227 * 1024) return VS_ERR_UNSUPPORTED;
   if (launch_index_scores(a, s) != cudaSuccess) return VS_ERR_CUDA;
   if (launch_select(a, s) != cudaSuccess) return VS_ERR_CUDA;
   return VS_OK;
@@ -218,24 +220,15 @@ namespace {
 // earlier call left behind does not matter.
 static __device__ __align__(256) unsigned char g_index_scratch[VS_INDEX_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_addr[kMaxDevices];  // device address of g_index_scratch, per device
-
 // Host code sees g_index_scratch only as a host-side shadow symbol, never as
-// a device address: the address is resolved with cudaGetSymbolAddress, once
-// per device with that device current (on its first use there), and cached.
+// a device address.  Every call resolves the array's address on the current
+// device with cudaGetSymbolAddress (a host-side query that allocates
+// nothing).  Nothing is cached, so the address stays right after a
+// cudaDeviceReset or a change of the current device between calls.
 vs_status noalloc_scratch(void** out) {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return VS_ERR_CUDA;
-  if (dev < 0 || dev >= kMaxDevices) return VS_ERR_UNSUPPORTED;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_addr[dev]) {
-    void* a = nullptr;
-    if (cudaGetSymbolAddress(&a, g_index_scratch) != cudaSuccess || !a) return VS_ERR_CUDA;
-    g_scratch_addr[dev] = a;
-  }
-  *out = g_scratch_addr[dev];
+  void* a = nullptr;
+  if (cudaGetSymbolAddress(&a, g_index_scratch) != cudaSuccess || !a) return VS_ERR_CUDA;
+  *out = a;
   return VS_OK;
 }
 
@@ -274,6 +267,7 @@ vs_status vs_sparse_attn_bwd(const vs_params* p, const vs_index* index, const vo
   vs_status st = check_params(p);
   if (st != VS_OK) return st;
   if ((st = check_index_ptrs(index)) != VS_OK) return st;
+  if (p->d != 128) return VS_ERR_UNSUPPORTED;  // the backward kernels are built for d = 128
   if (!Q || !K || !V || !O || !lse || !dO || !dQ || !dK || !dV) return VS_ERR_INVALID_ARG;
   const void* ptrs[] = {Q, K, V, O, lse, dO, dQ, dK, dV};
   for (const void* q : ptrs)

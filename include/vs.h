@@ -133,8 +133,10 @@ VS_API vs_status vs_index_build(const vs_params* p, const void* Q, const void* K
  *     VS_INDEX_NOALLOC_SCRATCH_BYTES are rejected with VS_ERR_WORKSPACE
  *     before anything is launched (e.g. L = 32768, Hq = 16, last_q = 64
  *     needs 5 MiB and fits; L = 131072 with 16 heads does not).
- *   - Set-up: the first call on a device resolves the array's address on
- *     that device (which must be current) and caches it; make that first
+ *   - Set-up: every call looks up the array's address on the current
+ *     device (cudaGetSymbolAddress, a host-side query; nothing is cached,
+ *     so a cudaDeviceReset between calls is harmless).  The first call on a
+ *     device also loads the library's device code there: make that first
  *     call before any stream capture begins.
  *   - Zeroing: the array keeps what the last call left in it.  Only the
  *     status block at its head must start at zero, and every call clears it

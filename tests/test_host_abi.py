@@ -88,9 +88,15 @@ def test_attention_rejects_bad_args(vs):
     assert r == vs.VS_ERR_INVALID_ARG
     r = L.vs_sparse_attn_fwd(ctypes.byref(p), ctypes.byref(ix), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 8, None)
     assert r == vs.VS_ERR_WORKSPACE
-    r = L.vs_sparse_attn_bwd(ctypes.byref(p), ctypes.byref(ix), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+    p128 = vs.make_params(4096, 4, 2, 128)
+    r = L.vs_sparse_attn_bwd(ctypes.byref(p128), ctypes.byref(ix), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
                              FAKE, None, FAKE, 1 << 40, None)
     assert r == vs.VS_ERR_INVALID_ARG
+    d64 = vs.make_params(4096, 4, 2, 64)
+    assert vs.vs_workspace_bytes(d64, vs.VS_OP_BWD) == 0
+    r = L.vs_sparse_attn_bwd(ctypes.byref(d64), ctypes.byref(ix), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+                             FAKE, FAKE, FAKE, 1 << 40, None)
+    assert r == vs.VS_ERR_UNSUPPORTED  # the backward is built for d = 128 only; rejected before any launch
     bad = vs.make_params(4096, 4, 2, 80)
     r = L.vs_sparse_attn_fwd(ctypes.byref(bad), ctypes.byref(ix), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 40, None)
     assert r == vs.VS_ERR_UNSUPPORTED

@@ -3,10 +3,12 @@
 vs_index_build_noalloc serves callers that cannot hand the library a
 workspace (an allocator at its cap, a device footprint fixed at load time, a
 pipeline that must not stall on cudaMalloc): it runs the same kernels on a
-static scratch array inside the library.  Two calls are issued back to back on
-one stream with no synchronisation between them (different problems; the
-second without score outputs, so the scratch's own score arrays are used) and
-each result is compared with vs_index_build on the same inputs.  Index work is
+static scratch array inside the library.  The calls are issued back to back on
+one stream with no synchronisation between them (different problems; some
+without score outputs, so the scratch's own score arrays are used; a small
+problem repeated after a large one, so its scratch holds leftovers at every
+offset the small layout reads; a striped problem) and each result is
+compared with vs_index_build on the same inputs.  Index work is
 compared bit for bit, as everywhere in these tests.  The file sorts last, so
 a run that stops at the first failure has run every other test before it.
 """
@@ -19,9 +21,9 @@ from _util import to_dev
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(vs, dev, wid, L, Hq, Hkv, density, scores):
+def _inputs(vs, dev, wid, L, Hq, Hkv, density, scores, stripes=1):
     w = synth.make_workload(wid, L=L, Hq=Hq, Hkv=Hkv, d=128)
-    p = vs.make_params(L, Hq, Hkv, 128, last_q=w.last_q, top_p=w.top_p, density=density)
+    p = vs.make_params(L, Hq, Hkv, 128, last_q=w.last_q, top_p=w.top_p, density=density, stripes=stripes)
     Q, K = to_dev(w.q, dev), to_dev(w.k, dev)
     return p, Q, K, vs.IndexBuffers.allocate(p, dev, scores=scores)
 
@@ -42,13 +44,17 @@ def _same(a, b):
             assert np.array_equal(a[k], b[k]), k
 
 
-def test_noalloc_two_calls_match_index_build():
+def test_noalloc_calls_in_a_row_match_index_build():
     import torch
     import dynamic_sparse_attention_index_gb300 as vs
     dev = torch.device("cuda:0")
     problems = [
         dict(wid=3, L=4096, Hq=8, Hkv=2, density=0.0, scores=True),      # top-p selection
         dict(wid=1, L=32768, Hq=16, Hkv=2, density=0.05, scores=False),  # budget fill, near the size limit
+        # the first problem again, now over the larger problem's leftovers at
+        # every scratch offset it reads
+        dict(wid=3, L=4096, Hq=8, Hkv=2, density=0.0, scores=True),
+        dict(wid=4, L=8192, Hq=4, Hkv=2, density=0.05, scores=False, stripes=4),  # striped bands
     ]
     cases = [_inputs(vs, dev, **c) for c in problems]
     for p, _, _, _ in cases:
