@@ -35,16 +35,27 @@ import numpy as np  # noqa: E402
 import synth  # noqa: E402
 
 WORKLOADS = {
-    # name -> (recipe id, overrides)
+    # name -> (recipe id, overrides); forward-only recipes time RoPE, index and forward
     "gqa16x2_L131072_d128_fwdbwd": (3, {}),
     "gqa16x2_L32768_d128_fwdbwd": (3, {"L": 32768}),   # small case for profiling
     # striped layout emulation: 32 round-robin shards (slash tiles of 64 x 32 tokens)
     "gqa16x2_L262144_d128_striped32_fwdbwd": (4, {}),
     "gqa16x2_L65536_d128_striped32_fwdbwd": (4, {"L": 65536}),
+    # single head, L = 4096, d = 64, forward only (8 outlier keys x 8)
+    "mha1_L4096_d64_fwd": (1, {}),
+    # 8-head MHA, L = 32768, forward only, per-head slash-shaped local bias
+    "mha8_L32768_d128_fwd_localbias": (2, {}),
+    # Llama-3.1-8B attention shape: GQA 32/8, L = 524288, YaRN x32 (base 5e5)
+    "gqa32x8_L524288_d128_fwdbwd_yarn32": (5, {}),
 }
 DENSITY = 0.05     # budget fill: 95 % sparsity (fixed in the pages' experiments)
 LAST_Q, TOP_P = 64, 0.95
 KERNELS_PER_STEP = {"rope": 4, "index": 5, "fwd": 4, "bwd": 8}
+KERNELS_PER_STEP_FWD = {"rope": 2, "index": 5, "fwd": 4}
+# ex2.approx issue rate of one SM per clock (the index's exponentials;
+# measured with a standalone microbenchmark on this GPU)
+MUFU_EX2_PER_CLK_SM = 32
+N_SM = 152
 # DRAM bytes of one backward call (dram__bytes_read.sum + dram__bytes_write.sum
 # over its kernels, one-pass ncu capture of this workload); measured for the
 # current backward kernels and to be taken again whenever they change
@@ -138,6 +149,36 @@ def replica_throughput(dist, world, flops_per_rank, ms, e2e_ms, device):
             e2e_ms)
 
 
+def index_roofline(w, A_index_time_ms, kept, pk, sm_mhz):
+    """Index build against its binding roof.  Algorithmic work of one build
+    (the minimum the method needs): K read once, the last_q query rows read,
+    the vertical and slash masses written once and read once by the
+    selection, the kept lists written; one QK^T over the last_q rows
+    (2 d last_q Hq L flop) and one exponential per score (last_q Hq L).
+    The roof is the largest of the three times at the measured HBM and bf16
+    peaks and the ex2 rate (MUFU_EX2_PER_CLK_SM x SMs x the maximum SM
+    clock)."""
+    L, Hq, Hkv, d, q = w.L, w.Hq, w.Hkv, w.d, LAST_Q
+    nbs = L // (64 * w.stripes)
+    bytes_ = 2 * L * Hkv * d + 2 * q * Hq * d + 2 * 4 * Hq * (L + nbs) + 4 * kept
+    flops = 2.0 * d * q * Hq * L
+    exps = float(q * Hq * L)
+    mufu = MUFU_EX2_PER_CLK_SM * N_SM * sm_mhz * 1e6          # ex2 per second
+    t = {"hbm": bytes_ / (pk["hbm_gbs"] * 1e9), "tensor": flops / (pk["bf16_tflops"] * 1e12),
+         "alu": exps / mufu}
+    bound = max(t, key=t.get)
+    sec = A_index_time_ms * 1e-3
+    ach = {"hbm": bytes_ / sec / 1e9, "tensor": flops / sec / 1e12, "alu": exps / sec / 1e12}[bound]
+    peak = {"hbm": pk["hbm_gbs"], "tensor": pk["bf16_tflops"], "alu": mufu / 1e12}[bound]
+    unit = {"hbm": "GB/s", "tensor": "TFLOP/s", "alu": "Tex2/s"}[bound]
+    return {"kernel": "vs_index_build (scores, row statistics, slash bands, selection)", "bound": bound,
+            "achieved": round(ach, 3), "peak": round(peak, 3), "unit": unit, "frac": round(ach / peak, 4),
+            "algorithmic": {"bytes": int(bytes_), "flop": flops, "ex2": exps},
+            "roof_us": {k: round(v * 1e6, 2) for k, v in t.items()}, "index_us": round(A_index_time_ms * 1e3, 2),
+            "peak_src": pk["src"] + (" HBM copy" if bound == "hbm" else " bf16 burst" if bound == "tensor"
+                                     else " ex2 rate x SMs x max SM clock")}
+
+
 def run_gpu(args):
     import torch
 
@@ -152,35 +193,35 @@ def run_gpu(args):
     w = synth.make_workload(wid, **ov)
     L, Hq, Hkv, d = w.L, w.Hq, w.Hkv, w.d
     W = w.stripes
-    p = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=DENSITY, rope_theta=w.rope_theta,
-                       stripes=W)
-    p_nat = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=0.0, rope_theta=w.rope_theta,
-                           stripes=W)
+    bwd = w.backward
+    rope_kw = dict(rope_theta=w.rope_theta, yarn_factor=w.yarn_factor, yarn_orig_len=w.yarn_orig_len)
+    p = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=DENSITY, stripes=W, **rope_kw)
+    p_nat = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=0.0, stripes=W, **rope_kw)
 
     def pinned(bits):
         t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
         return t.pin_memory()
 
-    hQ, hK, hV, hdO = pinned(w.q), pinned(w.k), pinned(w.v), pinned(w.do)
-    Qr, Kr, V, dO = (t.to(dev) for t in (hQ, hK, hV, hdO))
+    h_in = [pinned(w.q), pinned(w.k), pinned(w.v)] + ([pinned(w.do)] if bwd else [])
+    d_in = [t.to(dev) for t in h_in]
+    Qr, Kr, V = d_in[:3]
     Q, K = torch.empty_like(Qr), torch.empty_like(Kr)
     O = torch.empty_like(Q)
     lse = torch.empty((Hq, L), dtype=torch.float32, device=dev)
-    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    d_out = [torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)] if bwd else [O]
     ix = vs.IndexBuffers.allocate(p, dev)
     ws_i = vs.workspace(p, vs.VS_OP_INDEX, dev)
     ws_f = vs.workspace(p, vs.VS_OP_FWD, dev)
-    ws_b = vs.workspace(p, vs.VS_OP_BWD, dev)
-    hdQ = torch.empty(dQ.shape, dtype=dQ.dtype).pin_memory()
-    hdK = torch.empty(dK.shape, dtype=dK.dtype).pin_memory()
-    hdV = torch.empty(dV.shape, dtype=dV.dtype).pin_memory()
+    ws_b = vs.workspace(p, vs.VS_OP_BWD, dev) if bwd else None
+    h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in d_out]
     stream = torch.cuda.current_stream()
-    ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for k in ("rope", "index", "fwd", "bwd")}
+    phases = ("rope", "index", "fwd", "bwd") if bwd else ("rope", "index", "fwd")
+    ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in phases}
 
     def step(timed=False, io=None):
-        # io: the step's input and output device buffers (Qr, Kr, V, dO, dQ, dK, dV)
-        qr, kr, v_, do_, dq, dk, dv = io if io is not None else (Qr, Kr, V, dO, dQ, dK, dV)
+        # io: the step's input and output device buffers
+        ins, outs = io if io is not None else (d_in, d_out)
+        qr, kr, v_ = ins[:3]
 
         def rec(k, i):
             if timed:
@@ -193,13 +234,15 @@ def run_gpu(args):
         vs.vs_index_build(p, Q, K, ix, ws_i)
         rec("index", 1)
         rec("fwd", 0)
-        vs.vs_sparse_attn_fwd(p, ix, Q, K, v_, O, lse, ws_f)
+        vs.vs_sparse_attn_fwd(p, ix, Q, K, v_, O if bwd else outs[0], lse, ws_f)
         rec("fwd", 1)
-        rec("bwd", 0)
-        vs.vs_sparse_attn_bwd(p, ix, Q, K, v_, O, lse, do_, dq, dk, dv, ws_b)
-        rec("bwd", 1)
-        vs.vs_rope(p, Hq, dq, dq, True)
-        vs.vs_rope(p, Hkv, dk, dk, True)
+        if bwd:
+            dq, dk, dv = outs
+            rec("bwd", 0)
+            vs.vs_sparse_attn_bwd(p, ix, Q, K, v_, O, lse, ins[3], dq, dk, dv, ws_b)
+            rec("bwd", 1)
+            vs.vs_rope(p, Hq, dq, dq, True)
+            vs.vs_rope(p, Hkv, dk, dk, True)
 
     # natural top-p sparsity (reported; not the timed operating point)
     vs.vs_rope(p, Hq, Qr, Q, False)
@@ -212,12 +255,13 @@ def run_gpu(args):
     T = L * (L + 1) // 2
     A = int(ix.active_entries.sum().item())
     A_nat = int(ix_nat.active_entries.sum().item())
+    kept = int(ix.v_cnt.sum().item() + ix.s_cnt.sum().item())
     del ix_nat
     balance = None
     if W > 1:
         # per-shard work of the striped layout against contiguous and ZigZag
         # splits of the contiguous (W = 1) index built on the same inputs
-        p1 = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=DENSITY, rope_theta=w.rope_theta)
+        p1 = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=DENSITY, **rope_kw)
         ix1 = vs.IndexBuffers.allocate(p1, dev)
         vs.vs_index_build(p1, Q, K, ix1, vs.workspace(p1, vs.VS_OP_INDEX, dev))
         ix_w = vs.IndexBuffers.allocate(p, dev)
@@ -225,7 +269,8 @@ def run_gpu(args):
         torch.cuda.synchronize()
         balance = shard_balance(L, W, index_lists(ix_w, Hq), index_lists(ix1, Hq))
         del ix1, ix_w
-    assert vs.vs_device_status(ws_f) == vs.VS_OK and vs.vs_device_status(ws_b) == vs.VS_OK
+    assert vs.vs_device_status(ws_f) == vs.VS_OK
+    assert ws_b is None or vs.vs_device_status(ws_b) == vs.VS_OK
 
     sampler = ClockSampler(local)
     if dist:
@@ -234,18 +279,14 @@ def run_gpu(args):
     sampler.start()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
-    phase = {k: 0.0 for k in ev}
     t0.record(stream)
     for _ in range(args.steps):
-        step(timed=True)
-        # per-phase times are read after the loop; keep the last step's
+        step()
     t1.record(stream)
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
     ms = t0.elapsed_time(t1) / args.steps
-    for k in ev:
-        phase[k] = ev[k][0].elapsed_time(ev[k][1])
     # per-phase averages over K extra steps (events on every step)
     acc = {k: 0.0 for k in ev}
     for _ in range(args.steps):
@@ -257,13 +298,14 @@ def run_gpu(args):
     clocks = sampler.stop()
 
     # End to end through the C ABI with host buffers: every step copies its
-    # inputs (Q, K, V, dO) in from pinned host memory and its results (dQ,
-    # dK, dV) back out.  The copies run on their own streams over two sets of
-    # device and host buffers, so one step's transfers overlap its
-    # neighbours' kernels, as a training loop's input pipeline would; the
-    # timed region runs from the first copy in to the last copy out.
-    io = [(Qr, Kr, V, dO, dQ, dK, dV), tuple(torch.empty_like(t) for t in (Qr, Kr, V, dO, dQ, dK, dV))]
-    hout = [(hdQ, hdK, hdV), tuple(torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (hdQ, hdK, hdV))]
+    # inputs (Q, K, V and, with a backward, dO) in from pinned host memory and
+    # its results (dQ, dK, dV, or O for a forward-only step) back out.  The
+    # copies run on their own streams over two sets of device and host
+    # buffers, so one step's transfers overlap its neighbours' kernels, as a
+    # training loop's input pipeline would; the timed region runs from the
+    # first copy in to the last copy out.
+    io = [(d_in, d_out), ([torch.empty_like(t) for t in d_in], [torch.empty_like(t) for t in d_out])]
+    hout = [h_out, [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in h_out]]
     s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
     in_done = [torch.cuda.Event() for _ in range(2)]
     comp_done = [torch.cuda.Event() for _ in range(2)]
@@ -275,21 +317,21 @@ def run_gpu(args):
         s_in.wait_event(e0)
         for i in range(n):
             b = i & 1
-            slot = io[b]
+            ins, outs = io[b]
             with torch.cuda.stream(s_in):
                 if i >= 2:
                     s_in.wait_event(comp_done[b])  # step i - 2 no longer reads these inputs
-                for dst, src in zip(slot[:4], (hQ, hK, hV, hdO)):
+                for dst, src in zip(ins, h_in):
                     dst.copy_(src, non_blocking=True)
                 in_done[b].record(s_in)
             stream.wait_event(in_done[b])
             if i >= 2:
                 stream.wait_event(out_done[b])  # step i - 2's results were copied out
-            step(io=slot)
+            step(io=(ins, outs))
             comp_done[b].record(stream)
             with torch.cuda.stream(s_out):
                 s_out.wait_event(comp_done[b])
-                for dst, src in zip(hout[b], slot[4:]):
+                for dst, src in zip(hout[b], outs):
                     dst.copy_(src, non_blocking=True)
                 out_done[b].record(s_out)
         for b in range(min(2, n)):
@@ -306,43 +348,53 @@ def run_gpu(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / args.steps
-    h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hV, hdO))
-    d2h = sum(t.numel() * t.element_size() for t in (hdQ, hdK, hdV))
+    h2d = sum(t.numel() * t.element_size() for t in h_in)
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
 
-    flops = 14.0 * d * A
+    flops = (14.0 if bwd else 4.0) * d * A
     value, e2e_val, ms, e2e_ms = replica_throughput(dist, world, flops, ms, e2e_ms, dev)
     pk = _peaks()
-    # dominant kernel group: the backward call (dK/dV + dQ kernels), 10 d A per launch
-    bwd_tf = 10.0 * d * A / (phase["bwd"] * 1e-3) / 1e12
     fwd_tf = 4.0 * d * A / (phase["fwd"] * 1e-3) / 1e12
-    peak = pk["bf16_tflops_sustained"]
+    bwd_tf = 10.0 * d * A / (phase["bwd"] * 1e-3) / 1e12 if bwd else None
+    # dominant call: the backward (dK/dV + dQ kernels, 10 d A) when there is
+    # one, else the forward (4 d A); each phase lasts milliseconds, so the
+    # burst peak is the denominator (the sustained one is listed beside it)
+    dom = ("vs_sparse_attn_bwd (dK/dV + dQ)", bwd_tf) if bwd else ("vs_sparse_attn_fwd", fwd_tf)
+    peak, peak_s = pk["bf16_tflops"], pk["bf16_tflops_sustained"]
+    kps = KERNELS_PER_STEP if bwd else KERNELS_PER_STEP_FWD
     out = {
         "metric": "VS sparse attn fwd+bwd ms and effective TFLOP/s at 128K (% bf16 peak)",
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "L": L, "Hq": Hq, "Hkv": Hkv, "d": d, "batch": 1,
-                   "last_q": LAST_Q, "index": f"budget fill to density {DENSITY}",
+                   "pass": "fwd+bwd" if bwd else "fwd", "last_q": LAST_Q,
+                   "index": f"budget fill to density {DENSITY}",
                    "sparsity": round(1 - A / (Hq * T), 5),
                    "natural_top_p_sparsity": round(1 - A_nat / (Hq * T), 5), "top_p": TOP_P,
-                   "active_entries": A, "l2": "inputs larger than L2 (no flush)", "stripes": W,
+                   "active_entries": A, "l2": "inputs larger than L2 (no flush)" if L * Hq * d * 2 > 2 * (126 << 20)
+                   else "no flush (inputs smaller than L2)", "stripes": W,
+                   "rope": {"theta": w.rope_theta, "yarn_factor": w.yarn_factor},
                    "parallelism": f"replicas x{world}"},
         "breakdown_ms": {k: round(v, 4) for k, v in phase.items()},
         **({"shard_balance": balance} if balance else {}),
-        "fwd_tflops": round(fwd_tf, 2), "bwd_tflops": round(bwd_tf, 2),
+        "fwd_tflops": round(fwd_tf, 2), **({"bwd_tflops": round(bwd_tf, 2)} if bwd else {}),
         "index_overhead": round(phase["index"] / max(ms, 1e-9), 4),
-        "roofline": {"kernel": "vs_sparse_attn_bwd (dK/dV + dQ)", "bound": "tensor",
-                     "achieved": round(bwd_tf, 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(bwd_tf / peak, 4), "traffic": BWD_TRAFFIC_BYTES.get(args.workload),
-                     "peak_src": pk["src"] + " bf16 sustained"},
+        "roofline": {"kernel": dom[0], "bound": "tensor",
+                     "achieved": round(dom[1], 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(dom[1] / peak, 4), "traffic": BWD_TRAFFIC_BYTES.get(args.workload) if bwd else None,
+                     "peak_src": pk["src"] + " bf16 burst",
+                     "frac_of_sustained": round(dom[1] / peak_s, 4)},
+        "index_roofline": index_roofline(w, phase["index"], kept, pk, clocks.get("sm_max_mhz") or 2070.0),
         "e2e": {"value": round(e2e_val, 2), "unit": "TFLOP/s", "copies": "own streams, two buffer sets",
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
-        "gpu_launches": sum(KERNELS_PER_STEP.values()) * args.steps,
+        "gpu_launches": sum(kps.values()) * args.steps,
         "clocks": clocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(w, index_lists(ix, Hq), d, args.cpu_rows)
+        rows = max(16, int(args.cpu_rows * (131072 / L) * (16 / Hq)))
+        out["cpu_baseline"] = cpu_baseline(w, index_lists(ix, Hq), d, min(rows, args.cpu_rows), bwd)
     if dist:
         dist.destroy_process_group()
     if rank == 0:
@@ -391,17 +443,25 @@ def shard_balance(L, W, index_striped, index_contig):
             "striped_total": int(striped.sum()), "contiguous_index_total": int(rows.sum())}
 
 
-def cpu_baseline(w, index, d, nrows):
+def cpu_baseline(w, index, d, nrows, bwd=True):
     """The fp64 oracle, as it stands, on a bounded sample of the step: the
-    forward and dQ of `nrows` query rows spread over the sequence, every
-    head.  Reported in TFLOP/s counting the work those calls do on the
-    sampled rows' active entries: 4 d for the forward and 6 d for dQ (S and
-    dP recomputed, dS K); the rows' dK / dV contributions are not run."""
+    forward (and, for a training step, dQ) of `nrows` query rows spread over
+    the sequence, every head.  Reported in TFLOP/s counting the work those
+    calls do on the sampled rows' active entries: 4 d for the forward and
+    6 d for dQ (S and dP recomputed, dS K); the rows' dK / dV contributions
+    are not run."""
     import oracle
     f = synth.bf16_bits_to_f64
-    Q, K, V, dO = f(w.q), f(w.k), f(w.v), f(w.do)
     rows = np.linspace(0, w.L - 1, nrows).astype(np.int64)
-    bs = 64
+
+    def sampled(bits):
+        # the oracle reads only the sampled query rows: the rest stay zero
+        # pages that are never touched
+        x = np.zeros(bits.shape, np.float64)
+        x[rows] = f(bits[rows])
+        return x
+    Q, K, V = sampled(w.q), f(w.k), f(w.v)
+    bs = 64 * w.stripes
     act = 0
     for (Vh, Sh) in index:
         inS = np.zeros(w.L // bs, bool)
@@ -412,16 +472,19 @@ def cpu_baseline(w, index, d, nrows):
             m = np.arange(n + 1)
             act += int((inS[n // bs - m // bs] | isV[m]).sum())
     t0 = time.perf_counter()
-    oracle.attention_forward_rows(Q, K, V, index, rows)
-    oracle.attention_backward_dq_rows(Q, K, V, dO, index, rows)
+    oracle.attention_forward_rows(Q, K, V, index, rows, stripes=w.stripes)
+    if bwd:
+        oracle.attention_backward_dq_rows(Q, K, V, sampled(w.do), index, rows, stripes=w.stripes)
     dt = time.perf_counter() - t0
     try:
         cores = len(os.sched_getaffinity(0))
     except Exception:
         cores = os.cpu_count()
-    return {"value": round(10.0 * d * act / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-            "sample": f"fp64 forward + dQ of {nrows} query rows x {w.Hq} heads ({act} active entries, "
-                      f"10 d flop each), {dt:.1f} s"}
+    per = 10 if bwd else 4
+    what = "forward + dQ" if bwd else "forward"
+    return {"value": round(per * d * act / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"fp64 {what} of {nrows} query rows x {w.Hq} heads ({act} active entries, "
+                      f"{per} d flop each), {dt:.1f} s"}
 
 
 def run_reference(args):
@@ -434,11 +497,12 @@ def run_reference(args):
     w = synth.make_workload(wid, **ov)
     f = synth.bf16_bits_to_f64
     Q, K = f(w.q), f(w.k)
-    index, _, _ = oracle.build_index(Q, K, LAST_Q, TOP_P, density=DENSITY)
+    index, _, _ = oracle.build_index(Q, K, LAST_Q, TOP_P, density=DENSITY, stripes=w.stripes)
     vals = []
     base = None
+    rows = max(4, int(args.cpu_rows // 8 * (131072 / w.L) * (16 / w.Hq)))
     for i in range(args.warmup + args.steps):
-        r = cpu_baseline(w, index, w.d, max(4, args.cpu_rows // 8))
+        r = cpu_baseline(w, index, w.d, min(rows, args.cpu_rows), w.backward)
         if i >= args.warmup:
             vals.append(r["value"])
             base = r

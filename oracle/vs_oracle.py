@@ -48,6 +48,7 @@ __all__ = [
     "select_top_p", "select_budget", "build_index", "active_entries",
     "sparsity_ratio", "explicit_mask", "attention_forward", "attention_backward",
     "attention_forward_rows", "attention_backward_dq_rows", "total_causal_entries",
+    "attention_backward_bf16_products",
 ]
 
 
@@ -358,6 +359,51 @@ def attention_backward(Q, K, V, dO, index, scale=None, stripes=1, block=64):
             dV[:, g, :] += p.T @ dO[r, h, :]
             dQ[r, h, :] = scale * (dS @ kh)
             dK[:, g, :] += scale * (dS.T @ Q[r, h, :])
+    return dQ, dK, dV
+
+
+def attention_backward_bf16_products(Q, K, V, dO, index, scale=None, stripes=1, block=64):
+    """``attention_backward`` with the roundings of an implementation whose
+    tensor-core products take bf16 operands and accumulate in higher
+    precision (the precision reading: bf16 inputs, fp32 accumulation,
+    probabilities rounded to bf16 before they enter a product).  The
+    definitions are unchanged; exactly three values are rounded to bf16,
+    everything else is fp64:
+      * O, the forward output, is stored as bf16 and D_n = sum_c dO_nc O_nc
+        is formed from the stored O;
+      * P enters dV = P^T dO as bf16;
+      * dS = P * (dP - D) (with the unrounded P) enters dQ = scale dS K and
+        dK = scale dS^T Q as bf16.
+    It measures what that arithmetic itself costs, so a kernel that follows
+    it can be held to a per-element tolerance."""
+    Q = np.asarray(Q, np.float64)
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    dO = np.asarray(dO, np.float64)
+    L, Hq, d = Q.shape
+    G = Hq // K.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    bs = block * stripes
+    dQ = np.zeros_like(Q)
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    for h in range(Hq):
+        Vh, Sh = index[h]
+        g = h // G
+        kh, vh = K[:, g, :], V[:, g, :]
+        for r in _chunks(L, np.arange(L)):
+            msk = _row_mask(r, L, Vh, Sh, bs)
+            s = np.where(msk, scale * (Q[r, h, :] @ kh.T), -np.inf)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            p /= p.sum(axis=1, keepdims=True)
+            O_b = bf16_round(p @ vh)
+            D = (dO[r, h, :] * O_b).sum(axis=1, keepdims=True)
+            dP = dO[r, h, :] @ vh.T
+            dS_b = bf16_round(p * (dP - D))
+            dV[:, g, :] += bf16_round(p).T @ dO[r, h, :]
+            dQ[r, h, :] = scale * (dS_b @ kh)
+            dK[:, g, :] += scale * (dS_b.T @ Q[r, h, :])
     return dQ, dK, dV
 
 

@@ -96,6 +96,41 @@ def normal_f64(seed: int, n: int, threads: int | None = None) -> np.ndarray:
     return out[:n]
 
 
+def normal_bf16_rows(seed: int, shape, transform=None, rows_per_chunk: int | None = None) -> np.ndarray:
+    """bf16 bit patterns of ``normal_f64(seed, prod(shape))`` reshaped to
+    ``shape``, built a block of rows at a time so that the fp64 copy of a
+    large tensor never exists whole.  ``transform(block, r0)`` may change a
+    block of rows (starting at row ``r0``) in fp64 before rounding.  The
+    result is bit-identical to rounding the whole fp64 tensor at once (both
+    steps are elementwise and the stream is addressed by element index)."""
+    shape = tuple(shape)
+    row = int(np.prod(shape[1:]))
+    if rows_per_chunk is None:
+        rows_per_chunk = max(2, (1 << 24) // max(row, 1))
+    rows_per_chunk += rows_per_chunk % 2          # even element offsets keep Box-Muller pairs whole
+    out = np.empty(shape, dtype=np.uint16)
+    starts = list(range(0, shape[0], rows_per_chunk))
+
+    def work(r0):
+        r1 = min(shape[0], r0 + rows_per_chunk)
+        e0, e1 = r0 * row, r1 * row
+        p0 = e0 // 2
+        blk = _normal_chunk(seed, p0, (e1 - 2 * p0 + 1) // 2)[e0 - 2 * p0: e1 - 2 * p0]
+        blk = blk.reshape((r1 - r0,) + shape[1:])
+        if transform is not None:
+            blk = transform(blk, r0)
+        out[r0:r1] = f64_to_bf16_bits(blk)
+
+    nt = min(len(starts), os.cpu_count() or 1)
+    if nt <= 1:
+        for r0 in starts:
+            work(r0)
+    else:
+        with ThreadPoolExecutor(nt) as ex:
+            list(ex.map(work, starts))
+    return out
+
+
 def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """fp64 -> fp32 (RNE) -> bf16 (RNE); returns uint16 bit patterns."""
     b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
@@ -186,37 +221,47 @@ def make_workload(wid: int, L: int | None = None, Hq: int | None = None,
     sb = wid if seed_base is None else seed_base
     s = lambda t: 1000 * sb + t
 
-    q = normal_f64(s(T_Q), L * Hq * d).reshape(L, Hq, d)
-    k = normal_f64(s(T_K), L * Hkv * d).reshape(L, Hkv, d)
-    v = normal_f64(s(T_V), L * Hkv * d).reshape(L, Hkv, d)
     if "outlier_count" in r:
         n_out = r["outlier_count"]
     else:
         n_out = max(1, int(round(r["outlier_frac"] * L)))
     outl = permutation_prefix(s(T_OUTLIER), L, min(n_out, L))
     meta = {}
+    bq = bk = None
     if r["bias"]:
         # per-head constant added to every channel of q and k before RoPE;
         # beta_h ~ U[0.25, 0.5]
         bq = 0.25 + 0.25 * uniform01(s(T_BIAS), 0, Hq)
-        q += bq[None, :, None]
         G = Hq // Hkv
         bk = bq.reshape(Hkv, G).mean(axis=1)
-        k += bk[None, :, None]
         meta["beta_q"] = bq
         meta["beta_k"] = bk
-    # outlier keys: whole row (all KV heads) scaled
-    k[outl] *= r["outlier_scale"]
-    do = None
-    if backward:
-        do = normal_f64(s(T_DO), L * Hq * d).reshape(L, Hq, d)
+    is_out = np.zeros(L, bool)
+    is_out[outl] = True
+
+    def q_tf(blk, r0):
+        if bq is not None:
+            blk += bq[None, :, None]
+        return blk
+
+    def k_tf(blk, r0):
+        if bk is not None:
+            blk += bk[None, :, None]
+        # outlier keys: whole row (all KV heads) scaled
+        rows = is_out[r0:r0 + blk.shape[0]]
+        blk[rows] *= r["outlier_scale"]
+        return blk
+
+    q = normal_bf16_rows(s(T_Q), (L, Hq, d), q_tf)
+    k = normal_bf16_rows(s(T_K), (L, Hkv, d), k_tf)
+    v = normal_bf16_rows(s(T_V), (L, Hkv, d))
+    do = normal_bf16_rows(s(T_DO), (L, Hq, d)) if backward else None
     return Workload(
         name=r["name"], L=L, Hq=Hq, Hkv=Hkv, d=d, last_q=last_q, top_p=top_p,
         backward=backward, rope_theta=r["theta"], yarn_factor=r["yarn"],
         yarn_orig_len=int(L // r["yarn"]) if r["yarn"] > 1 else 0,
         needs_rope=bool(r["bias"]), stripes=stripes,
-        q=f64_to_bf16_bits(q), k=f64_to_bf16_bits(k), v=f64_to_bf16_bits(v),
-        do=None if do is None else f64_to_bf16_bits(do), outliers=outl, meta=meta)
+        q=q, k=k, v=v, do=do, outliers=outl, meta=meta)
 
 
 def normal_bf16(seed: int, shape) -> np.ndarray:

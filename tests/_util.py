@@ -76,3 +76,24 @@ def inject_index(vs, p, index, dev):
 
 def rel_l2(a, b):
     return float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30))
+
+
+def budget_sets_agree(v_or, S_or, kept_or, kept_gpu, tol=1e-6):
+    """True if a budget-fill selection on the GPU equals the oracle's fp64
+    one except for candidates at the threshold: every vertical or band
+    (band 0 is forced on both sides) in the symmetric difference must have
+    a normalised mass (mass / total mass of its direction) within `tol` of
+    the oracle's threshold, the smallest kept candidate mass, normalised the
+    same way."""
+    (Vo, So), (Vg, Sg) = kept_or, kept_gpu
+    tv, ts = v_or.sum(), S_or.sum()
+    masses = [v_or[Vo] / tv] + ([S_or[So[So > 0]] / ts] if (So > 0).any() else [])
+    thr = min(float(m.min()) for m in masses if m.size) if any(m.size for m in masses) else 0.0
+    bad = []
+    for e in set(Vo.tolist()) ^ set(Vg.tolist()):
+        if abs(v_or[e] / tv - thr) > tol:
+            bad.append(("v", e, v_or[e] / tv, thr))
+    for e in (set(So.tolist()) ^ set(Sg.tolist())) - {0}:
+        if abs(S_or[e] / ts - thr) > tol:
+            bad.append(("s", e, S_or[e] / ts, thr))
+    return not bad, bad

@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import synth
-from _util import f64, gpu_index_lists, to_dev, topp_sets_agree
+from _util import budget_sets_agree, f64, gpu_index_lists, to_dev, topp_sets_agree
 
 pytestmark = pytest.mark.gpu
 
@@ -94,6 +94,12 @@ def test_index_budget_fill(wid, L, Hq, Hkv, d, W, density):
         np.testing.assert_array_equal(lists[h][1], So)
         assert act[h] == oracle.active_entries(L, Vo, So, bs)
         assert act[h] >= dens32 * oracle.total_causal_entries(L)
+    # end to end against the fp64 oracle (fp64 masses), ties at the threshold excepted
+    v_or, S_or = oracle.index_scores(f64(w.q), f64(w.k), w.last_q, stripes=W)
+    for h in range(Hq):
+        kept_or = oracle.select_budget(v_or[h], S_or[h], L, bs, dens32)  # the density the call passed
+        ok, bad = budget_sets_agree(v_or[h], S_or[h], kept_or, lists[h])
+        assert ok, bad[:5]
 
 
 def test_index_full_size_gqa_128k():
@@ -102,9 +108,24 @@ def test_index_full_size_gqa_128k():
     p, ix = _run(w)
     v_or, S_or = oracle.index_scores(f64(w.q), f64(w.k), w.last_q)
     np.testing.assert_allclose(ix.v_score.double().cpu().numpy(), v_or, rtol=1e-4, atol=1e-10)
+    np.testing.assert_allclose(ix.s_score.double().cpu().numpy(), S_or, rtol=1e-4, atol=1e-10)
     lists = gpu_index_lists(ix, w.Hq)
     for h in range(w.Hq):
         ok, bad = topp_sets_agree(v_or[h], oracle.select_top_p(v_or[h], w.top_p), lists[h][0], w.top_p)
         assert ok, bad[:5]
+        ok, bad = topp_sets_agree(S_or[h], oracle.select_top_p(S_or[h], w.top_p), lists[h][1], w.top_p,
+                                  forced=(0,))
+        assert ok, bad[:5]
+        assert 0 in lists[h][1].tolist()
         # planted outliers carry most of the mass: all of them are verticals
         assert set(w.outliers.tolist()) <= set(lists[h][0].tolist())
+    # the measured operating point: budget fill to 5 % density, end to end
+    # against the oracle's fp64 selection, and the exact active counts
+    _, ixb = _run(w, density=0.05)
+    listsb = gpu_index_lists(ixb, w.Hq)
+    act = ixb.active_entries.cpu().numpy()
+    for h in range(w.Hq):
+        kept_or = oracle.select_budget(v_or[h], S_or[h], w.L, 64, float(np.float32(0.05)))
+        ok, bad = budget_sets_agree(v_or[h], S_or[h], kept_or, listsb[h])
+        assert ok, bad[:5]
+        assert act[h] == oracle.active_entries(w.L, listsb[h][0], listsb[h][1], 64)

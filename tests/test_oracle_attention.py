@@ -152,3 +152,86 @@ def test_gradient_column_identities():
     for g in range(Hkv):
         np.testing.assert_allclose(dV[:, g].sum(0), dO[:, g * 2:(g + 1) * 2].sum((0, 1)), atol=1e-10)
         np.testing.assert_allclose(dK[:, g].sum(0), 0.0, atol=1e-10)
+
+
+def test_bf16_round_known_values():
+    from oracle import bf16_round
+    # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: the even significand (1) wins;
+    # 1 + 3 * 2^-8 ties up to 1 + 2^-6 (even); 1 + 2^-20 rounds down; 3e38
+    # rounds to the bf16 pattern 0x7F62 (fp32 first, then bf16, both RNE)
+    x = np.array([1.0, 1.00390625, 1.01171875, 1.0078125, -2.5, 1.0 + 2.0 ** -20, 0.0, 3.0e38])
+    big = float(np.array([0x7F62 << 16], np.uint32).view(np.float32)[0])
+    np.testing.assert_array_equal(bf16_round(x), [1.0, 1.0, 1.015625, 1.0078125, -2.5, 1.0, 0.0, big])
+
+
+def _explicit_bf16_backward(Q, K, V, dO, masks, scale):
+    """Per-entry loops: the stated roundings applied element by element."""
+    from oracle import bf16_round
+    L, Hq, d = Q.shape
+    G = Hq // K.shape[1]
+    dQ, dK, dV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    r = lambda x: float(bf16_round(np.array([x]))[0])
+    for h in range(Hq):
+        g = h // G
+        for n in range(L):
+            act = [m for m in range(L) if masks[h][n, m]]
+            s = {m: scale * sum(Q[n, h, c] * K[m, g, c] for c in range(d)) for m in act}
+            mx = max(s.values())
+            z = sum(math.exp(s[m] - mx) for m in act)
+            P = {m: math.exp(s[m] - mx) / z for m in act}
+            O = [r(sum(P[m] * V[m, g, c] for m in act)) for c in range(d)]
+            D = sum(dO[n, h, c] * O[c] for c in range(d))
+            for m in act:
+                dP = sum(dO[n, h, c] * V[m, g, c] for c in range(d))
+                dS = r(P[m] * (dP - D))
+                pb = r(P[m])
+                for c in range(d):
+                    dV[m, g, c] += pb * dO[n, h, c]
+                    dQ[n, h, c] += scale * dS * K[m, g, c]
+                    dK[m, g, c] += scale * dS * Q[n, h, c]
+    return dQ, dK, dV
+
+
+def test_bf16_products_backward_explicit_loops():
+    from oracle import attention_backward_bf16_products
+    L, Hq, Hkv, d = 40, 2, 1, 8
+    Q, K, V, dO = _inputs(L, Hq, Hkv, d, 11)
+    index = [(np.array([3, 17, 30]), np.array([0, 2])), (np.array([1, 8]), np.array([0, 1, 3]))]
+    masks = [explicit_mask(L, Vh, Sh, 8) for Vh, Sh in index]
+    scale = 1.0 / math.sqrt(d)
+    ref = _explicit_bf16_backward(Q, K, V, dO, masks, scale)
+    got = attention_backward_bf16_products(Q, K, V, dO, index, block=8)
+    for g, e in zip(got, ref):
+        np.testing.assert_allclose(g, e, rtol=1e-12, atol=1e-12)
+
+
+def test_bf16_products_backward_within_first_order_bound():
+    """|emulated - exact| is bounded entry by entry by the unit roundoff
+    u = 2^-8 times the magnitudes the three roundings touch: dV by
+    u sum_n P |dO|; dQ and dK by scale sum (u |dS'| + P u sum_c |dO O|) |k|
+    (resp. |q|), with dS' = P (dP - D) formed from the rounded O."""
+    from oracle import attention_backward_bf16_products, bf16_round
+    L, Hq, Hkv, d = 96, 2, 1, 16
+    Q, K, V, dO = _inputs(L, Hq, Hkv, d, 5)
+    K[[7, 50]] *= 6.0
+    index = [(np.array([7, 50, 71]), np.array([0, 1, 4])), (np.array([7, 50]), np.array([0, 2]))]
+    u = 2.0 ** -8
+    scale = 1.0 / math.sqrt(d)
+    exact = attention_backward(Q, K, V, dO, index, block=16)
+    emu = attention_backward_bf16_products(Q, K, V, dO, index, block=16)
+    bQ, bK, bV = np.zeros_like(Q), np.zeros_like(K), np.zeros_like(V)
+    for h, (Vh, Sh) in enumerate(index):
+        m = explicit_mask(L, Vh, Sh, 16)
+        s = np.where(m, scale * Q[:, h] @ K[:, 0].T, -np.inf)
+        P = np.exp(s - s.max(1, keepdims=True))
+        P /= P.sum(1, keepdims=True)
+        O = P @ V[:, 0]
+        Ob = bf16_round(O)
+        dSp = P * (dO[:, h] @ V[:, 0].T - (dO[:, h] * Ob).sum(1, keepdims=True))
+        w = u * np.abs(dSp) + P * u * (np.abs(dO[:, h]) * np.abs(O)).sum(1, keepdims=True)
+        bV[:, 0] += u * P.T @ np.abs(dO[:, h])
+        bQ[:, h] = scale * w @ np.abs(K[:, 0])
+        bK[:, 0] += scale * w.T @ np.abs(Q[:, h])
+    for e, x, b in zip(emu, exact, (bQ, bK, bV)):
+        assert (np.abs(e - x) <= b * (1 + 1e-6) + 1e-12).all()
+        assert np.abs(e - x).max() > 0      # the roundings do happen

@@ -41,3 +41,23 @@ def test_workload_shapes_and_outliers():
     assert norms[w.outliers].mean() > 6 * others.mean()
     w3 = synth.make_workload(3, L=1024)
     assert w3.q.shape == (1024, 16, 128) and w3.k.shape == (1024, 2, 128) and w3.do is not None
+
+
+def test_row_chunked_generation_is_bit_identical():
+    # odd row length, chunk boundaries in the middle of Box-Muller pairs of
+    # the flat stream are impossible (even row offsets), odd tensor end
+    for shape, rpc in [((7, 3, 5), 1), ((9, 2, 8), 4), ((64, 16, 128), None)]:
+        n = int(np.prod(shape))
+        ref = synth.f64_to_bf16_bits(synth.normal_f64(21, n)).reshape(shape)
+        np.testing.assert_array_equal(synth.normal_bf16_rows(21, shape, rows_per_chunk=rpc), ref)
+    # a per-row transform sees the right rows
+    shape = (10, 2, 3)
+    x = synth.normal_f64(5, 60).reshape(shape)
+    x[3] *= 4.0
+    ref = synth.f64_to_bf16_bits(x)
+
+    def tf(blk, r0):
+        rows = np.arange(r0, r0 + blk.shape[0])
+        blk[rows == 3] *= 4.0
+        return blk
+    np.testing.assert_array_equal(synth.normal_bf16_rows(5, shape, tf, rows_per_chunk=2), ref)
