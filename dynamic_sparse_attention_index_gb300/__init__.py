@@ -7,7 +7,7 @@ library is missing or fails to load, every call raises.
 
 Entry points mirror the C names: ``vs_workspace_bytes``, ``vs_rope``,
 ``vs_index_build``, ``vs_index_build_noalloc``, ``vs_sparse_attn_fwd``, ``vs_sparse_attn_bwd``,
-``vs_device_status``, ``vs_status_string``.
+``vs_striped_ring_fwd``, ``vs_striped_ring_bwd``, ``vs_device_status``, ``vs_status_string``.
 """
 from __future__ import annotations
 
@@ -19,11 +19,12 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libvs.so")
 
 VS_OK, VS_ERR_INVALID_ARG, VS_ERR_UNSUPPORTED, VS_ERR_WORKSPACE, VS_ERR_CUDA, VS_ERR_TIMEOUT = range(6)
-VS_OP_INDEX, VS_OP_FWD, VS_OP_BWD, VS_OP_ROPE = range(4)
+VS_OP_INDEX, VS_OP_FWD, VS_OP_BWD, VS_OP_ROPE, VS_OP_RING_FWD, VS_OP_RING_BWD = range(6)
 
 #: every symbol the header declares
 EXPORTED = ("vs_workspace_bytes", "vs_status_string", "vs_rope", "vs_index_build",
-            "vs_index_build_noalloc", "vs_sparse_attn_fwd", "vs_sparse_attn_bwd", "vs_device_status")
+            "vs_index_build_noalloc", "vs_sparse_attn_fwd", "vs_sparse_attn_bwd", "vs_device_status",
+            "vs_striped_ring_fwd", "vs_striped_ring_bwd")
 
 #: size of the static scratch behind vs_index_build_noalloc (VS_INDEX_NOALLOC_SCRATCH_BYTES)
 INDEX_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -74,8 +75,11 @@ def lib() -> ctypes.CDLL:
         L.vs_sparse_attn_fwd.argtypes = [P, I, VP, VP, VP, VP, VP, VP, SZ, VP]
         L.vs_sparse_attn_bwd.argtypes = [P, I, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]
         L.vs_device_status.argtypes = [VP, VP]
+        EV = ctypes.POINTER(ctypes.c_void_p)
+        L.vs_striped_ring_fwd.argtypes = [P, I, VP, VP, VP, VP, VP, VP, SZ, EV, i32, VP]
+        L.vs_striped_ring_bwd.argtypes = [P, I, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ, EV, i32, VP]
         for f in ("vs_rope", "vs_index_build", "vs_index_build_noalloc", "vs_sparse_attn_fwd",
-                  "vs_sparse_attn_bwd", "vs_device_status"):
+                  "vs_sparse_attn_bwd", "vs_device_status", "vs_striped_ring_fwd", "vs_striped_ring_bwd"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -176,6 +180,35 @@ def vs_sparse_attn_bwd(p: vs_params, index: IndexBuffers, Q, K, V, O, lse, dO, d
     _check(lib().vs_sparse_attn_bwd(ctypes.byref(p), ctypes.byref(ix), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
                                     _ptr(lse), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(),
                                     _stream(stream)), "vs_sparse_attn_bwd")
+
+
+def _events(events):
+    if not events:
+        return None, 0
+    for e in events:
+        if not e.cuda_event:  # torch creates the CUDA event on its first record
+            e.record()
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    return arr, len(events)
+
+
+def vs_striped_ring_fwd(p: vs_params, index: IndexBuffers, Q, K, V, O, lse, ws, events=None, stream=None):
+    """Striped sparse ring forward (W = p.stripes workers, step by step);
+    ``events``: optional list of W*W+1 torch.cuda.Event(enable_timing=True)
+    recorded before every step and after the last."""
+    ix = index.c()
+    ev, n = _events(events)
+    _check(lib().vs_striped_ring_fwd(ctypes.byref(p), ctypes.byref(ix), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
+                                     _ptr(lse), _ptr(ws), ws.numel(), ev, n, _stream(stream)), "vs_striped_ring_fwd")
+
+
+def vs_striped_ring_bwd(p: vs_params, index: IndexBuffers, Q, K, V, O, lse, dO, dQ, dK, dV, ws, events=None,
+                        stream=None):
+    ix = index.c()
+    ev, n = _events(events)
+    _check(lib().vs_striped_ring_bwd(ctypes.byref(p), ctypes.byref(ix), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
+                                     _ptr(lse), _ptr(dO), _ptr(dQ), _ptr(dK), _ptr(dV), _ptr(ws), ws.numel(), ev,
+                                     n, _stream(stream)), "vs_striped_ring_bwd")
 
 
 def vs_device_status(ws, stream=None) -> int:

@@ -17,6 +17,12 @@ cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* 
                             const void* O, const float* lse, const void* dO, void* dQ, void* dK, void* dV, void* ws,
                             cudaStream_t s);
 size_t attn_bwd_ws_bytes(const vs_params& p);
+size_t ring_ws_bytes(const vs_params& p, bool bwd);
+cudaError_t launch_ring_fwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
+                            void* O, float* lse, void* ws, void* const* ev, int n_ev, cudaStream_t st);
+cudaError_t launch_ring_bwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
+                            const void* O, const float* lse, const void* dO, void* dQ, void* dK, void* dV, void* ws,
+                            void* const* ev, int n_ev, cudaStream_t st);
 
 namespace {
 
@@ -112,6 +118,8 @@ size_t vs_workspace_bytes(const vs_params* p, int op) {
   if (check_params(p) != VS_OK) return 0;
   if (op == VS_OP_FWD) return attn_fwd_ws_bytes(*p);
   if (op == VS_OP_BWD) return p->d == 128 ? attn_bwd_ws_bytes(*p) : 0;
+  if (op == VS_OP_RING_FWD) return ring_ws_bytes(*p, false);
+  if (op == VS_OP_RING_BWD) return p->d == 128 ? ring_ws_bytes(*p, true) : 0;
   return 0;
 }
 
@@ -276,6 +284,43 @@ vs_status vs_sparse_attn_bwd(const vs_params* p, const vs_index* index, const vo
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
   return launch_attn_bwd(*p, *index, Q, K, V, O, lse, dO, dQ, dK, dV, ws, s) == cudaSuccess ? VS_OK : VS_ERR_CUDA;
+}
+
+vs_status vs_striped_ring_fwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,
+                              const void* V, void* O, float* lse, void* ws, size_t ws_bytes, void* const* step_events,
+                              int32_t n_events, void* stream) {
+  vs_status st = check_params(p);
+  if (st != VS_OK) return st;
+  if ((st = check_index_ptrs(index)) != VS_OK) return st;
+  if (!Q || !K || !V || !O || !lse) return VS_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(lse)) return VS_ERR_INVALID_ARG;
+  if (n_events < 0 || (n_events > 0 && !step_events)) return VS_ERR_INVALID_ARG;
+  if ((st = check_ws(ws, ws_bytes, ring_ws_bytes(*p, false))) != VS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
+  return launch_ring_fwd(*p, *index, Q, K, V, O, lse, ws, step_events, n_events, s) == cudaSuccess ? VS_OK
+                                                                                                  : VS_ERR_CUDA;
+}
+
+vs_status vs_striped_ring_bwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,
+                              const void* V, const void* O, const float* lse, const void* dO, void* dQ, void* dK,
+                              void* dV, void* ws, size_t ws_bytes, void* const* step_events, int32_t n_events,
+                              void* stream) {
+  vs_status st = check_params(p);
+  if (st != VS_OK) return st;
+  if ((st = check_index_ptrs(index)) != VS_OK) return st;
+  if (p->d != 128) return VS_ERR_UNSUPPORTED;
+  if (!Q || !K || !V || !O || !lse || !dO || !dQ || !dK || !dV) return VS_ERR_INVALID_ARG;
+  const void* ptrs[] = {Q, K, V, O, lse, dO, dQ, dK, dV};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return VS_ERR_INVALID_ARG;
+  if (n_events < 0 || (n_events > 0 && !step_events)) return VS_ERR_INVALID_ARG;
+  if ((st = check_ws(ws, ws_bytes, ring_ws_bytes(*p, true))) != VS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
+  return launch_ring_bwd(*p, *index, Q, K, V, O, lse, dO, dQ, dK, dV, ws, step_events, n_events, s) == cudaSuccess
+             ? VS_OK
+             : VS_ERR_CUDA;
 }
 
 vs_status vs_device_status(void* ws, void* stream) {

@@ -26,10 +26,6 @@
 
 namespace vs {
 
-cudaError_t launch_attn_dq(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const void* Q, const void* K,
-                           const void* V, const void* dO, const float* lse, const float* Dsum, void* dQ,
-                           DevStatus* st, cudaStream_t s);
-
 namespace {
 
 constexpr int kThreads = 384;
@@ -76,6 +72,8 @@ struct BwdParams {
   __nv_bfloat16* dV;
   float* part_k;  // vertical partials [nvg][L][d] (fp32), split slots inside
   float* part_v;
+  float* dk32;    // ring steps: fp32 dK / dV sums [L_glob][Hkv][d] that each step adds to
+  float* dv32;    // (null: dK / dV written as bf16)
   float scale;
   float log2e;
   DevStatus* status;
@@ -130,10 +128,10 @@ __device__ __forceinline__ int src_mode(uint32_t w0, uint32_t w1, bool is_diag) 
   return kSrcBits;
 }
 // Active keys of the 64-key block for row rr of its source, as a 64-bit mask.
-__device__ __forceinline__ uint64_t active_bits(int mode, uint32_t w0, uint32_t w1, int rr) {
+__device__ __forceinline__ uint64_t active_bits(int mode, uint32_t w0, uint32_t w1, int rr, int strict) {
   if (mode == kSrcOff) return 0ull;
   if (mode == kSrcFull) return ~0ull;
-  if (mode == kSrcDiag) return rr >= 63 ? ~0ull : ((2ull << rr) - 1ull);
+  if (mode == kSrcDiag) return diag_bits(rr, strict);
   return (uint64_t)w0 | ((uint64_t)w1 << 32);
 }
 
@@ -628,8 +626,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(&mq_empty[t % kMQ]);
         float lse2 = 0.f, Dr = 0.f;
         if (valid) {
-          lse2 = P.lse[(size_t)h * g.L + tok] * P.log2e;
-          Dr = P.Dsum[(size_t)h * g.L + tok];
+          lse2 = P.lse[(size_t)h * g.L_glob + g.tq(tok)] * P.log2e;
+          Dr = P.Dsum[(size_t)h * g.L_glob + g.tq(tok)];
         }
         if (!wait_warp(&sdp_full[t & 1], (t >> 1) & 1, 21)) break;
         const long long ph0 = kWaitProfileKv ? clock64() : 0;
@@ -641,7 +639,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // warp-uniform masking mode of this row's source for the 64 keys,
         // then this group's 32 of them
         const int mode = src_mode(mw0, mw1, diag != 0);
-        const uint32_t act = (uint32_t)(active_bits(mode, mw0, mw1, rr) >> col0);
+        const uint32_t act = (uint32_t)(active_bits(mode, mw0, mw1, rr, g.strict_diag) >> col0);
         uint32_t pk[16], dk[16];
         if (mode == kSrcOff) {
 #pragma unroll
@@ -742,11 +740,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                   }
               }
             }
+            if (P.dk32) {
+              // a ring step: add into the fp32 sums of the keys' global rows
 #pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              const size_t o = ((size_t)(kb * kBlock + (int)col0 + jj) * g.Hkv + kvh) * D + dcol;
-              P.dV[o] = __float2bfloat16_rn(__uint_as_float(av[jj]));
-              P.dK[o] = __float2bfloat16_rn(__uint_as_float(ak[jj]) * P.scale);
+              for (int jj = 0; jj < 32; ++jj) {
+                const size_t o = ((size_t)g.tk(kb * kBlock + (int)col0 + jj) * g.Hkv + kvh) * D + dcol;
+                P.dv32[o] += __uint_as_float(av[jj]);
+                P.dk32[o] += __uint_as_float(ak[jj]) * P.scale;
+              }
+            } else {
+#pragma unroll
+              for (int jj = 0; jj < 32; ++jj) {
+                const size_t o = ((size_t)(kb * kBlock + (int)col0 + jj) * g.Hkv + kvh) * D + dcol;
+                P.dV[o] = __float2bfloat16_rn(__uint_as_float(av[jj]));
+                P.dK[o] = __float2bfloat16_rn(__uint_as_float(ak[jj]) * P.scale);
+              }
             }
           }
         }
@@ -786,6 +794,64 @@ BwdWs bwd_layout(const AttnGeom& g) {
 
 size_t attn_bwd_ws_bytes(const vs_params& p) { return bwd_layout(make_geom(p)).total; }
 
+cudaError_t launch_bwd_dsum(const void* O, const void* dO, float* Dsum, int L, int Hq, int d, cudaStream_t s) {
+  const long long rows = (long long)L * Hq;
+  const long long threads = rows * 16;
+  bwd_dsum_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
+      static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), Dsum, L, Hq, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_dkdv_core(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const vs_index& ix,
+                             const void* Q, const void* K, const void* V, const void* dO, const float* lse,
+                             const float* Dsum, void* dK, void* dV, float* part_k, float* part_v, float* dk32,
+                             float* dv32, DevStatus* st, cudaStream_t s) {
+  CUtensorMap mQ, mdO, mK, mV, mKp, mVp;
+  if (!make_map_heads(&mQ, Q, g.L, g.Hq, 128, g.tq_mul, g.tq_add) ||
+      !make_map_heads(&mdO, dO, g.L, g.Hq, 128, g.tq_mul, g.tq_add) ||
+      !make_map_heads(&mK, K, g.L, g.Hkv, 128, g.tk_mul, g.tk_add) ||
+      !make_map_heads(&mV, V, g.L, g.Hkv, 128, g.tk_mul, g.tk_add) ||
+      !make_map_rows(&mKp, pp.Kp, (long long)g.nvg * g.L, 128) ||
+      !make_map_rows(&mVp, pp.Vp, (long long)g.nvg * g.L, 128))
+    return cudaErrorInvalidValue;
+  BwdParams P;
+  P.g = g;
+  P.inS = pp.inS;
+  P.vlist = pp.vlist;
+  P.vcnt = pp.vcnt;
+  P.s_idx = ix.s_idx;
+  P.s_cnt = ix.s_cnt;
+  P.lse = lse;
+  P.Dsum = Dsum;
+  P.dK = static_cast<__nv_bfloat16*>(dK);
+  P.dV = static_cast<__nv_bfloat16*>(dV);
+  P.part_k = part_k;
+  P.part_v = part_v;
+  P.dk32 = dk32;
+  P.dv32 = dv32;
+  P.scale = default_scale(p);
+  P.log2e = 1.4426950408889634f;
+  P.status = st;
+  const size_t smem = kSmemBytes + 1024;
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(attn_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
+      cudaSuccess)
+    return e;
+  int dev = 0, nsm = 152;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  // vertical units first: their partials feed the slash units' epilogue
+  P.vertical = 1;
+  attn_dkdv_kernel<<<nsm, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, P);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  P.vertical = 0;
+  const int nunits = g.Hkv * g.nb;
+  attn_dkdv_kernel<<<nunits < nsm ? nunits : nsm, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, P);
+  return cudaGetLastError();
+}
+
+size_t bwd_partials_bytes(const AttnGeom& g) { return (size_t)g.nvg * g.L * g.d * 4; }
+
 cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
                             const void* O, const float* lse, const void* dO, void* dQ, void* dK, void* dV, void* ws,
                             cudaStream_t s) {
@@ -804,51 +870,11 @@ cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* 
   DevStatus* st = reinterpret_cast<DevStatus*>(w + lay.status);
   cudaError_t e = launch_attn_prep(g, ix, K, V, pp, s);
   if (e != cudaSuccess) return e;
-  {
-    const long long rows = (long long)g.L * g.Hq;
-    const long long threads = rows * 16;
-    bwd_dsum_kernel<<<(unsigned)((threads + 255) / 256), 256, 0, s>>>(
-        static_cast<const __nv_bfloat16*>(O), static_cast<const __nv_bfloat16*>(dO), dsum, g.L, g.Hq, g.d);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  }
-  CUtensorMap mQ, mdO, mK, mV, mKp, mVp;
-  if (!make_map_heads(&mQ, Q, g.L, g.Hq, 128) || !make_map_heads(&mdO, dO, g.L, g.Hq, 128) ||
-      !make_map_heads(&mK, K, g.L, g.Hkv, 128) || !make_map_heads(&mV, V, g.L, g.Hkv, 128) ||
-      !make_map_rows(&mKp, pp.Kp, (long long)g.nvg * g.L, 128) ||
-      !make_map_rows(&mVp, pp.Vp, (long long)g.nvg * g.L, 128))
-    return cudaErrorInvalidValue;
-  BwdParams P;
-  P.g = g;
-  P.inS = pp.inS;
-  P.vlist = pp.vlist;
-  P.vcnt = pp.vcnt;
-  P.s_idx = ix.s_idx;
-  P.s_cnt = ix.s_cnt;
-  P.lse = lse;
-  P.Dsum = dsum;
-  P.dK = static_cast<__nv_bfloat16*>(dK);
-  P.dV = static_cast<__nv_bfloat16*>(dV);
-  P.part_k = reinterpret_cast<float*>(w + lay.part_k);
-  P.part_v = reinterpret_cast<float*>(w + lay.part_v);
-  P.scale = default_scale(p);
-  P.log2e = 1.4426950408889634f;
-  P.status = st;
-  const size_t smem = kSmemBytes + 1024;
-  if ((e = cudaFuncSetAttribute(attn_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-      cudaSuccess)
+  if ((e = launch_bwd_dsum(O, dO, dsum, g.L, g.Hq, g.d, s)) != cudaSuccess) return e;
+  if ((e = launch_dkdv_core(p, g, pp, ix, Q, K, V, dO, lse, dsum, dK, dV, reinterpret_cast<float*>(w + lay.part_k),
+                            reinterpret_cast<float*>(w + lay.part_v), nullptr, nullptr, st, s)) != cudaSuccess)
     return e;
-  int dev = 0, nsm = 152;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  // vertical units first: their partials feed the slash units' epilogue
-  P.vertical = 1;
-  attn_dkdv_kernel<<<nsm, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, P);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  P.vertical = 0;
-  const int nunits = g.Hkv * g.nb;
-  attn_dkdv_kernel<<<nunits < nsm ? nunits : nsm, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, P);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  return launch_attn_dq(p, g, pp, Q, K, V, dO, lse, dsum, dQ, st, s);
+  return launch_attn_dq(p, g, pp, Q, K, V, dO, lse, dsum, dQ, st, StepCtl(), s);
 }
 
 }  // namespace vs

@@ -35,6 +35,15 @@ struct AttnGeom {
   int nvg;          // vertical union groups (head pairs, or heads)
   int nitems;       // row tiles
   int items_per_row;  // tiles per block index (pair_heads) or per block pair
+  // One step of the striped sparse ring (worker r, KV shard s) runs as a
+  // problem of L = L_glob / W local tokens: local query row i is global token
+  // i * tq_mul + tq_add, local key row j is j * tk_mul + tk_add.  A plain call
+  // has the identity maps and L_glob = L.
+  int L_glob;       // global tokens: row stride of lse / D, token range of outputs
+  int tq_mul, tq_add, tk_mul, tk_add;
+  int strict_diag;  // 1: the diagonal tile admits key j only for j < i (KV shard after the worker's)
+  __host__ __device__ int tq(int i) const { return i * tq_mul + tq_add; }
+  __host__ __device__ int tk(int j) const { return j * tk_mul + tk_add; }
 };
 
 inline AttnGeom make_geom(const vs_params& p) {
@@ -58,8 +67,23 @@ inline AttnGeom make_geom(const vs_params& p) {
     g.items_per_row = p.Hq;
     g.nitems = ((g.nb + 1) / 2) * g.items_per_row;
   }
+  g.L_glob = p.L;
+  g.tq_mul = g.tk_mul = 1;
+  g.tq_add = g.tk_add = 0;
+  g.strict_diag = 0;
   return g;
 }
+
+// Active keys of the causal diagonal tile for row rr (keys 0..rr, or
+// 0..rr-1 when the step's KV shard comes after the worker's own).
+__host__ __device__ inline uint64_t diag_bits(int rr, int strict) {
+  if (strict) return (1ull << rr) - 1ull;
+  return rr >= 63 ? ~0ull : ((2ull << rr) - 1ull);
+}
+
+// Where a call's results go: written directly (a plain call), or one step
+// of a ring whose partial results are carried across steps in fp32 scratch.
+enum : int { kAccPlain = 0, kAccFirst = 1, kAccMid = 2, kAccLast = 3 };
 
 struct Item {
   int g;        // key/value head
@@ -134,11 +158,33 @@ struct PrepPtrs {
 
 cudaError_t launch_attn_prep(const AttnGeom& g, const vs_index& ix, const void* K, const void* V,
                              const PrepPtrs& pp, cudaStream_t s);
+// the kept-band bitmaps only, and the vertical union + packed rows only
+cudaError_t launch_prep_bands(const AttnGeom& g, const vs_index& ix, const PrepPtrs& pp, cudaStream_t s);
+cudaError_t launch_prep_verticals(const AttnGeom& g, const vs_index& ix, const void* K, const void* V,
+                                  const PrepPtrs& pp, cudaStream_t s);
+
+// How one launch of the query-major kernel stores its results: directly
+// (kAccPlain) or as one step of a ring whose state is carried in fp32
+// scratch between steps; and which row tiles it processes.
+struct StepCtl {
+  int acc_mode = kAccPlain;
+  float* carry_o = nullptr;     // [L][Hq][d] local rows
+  float* carry_lse2 = nullptr;  // [Hq][L] (forward)
+  int item_lo = 0, item_hi = -1;  // -1: every row tile
+};
+
+cudaError_t launch_fwd_core(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const void* Q, const void* K,
+                            const void* V, void* O, float* lse, DevStatus* st, const StepCtl& ctl, cudaStream_t s);
+cudaError_t launch_attn_dq(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const void* Q, const void* K,
+                           const void* V, const void* dO, const float* lse, const float* Dsum, void* dQ,
+                           DevStatus* st, const StepCtl& ctl, cudaStream_t s);
 
 // Tensor-map helpers (host): 3-D view (d, heads, tokens) of a [L][H][d] bf16
 // tensor with a (64, 1, 64) box, and a 2-D view (d, rows) with a (64, 64) box,
 // both with 128-byte swizzle (the tcgen05 K-major / MN-major SW128 layouts).
-bool make_map_heads(CUtensorMap* m, const void* base, int L, int H, int d);
+// make_map_heads can view every tok_mul-th token starting at tok_add (one
+// shard of the striped layout) as L consecutive rows.
+bool make_map_heads(CUtensorMap* m, const void* base, int L, int H, int d, int tok_mul = 1, int tok_add = 0);
 bool make_map_rows(CUtensorMap* m, const void* base, long long rows, int d);
 
 }  // namespace vs

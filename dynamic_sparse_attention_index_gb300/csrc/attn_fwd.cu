@@ -60,12 +60,19 @@ struct QmParams {
   const uint32_t* inS;
   const uint32_t* vlist;
   const int32_t* vcnt;
-  __nv_bfloat16* out;  // O (forward) or dQ
-  float* lse;          // forward: written; dQ: read
-  const float* Dsum;   // dQ: rowsum(dO * O)
+  __nv_bfloat16* out;  // O (forward) or dQ, rows of global tokens
+  float* lse;          // forward: written; dQ: read ([Hq][L_glob])
+  const float* Dsum;   // dQ: rowsum(dO * O) ([Hq][L_glob])
   float scale_log2;
   float scale;
   DevStatus* status;
+  // ring steps: kAcc* mode and the fp32 state carried between steps, in
+  // local rows: the output [L][Hq][D] (forward: normalised O; dQ: the sum so
+  // far) and, forward only, the log2-domain log-sum-exp [Hq][L]
+  int acc_mode;
+  float* carry_o;
+  float* carry_lse2;
+  int item_lo, item_hi;  // row tiles [item_lo, item_hi) of the heaviest-first order
 };
 
 template <int D, bool kDQ>
@@ -111,10 +118,10 @@ __device__ __forceinline__ int src_mode(uint32_t w0, uint32_t w1, bool is_diag) 
   return kSrcBits;
 }
 // Active columns of a 64-key source for row rr of the segment, as a 64-bit mask.
-__device__ __forceinline__ uint64_t active_bits(int mode, uint32_t w0, uint32_t w1, int rr) {
+__device__ __forceinline__ uint64_t active_bits(int mode, uint32_t w0, uint32_t w1, int rr, int strict) {
   if (mode == kSrcOff) return 0ull;
   if (mode == kSrcFull) return ~0ull;
-  if (mode == kSrcDiag) return rr >= 63 ? ~0ull : ((2ull << rr) - 1ull);
+  if (mode == kSrcDiag) return diag_bits(rr, strict);
   return (uint64_t)w0 | ((uint64_t)w1 << 32);
 }
 // Multiply one row of the TMEM accumulator by f (warp-collective; kept out of
@@ -246,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&mVp);
       }
     }
-    for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
+    for (int id = P.item_lo + (int)blockIdx.x; id < P.item_hi && !*abort_flag; id += gridDim.x, ++it_local) {
       const Item it = decode_item(g, id);
       const int qslot = it_local % Ly::kQSlots;
       const uint32_t* bm0 = P.inS + (size_t)it.h[0] * g.nw;
@@ -515,7 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kMmaProfileQm) atomicAdd(&wcyc[19], (unsigned long long)(clock64() - a0));
         return true;
       };
-      for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
+      for (int id = P.item_lo + (int)blockIdx.x; id < P.item_hi && !*abort_flag; id += gridDim.x, ++it_local) {
         bool last = false;
         do {
           const int sk = t % Ly::kRK, sv = t % Ly::kRV;
@@ -602,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xch = reinterpret_cast<float*>(sm + Ly::kXchg);
     long long pw = 0, pk_ = 0, pe = 0;  // profiling: wait / work / epilogue cycles of this warp
     int t = 0, it_local = 0;
-    for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
+    for (int id = P.item_lo + (int)blockIdx.x; id < P.item_hi && !*abort_flag; id += gridDim.x, ++it_local) {
       const Item it = decode_item(g, id);
       const int tok = it.I[seg] * kBlock + rr;
       const int h = it.h[seg];
@@ -610,8 +617,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       float m_ref = kNegInf, l = 0.f;
       float lse2 = 0.f, Dr = 0.f;
       if (kDQ && valid) {
-        lse2 = P.lse[(size_t)h * g.L + tok] * 1.4426950408889634f;
-        Dr = P.Dsum[(size_t)h * g.L + tok];
+        lse2 = P.lse[(size_t)h * g.L_glob + g.tq(tok)] * 1.4426950408889634f;
+        Dr = P.Dsum[(size_t)h * g.L_glob + g.tq(tok)];
       }
       bool last = false;
       do {
@@ -665,7 +672,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[k] = pack_bf16(t0, t1);
               }
             } else {
-              const uint64_t act = active_bits(md, mw0, mw1, rr);
+              const uint64_t act = active_bits(md, mw0, mw1, rr, g.strict_diag);
 #pragma unroll
               for (int k = 0; k < 32; ++k) {
                 const int c = 2 * k;
@@ -685,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
             if (md != kSrcFull) {
               // masked entries become -inf in place, so neither pass needs the mask
-              act = active_bits(md, mw0, mw1, rr);
+              act = active_bits(md, mw0, mw1, rr, g.strict_diag);
 #pragma unroll
               for (int c = 0; c < 64; ++c)
                 if (!((act >> c) & 1ull)) v[c] = __float_as_uint(kNegInf);
@@ -718,7 +725,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int k = 0; k < 32; ++k) pk[k] = 0u;
           } else {
-            const uint64_t cc = f2pack(c2, c2), mm = f2pack(-m_ref, -m_ref);
+            // a row with no active key so far (only with a strict diagonal)
+            // keeps m_ref = -inf: its masked scores give exp2(-inf) = 0
+            const float mneg = m_ref == kNegInf ? 0.f : -m_ref;
+            const uint64_t cc = f2pack(c2, c2), mm = f2pack(mneg, mneg);
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
@@ -754,26 +764,54 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_warp(pv_done, (t - 1) & 1, 25)) break;
           if (!wait_warp(pv_done, t & 1, 23)) break;
           tc_fence_after();
-          __nv_bfloat16* orow = P.out + ((size_t)tok * g.Hq + h) * D;
+          __nv_bfloat16* orow = P.out + ((size_t)g.tq(tok) * g.Hq + h) * D;
+          // ring steps carry an fp32 row of local token tok between steps
+          float* crow = P.carry_o ? P.carry_o + ((size_t)tok * g.Hq + h) * D + grp * (D / 2) : nullptr;
+          const bool final_out = P.acc_mode == kAccPlain || P.acc_mode == kAccLast;
+          const bool read_carry = P.acc_mode == kAccMid || P.acc_mode == kAccLast;
           if (kDQ) {
-            // this group's half of the dQ columns
+            // this group's half of the dQ columns (a ring step adds the
+            // carried sum of the earlier steps)
             for (int c0 = 0; c0 < D / 2; c0 += 16) {
               uint32_t o[16];
               tmem_ld16(tAcc + c0, o);
               tmem_ld_wait();
-              uint32_t q8[8];
-              for (int k = 0; k < 8; ++k)
-                q8[k] = pack_bf16(__uint_as_float(o[2 * k]) * P.scale, __uint_as_float(o[2 * k + 1]) * P.scale);
-              if (valid) {
+              float x[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k) x[k] = __uint_as_float(o[k]) * P.scale;
+              if (valid && read_carry) {
+                const float4* cr = reinterpret_cast<const float4*>(crow + c0);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const float4 v4 = cr[k];
+                  x[4 * k] += v4.x;
+                  x[4 * k + 1] += v4.y;
+                  x[4 * k + 2] += v4.z;
+                  x[4 * k + 3] += v4.w;
+                }
+              }
+              if (valid && final_out) {
+                uint32_t q8[8];
+                for (int k = 0; k < 8; ++k) q8[k] = pack_bf16(x[2 * k], x[2 * k + 1]);
                 uint4* dst = reinterpret_cast<uint4*>(orow + grp * (D / 2) + c0);
                 dst[0] = make_uint4(q8[0], q8[1], q8[2], q8[3]);
                 dst[1] = make_uint4(q8[4], q8[5], q8[6], q8[7]);
+              } else if (valid) {
+                float4* cw = reinterpret_cast<float4*>(crow + c0);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) cw[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
               }
             }
           } else {
-            // combine the two groups' partial softmax states of this row:
-            // group 1 posts (m, l); group 0 forms the normalised factors and LSE
-            float ca, cb;
+            // Combine the row's softmax states into normalised factors: the
+            // two groups' accumulators (running max m, sum l each) and, for a
+            // ring step after the first, the state carried from the earlier
+            // steps (a normalised output and its log2-domain log-sum-exp).
+            // lse2n = log2(2^lc2 + l_A 2^m_A + l_B 2^m_B); each part's factor
+            // is 2^(its max - lse2n).  Group 1 posts (m, l), group 0 posts
+            // its own factor and lse2n, and each side forms the rest.
+            const float lc2 = (valid && read_carry) ? P.carry_lse2[(size_t)h * g.L + tok] : kNegInf;
+            float ca, cb, cc;
             if (grp == 1) {
               xch[2 * r] = m_ref;
               xch[2 * r + 1] = l;
@@ -781,43 +819,69 @@ __global__ void __launch_bounds__(kThreads, 1)
               if (lane == 0) mbar_arrive(ep_a);
               if (!wait_warp(ep_b, it_local & 1, 5)) break;
               ca = xch[2 * r];
-              cb = xch[2 * r + 1];
+              const float lse2n = xch[2 * r + 1];
+              cb = (l > 0.f) ? fast_exp2(m_ref - lse2n) : 0.f;
+              cc = (lc2 != kNegInf) ? fast_exp2(lc2 - lse2n) : 0.f;
             } else {
               if (!wait_warp(ep_a, it_local & 1, 6)) break;
               const float mb = xch[2 * r], lb = xch[2 * r + 1];
-              const float m = fmaxf(m_ref, mb);
-              const float fa = (l > 0.f) ? fast_exp2(m_ref - m) : 0.f;
-              const float fb = (lb > 0.f) ? fast_exp2(mb - m) : 0.f;
-              const float ltot = l * fa + lb * fb;
-              const float inv = ltot > 0.f ? 1.0f / ltot : 0.f;
-              ca = fa * inv;
-              cb = fb * inv;
-              if (valid)
-                P.lse[(size_t)h * g.L + tok] = ltot > 0.f ? (m + __log2f(ltot)) * 0.69314718055994531f : kNegInf;
+              float mx = lc2;
+              if (l > 0.f) mx = fmaxf(mx, m_ref);
+              if (lb > 0.f) mx = fmaxf(mx, mb);
+              float sum = 0.f;
+              if (lc2 != kNegInf) sum += fast_exp2(lc2 - mx);
+              if (l > 0.f) sum += l * fast_exp2(m_ref - mx);
+              if (lb > 0.f) sum += lb * fast_exp2(mb - mx);
+              const float lse2n = sum > 0.f ? mx + __log2f(sum) : kNegInf;
+              ca = (l > 0.f) ? fast_exp2(m_ref - lse2n) : 0.f;
+              cb = (lb > 0.f) ? fast_exp2(mb - lse2n) : 0.f;
+              cc = (lc2 != kNegInf) ? fast_exp2(lc2 - lse2n) : 0.f;
+              if (valid) {
+                if (final_out)
+                  P.lse[(size_t)h * g.L_glob + g.tq(tok)] =
+                      lse2n != kNegInf ? lse2n * 0.69314718055994531f : kNegInf;
+                else
+                  P.carry_lse2[(size_t)h * g.L + tok] = lse2n;
+              }
               xch[2 * r] = ca;
-              xch[2 * r + 1] = cb;
+              xch[2 * r + 1] = lse2n;
               __syncwarp();
               if (lane == 0) mbar_arrive(ep_b);
             }
             // this group's half of the output columns from both accumulators
+            // (and the carried output of the earlier ring steps)
             const uint32_t tA = tbase + 256 + lane_off + grp * (D / 2), tB = tA + 128;
             for (int c0 = 0; c0 < D / 2; c0 += 16) {
               uint32_t oa[16], ob[16];
               tmem_ld16(tA + c0, oa);
               tmem_ld16(tB + c0, ob);
               tmem_ld_wait();
-              uint32_t q8[8];
-              for (int k = 0; k < 8; ++k) {
+              float x[16];
+#pragma unroll
+              for (int k = 0; k < 16; ++k)
                 // an accumulator with no contribution (factor 0) may hold stale data
-                const float a0 = ca * __uint_as_float(oa[2 * k]) + (cb != 0.f ? cb * __uint_as_float(ob[2 * k]) : 0.f);
-                const float a1 =
-                    ca * __uint_as_float(oa[2 * k + 1]) + (cb != 0.f ? cb * __uint_as_float(ob[2 * k + 1]) : 0.f);
-                q8[k] = pack_bf16(a0, a1);
+                x[k] = ca * __uint_as_float(oa[k]) + (cb != 0.f ? cb * __uint_as_float(ob[k]) : 0.f);
+              if (valid && cc != 0.f) {
+                const float4* cr = reinterpret_cast<const float4*>(crow + c0);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                  const float4 v4 = cr[k];
+                  x[4 * k] += cc * v4.x;
+                  x[4 * k + 1] += cc * v4.y;
+                  x[4 * k + 2] += cc * v4.z;
+                  x[4 * k + 3] += cc * v4.w;
+                }
               }
-              if (valid) {
+              if (valid && final_out) {
+                uint32_t q8[8];
+                for (int k = 0; k < 8; ++k) q8[k] = pack_bf16(x[2 * k], x[2 * k + 1]);
                 uint4* dst = reinterpret_cast<uint4*>(orow + grp * (D / 2) + c0);
                 dst[0] = make_uint4(q8[0], q8[1], q8[2], q8[3]);
                 dst[1] = make_uint4(q8[4], q8[5], q8[6], q8[7]);
+              } else if (valid) {
+                float4* cw = reinterpret_cast<float4*>(crow + c0);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) cw[k] = make_float4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
               }
             }
           }
@@ -855,8 +919,10 @@ cudaError_t launch_qmajor(const AttnGeom& g, const PrepPtrs& pp, const void* Q, 
                           const void* V, const QmParams& P, cudaStream_t s) {
   using Ly = Layout<D, kDQ>;
   CUtensorMap mQ, mdO, mK, mV, mKp, mVp;
-  if (!make_map_heads(&mQ, Q, g.L, g.Hq, D) || !make_map_heads(&mdO, kDQ ? dO : Q, g.L, g.Hq, D) ||
-      !make_map_heads(&mK, K, g.L, g.Hkv, D) || !make_map_heads(&mV, V, g.L, g.Hkv, D) ||
+  if (!make_map_heads(&mQ, Q, g.L, g.Hq, D, g.tq_mul, g.tq_add) ||
+      !make_map_heads(&mdO, kDQ ? dO : Q, g.L, g.Hq, D, g.tq_mul, g.tq_add) ||
+      !make_map_heads(&mK, K, g.L, g.Hkv, D, g.tk_mul, g.tk_add) ||
+      !make_map_heads(&mV, V, g.L, g.Hkv, D, g.tk_mul, g.tk_add) ||
       !make_map_rows(&mKp, pp.Kp, (long long)g.nvg * g.L, D) ||
       !make_map_rows(&mVp, pp.Vp, (long long)g.nvg * g.L, D))
     return cudaErrorInvalidValue;
@@ -867,7 +933,9 @@ cudaError_t launch_qmajor(const AttnGeom& g, const PrepPtrs& pp, const void* Q, 
   int dev = 0, nsm = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = g.nitems < nsm ? g.nitems : nsm;
+  const int n = P.item_hi - P.item_lo;
+  if (n <= 0) return cudaSuccess;
+  const int grid = n < nsm ? n : nsm;
   attn_qmajor_kernel<D, kDQ><<<grid, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, P);
   return cudaGetLastError();
 }
@@ -880,6 +948,34 @@ size_t attn_fwd_ws_bytes(const vs_params& p) {
   w.take(sizeof(DevStatus));
   prep_layout(g, w);
   return w.off;
+}
+
+namespace {
+void set_step(QmParams& P, const AttnGeom& g, const StepCtl& ctl) {
+  P.acc_mode = ctl.acc_mode;
+  P.carry_o = ctl.carry_o;
+  P.carry_lse2 = ctl.carry_lse2;
+  P.item_lo = ctl.item_lo < 0 ? 0 : ctl.item_lo;
+  P.item_hi = (ctl.item_hi < 0 || ctl.item_hi > g.nitems) ? g.nitems : ctl.item_hi;
+}
+}  // namespace
+
+cudaError_t launch_fwd_core(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const void* Q, const void* K,
+                            const void* V, void* O, float* lse, DevStatus* st, const StepCtl& ctl, cudaStream_t s) {
+  QmParams P;
+  P.g = g;
+  P.inS = pp.inS;
+  P.vlist = pp.vlist;
+  P.vcnt = pp.vcnt;
+  P.out = static_cast<__nv_bfloat16*>(O);
+  P.lse = lse;
+  P.Dsum = nullptr;
+  P.scale = default_scale(p);
+  P.scale_log2 = P.scale * 1.4426950408889634f;
+  P.status = st;
+  set_step(P, g, ctl);
+  if (p.d == 128) return launch_qmajor<128, false>(g, pp, Q, nullptr, K, V, P, s);
+  return launch_qmajor<64, false>(g, pp, Q, nullptr, K, V, P, s);
 }
 
 cudaError_t launch_attn_fwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
@@ -898,24 +994,12 @@ cudaError_t launch_attn_fwd(const vs_params& p, const vs_index& ix, const void* 
   pp.vbits = pw.vbits != pw.end ? reinterpret_cast<uint32_t*>(w + pw.vbits) : nullptr;
   cudaError_t e = launch_attn_prep(g, ix, K, V, pp, s);
   if (e != cudaSuccess) return e;
-  QmParams P;
-  P.g = g;
-  P.inS = pp.inS;
-  P.vlist = pp.vlist;
-  P.vcnt = pp.vcnt;
-  P.out = static_cast<__nv_bfloat16*>(O);
-  P.lse = lse;
-  P.Dsum = nullptr;
-  P.scale = default_scale(p);
-  P.scale_log2 = P.scale * 1.4426950408889634f;
-  P.status = reinterpret_cast<DevStatus*>(w + st_off);
-  if (p.d == 128) return launch_qmajor<128, false>(g, pp, Q, nullptr, K, V, P, s);
-  return launch_qmajor<64, false>(g, pp, Q, nullptr, K, V, P, s);
+  return launch_fwd_core(p, g, pp, Q, K, V, O, lse, reinterpret_cast<DevStatus*>(w + st_off), StepCtl(), s);
 }
 
 cudaError_t launch_attn_dq(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const void* Q, const void* K,
                            const void* V, const void* dO, const float* lse, const float* Dsum, void* dQ,
-                           DevStatus* st, cudaStream_t s) {
+                           DevStatus* st, const StepCtl& ctl, cudaStream_t s) {
   QmParams P;
   P.g = g;
   P.inS = pp.inS;
@@ -927,6 +1011,7 @@ cudaError_t launch_attn_dq(const vs_params& p, const AttnGeom& g, const PrepPtrs
   P.scale = default_scale(p);
   P.scale_log2 = P.scale * 1.4426950408889634f;
   P.status = st;
+  set_step(P, g, ctl);
   if (p.d == 128) return launch_qmajor<128, true>(g, pp, Q, dO, K, V, P, s);
   return launch_qmajor<64, true>(g, pp, Q, dO, K, V, P, s);
 }

@@ -127,7 +127,7 @@ __global__ void prep_pack_kernel(AttnGeom g, const __nv_bfloat16* __restrict__ K
     } else {
       kv = vg / g.G;
     }
-    const size_t src = ((size_t)m * g.Hkv + kv) * g.d + piece * 8;
+    const size_t src = ((size_t)g.tk(m) * g.Hkv + kv) * g.d + piece * 8;
     *reinterpret_cast<uint4*>(Kp + dst) = *reinterpret_cast<const uint4*>(K + src);
     *reinterpret_cast<uint4*>(Vp + dst) = *reinterpret_cast<const uint4*>(V + src);
   }
@@ -148,11 +148,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 }  // namespace
 
-bool make_map_heads(CUtensorMap* m, const void* base, int L, int H, int d) {
+bool make_map_heads(CUtensorMap* m, const void* base, int L, int H, int d, int tok_mul, int tok_add) {
   auto enc = encode_fn();
   if (!enc) return false;
+  const char* b = static_cast<const char*>(base) + (size_t)tok_add * H * d * 2;
+  base = b;
   cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)L};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)tok_mul * H * d * 2};
   cuuint32_t box[3] = {64, 1, 64};
   cuuint32_t es[3] = {1, 1, 1};
   return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
@@ -172,11 +174,21 @@ bool make_map_rows(CUtensorMap* m, const void* base, long long rows, int d) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+cudaError_t launch_prep_bands(const AttnGeom& g, const vs_index& ix, const PrepPtrs& pp, cudaStream_t s) {
+  prep_bands_kernel<<<g.Hq, 256, g.nw * 4, s>>>(g, ix.s_idx, ix.s_cnt, pp.inS);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_attn_prep(const AttnGeom& g, const vs_index& ix, const void* K, const void* V,
                              const PrepPtrs& pp, cudaStream_t s) {
-  prep_bands_kernel<<<g.Hq, 256, g.nw * 4, s>>>(g, ix.s_idx, ix.s_cnt, pp.inS);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_prep_bands(g, ix, pp, s);
   if (e != cudaSuccess) return e;
+  return launch_prep_verticals(g, ix, K, V, pp, s);
+}
+
+cudaError_t launch_prep_verticals(const AttnGeom& g, const vs_index& ix, const void* K, const void* V,
+                                  const PrepPtrs& pp, cudaStream_t s) {
+  cudaError_t e;
   const size_t bits = (size_t)2 * (g.L / 32) * 4;
   const size_t sm = pp.vbits ? 0 : bits;
   e = cudaFuncSetAttribute(prep_vunion_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);

@@ -89,7 +89,7 @@ typedef struct vs_index {
   int64_t* active_entries; /* optional [Hq] exact active (n, m) entries per head             */
 } vs_index;
 
-enum { VS_OP_INDEX = 0, VS_OP_FWD = 1, VS_OP_BWD = 2, VS_OP_ROPE = 3 };
+enum { VS_OP_INDEX = 0, VS_OP_FWD = 1, VS_OP_BWD = 2, VS_OP_ROPE = 3, VS_OP_RING_FWD = 4, VS_OP_RING_BWD = 5 };
 
 /* Bytes of scratch `op` needs for problem `p` (0 if p is invalid). */
 VS_API size_t vs_workspace_bytes(const vs_params* p, int op);
@@ -172,6 +172,44 @@ VS_API vs_status vs_sparse_attn_fwd(const vs_params* p, const vs_index* index, c
 VS_API vs_status vs_sparse_attn_bwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,
                              const void* V, const void* O, const float* lse, const void* dO, void* dQ,
                              void* dK, void* dV, void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Striped sparse ring attention, forward ("平衡稀疏环注意力" section: W =
+ * p->stripes workers, token t on worker t mod W at local position t div W;
+ * ring-attention page, sections 2.1 and 3.1).  The W workers' ring is run
+ * step by step on this GPU: worker r, at step t, attends its queries to KV
+ * shard s = (r - t) mod W under the shared index (slash bands in the
+ * shard-local 64 x 64 tiles, i.e. the index vs_index_build builds with the
+ * same p->stripes; verticals as global tokens) and the local causal rule
+ * (key j <= query i when s <= r, j < i when s > r), and folds the step into
+ * a carried fp32 (output, log-sum-exp) state.  The result equals
+ * vs_sparse_attn_fwd on the same index up to rounding.  Steps run worker by
+ * worker (r = 0..W-1, t = 0..W-1).
+ *   step_events: optional array of n_events cudaEvent_t (passed as void*),
+ *   created by the caller; event r * W + t is recorded on `stream` before
+ *   step (r, t) and event W * W after the last step, so that
+ *   cudaEventElapsedTime gives each step's time.  NULL / 0: no events;
+ *   events beyond n_events are not recorded.
+ * Layouts, ownership and errors as vs_sparse_attn_fwd; ws of
+ * vs_workspace_bytes(p, VS_OP_RING_FWD) bytes.
+ */
+VS_API vs_status vs_striped_ring_fwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,
+                                     const void* V, void* O, float* lse, void* ws, size_t ws_bytes,
+                                     void* const* step_events, int32_t n_events, void* stream);
+
+/*
+ * Backward of the striped sparse ring (same ring order): with the final O
+ * and lse of every query, each step (r, t) adds its exact share of dQ of
+ * worker r (summed in fp32 across the worker's steps) and of dK, dV of shard
+ * s (summed in fp32 across workers), written as bf16 at the end.  Equals
+ * vs_sparse_attn_bwd on the same index up to rounding.  d = 128 only
+ * (VS_ERR_UNSUPPORTED otherwise).  Events, layouts and errors as
+ * vs_striped_ring_fwd; ws of vs_workspace_bytes(p, VS_OP_RING_BWD) bytes.
+ */
+VS_API vs_status vs_striped_ring_bwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,
+                                     const void* V, const void* O, const float* lse, const void* dO, void* dQ,
+                                     void* dK, void* dV, void* ws, size_t ws_bytes, void* const* step_events,
+                                     int32_t n_events, void* stream);
 
 /*
  * Reads the device-side status word of workspace `ws` (synchronises

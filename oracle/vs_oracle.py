@@ -48,7 +48,7 @@ __all__ = [
     "select_top_p", "select_budget", "build_index", "active_entries",
     "sparsity_ratio", "explicit_mask", "attention_forward", "attention_backward",
     "attention_forward_rows", "attention_backward_dq_rows", "total_causal_entries",
-    "attention_backward_bf16_products",
+    "attention_backward_bf16_products", "striped_ring_forward", "striped_ring_backward",
 ]
 
 
@@ -404,6 +404,114 @@ def attention_backward_bf16_products(Q, K, V, dO, index, scale=None, stripes=1, 
             dV[:, g, :] += bf16_round(p).T @ dO[r, h, :]
             dQ[r, h, :] = scale * (dS_b @ kh)
             dK[:, g, :] += scale * (dS_b.T @ Q[r, h, :])
+    return dQ, dK, dV
+
+
+# ----------------------------------------------------------------------------
+# Striped sparse ring attention ([MT] 三/核心创新/3 "平衡稀疏环注意力": striped
+# layout over W workers; [RA] §2.1 block-wise ring computation with an
+# incremental softmax, §3.1 striped round-robin layout)
+
+def _ring_step_mask(Ls, W, r, s, Vh, Sh, block):
+    """Active entries of ring step (worker r, KV shard s) in local
+    coordinates: worker r holds global tokens n = i W + r, shard s holds
+    m = j W + s.  Local causal rule: j <= i when s <= r, else j < i (the
+    global rule m <= n).  The shared index: slash band floor(i / block) -
+    floor(j / block) kept (tiles of the shard-local order), or m a kept
+    vertical."""
+    i = np.arange(Ls)[:, None]
+    j = np.arange(Ls)[None, :]
+    causal = (j <= i) if s <= r else (j < i)
+    nb = Ls // block
+    inS = np.zeros(nb, bool)
+    inS[np.asarray(Sh, np.int64)] = True
+    band = i // block - j // block
+    isV = np.zeros(Ls, bool)
+    Vh = np.asarray(Vh, np.int64)
+    isV[(Vh[Vh % W == s] - s) // W] = True
+    return causal & (inS[np.clip(band, 0, nb - 1)] | isV[None, :].repeat(Ls, 0))
+
+
+def striped_ring_forward(Q, K, V, index, W, scale=None, block=64):
+    """Sparse ring attention over W striped workers, step by step.
+
+    Worker r holds the queries of tokens r, r + W, ...; at step t it holds
+    KV shard s = (r - t) mod W and folds that step's active entries into its
+    running (M, l, O) (max, sum of exponentials, unnormalised output):
+    M' = max(M, max s), l' = l e^(M - M') + sum e^(s - M'),
+    O' = O e^(M - M') + sum e^(s - M') v.  After W steps O / l is the output
+    and M + ln l the log-sum-exp.  ``index`` is the shared striped index
+    (slash bands in shard-local 64 x 64 tiles, verticals as global tokens).
+    Returns O [L, Hq, d] and LSE [Hq, L] in the global token order."""
+    Q = np.asarray(Q, np.float64)
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    L, Hq, d = Q.shape
+    G = Hq // K.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    Ls = L // W
+    O = np.zeros_like(Q)
+    LSE = np.zeros((Hq, L))
+    for h in range(Hq):
+        Vh, Sh = index[h]
+        g = h // G
+        for r in range(W):
+            q = Q[r::W, h, :]
+            M = np.full(Ls, -np.inf)
+            l = np.zeros(Ls)
+            acc = np.zeros((Ls, d))
+            for t in range(W):
+                sh = (r - t) % W
+                msk = _ring_step_mask(Ls, W, r, sh, Vh, Sh, block)
+                sc = np.where(msk, scale * (q @ K[sh::W, g, :].T), -np.inf)
+                mx = np.maximum(M, sc.max(axis=1))
+                live = np.isfinite(mx)
+                f = np.where(live, np.exp(np.where(live, M - mx, 0.0)), 0.0)
+                p = np.where(msk, np.exp(sc - np.where(live, mx, 0.0)[:, None]), 0.0)
+                l = l * f + p.sum(axis=1)
+                acc = acc * f[:, None] + p @ V[sh::W, g, :]
+                M = mx
+            O[r::W, h, :] = acc / l[:, None]
+            LSE[h, r::W] = M + np.log(l)
+    return O, LSE
+
+
+def striped_ring_backward(Q, K, V, dO, index, W, scale=None, block=64):
+    """Gradients of ``striped_ring_forward``, step by step in the same ring
+    order: with the final O and LSE of every query, D_n = sum_c dO_nc O_nc;
+    at step (r, s) P = exp(scale q k - LSE) on the step's active entries,
+    dV_s += P^T dO_r, dS = P (dO_r V_s^T - D), dQ_r += scale dS K_s,
+    dK_s += scale dS^T Q_r (dK, dV summed over the query heads of a group)."""
+    Q = np.asarray(Q, np.float64)
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    dO = np.asarray(dO, np.float64)
+    L, Hq, d = Q.shape
+    G = Hq // K.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    Ls = L // W
+    O, LSE = striped_ring_forward(Q, K, V, index, W, scale, block)
+    dQ = np.zeros_like(Q)
+    dK = np.zeros_like(K)
+    dV = np.zeros_like(V)
+    for h in range(Hq):
+        Vh, Sh = index[h]
+        g = h // G
+        for r in range(W):
+            q, do = Q[r::W, h, :], dO[r::W, h, :]
+            D = (do * O[r::W, h, :]).sum(axis=1, keepdims=True)
+            lse = LSE[h, r::W][:, None]
+            for t in range(W):
+                sh = (r - t) % W
+                msk = _ring_step_mask(Ls, W, r, sh, Vh, Sh, block)
+                k, v = K[sh::W, g, :], V[sh::W, g, :]
+                p = np.where(msk, np.exp(scale * (q @ k.T) - lse), 0.0)
+                dS = p * (do @ v.T - D)
+                dV[sh::W, g, :] += p.T @ do
+                dQ[r::W, h, :] += scale * (dS @ k)
+                dK[sh::W, g, :] += scale * (dS.T @ q)
     return dQ, dK, dV
 
 

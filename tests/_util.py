@@ -97,3 +97,28 @@ def budget_sets_agree(v_or, S_or, kept_or, kept_gpu, tol=1e-6):
         if abs(S_or[e] / ts - thr) > tol:
             bad.append(("s", e, S_or[e] / ts, thr))
     return not bad, bad
+
+
+def ulp_bf16(x):
+    """Spacing of bf16 values at |x| (2^(e - 7) for |x| in [2^e, 2^(e+1)))."""
+    a = np.abs(np.asarray(x, np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(e - 7), 2.0 ** -133)
+
+
+def grad_close(name, got, ref, emu):
+    """Backward parity, element by element.  ``ref`` is the exact fp64
+    gradient, ``emu`` the same gradient with the bf16 roundings of the
+    stated arithmetic (oracle.attention_backward_bf16_products).  The kernel
+    must follow that arithmetic: every element within 2e-2 + half a bf16 ulp
+    of ``emu`` (the output is stored as bf16); and the result must be close
+    to the exact gradient: relative L2 <= 1e-2, every element within
+    2e-2 + half an ulp of ``ref`` plus the arithmetic's own distance
+    |emu - ref| at that element."""
+    err_e = np.abs(got - emu)
+    bad = err_e > 2e-2 + 0.5 * ulp_bf16(emu)
+    assert not bad.any(), (name, "vs bf16-products oracle", int(bad.sum()), float(err_e.max()))
+    err = np.abs(got - ref)
+    bad = err > 2e-2 + 0.5 * ulp_bf16(ref) + np.abs(emu - ref)
+    assert not bad.any(), (name, "vs exact oracle", int(bad.sum()), float(err.max()))
+    assert rel_l2(got, ref) <= 1e-2, (name, rel_l2(got, ref))

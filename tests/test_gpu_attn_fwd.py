@@ -110,24 +110,22 @@ def test_fwd_striped_32_shards():
 
 
 def test_fwd_full_size_gqa_128k_sampled():
-    """The 128K GQA workload at full size, budget-fill index built on the GPU,
-    checked on sampled rows (first, middle, last blocks; every head)."""
+    """The 128K GQA workload at full size under the oracle's budget-fill
+    index, checked on sampled rows (first, middle, last blocks; every head)."""
     import torch
     import dynamic_sparse_attention_index_gb300 as vs
-    from _util import gpu_index_lists
     w = synth.make_workload(3, backward=False)
     dev = torch.device("cuda:0")
     p = vs.make_params(w.L, w.Hq, w.Hkv, w.d, last_q=64, top_p=0.95, density=0.05)
     Q, K, V = to_dev(w.q, dev), to_dev(w.k, dev), to_dev(w.v, dev)
-    ix = vs.IndexBuffers.allocate(p, dev)
-    vs.vs_index_build(p, Q, K, ix, vs.workspace(p, vs.VS_OP_INDEX, dev))
+    index, _, _ = oracle.build_index(f64(w.q), f64(w.k), 64, 0.95, density=float(np.float32(0.05)))
+    ix = inject_index(vs, p, index, dev)
     O = torch.empty_like(Q)
     lse = torch.empty((w.Hq, w.L), dtype=torch.float32, device=dev)
     ws = vs.workspace(p, vs.VS_OP_FWD, dev)
     vs.vs_sparse_attn_fwd(p, ix, Q, K, V, O, lse, ws)
     torch.cuda.synchronize()
     assert vs.vs_device_status(ws) == vs.VS_OK
-    index = gpu_index_lists(ix, w.Hq)
     rows = np.concatenate([np.arange(0, 70), np.arange(65536 - 3, 65536 + 67), np.arange(w.L - 70, w.L)])
     Or, lser = oracle.attention_forward_rows(f64(w.q), f64(w.k), f64(w.v), index, rows)
     got = f64(bf16_bits_of(O[torch.from_numpy(rows).to(dev)]))

@@ -1,8 +1,10 @@
 """The largest supported sequence, L = 2^20 tokens (GQA 2/1, d = 128).
 
 Index (budget fill to density 0.05): the GPU's masses against the oracle's,
-and its kept sets exactly equal to the oracle's selection on those masses.
-Forward on sampled rows against the oracle; backward dQ on sampled rows and
+its kept sets exactly equal to the oracle's selection on those masses, and
+equal to the oracle's fp64 selection up to ties at the threshold.  Under the
+oracle's index: forward on sampled rows against the oracle; backward dQ on
+sampled rows and
 dK / dV through the identities that hold for any mask (summed over keys, dV
 gives the sum of dO over the group's rows and dK gives zero)."""
 import numpy as np
@@ -10,7 +12,7 @@ import pytest
 
 import oracle
 import synth
-from _util import bf16_bits_of, f64, gpu_index_lists, rel_l2, to_dev
+from _util import bf16_bits_of, budget_sets_agree, f64, gpu_index_lists, inject_index, rel_l2, to_dev
 
 pytestmark = pytest.mark.gpu
 
@@ -27,30 +29,39 @@ def test_max_length_index_forward_backward():
     Q, K, V, dO = (to_dev(a, dev) for a in (w.q, w.k, w.v, w.do))
     ix = vs.IndexBuffers.allocate(p, dev)
     vs.vs_index_build(p, Q, K, ix, vs.workspace(p, vs.VS_OP_INDEX, dev))
-    O = torch.empty_like(Q)
-    lse = torch.empty((w.Hq, w.L), dtype=torch.float32, device=dev)
-    wsf = vs.workspace(p, vs.VS_OP_FWD, dev)
-    vs.vs_sparse_attn_fwd(p, ix, Q, K, V, O, lse, wsf)
-    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
-    wsb = vs.workspace(p, vs.VS_OP_BWD, dev)
-    vs.vs_sparse_attn_bwd(p, ix, Q, K, V, O, lse, dO, dQ, dK, dV, wsb)
     torch.cuda.synchronize()
-    assert vs.vs_device_status(wsf) == vs.VS_OK and vs.vs_device_status(wsb) == vs.VS_OK
 
-    # index
+    # index: masses, same-precision decisions, and end to end against fp64
     q, k = f64(w.q), f64(w.k)
-    v_or, _ = oracle.index_scores(q, k, 64)
+    v_or, S_or = oracle.index_scores(q, k, 64)
     np.testing.assert_allclose(ix.v_score.double().cpu().numpy(), v_or, rtol=1e-4, atol=1e-12)
-    index = gpu_index_lists(ix, w.Hq)
+    lists = gpu_index_lists(ix, w.Hq)
     act = ix.active_entries.cpu().numpy()
     dens32 = float(np.float32(density))
+    index = []
     for h in range(w.Hq):
         v32 = ix.v_score[h].cpu().numpy().astype(np.float64)
         S32 = ix.s_score[h].cpu().numpy().astype(np.float64)
         Vo, So = oracle.select_budget(v32, S32, w.L, 64, dens32)
-        np.testing.assert_array_equal(index[h][0], Vo)
-        np.testing.assert_array_equal(index[h][1], So)
+        np.testing.assert_array_equal(lists[h][0], Vo)
+        np.testing.assert_array_equal(lists[h][1], So)
         assert act[h] == oracle.active_entries(w.L, Vo, So, 64)
+        kept_or = oracle.select_budget(v_or[h], S_or[h], w.L, 64, dens32)
+        ok, bad = budget_sets_agree(v_or[h], S_or[h], kept_or, lists[h])
+        assert ok, bad[:5]
+        index.append(kept_or)
+
+    # forward then backward (a training step) under the oracle's index
+    ix_or = inject_index(vs, p, index, dev)
+    O = torch.empty_like(Q)
+    lse = torch.empty((w.Hq, w.L), dtype=torch.float32, device=dev)
+    wsf = vs.workspace(p, vs.VS_OP_FWD, dev)
+    vs.vs_sparse_attn_fwd(p, ix_or, Q, K, V, O, lse, wsf)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    wsb = vs.workspace(p, vs.VS_OP_BWD, dev)
+    vs.vs_sparse_attn_bwd(p, ix_or, Q, K, V, O, lse, dO, dQ, dK, dV, wsb)
+    torch.cuda.synchronize()
+    assert vs.vs_device_status(wsf) == vs.VS_OK and vs.vs_device_status(wsb) == vs.VS_OK
 
     # forward and dQ on sampled rows (first, middle and last blocks)
     rows = np.concatenate([np.arange(0, 64), np.arange(L_MAX // 2, L_MAX // 2 + 64), np.arange(L_MAX - 64, L_MAX)])
