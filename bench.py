@@ -211,12 +211,15 @@ def run_gpu(args):
     d_out = [torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)] if bwd else [O]
     ix = vs.IndexBuffers.allocate(p, dev)
     ws_i = vs.workspace(p, vs.VS_OP_INDEX, dev)
-    ws_f = vs.workspace(p, vs.VS_OP_FWD, dev)
-    ws_b = vs.workspace(p, vs.VS_OP_BWD, dev) if bwd else None
+    ring = W > 1  # striped layout: the W-worker ring, run step by step
+    ws_f = vs.workspace(p, vs.VS_OP_RING_FWD if ring else vs.VS_OP_FWD, dev)
+    ws_b = vs.workspace(p, vs.VS_OP_RING_BWD if ring else vs.VS_OP_BWD, dev) if bwd else None
     h_out = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in d_out]
     stream = torch.cuda.current_stream()
     phases = ("rope", "index", "fwd", "bwd") if bwd else ("rope", "index", "fwd")
     ev = {k: (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for k in phases}
+
+    step_ev = {}  # ring: per-step events of one instrumented pass ("fwd", "bwd" -> W * W + 1 events)
 
     def step(timed=False, io=None):
         # io: the step's input and output device buffers
@@ -234,12 +237,18 @@ def run_gpu(args):
         vs.vs_index_build(p, Q, K, ix, ws_i)
         rec("index", 1)
         rec("fwd", 0)
-        vs.vs_sparse_attn_fwd(p, ix, Q, K, v_, O if bwd else outs[0], lse, ws_f)
+        if ring:
+            vs.vs_striped_ring_fwd(p, ix, Q, K, v_, O if bwd else outs[0], lse, ws_f, events=step_ev.get("fwd"))
+        else:
+            vs.vs_sparse_attn_fwd(p, ix, Q, K, v_, O if bwd else outs[0], lse, ws_f)
         rec("fwd", 1)
         if bwd:
             dq, dk, dv = outs
             rec("bwd", 0)
-            vs.vs_sparse_attn_bwd(p, ix, Q, K, v_, O, lse, ins[3], dq, dk, dv, ws_b)
+            if ring:
+                vs.vs_striped_ring_bwd(p, ix, Q, K, v_, O, lse, ins[3], dq, dk, dv, ws_b, events=step_ev.get("bwd"))
+            else:
+                vs.vs_sparse_attn_bwd(p, ix, Q, K, v_, O, lse, ins[3], dq, dk, dv, ws_b)
             rec("bwd", 1)
             vs.vs_rope(p, Hq, dq, dq, True)
             vs.vs_rope(p, Hkv, dk, dk, True)
@@ -268,6 +277,7 @@ def run_gpu(args):
         vs.vs_index_build(p, Q, K, ix_w, vs.workspace(p, vs.VS_OP_INDEX, dev))
         torch.cuda.synchronize()
         balance = shard_balance(L, W, index_lists(ix_w, Hq), index_lists(ix1, Hq))
+        balance["timed"] = ring_balance(vs, p1, ix1, Q, K, V, W, dev, step, step_ev, bwd)
         del ix1, ix_w
     assert vs.vs_device_status(ws_f) == vs.VS_OK
     assert ws_b is None or vs.vs_device_status(ws_b) == vs.VS_OK
@@ -361,7 +371,14 @@ def run_gpu(args):
     # burst peak is the denominator (the sustained one is listed beside it)
     dom = ("vs_sparse_attn_bwd (dK/dV + dQ)", bwd_tf) if bwd else ("vs_sparse_attn_fwd", fwd_tf)
     peak, peak_s = pk["bf16_tflops"], pk["bf16_tflops_sustained"]
-    kps = KERNELS_PER_STEP if bwd else KERNELS_PER_STEP_FWD
+    kps = dict(KERNELS_PER_STEP if bwd else KERNELS_PER_STEP_FWD)
+    if ring:
+        # ring setup (shard lists, band bitmaps, a vertical union and packed
+        # rows per shard) and W x W steps: one forward kernel per step; D, the
+        # two dK / dV kernels and the dQ kernel per step, two final casts
+        kps["fwd"] = 2 + 2 * W + W * W
+        if bwd:
+            kps["bwd"] = 1 + 2 + 2 * W + 3 * W * W + 2
     out = {
         "metric": "VS sparse attn fwd+bwd ms and effective TFLOP/s at 128K (% bf16 peak)",
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
@@ -425,6 +442,56 @@ def row_active_counts(L, V, S, bs):
     for B in np.flatnonzero(kept[1:]) + 1:
         inband[B:] += cnt_v[:nbs - B]
     return slash + (before - inband)[qb]
+
+
+def ring_balance(vs, p1, ix1, Q, K, V, W, dev, step, step_ev, bwd):
+    """Timed per-worker and per-step balance.  Striped layout: one step of
+    the bench run with CUDA events around each of the W x W ring steps
+    (worker r, step t); a worker's time is the sum of its W steps, a ring
+    step's time the slowest worker's (the ring advances together).
+    Contiguous and ZigZag splits of the contiguous index: each worker's rows
+    of the forward, timed as one vs_sparse_attn_fwd_rows call (contiguous:
+    rows [r L/W, (r+1) L/W); ZigZag: 2 W chunks, worker k holds chunks k and
+    2 W - 1 - k)."""
+    import torch
+    mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(W * W + 1)]
+    step_ev["fwd"] = mk()
+    if bwd:
+        step_ev["bwd"] = mk()
+    step()
+    torch.cuda.synchronize()
+    out = {"unit": "ms (CUDA events)"}
+    for k, ev in list(step_ev.items()):
+        t = np.array([ev[i].elapsed_time(ev[i + 1]) for i in range(W * W)]).reshape(W, W)
+        worker = t.sum(1)
+        per_step = t.max(0)
+        out[f"striped_ring_{k}"] = {
+            "total_ms": round(float(t.sum()), 3), "worker_max_over_mean": round(float(worker.max() / worker.mean()), 4),
+            "step_max_over_mean": round(float((t.max(0) / t.mean(0)).max()), 4),
+            "step_ms_slowest_worker": [round(float(x), 4) for x in per_step]}
+    step_ev.clear()
+    L = p1.L
+    O = torch.empty_like(Q)
+    lse = torch.empty((p1.Hq, L), dtype=torch.float32, device=dev)
+    ws = vs.workspace(p1, vs.VS_OP_FWD, dev)
+    Ls, Lz = L // W, L // (2 * W)
+
+    def timed(ranges):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for lo, hi in ranges:
+            vs.vs_sparse_attn_fwd_rows(p1, ix1, Q, K, V, O, lse, ws, lo, hi)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1)
+    timed([(0, Ls)])  # warm-up
+    for name, workers in (("contiguous", [[(r * Ls, (r + 1) * Ls)] for r in range(W)]),
+                          ("zigzag", [[(k * Lz, (k + 1) * Lz), ((2 * W - 1 - k) * Lz, (2 * W - k) * Lz)]
+                                      for k in range(W)])):
+        t = np.array([timed(rg) for rg in workers])
+        out[f"{name}_fwd_rows"] = {"worker_max_over_mean": round(float(t.max() / t.mean()), 4),
+                                   "worker_ms_max": round(float(t.max()), 4), "worker_ms_mean": round(float(t.mean()), 4)}
+    return out
 
 
 def shard_balance(L, W, index_striped, index_contig):

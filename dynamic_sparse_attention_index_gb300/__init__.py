@@ -7,7 +7,8 @@ library is missing or fails to load, every call raises.
 
 Entry points mirror the C names: ``vs_workspace_bytes``, ``vs_rope``,
 ``vs_index_build``, ``vs_index_build_noalloc``, ``vs_sparse_attn_fwd``, ``vs_sparse_attn_bwd``,
-``vs_striped_ring_fwd``, ``vs_striped_ring_bwd``, ``vs_device_status``, ``vs_status_string``.
+``vs_sparse_attn_fwd_rows``, ``vs_striped_ring_fwd``, ``vs_striped_ring_bwd``, ``vs_device_status``,
+``vs_status_string``.
 """
 from __future__ import annotations
 
@@ -24,7 +25,7 @@ VS_OP_INDEX, VS_OP_FWD, VS_OP_BWD, VS_OP_ROPE, VS_OP_RING_FWD, VS_OP_RING_BWD = 
 #: every symbol the header declares
 EXPORTED = ("vs_workspace_bytes", "vs_status_string", "vs_rope", "vs_index_build",
             "vs_index_build_noalloc", "vs_sparse_attn_fwd", "vs_sparse_attn_bwd", "vs_device_status",
-            "vs_striped_ring_fwd", "vs_striped_ring_bwd")
+            "vs_striped_ring_fwd", "vs_striped_ring_bwd", "vs_sparse_attn_fwd_rows")
 
 #: size of the static scratch behind vs_index_build_noalloc (VS_INDEX_NOALLOC_SCRATCH_BYTES)
 INDEX_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -77,9 +78,11 @@ def lib() -> ctypes.CDLL:
         L.vs_device_status.argtypes = [VP, VP]
         EV = ctypes.POINTER(ctypes.c_void_p)
         L.vs_striped_ring_fwd.argtypes = [P, I, VP, VP, VP, VP, VP, VP, SZ, EV, i32, VP]
+        L.vs_sparse_attn_fwd_rows.argtypes = [P, I, VP, VP, VP, VP, VP, VP, SZ, i32, i32, VP]
         L.vs_striped_ring_bwd.argtypes = [P, I, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ, EV, i32, VP]
         for f in ("vs_rope", "vs_index_build", "vs_index_build_noalloc", "vs_sparse_attn_fwd",
-                  "vs_sparse_attn_bwd", "vs_device_status", "vs_striped_ring_fwd", "vs_striped_ring_bwd"):
+                  "vs_sparse_attn_bwd", "vs_device_status", "vs_striped_ring_fwd", "vs_striped_ring_bwd",
+                  "vs_sparse_attn_fwd_rows"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -173,6 +176,14 @@ def vs_sparse_attn_fwd(p: vs_params, index: IndexBuffers, Q, K, V, O, lse, ws, s
     ix = index.c()
     _check(lib().vs_sparse_attn_fwd(ctypes.byref(p), ctypes.byref(ix), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
                                     _ptr(lse), _ptr(ws), ws.numel(), _stream(stream)), "vs_sparse_attn_fwd")
+
+
+def vs_sparse_attn_fwd_rows(p: vs_params, index: IndexBuffers, Q, K, V, O, lse, ws, row_lo: int, row_hi: int,
+                            stream=None):
+    ix = index.c()
+    _check(lib().vs_sparse_attn_fwd_rows(ctypes.byref(p), ctypes.byref(ix), _ptr(Q), _ptr(K), _ptr(V), _ptr(O),
+                                         _ptr(lse), _ptr(ws), ws.numel(), row_lo, row_hi, _stream(stream)),
+           "vs_sparse_attn_fwd_rows")
 
 
 def vs_sparse_attn_bwd(p: vs_params, index: IndexBuffers, Q, K, V, O, lse, dO, dQ, dK, dV, ws, stream=None):

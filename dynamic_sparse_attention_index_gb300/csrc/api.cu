@@ -11,7 +11,7 @@ cudaError_t launch_index_scores(const IndexArgs& a, cudaStream_t s);
 cudaError_t launch_select(const IndexArgs& a, cudaStream_t s);
 size_t select_smem_bytes(int nbs);
 cudaError_t launch_attn_fwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
-                            void* O, float* lse, void* ws, cudaStream_t s);
+                            void* O, float* lse, void* ws, cudaStream_t s, int blk_lo, int blk_hi);
 size_t attn_fwd_ws_bytes(const vs_params& p);
 cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
                             const void* O, const float* lse, const void* dO, void* dQ, void* dK, void* dV, void* ws,
@@ -266,7 +266,25 @@ vs_status vs_sparse_attn_fwd(const vs_params* p, const vs_index* index, const vo
   if ((st = check_ws(ws, ws_bytes, attn_fwd_ws_bytes(*p))) != VS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
-  return launch_attn_fwd(*p, *index, Q, K, V, O, lse, ws, s) == cudaSuccess ? VS_OK : VS_ERR_CUDA;
+  return launch_attn_fwd(*p, *index, Q, K, V, O, lse, ws, s, 0, p->L / kBlock) == cudaSuccess ? VS_OK : VS_ERR_CUDA;
+}
+
+vs_status vs_sparse_attn_fwd_rows(const vs_params* p, const vs_index* index, const void* Q, const void* K,
+                                  const void* V, void* O, float* lse, void* ws, size_t ws_bytes, int32_t row_lo,
+                                  int32_t row_hi, void* stream) {
+  vs_status st = check_params(p);
+  if (st != VS_OK) return st;
+  if (row_lo < 0 || row_hi > p->L || row_lo >= row_hi || row_lo % kBlock || row_hi % kBlock)
+    return VS_ERR_INVALID_ARG;
+  if ((st = check_index_ptrs(index)) != VS_OK) return st;
+  if (!Q || !K || !V || !O || !lse) return VS_ERR_INVALID_ARG;
+  if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(lse)) return VS_ERR_INVALID_ARG;
+  if ((st = check_ws(ws, ws_bytes, attn_fwd_ws_bytes(*p))) != VS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
+  return launch_attn_fwd(*p, *index, Q, K, V, O, lse, ws, s, row_lo / kBlock, row_hi / kBlock) == cudaSuccess
+             ? VS_OK
+             : VS_ERR_CUDA;
 }
 
 vs_status vs_sparse_attn_bwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,

@@ -978,8 +978,23 @@ cudaError_t launch_fwd_core(const vs_params& p, const AttnGeom& g, const PrepPtr
   return launch_qmajor<64, false>(g, pp, Q, nullptr, K, V, P, s);
 }
 
+// Row tiles covering query blocks [blk_lo, blk_hi) in the heaviest-first
+// numbering of decode_item (head-paired tiles: one block each; otherwise
+// block pairs, so the range is widened to whole pairs).
+void item_range(const AttnGeom& g, int blk_lo, int blk_hi, int* lo, int* hi) {
+  if (g.pair_heads) {
+    *lo = (g.nb - blk_hi) * g.items_per_row;
+    *hi = (g.nb - blk_lo) * g.items_per_row;
+  } else {
+    const int npair = (g.nb + 1) / 2;
+    const int u_lo = blk_lo / 2, u_hi = (blk_hi + 1) / 2;
+    *lo = (npair - u_hi) * g.items_per_row;
+    *hi = (npair - u_lo) * g.items_per_row;
+  }
+}
+
 cudaError_t launch_attn_fwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
-                            void* O, float* lse, void* ws, cudaStream_t s) {
+                            void* O, float* lse, void* ws, cudaStream_t s, int blk_lo, int blk_hi) {
   const AttnGeom g = make_geom(p);
   uint8_t* w = static_cast<uint8_t*>(ws);
   WsLayout lay;
@@ -994,7 +1009,9 @@ cudaError_t launch_attn_fwd(const vs_params& p, const vs_index& ix, const void* 
   pp.vbits = pw.vbits != pw.end ? reinterpret_cast<uint32_t*>(w + pw.vbits) : nullptr;
   cudaError_t e = launch_attn_prep(g, ix, K, V, pp, s);
   if (e != cudaSuccess) return e;
-  return launch_fwd_core(p, g, pp, Q, K, V, O, lse, reinterpret_cast<DevStatus*>(w + st_off), StepCtl(), s);
+  StepCtl ctl;
+  if (blk_lo > 0 || blk_hi < g.nb) item_range(g, blk_lo, blk_hi, &ctl.item_lo, &ctl.item_hi);
+  return launch_fwd_core(p, g, pp, Q, K, V, O, lse, reinterpret_cast<DevStatus*>(w + st_off), ctl, s);
 }
 
 cudaError_t launch_attn_dq(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const void* Q, const void* K,

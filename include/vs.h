@@ -164,6 +164,19 @@ VS_API vs_status vs_sparse_attn_fwd(const vs_params* p, const vs_index* index, c
                              const void* V, void* O, float* lse, void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * vs_sparse_attn_fwd restricted to the query rows [row_lo, row_hi) (both
+ * multiples of 64; the rows of every head): the same results for those rows,
+ * the other rows of O and lse untouched.  A worker of a context-parallel
+ * split that holds a range of query rows computes exactly this.  When
+ * Hq / Hkv is odd, rows are processed in pairs of 64-row blocks, so the
+ * range is widened to whole 128-row pairs.  Arguments and errors as
+ * vs_sparse_attn_fwd; VS_ERR_INVALID_ARG for a bad row range.
+ */
+VS_API vs_status vs_sparse_attn_fwd_rows(const vs_params* p, const vs_index* index, const void* Q, const void* K,
+                                         const void* V, void* O, float* lse, void* ws, size_t ws_bytes,
+                                         int32_t row_lo, int32_t row_hi, void* stream);
+
+/*
  * Backward of vs_sparse_attn_fwd with the mask held fixed:
  * dV = P^T dO, dS = P * (dO V^T - rowsum(dO * O)), dQ = scale dS K,
  * dK = scale dS^T Q; dK and dV sum over the Hq/Hkv query heads sharing a

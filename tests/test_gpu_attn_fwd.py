@@ -132,3 +132,32 @@ def test_fwd_full_size_gqa_128k_sampled():
     assert np.abs(got - Or).max() <= 2e-2
     assert rel_l2(got, Or) <= 1e-2
     assert np.abs(lse.double().cpu().numpy()[:, rows] - lser).max() <= 1e-3
+
+
+@pytest.mark.parametrize("Hq,Hkv,lo,hi", [(4, 2, 512, 1536), (3, 1, 256, 768), (2, 1, 0, 2048)])
+def test_fwd_row_range(Hq, Hkv, lo, hi):
+    """vs_sparse_attn_fwd_rows: the rows of a context-parallel worker.  Its
+    rows are bit-identical to the full call's (each row tile is computed the
+    same way whichever others run) and the other rows stay untouched."""
+    import torch
+    import dynamic_sparse_attention_index_gb300 as vs
+    dev = torch.device("cuda:0")
+    w = synth.make_workload(3, L=2048, Hq=Hq, Hkv=Hkv, d=128)
+    index, _, _ = oracle.build_index(f64(w.q), f64(w.k), 64, 0.95, density=0.1)
+    p = vs.make_params(w.L, w.Hq, w.Hkv, w.d, last_q=64, top_p=0.95)
+    ix = inject_index(vs, p, index, dev)
+    Q, K, V = to_dev(w.q, dev), to_dev(w.k, dev), to_dev(w.v, dev)
+    ws = vs.workspace(p, vs.VS_OP_FWD, dev)
+    O = torch.empty_like(Q)
+    lse = torch.empty((w.Hq, w.L), dtype=torch.float32, device=dev)
+    vs.vs_sparse_attn_fwd(p, ix, Q, K, V, O, lse, ws)
+    O2 = torch.full_like(Q, 7.0)
+    lse2 = torch.full((w.Hq, w.L), 7.0, dtype=torch.float32, device=dev)
+    vs.vs_sparse_attn_fwd_rows(p, ix, Q, K, V, O2, lse2, ws, lo, hi)
+    torch.cuda.synchronize()
+    # odd group sizes work on pairs of 64-row blocks: widen to whole pairs
+    if (Hq // Hkv) % 2:
+        lo, hi = lo // 128 * 128, (hi + 127) // 128 * 128
+    assert torch.equal(O2[lo:hi], O[lo:hi]) and torch.equal(lse2[:, lo:hi], lse[:, lo:hi])
+    assert (O2[:lo] == 7.0).all() and (O2[hi:] == 7.0).all()
+    assert (lse2[:, :lo] == 7.0).all() and (lse2[:, hi:] == 7.0).all()
