@@ -10,6 +10,8 @@ namespace vs {
 cudaError_t launch_index_scores(const IndexArgs& a, cudaStream_t s);
 cudaError_t launch_select(const IndexArgs& a, cudaStream_t s);
 size_t select_smem_bytes(int nbs);
+size_t group_union_smem_bytes(int L, int bs);
+cudaError_t launch_group_union(const vs_params& p, const vs_index& ix, cudaStream_t s);
 cudaError_t launch_attn_fwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
                             void* O, float* lse, void* ws, cudaStream_t s, int blk_lo, int blk_hi);
 size_t attn_fwd_ws_bytes(const vs_params& p);
@@ -41,6 +43,7 @@ vs_status check_params(const vs_params* p) {
   if (!(p->top_p > 0.f && p->top_p <= 1.f)) return VS_ERR_INVALID_ARG;
   if (!(p->density >= 0.f && p->density <= 1.f)) return VS_ERR_INVALID_ARG;
   if (!(p->softmax_scale >= 0.f) || !std::isfinite(p->softmax_scale)) return VS_ERR_INVALID_ARG;
+  if (p->index_mode != 0 && p->index_mode != 1) return VS_ERR_INVALID_ARG;
   return VS_OK;
 }
 
@@ -168,6 +171,8 @@ vs_status vs_index_build(const vs_params* p, const void* Q, const void* K, const
   // leaves the stream and the workspace untouched
   const int nbs_check = p->L / (kBlock * p->stripes);
   if (select_smem_bytes(nbs_check) + 26 * 1024 > 227 * 1024) return VS_ERR_UNSUPPORTED;
+  if (p->index_mode == 1 && group_union_smem_bytes(p->L, kBlock * p->stripes) > 227 * 1024 - 2048)
+    return VS_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
   if (cudaMemsetAsync(w + lay.status, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
@@ -203,6 +208,7 @@ vs_status vs_index_build(const vs_params* p, const void* Q, const void* K, const
   a.status = reinterpret_cast<DevStatus*>(w + lay.status);
   if (launch_index_scores(a, s) != cudaSuccess) return VS_ERR_CUDA;
   if (launch_select(a, s) != cudaSuccess) return VS_ERR_CUDA;
+  if (p->index_mode == 1 && launch_group_union(*p, *out, s) != cudaSuccess) return VS_ERR_CUDA;
   return VS_OK;
 }
 

@@ -72,6 +72,10 @@ typedef struct vs_params {
   double rope_theta;     /* RoPE base (vs_rope only)                                 */
   float yarn_factor;     /* YaRN scale s (1 = plain RoPE)       (vs_rope only)       */
   int32_t yarn_orig_len; /* YaRN original context length        (vs_rope only)       */
+  int32_t index_mode;    /* 0: one index per query head (the method);                */
+                         /* 1: shared by each GQA group: every head of a key/value   */
+                         /*    group uses the union of the group's per-head sets     */
+                         /*    (vs_index_build; the attention calls read the arrays) */
 } vs_params;
 
 /*
@@ -114,6 +118,10 @@ VS_API vs_status vs_rope(const vs_params* p, int32_t H, const void* x, void* y, 
  * each direction's mass; band 0 is always kept.  With density > 0 the kept
  * set is instead the largest-mass candidates (verticals and bands ranked
  * together) whose active entries reach `density` of the causal entries.
+ * With index_mode = 1 each head's lists and active count are then replaced
+ * by those of the union over its GQA group (kernel-aware granularity
+ * trade-off of the same section: fewer distinct index lines per key, more
+ * entries); v_score / s_score stay per head.
  * Fills every non-NULL field of *out.
  */
 VS_API vs_status vs_index_build(const vs_params* p, const void* Q, const void* K, const vs_index* out, void* ws,

@@ -49,6 +49,7 @@ __all__ = [
     "sparsity_ratio", "explicit_mask", "attention_forward", "attention_backward",
     "attention_forward_rows", "attention_backward_dq_rows", "total_causal_entries",
     "attention_backward_bf16_products", "striped_ring_forward", "striped_ring_backward",
+    "group_shared_index",
 ]
 
 
@@ -244,10 +245,11 @@ def select_budget(v: np.ndarray, S: np.ndarray, L: int, bs: int, density: float)
 
 
 def build_index(Q, K, last_q: int, top_p: float, scale: float | None = None,
-                stripes: int = 1, block: int = 64, density: float = 0.0):
+                stripes: int = 1, block: int = 64, density: float = 0.0, index_mode: int = 0):
     """Per query head (V_h, S_h): ascending kept verticals (token ids) and
     kept slash bands (band 0 always included).  ``density > 0`` selects by
-    budget fill instead of top-p.  Returns (index list, v, S)."""
+    budget fill instead of top-p; ``index_mode = 1`` then gives every head
+    its GQA group's union (``group_shared_index``).  Returns (index list, v, S)."""
     L = Q.shape[0]
     bs = block * stripes
     v, S = index_scores(Q, K, last_q, scale, stripes, block)
@@ -259,7 +261,23 @@ def build_index(Q, K, last_q: int, top_p: float, scale: float | None = None,
             Vh = select_top_p(v[h], top_p)
             Sh = np.union1d(select_top_p(S[h], top_p), [0]).astype(np.int64)
         index.append((Vh, Sh))
+    if index_mode == 1:
+        index = group_shared_index(index, Q.shape[1] // K.shape[1])
     return index, v, S
+
+
+def group_shared_index(index, G: int):
+    """GQA-group-shared index ([MT] 三/核心创新/2, the kernel-aware granularity
+    trade-off): every query head of a key/value group (heads g G .. g G + G - 1)
+    gets the union of the group's kept verticals and the union of its kept
+    bands (band 0 stays kept).  Returns a new per-head list."""
+    out = []
+    for g in range(len(index) // G):
+        heads = index[g * G:(g + 1) * G]
+        Vu = np.unique(np.concatenate([np.asarray(V, np.int64) for V, _ in heads]))
+        Su = np.unique(np.concatenate([np.asarray(S, np.int64) for _, S in heads] + [np.array([0])]))
+        out.extend([(Vu, Su)] * G)
+    return out
 
 
 # ----------------------------------------------------------------------------

@@ -132,3 +132,52 @@ def test_index_full_size_gqa_128k():
         assert ok, bad[:5]
         if all(np.array_equal(a, b) for a, b in zip(kept_or, listsb[h])):
             assert act[h] == oracle.active_entries(w.L, kept_or[0], kept_or[1], 64)
+
+
+@pytest.mark.parametrize("wid,L,Hq,Hkv,d,W,dens", [(3, 2048, 8, 2, 128, 1, 0.0), (3, 4096, 16, 2, 128, 1, 0.05),
+                                                  (1, 4096, 1, 1, 64, 1, 0.0), (4, 4096, 4, 1, 128, 4, 0.0),
+                                                  (3, 2048, 6, 2, 64, 1, 0.2)])
+def test_index_group_shared(wid, L, Hq, Hkv, d, W, dens):
+    """index_mode = 1: each head's lists are exactly the union of its group's
+    per-head lists of the same call in per-head mode (same masses, same
+    decisions), the active counts are the union's, and the union equals the
+    oracle's fp64 group union except for per-head threshold ties."""
+    import dynamic_sparse_attention_index_gb300 as vs
+    w = synth.make_workload(wid, L=L, Hq=Hq, Hkv=Hkv, d=d)
+    G = Hq // Hkv
+    p0, ix0 = _run(w, density=dens, stripes=W)
+    import torch
+    dev = torch.device("cuda:0")
+    p1 = vs.make_params(w.L, w.Hq, w.Hkv, w.d, last_q=w.last_q, top_p=w.top_p, stripes=W, density=dens,
+                        index_mode=vs.VS_INDEX_GROUP_SHARED)
+    Q, K = to_dev(w.q, dev), to_dev(w.k, dev)
+    ix1 = vs.IndexBuffers.allocate(p1, dev)
+    vs.vs_index_build(p1, Q, K, ix1, vs.workspace(p1, vs.VS_OP_INDEX, dev))
+    torch.cuda.synchronize()
+    per, grp = gpu_index_lists(ix0, Hq), gpu_index_lists(ix1, Hq)
+    assert torch.equal(ix0.v_score, ix1.v_score) and torch.equal(ix0.s_score, ix1.s_score)
+    union = oracle.group_shared_index(per, G)
+    act = ix1.active_entries.cpu().numpy()
+    bs = 64 * W
+    for h in range(Hq):
+        np.testing.assert_array_equal(grp[h][0], union[h][0])
+        np.testing.assert_array_equal(grp[h][1], union[h][1])
+        assert act[h] == oracle.active_entries(L, union[h][0], union[h][1], bs)
+    # end to end: the fp64 oracle's union, differences only at per-head ties
+    v_or, S_or = oracle.index_scores(f64(w.q), f64(w.k), w.last_q, stripes=W)
+    idx_or, _, _ = oracle.build_index(f64(w.q), f64(w.k), w.last_q, w.top_p, stripes=W,
+                                      density=float(np.float32(dens)) if dens else 0.0)
+    shared_or = oracle.group_shared_index(idx_or, G)
+    for g in range(Hkv):
+        dv = set(shared_or[g * G][0].tolist()) ^ set(grp[g * G][0].tolist())
+        ds = set(shared_or[g * G][1].tolist()) ^ set(grp[g * G][1].tolist())
+        for h in range(g * G, (g + 1) * G):
+            if dens:
+                ok, bad = budget_sets_agree(v_or[h], S_or[h], idx_or[h], per[h])
+            else:
+                ok = topp_sets_agree(v_or[h], idx_or[h][0], per[h][0], w.top_p)[0] and \
+                     topp_sets_agree(S_or[h], idx_or[h][1], per[h][1], w.top_p, forced=(0,))[0]
+            assert ok
+        tie_v = set().union(*[set(idx_or[h][0].tolist()) ^ set(per[h][0].tolist()) for h in range(g * G, (g + 1) * G)])
+        tie_s = set().union(*[set(idx_or[h][1].tolist()) ^ set(per[h][1].tolist()) for h in range(g * G, (g + 1) * G)])
+        assert dv <= tie_v and ds <= tie_s

@@ -61,6 +61,7 @@ def _call_index(vs, p, q=FAKE, k=FAKE, ws=FAKE, ws_bytes=1 << 40, ix=None):
     (dict(L=4000), "VS_ERR_INVALID_ARG"),
     (dict(stripes=3), "VS_ERR_INVALID_ARG"),
     (dict(density=-0.1), "VS_ERR_INVALID_ARG"),
+    (dict(index_mode=2), "VS_ERR_INVALID_ARG"),
 ])
 def test_index_rejects_bad_params(vs, kw, code):
     args = dict(L=4096, Hq=4, Hkv=2, d=64, last_q=64, top_p=0.9)

@@ -216,3 +216,46 @@ def test_build_index_recall_at_least_p():
             assert v[h, Vh].sum() >= p * v[h].sum() * (1 - 1e-14)
             assert S[h, Sh].sum() >= p * S[h].sum() * (1 - 1e-14)
             assert np.all(np.diff(Vh) > 0) and np.all(np.diff(Sh) > 0) and Sh[0] == 0
+
+
+def test_group_shared_index_is_the_union_of_masks():
+    """Brute force: each head's mask under the group-shared index is the OR of
+    the explicit masks of its group's per-head indices, the exact active
+    count equals the mask's, and every head's vertical recall is at least
+    that of its own selection."""
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(4)
+    L, G, Hkv, bs = 256, 4, 2, 64
+    nb = L // bs
+    per_head = [(np.sort(rng.choice(L, rng.integers(0, 9), replace=False)),
+                 np.union1d(rng.choice(nb, rng.integers(0, 3), replace=False), [0])) for _ in range(G * Hkv)]
+    shared = oracle.group_shared_index(per_head, G)
+    for h in range(G * Hkv):
+        g = h // G
+        want = np.zeros((L, L), bool)
+        for hh in range(g * G, (g + 1) * G):
+            want |= oracle.explicit_mask(L, *per_head[hh], bs)
+        got = oracle.explicit_mask(L, *shared[h], bs)
+        assert (got == want).all()
+        assert oracle.active_entries(L, *shared[h], bs) == int(want.sum())
+        assert set(per_head[h][0].tolist()) <= set(shared[h][0].tolist())
+        assert set(per_head[h][1].tolist()) <= set(shared[h][1].tolist())
+
+
+def test_build_index_group_mode():
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(8)
+    L, Hq, Hkv, d = 512, 4, 2, 16
+    Q, K = rng.standard_normal((L, Hq, d)), rng.standard_normal((L, Hkv, d))
+    K[[10, 300]] *= 5
+    per, v, S = oracle.build_index(Q, K, 32, 0.9)
+    grp, v2, S2 = oracle.build_index(Q, K, 32, 0.9, index_mode=1)
+    assert np.array_equal(v, v2) and np.array_equal(S, S2)
+    for h in range(Hq):
+        ref = oracle.group_shared_index(per, Hq // Hkv)[h]
+        assert np.array_equal(grp[h][0], ref[0]) and np.array_equal(grp[h][1], ref[1])
+        # recall of every head's own mass stays >= top_p under the union
+        assert v[h][grp[h][0]].sum() >= 0.9 * v[h].sum() - 1e-12
+        assert S[h][grp[h][1]].sum() >= 0.9 * S[h].sum() - 1e-12
