@@ -195,8 +195,11 @@ def run_gpu(args):
     W = w.stripes
     bwd = w.backward
     rope_kw = dict(rope_theta=w.rope_theta, yarn_factor=w.yarn_factor, yarn_orig_len=w.yarn_orig_len)
-    p = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=DENSITY, stripes=W, **rope_kw)
-    p_nat = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=0.0, stripes=W, **rope_kw)
+    imode = 1 if args.index_mode == "group" else 0
+    p = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=DENSITY, stripes=W, index_mode=imode,
+                       **rope_kw)
+    p_nat = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=0.0, stripes=W, index_mode=imode,
+                           **rope_kw)
 
     def pinned(bits):
         t = torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16)
@@ -386,7 +389,8 @@ def run_gpu(args):
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": args.workload, "L": L, "Hq": Hq, "Hkv": Hkv, "d": d, "batch": 1,
                    "pass": "fwd+bwd" if bwd else "fwd", "last_q": LAST_Q,
-                   "index": f"budget fill to density {DENSITY}",
+                   "index": f"budget fill to density {DENSITY}"
+                            + (", shared by each GQA group (union of its heads' sets)" if imode else ""),
                    "sparsity": round(1 - A / (Hq * T), 5),
                    "natural_top_p_sparsity": round(1 - A_nat / (Hq * T), 5), "top_p": TOP_P,
                    "active_entries": A, "l2": "inputs larger than L2 (no flush)" if L * Hq * d * 2 > 2 * (126 << 20)
@@ -594,6 +598,8 @@ def main():
     ap.add_argument("--workload", default="gqa16x2_L131072_d128_fwdbwd", choices=sorted(WORKLOADS))
     ap.add_argument("--cpu-rows", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--index-mode", default="head", choices=["head", "group"],
+                    help="one index per query head (the method) or one per GQA group (union)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
