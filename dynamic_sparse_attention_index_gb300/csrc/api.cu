@@ -1,6 +1,7 @@
 // extern "C" entry points of the VS sparse attention library: argument
 // validation (host, before any launch), workspace layout, and launches.
 #include <cmath>
+#include <cstdlib>
 #include <cstring>
 
 #include "common.cuh"
@@ -25,6 +26,16 @@ cudaError_t launch_ring_fwd(const vs_params& p, const vs_index& ix, const void* 
 cudaError_t launch_ring_bwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
                             const void* O, const float* lse, const void* dO, void* dQ, void* dK, void* dV, void* ws,
                             void* const* ev, int n_ev, cudaStream_t st);
+
+WaitCtl wait_ctl() {
+  WaitCtl c{kWaitLimitNs, 0};
+  if (const char* e = std::getenv("VS_TEST_WAIT_LIMIT_NS")) {
+    const unsigned long long v = std::strtoull(e, nullptr, 10);
+    if (v > 0 && v <= kWaitLimitNs) c.limit_ns = v;
+  }
+  if (const char* e = std::getenv("VS_TEST_STALL_PRODUCERS")) c.stall_producers = std::atoi(e) == 1 ? 1 : 0;
+  return c;
+}
 
 namespace {
 

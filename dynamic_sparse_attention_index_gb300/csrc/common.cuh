@@ -42,6 +42,20 @@ struct DevStatus {
   unsigned long long wait_cycles[kWaitSites];
 };
 
+// Bounded-wait test hooks of the attention kernels, read from the
+// environment at every launch (both unset in normal use):
+//   VS_TEST_STALL_PRODUCERS=1  the producer warps issue no copy and arrive on
+//                              no barrier, so every consumer's first wait runs
+//                              out (no copy or MMA is ever in flight);
+//   VS_TEST_WAIT_LIMIT_NS=n    the wait limit in nanoseconds (default 2 s).
+// The kernels then record VS_ERR_TIMEOUT, free their tensor memory and
+// return; vs_device_status reports it.
+struct WaitCtl {
+  uint64_t limit_ns;
+  int stall_producers;
+};
+WaitCtl wait_ctl();
+
 __device__ __forceinline__ void report_timeout(DevStatus* st, int where) {
   if (st) {
     atomicExch(&st->code, (int32_t)VS_ERR_TIMEOUT);
