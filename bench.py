@@ -57,9 +57,31 @@ KERNELS_PER_STEP_FWD = {"rope": 2, "index": 5, "fwd": 4}
 MUFU_EX2_PER_CLK_SM = 32
 N_SM = 152
 # DRAM bytes of one backward call (dram__bytes_read.sum + dram__bytes_write.sum
-# over its kernels, one-pass ncu capture of this workload); measured for the
-# current backward kernels and to be taken again whenever they change
-BWD_TRAFFIC_BYTES = {"gqa16x2_L131072_d128_fwdbwd": 32788239616}
+# over its kernels, from a one-pass ncu capture of the workload), read from the
+# profile summary together with the SHA-256 of the kernel sources it was taken
+# on: when the sources have changed since, the figure no longer applies and
+# the line reports null.
+TRAFFIC_SOURCES = ("attn_bwd.cu", "attn_fwd.cu", "attn_prep.cu", "attn_common.cuh", "ptx.cuh", "common.cuh")
+
+
+def kernel_sources_sha() -> str:
+    import hashlib
+    h = hashlib.sha256()
+    for f in TRAFFIC_SOURCES:
+        with open(os.path.join(ROOT, "dynamic_sparse_attention_index_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
+def bwd_traffic_bytes(workload: str):
+    path = os.path.join(ROOT, "profiles", f"dram_traffic_{workload}_backward.txt")
+    try:
+        kv = dict(ln.split(None, 1) for ln in open(path) if ln.strip() and not ln.startswith("#"))
+    except (OSError, ValueError):
+        return None
+    if kv.get("kernel_sources_sha256", "").strip() != kernel_sources_sha():
+        return None
+    return int(kv["bytes_per_backward_call"])
 
 
 def _peaks():
@@ -403,7 +425,7 @@ def run_gpu(args):
         "index_overhead": round(phase["index"] / max(ms, 1e-9), 4),
         "roofline": {"kernel": dom[0], "bound": "tensor",
                      "achieved": round(dom[1], 2), "peak": peak, "unit": "TFLOP/s",
-                     "frac": round(dom[1] / peak, 4), "traffic": BWD_TRAFFIC_BYTES.get(args.workload) if bwd else None,
+                     "frac": round(dom[1] / peak, 4), "traffic": bwd_traffic_bytes(args.workload) if bwd else None,
                      "peak_src": pk["src"] + " bf16 burst",
                      "frac_of_sustained": round(dom[1] / peak_s, 4)},
         "index_roofline": index_roofline(w, phase["index"], kept, pk, clocks.get("sm_max_mhz") or 2070.0),

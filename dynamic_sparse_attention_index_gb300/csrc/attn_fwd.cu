@@ -140,7 +140,7 @@ __device__ __noinline__ void rescale_acc_row(uint32_t taddr, float f) {
   tmem_st_wait();
 }
 
-template <int D, bool kDQ>
+template <int D, bool kDQ, bool kRing>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_qmajor_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
                        const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
@@ -618,9 +618,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool valid = it.valid[seg];
       float m_ref = kNegInf, l = 0.f;
       float lse2 = 0.f, Dr = 0.f;
+      // global token of this row (a ring step views one shard of the layout)
+      const int gtok = kRing ? g.tq(tok) : tok;
+      const size_t grow = (size_t)h * (kRing ? g.L_glob : g.L) + gtok;
       if (kDQ && valid) {
-        lse2 = P.lse[(size_t)h * g.L_glob + g.tq(tok)] * 1.4426950408889634f;
-        Dr = P.Dsum[(size_t)h * g.L_glob + g.tq(tok)];
+        lse2 = P.lse[grow] * 1.4426950408889634f;
+        Dr = P.Dsum[grow];
       }
       bool last = false;
       do {
@@ -674,7 +677,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[k] = pack_bf16(t0, t1);
               }
             } else {
-              const uint64_t act = active_bits(md, mw0, mw1, rr, g.strict_diag);
+              const uint64_t act = active_bits(md, mw0, mw1, rr, kRing ? g.strict_diag : 0);
 #pragma unroll
               for (int k = 0; k < 32; ++k) {
                 const int c = 2 * k;
@@ -694,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_ld_wait();
             if (md != kSrcFull) {
               // masked entries become -inf in place, so neither pass needs the mask
-              act = active_bits(md, mw0, mw1, rr, g.strict_diag);
+              act = active_bits(md, mw0, mw1, rr, kRing ? g.strict_diag : 0);
 #pragma unroll
               for (int c = 0; c < 64; ++c)
                 if (!((act >> c) & 1ull)) v[c] = __float_as_uint(kNegInf);
@@ -729,7 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             // a row with no active key so far (only with a strict diagonal)
             // keeps m_ref = -inf: its masked scores give exp2(-inf) = 0
-            const float mneg = m_ref == kNegInf ? 0.f : -m_ref;
+            const float mneg = (kRing && m_ref == kNegInf) ? 0.f : -m_ref;
             const uint64_t cc = f2pack(c2, c2), mm = f2pack(mneg, mneg);
             float ls[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -766,11 +769,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait_warp(pv_done, (t - 1) & 1, 25)) break;
           if (!wait_warp(pv_done, t & 1, 23)) break;
           tc_fence_after();
-          __nv_bfloat16* orow = P.out + ((size_t)g.tq(tok) * g.Hq + h) * D;
+          __nv_bfloat16* orow = P.out + ((size_t)gtok * g.Hq + h) * D;
           // ring steps carry an fp32 row of local token tok between steps
-          float* crow = P.carry_o ? P.carry_o + ((size_t)tok * g.Hq + h) * D + grp * (D / 2) : nullptr;
-          const bool final_out = P.acc_mode == kAccPlain || P.acc_mode == kAccLast;
-          const bool read_carry = P.acc_mode == kAccMid || P.acc_mode == kAccLast;
+          float* crow = kRing ? P.carry_o + ((size_t)tok * g.Hq + h) * D + grp * (D / 2) : nullptr;
+          const bool final_out = !kRing || P.acc_mode == kAccPlain || P.acc_mode == kAccLast;
+          const bool read_carry = kRing && (P.acc_mode == kAccMid || P.acc_mode == kAccLast);
           if (kDQ) {
             // this group's half of the dQ columns (a ring step adds the
             // carried sum of the earlier steps)
@@ -813,8 +816,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             // is 2^(its max - lse2n).  Group 1 posts (m, l), group 0 posts
             // its own factor and lse2n, and each side forms the rest.
             const float lc2 = (valid && read_carry) ? P.carry_lse2[(size_t)h * g.L + tok] : kNegInf;
-            float ca, cb, cc;
-            if (grp == 1) {
+            float ca, cb, cc = 0.f;
+            if constexpr (!kRing) {
+              // a plain call: group 1 posts (m, l); group 0 forms both groups'
+              // normalised factors and the row's LSE and posts the factors
+              if (grp == 1) {
+                xch[2 * r] = m_ref;
+                xch[2 * r + 1] = l;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ep_a);
+                if (!wait_warp(ep_b, it_local & 1, 5)) break;
+                ca = xch[2 * r];
+                cb = xch[2 * r + 1];
+              } else {
+                if (!wait_warp(ep_a, it_local & 1, 6)) break;
+                const float mb = xch[2 * r], lb = xch[2 * r + 1];
+                const float m = fmaxf(m_ref, mb);
+                const float fa = (l > 0.f) ? fast_exp2(m_ref - m) : 0.f;
+                const float fb = (lb > 0.f) ? fast_exp2(mb - m) : 0.f;
+                const float ltot = l * fa + lb * fb;
+                const float inv = ltot > 0.f ? 1.0f / ltot : 0.f;
+                ca = fa * inv;
+                cb = fb * inv;
+                if (valid) P.lse[grow] = ltot > 0.f ? (m + __log2f(ltot)) * 0.69314718055994531f : kNegInf;
+                xch[2 * r] = ca;
+                xch[2 * r + 1] = cb;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(ep_b);
+              }
+            } else if (grp == 1) {
               xch[2 * r] = m_ref;
               xch[2 * r + 1] = l;
               __syncwarp();
@@ -840,8 +870,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               cc = (lc2 != kNegInf) ? fast_exp2(lc2 - lse2n) : 0.f;
               if (valid) {
                 if (final_out)
-                  P.lse[(size_t)h * g.L_glob + g.tq(tok)] =
-                      lse2n != kNegInf ? lse2n * 0.69314718055994531f : kNegInf;
+                  P.lse[grow] = lse2n != kNegInf ? lse2n * 0.69314718055994531f : kNegInf;
                 else
                   P.carry_lse2[(size_t)h * g.L + tok] = lse2n;
               }
@@ -916,7 +945,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     atomicAdd(&P.status->wait_cycles[kWaitSites - 1], (unsigned long long)(clock64() - kernel_t0));
 }
 
-template <int D, bool kDQ>
+template <int D, bool kDQ, bool kRing>
 cudaError_t launch_qmajor(const AttnGeom& g, const PrepPtrs& pp, const void* Q, const void* dO, const void* K,
                           const void* V, const QmParams& P, cudaStream_t s) {
   using Ly = Layout<D, kDQ>;
@@ -930,7 +959,7 @@ cudaError_t launch_qmajor(const AttnGeom& g, const PrepPtrs& pp, const void* Q, 
     return cudaErrorInvalidValue;
   const size_t smem = Ly::kSmemEnd + 1024;
   cudaError_t e =
-      cudaFuncSetAttribute(attn_qmajor_kernel<D, kDQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      cudaFuncSetAttribute(attn_qmajor_kernel<D, kDQ, kRing>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int dev = 0, nsm = 152;
   cudaGetDevice(&dev);
@@ -938,7 +967,7 @@ cudaError_t launch_qmajor(const AttnGeom& g, const PrepPtrs& pp, const void* Q, 
   const int n = P.item_hi - P.item_lo;
   if (n <= 0) return cudaSuccess;
   const int grid = n < nsm ? n : nsm;
-  attn_qmajor_kernel<D, kDQ><<<grid, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, P);
+  attn_qmajor_kernel<D, kDQ, kRing><<<grid, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, P);
   return cudaGetLastError();
 }
 
@@ -953,6 +982,14 @@ size_t attn_fwd_ws_bytes(const vs_params& p) {
 }
 
 namespace {
+// a ring step (token-strided shard views, strict diagonal or carried state)
+// runs the kernel instance compiled with that support; a plain call runs
+// the one without it
+bool is_ring_step(const AttnGeom& g, const StepCtl& ctl) {
+  return ctl.acc_mode != kAccPlain || g.strict_diag || g.tq_mul != 1 || g.tk_mul != 1 || g.tq_add != 0 ||
+         g.tk_add != 0 || g.L_glob != g.L;
+}
+
 void set_step(QmParams& P, const AttnGeom& g, const StepCtl& ctl) {
   P.acc_mode = ctl.acc_mode;
   P.carry_o = ctl.carry_o;
@@ -977,8 +1014,12 @@ cudaError_t launch_fwd_core(const vs_params& p, const AttnGeom& g, const PrepPtr
   P.scale_log2 = P.scale * 1.4426950408889634f;
   P.status = st;
   set_step(P, g, ctl);
-  if (p.d == 128) return launch_qmajor<128, false>(g, pp, Q, nullptr, K, V, P, s);
-  return launch_qmajor<64, false>(g, pp, Q, nullptr, K, V, P, s);
+  if (is_ring_step(g, ctl)) {
+    if (p.d == 128) return launch_qmajor<128, false, true>(g, pp, Q, nullptr, K, V, P, s);
+    return launch_qmajor<64, false, true>(g, pp, Q, nullptr, K, V, P, s);
+  }
+  if (p.d == 128) return launch_qmajor<128, false, false>(g, pp, Q, nullptr, K, V, P, s);
+  return launch_qmajor<64, false, false>(g, pp, Q, nullptr, K, V, P, s);
 }
 
 // Row tiles covering query blocks [blk_lo, blk_hi) in the heaviest-first
@@ -1032,8 +1073,12 @@ cudaError_t launch_attn_dq(const vs_params& p, const AttnGeom& g, const PrepPtrs
   P.scale_log2 = P.scale * 1.4426950408889634f;
   P.status = st;
   set_step(P, g, ctl);
-  if (p.d == 128) return launch_qmajor<128, true>(g, pp, Q, dO, K, V, P, s);
-  return launch_qmajor<64, true>(g, pp, Q, dO, K, V, P, s);
+  if (is_ring_step(g, ctl)) {
+    if (p.d == 128) return launch_qmajor<128, true, true>(g, pp, Q, dO, K, V, P, s);
+    return launch_qmajor<64, true, true>(g, pp, Q, dO, K, V, P, s);
+  }
+  if (p.d == 128) return launch_qmajor<128, true, false>(g, pp, Q, dO, K, V, P, s);
+  return launch_qmajor<64, true, false>(g, pp, Q, dO, K, V, P, s);
 }
 
 }  // namespace vs
