@@ -614,49 +614,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int src = r >> 6, rr = r & 63;
     const uint32_t lane_off = (uint32_t)(((warp - 4) & 3) * 32) << 16;
     const uint32_t col0 = (uint32_t)(32 * grp);
-    // this row's view of one tile: its source's masks and row statistics
-    struct RowIn {
-      uint32_t mw0, mw1;
-      int diag, last;
-      float lse2, Dr;
-    };
-    // reads tile t's metadata, releases its ring slot and loads the row's
-    // LSE and D (global loads; the caller fetches one tile ahead, so their
-    // latency hides behind the tile before)
-    auto fetch = [&](int tt, RowIn* o) -> bool {
-      if (!wait_warp(&mq_full[tt % kMQ], (tt / kMQ) & 1, 20)) return false;
-      const SrcMeta& mref = mq[tt % kMQ];
-      const bool valid = src < mref.nsrc;
-      o->mw0 = valid ? mref.mask[src][0] : 0u;
-      o->mw1 = valid ? mref.mask[src][1] : 0u;
-      o->diag = valid ? mref.diag[src] : 0;
-      const int h = mref.h[valid ? src : 0];
-      const int tok = mref.I[valid ? src : 0] * kBlock + rr;
-      o->last = mref.last;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&mq_empty[tt % kMQ]);
-      o->lse2 = 0.f;
-      o->Dr = 0.f;
-      if (valid) {
-        o->lse2 = P.lse[(size_t)h * g.L_glob + g.tq(tok)] * P.log2e;
-        o->Dr = P.Dsum[(size_t)h * g.L_glob + g.tq(tok)];
-      }
-      return true;
-    };
     int t = 0, un = 0;
     for (int uid = blockIdx.x; uid < nunits && !*abort_flag; uid += gridDim.x, ++un) {
       bool last = false;
-      RowIn cur;
-      if (!fetch(t, &cur)) break;
       do {
-        // the next tile of this unit, fetched before this tile's wait
-        RowIn nxt = cur;
-        if (!cur.last && !fetch(t + 1, &nxt)) break;
-        const uint32_t mw0 = cur.mw0, mw1 = cur.mw1;
-        const int diag = cur.diag;
-        const float lse2 = cur.lse2, Dr = cur.Dr;
-        last = cur.last != 0;
-        cur = nxt;
+        if (!wait_warp(&mq_full[t % kMQ], (t / kMQ) & 1, 20)) break;
+        const SrcMeta& mref = mq[t % kMQ];
+        const bool valid = src < mref.nsrc;
+        const uint32_t mw0 = valid ? mref.mask[src][0] : 0u, mw1 = valid ? mref.mask[src][1] : 0u;
+        const int diag = valid ? mref.diag[src] : 0;
+        const int h = mref.h[valid ? src : 0];
+        const int tok = mref.I[valid ? src : 0] * kBlock + rr;
+        last = mref.last != 0;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&mq_empty[t % kMQ]);
+        float lse2 = 0.f, Dr = 0.f;
+        if (valid) {
+          lse2 = P.lse[(size_t)h * g.L_glob + g.tq(tok)] * P.log2e;
+          Dr = P.Dsum[(size_t)h * g.L_glob + g.tq(tok)];
+        }
         if (!wait_warp(&sdp_full[t & 1], (t >> 1) & 1, 21)) break;
         const long long ph0 = kWaitProfileKv ? clock64() : 0;
         if (t >= 2 && !wait_warp(&pds_free[t & 1], ((t >> 1) - 1) & 1, 22)) break;
