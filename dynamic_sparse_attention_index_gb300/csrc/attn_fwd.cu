@@ -73,7 +73,6 @@ struct QmParams {
   float* carry_o;
   float* carry_lse2;
   int item_lo, item_hi;  // row tiles [item_lo, item_hi) of the heaviest-first order
-  WaitCtl wc;            // wait limit; stall_producers: the bounded-wait test
 };
 
 template <int D, bool kDQ>
@@ -220,7 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = mbar_try_wait(bar, parity);
     if (!ok) {
       if (*abort_flag) return false;
-      ok = mbar_wait(bar, parity, P.wc.limit_ns);
+      ok = mbar_wait(bar, parity, wait_limit_ns(P.status));
     }
     if (kWaitProfileQm && (threadIdx.x & 31) == 0)
       atomicAdd(&wcyc[where & (kWaitSites - 1)], (unsigned long long)(clock64() - w0));
@@ -240,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // warp 0 (kprod): Q (+ dO) per row tile, per-tile metadata, K per source;
   // warp 3: V per source.  Both walk the same source enumeration.
   auto produce = [&](const bool kprod) {
-    if (P.wc.stall_producers) return;  // bounded-wait test: no copy, no arrival
+    if (test_stall(P.status)) return;  // bounded-wait test: no copy, no arrival
     const long long prod0 = (kWaitProfileQm || kSmProfileQm) ? clock64() : 0;
     const int W = g.bs / kBlock;
     int t = 0, it_local = 0;
@@ -996,7 +995,6 @@ void set_step(QmParams& P, const AttnGeom& g, const StepCtl& ctl) {
   P.carry_lse2 = ctl.carry_lse2;
   P.item_lo = ctl.item_lo < 0 ? 0 : ctl.item_lo;
   P.item_hi = (ctl.item_hi < 0 || ctl.item_hi > g.nitems) ? g.nitems : ctl.item_hi;
-  P.wc = wait_ctl();
 }
 }  // namespace
 
