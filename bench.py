@@ -480,6 +480,7 @@ def ring_balance(vs, p1, ix1, Q, K, V, W, dev, step, step_ev, bwd):
     rows [r L/W, (r+1) L/W); ZigZag: 2 W chunks, worker k holds chunks k and
     2 W - 1 - k)."""
     import torch
+    from dynamic_sparse_attention_index_gb300 import ring_model as rm
     mk = lambda: [torch.cuda.Event(enable_timing=True) for _ in range(W * W + 1)]
     step_ev["fwd"] = mk()
     if bwd:
@@ -495,6 +496,16 @@ def ring_balance(vs, p1, ix1, Q, K, V, W, dev, step, step_ev, bwd):
             "total_ms": round(float(t.sum()), 3), "worker_max_over_mean": round(float(worker.max() / worker.mean()), 4),
             "step_max_over_mean": round(float((t.max(0) / t.mean(0)).max()), 4),
             "step_ms_slowest_worker": [round(float(x), 4) for x in per_step]}
+        if k == "fwd" and W == rm.PAGES_A100_4x8.workers:
+            # the pages' hierarchical-ring model with these measured step times
+            # and the pages' link times (4 nodes x 8 GPUs, NVLink 0.13 ms,
+            # InfiniBand 0.98 ms per step)
+            r = rm.forward_latency_ms([float(x) for x in per_step], rm.PAGES_A100_4x8)
+            out["ring_model_fwd"] = {"topology": "4 nodes x 8, t_intra 0.13 ms, t_inter 0.98 ms",
+                                     "flat_ms": round(r["flat_ms"], 3),
+                                     "hierarchical_ms": round(r["hierarchical_ms"], 3),
+                                     "flat_comm_bound_steps": r["flat"]["comm_bound_steps"],
+                                     "hierarchical_exposed_outer_ms": round(r["hierarchical"]["exposed_outer_ms"], 3)}
     step_ev.clear()
     L = p1.L
     O = torch.empty_like(Q)
