@@ -27,19 +27,9 @@ cudaError_t launch_ring_bwd(const vs_params& p, const vs_index& ix, const void* 
                             const void* O, const float* lse, const void* dO, void* dQ, void* dK, void* dV, void* ws,
                             void* const* ev, int n_ev, cudaStream_t st);
 
-cudaError_t reset_status(void* status, cudaStream_t s) {
-  cudaError_t e = cudaMemsetAsync(status, 0, sizeof(DevStatus), s);
-  if (e != cudaSuccess) return e;
-  int32_t hdr[4] = {0, 0, 0, 0};
-  if (const char* v = std::getenv("VS_TEST_WAIT_LIMIT_US")) {
-    const long us = std::strtol(v, nullptr, 10);
-    if (us > 0 && us <= (long)(kWaitLimitNs / 1000)) hdr[2] = (int32_t)us;
-  }
-  if (const char* v = std::getenv("VS_TEST_STALL_PRODUCERS")) hdr[3] = std::atoi(v) == 1 ? 1 : 0;
-  if (hdr[2] == 0 && hdr[3] == 0) return cudaSuccess;
-  // a test run: the settings go with the reset (pageable source, copied
-  // before the call returns)
-  return cudaMemcpyAsync(status, hdr, sizeof(hdr), cudaMemcpyHostToDevice, s);
+bool test_stall_requested() {
+  const char* v = std::getenv("VS_TEST_STALL_PRODUCERS");
+  return v && std::atoi(v) == 1;
 }
 
 namespace {
@@ -191,7 +181,7 @@ vs_status vs_index_build(const vs_params* p, const void* Q, const void* K, const
     return VS_ERR_UNSUPPORTED;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   uint8_t* w = static_cast<uint8_t*>(ws);
-  if (reset_status(w + lay.status, s) != cudaSuccess) return VS_ERR_CUDA;
+  if (cudaMemsetAsync(w + lay.status, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
 
   IndexArgs a;
   std::memset(&a, 0, sizeof(a));
@@ -287,7 +277,7 @@ vs_status vs_sparse_attn_fwd(const vs_params* p, const vs_index* index, const vo
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(lse)) return VS_ERR_INVALID_ARG;
   if ((st = check_ws(ws, ws_bytes, attn_fwd_ws_bytes(*p))) != VS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (reset_status(ws, s) != cudaSuccess) return VS_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
   return launch_attn_fwd(*p, *index, Q, K, V, O, lse, ws, s, 0, p->L / kBlock) == cudaSuccess ? VS_OK : VS_ERR_CUDA;
 }
 
@@ -303,7 +293,7 @@ vs_status vs_sparse_attn_fwd_rows(const vs_params* p, const vs_index* index, con
   if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || !aligned16(lse)) return VS_ERR_INVALID_ARG;
   if ((st = check_ws(ws, ws_bytes, attn_fwd_ws_bytes(*p))) != VS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (reset_status(ws, s) != cudaSuccess) return VS_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
   return launch_attn_fwd(*p, *index, Q, K, V, O, lse, ws, s, row_lo / kBlock, row_hi / kBlock) == cudaSuccess
              ? VS_OK
              : VS_ERR_CUDA;
@@ -322,7 +312,7 @@ vs_status vs_sparse_attn_bwd(const vs_params* p, const vs_index* index, const vo
     if (!aligned16(q)) return VS_ERR_INVALID_ARG;
   if ((st = check_ws(ws, ws_bytes, attn_bwd_ws_bytes(*p))) != VS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (reset_status(ws, s) != cudaSuccess) return VS_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
   return launch_attn_bwd(*p, *index, Q, K, V, O, lse, dO, dQ, dK, dV, ws, s) == cudaSuccess ? VS_OK : VS_ERR_CUDA;
 }
 
@@ -337,7 +327,7 @@ vs_status vs_striped_ring_fwd(const vs_params* p, const vs_index* index, const v
   if (n_events < 0 || (n_events > 0 && !step_events)) return VS_ERR_INVALID_ARG;
   if ((st = check_ws(ws, ws_bytes, ring_ws_bytes(*p, false))) != VS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (reset_status(ws, s) != cudaSuccess) return VS_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
   return launch_ring_fwd(*p, *index, Q, K, V, O, lse, ws, step_events, n_events, s) == cudaSuccess ? VS_OK
                                                                                                   : VS_ERR_CUDA;
 }
@@ -357,7 +347,7 @@ vs_status vs_striped_ring_bwd(const vs_params* p, const vs_index* index, const v
   if (n_events < 0 || (n_events > 0 && !step_events)) return VS_ERR_INVALID_ARG;
   if ((st = check_ws(ws, ws_bytes, ring_ws_bytes(*p, true))) != VS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (reset_status(ws, s) != cudaSuccess) return VS_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
   return launch_ring_bwd(*p, *index, Q, K, V, O, lse, dO, dQ, dK, dV, ws, step_events, n_events, s) == cudaSuccess
              ? VS_OK
              : VS_ERR_CUDA;

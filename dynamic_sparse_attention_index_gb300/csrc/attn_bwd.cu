@@ -78,6 +78,7 @@ struct BwdParams {
   float log2e;
   DevStatus* status;
   int vertical;   // 1: vertical units, 0: slash units
+  int stall;      // bounded-wait test: the planner emits nothing
 };
 
 struct SrcMeta {
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = mbar_try_wait(bar, parity);
     if (!ok) {
       if (*abort_flag) return false;
-      ok = mbar_wait(bar, parity, wait_limit_ns(P.status));
+      ok = mbar_wait(bar, parity, kWaitLimitNs);
     }
     if (kWaitProfileKv && (threadIdx.x & 31) == 0)
       atomicAdd(&wcyc[where & (kWaitSites - 1)], (unsigned long long)(clock64() - w0));
@@ -273,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     nunits = g.Hkv * g.nb;
   }
 
-  if (warp == 0 && test_stall(P.status)) {
+  if (warp == 0 && P.stall) {
     // bounded-wait test: the planner emits nothing, so no unit starts and no
     // copy or MMA is ever issued; every other warp's first wait runs out
   } else if (warp == 0) {
@@ -522,7 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int ts = 0, ta = 0;
       int uid = blockIdx.x, un = 0;
       long long idle0 = clock64();
-      const long long idle_limit = (long long)(wait_limit_ns(P.status) * 21 / 10);
+      const long long idle_limit = (long long)(kWaitLimitNs * 21 / 10);
       while (true) {
         const bool more = uid < nunits;
         if (!more && ta == ts) break;
@@ -835,6 +836,7 @@ cudaError_t launch_dkdv_core(const vs_params& p, const AttnGeom& g, const PrepPt
   P.scale = default_scale(p);
   P.log2e = 1.4426950408889634f;
   P.status = st;
+  P.stall = test_stall_requested() ? 1 : 0;
   const size_t smem = kSmemBytes + 1024;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(attn_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=

@@ -73,6 +73,7 @@ struct QmParams {
   float* carry_o;
   float* carry_lse2;
   int item_lo, item_hi;  // row tiles [item_lo, item_hi) of the heaviest-first order
+  int prod_item_hi;      // the producers' bound: item_hi (item_lo in the bounded-wait test)
 };
 
 template <int D, bool kDQ>
@@ -219,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = mbar_try_wait(bar, parity);
     if (!ok) {
       if (*abort_flag) return false;
-      ok = mbar_wait(bar, parity, wait_limit_ns(P.status));
+      ok = mbar_wait(bar, parity, kWaitLimitNs);
     }
     if (kWaitProfileQm && (threadIdx.x & 31) == 0)
       atomicAdd(&wcyc[where & (kWaitSites - 1)], (unsigned long long)(clock64() - w0));
@@ -239,7 +240,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // warp 0 (kprod): Q (+ dO) per row tile, per-tile metadata, K per source;
   // warp 3: V per source.  Both walk the same source enumeration.
   auto produce = [&](const bool kprod) {
-    if (test_stall(P.status)) return;  // bounded-wait test: no copy, no arrival
     const long long prod0 = (kWaitProfileQm || kSmProfileQm) ? clock64() : 0;
     const int W = g.bs / kBlock;
     int t = 0, it_local = 0;
@@ -254,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&mVp);
       }
     }
-    for (int id = P.item_lo + (int)blockIdx.x; id < P.item_hi && !*abort_flag; id += gridDim.x, ++it_local) {
+    for (int id = P.item_lo + (int)blockIdx.x; id < P.prod_item_hi && !*abort_flag; id += gridDim.x, ++it_local) {
       const Item it = decode_item(g, id);
       const int qslot = it_local % Ly::kQSlots;
       const uint32_t* bm0 = P.inS + (size_t)it.h[0] * g.nw;
@@ -995,6 +995,7 @@ void set_step(QmParams& P, const AttnGeom& g, const StepCtl& ctl) {
   P.carry_lse2 = ctl.carry_lse2;
   P.item_lo = ctl.item_lo < 0 ? 0 : ctl.item_lo;
   P.item_hi = (ctl.item_hi < 0 || ctl.item_hi > g.nitems) ? g.nitems : ctl.item_hi;
+  P.prod_item_hi = test_stall_requested() ? P.item_lo : P.item_hi;
 }
 }  // namespace
 

@@ -35,38 +35,23 @@ constexpr int kWaitSites = 32;
 struct DevStatus {
   int32_t code;   // VS_OK or VS_ERR_TIMEOUT
   int32_t where;  // which wait gave up (kernel-specific tag)
-  // bounded-wait test settings, written by the host with the block's reset
-  // (zero in normal use): the wait limit in microseconds (0: the default),
-  // and 1 to make the producer warps issue and arrive on nothing
-  int32_t test_limit_us;
-  int32_t test_stall;
+  int32_t pad[2];
   // Cycles spent blocked at each wait site of the attention kernels, summed
   // over CTAs (lane 0 of each waiting warp), and the kernels' total cycles
   // per CTA in slot 31: a pipeline-balance diagnostic read by profiling tools.
   unsigned long long wait_cycles[kWaitSites];
 };
 
-// Bounded-wait test hooks of the attention kernels, read from the
-// environment when a call resets its status block (both unset in normal
-// use):
-//   VS_TEST_STALL_PRODUCERS=1  the producer warps issue no copy and arrive on
-//                              no barrier, so every consumer's first wait runs
-//                              out (no copy or MMA is ever in flight);
-//   VS_TEST_WAIT_LIMIT_US=n    the wait limit in microseconds (default 2 s).
+// Bounded-wait test hook of the attention kernels, read from the
+// environment by the launchers (unset in normal use):
+//   VS_TEST_STALL_PRODUCERS=1  the producer warps are given no work, so they
+//                              issue no copy and arrive on no barrier, and
+//                              every consumer's first wait runs out after the
+//                              2 s limit (no copy or MMA is ever in flight).
 // The kernels then record VS_ERR_TIMEOUT, free their tensor memory and
-// return; vs_device_status reports it.  The settings travel in the status
-// block and are read only where a wait has already failed once (and once per
-// producer warp), so the kernels' hot loops carry nothing for them.
-cudaError_t reset_status(void* status, cudaStream_t s);
-
-// the wait limit for a wait that has already failed once
-__device__ __forceinline__ uint64_t wait_limit_ns(const DevStatus* st) {
-  const int us = st ? *reinterpret_cast<const volatile int32_t*>(&st->test_limit_us) : 0;
-  return us > 0 ? (uint64_t)us * 1000ull : kWaitLimitNs;
-}
-__device__ __forceinline__ bool test_stall(const DevStatus* st) {
-  return st && *reinterpret_cast<const volatile int32_t*>(&st->test_stall) == 1;
-}
+// return; vs_device_status reports it.  The hook reaches the kernels as a
+// loop bound, so their code carries nothing for it.
+bool test_stall_requested();
 
 __device__ __forceinline__ void report_timeout(DevStatus* st, int where) {
   if (st) {
