@@ -227,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (kSmProfileQm && where < 20) wl[where] += clock64() - w0;
     if (ok) return true;
     *abort_flag = 1;
-    report_timeout(P.status, where);
+    report_timeout(P.status, (kDQ ? kTagDq : kTagForward) * 100 + where);
     return false;
   };
   // the same, agreed across the warp (callers then issue warp-collective

@@ -34,7 +34,7 @@ constexpr bool kSmProfileQm = VS_WAIT_PROFILE == 6;
 constexpr int kWaitSites = 32;
 struct DevStatus {
   int32_t code;   // VS_OK or VS_ERR_TIMEOUT
-  int32_t where;  // which wait gave up (kernel-specific tag)
+  int32_t where;  // the first wait that gave up: kernel tag * 100 + wait site
   int32_t pad[2];
   // Cycles spent blocked at each wait site of the attention kernels, summed
   // over CTAs (lane 0 of each waiting warp), and the kernels' total cycles
@@ -53,12 +53,14 @@ struct DevStatus {
 // loop bound, so their code carries nothing for it.
 bool test_stall_requested();
 
+// Records the first wait that gave up (later ones are its consequences):
+// `where` = kernel tag * 100 + the kernel's wait site.
 __device__ __forceinline__ void report_timeout(DevStatus* st, int where) {
-  if (st) {
-    atomicExch(&st->code, (int32_t)VS_ERR_TIMEOUT);
+  if (st && atomicCAS(&st->code, (int32_t)VS_OK, (int32_t)VS_ERR_TIMEOUT) == (int32_t)VS_OK)
     atomicExch(&st->where, where);
-  }
 }
+// kernel tags of the status word's wait site
+enum : int { kTagForward = 1, kTagDq = 2, kTagDkdvVertical = 3, kTagDkdvSlash = 4 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
