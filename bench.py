@@ -331,6 +331,10 @@ def run_gpu(args):
             acc[k] += ev[k][0].elapsed_time(ev[k][1])
     phase = {k: v / args.steps for k, v in acc.items()}
     clocks = sampler.stop()
+    # every bounded in-kernel wait of the timed steps completed (a wait that
+    # gave up would leave VS_ERR_TIMEOUT and its site in a status word)
+    dev_status = {k: vs.vs_status_string(vs.vs_device_status(ws))
+                  for k, ws in (("index", ws_i), ("fwd", ws_f), ("bwd", ws_b)) if ws is not None}
 
     # End to end through the C ABI with host buffers: every step copies its
     # inputs (Q, K, V and, with a backward, dO) in from pinned host memory and
@@ -434,6 +438,7 @@ def run_gpu(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
         "gpu_launches": sum(kps.values()) * args.steps,
         "clocks": clocks,
+        "device_status": dev_status,
     }
     if rank == 0 and not args.no_cpu_baseline:
         rows = max(16, int(args.cpu_rows * (131072 / L) * (16 / Hq)))
