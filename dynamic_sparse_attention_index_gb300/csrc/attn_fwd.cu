@@ -73,7 +73,7 @@ struct QmParams {
   float* carry_o;
   float* carry_lse2;
   int item_lo, item_hi;  // row tiles [item_lo, item_hi) of the heaviest-first order
-  int prod_item_hi;      // the producers' bound: item_hi (item_lo in the bounded-wait test)
+  int prod_item_hi;      // ring steps: the producers' bound, item_hi (item_lo in the bounded-wait test)
 };
 
 template <int D, bool kDQ>
@@ -254,7 +254,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&mVp);
       }
     }
-    for (int id = P.item_lo + (int)blockIdx.x; id < P.prod_item_hi && !*abort_flag; id += gridDim.x, ++it_local) {
+    for (int id = P.item_lo + (int)blockIdx.x; id < (kRing ? P.prod_item_hi : P.item_hi) && !*abort_flag;
+         id += gridDim.x, ++it_local) {
       const Item it = decode_item(g, id);
       const int qslot = it_local % Ly::kQSlots;
       const uint32_t* bm0 = P.inS + (size_t)it.h[0] * g.nw;

@@ -34,7 +34,7 @@ constexpr bool kSmProfileQm = VS_WAIT_PROFILE == 6;
 constexpr int kWaitSites = 32;
 struct DevStatus {
   int32_t code;   // VS_OK or VS_ERR_TIMEOUT
-  int32_t where;  // the first wait that gave up: kernel tag * 100 + wait site
+  int32_t where;  // a wait that gave up: kernel tag * 100 + wait site
   int32_t pad[2];
   // Cycles spent blocked at each wait site of the attention kernels, summed
   // over CTAs (lane 0 of each waiting warp), and the kernels' total cycles
@@ -42,22 +42,27 @@ struct DevStatus {
   unsigned long long wait_cycles[kWaitSites];
 };
 
-// Bounded-wait test hook of the attention kernels, read from the
-// environment by the launchers (unset in normal use):
-//   VS_TEST_STALL_PRODUCERS=1  the producer warps are given no work, so they
-//                              issue no copy and arrive on no barrier, and
-//                              every consumer's first wait runs out after the
-//                              2 s limit (no copy or MMA is ever in flight).
+// Bounded-wait test hook, read from the environment by the launchers (unset
+// in normal use):
+//   VS_TEST_STALL_PRODUCERS=1  the dK / dV kernel's planner, and the
+//                              producers of a ring step's query-major kernel,
+//                              are given no work: they issue no copy and
+//                              arrive on no barrier, and every consumer's
+//                              first wait runs out after the 2 s limit (no
+//                              copy or MMA is ever in flight).
 // The kernels then record VS_ERR_TIMEOUT, free their tensor memory and
 // return; vs_device_status reports it.  The hook reaches the kernels as a
-// loop bound, so their code carries nothing for it.
+// parameter read once per warp (a loop bound in the query-major kernel's
+// ring-step instance only, so a plain call's code carries nothing for it).
 bool test_stall_requested();
 
-// Records the first wait that gave up (later ones are its consequences):
-// `where` = kernel tag * 100 + the kernel's wait site.
+// Records a wait that gave up: `where` = kernel tag * 100 + the kernel's
+// wait site (when several give up, one of them).
 __device__ __forceinline__ void report_timeout(DevStatus* st, int where) {
-  if (st && atomicCAS(&st->code, (int32_t)VS_OK, (int32_t)VS_ERR_TIMEOUT) == (int32_t)VS_OK)
+  if (st) {
+    atomicExch(&st->code, (int32_t)VS_ERR_TIMEOUT);
     atomicExch(&st->where, where);
+  }
 }
 // kernel tags of the status word's wait site
 enum : int { kTagForward = 1, kTagDq = 2, kTagDkdvVertical = 3, kTagDkdvSlash = 4 };
