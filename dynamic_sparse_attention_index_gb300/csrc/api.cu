@@ -4,6 +4,8 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "common.cuh"
 
 namespace vs {
@@ -33,6 +35,15 @@ bool test_stall_requested() {
 }
 
 namespace {
+
+// An NVTX range around every entry point (a profiler shows each call of the
+// library by name; without a tool attached a push / pop costs nanoseconds).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -114,6 +125,7 @@ const char* vs_status_string(vs_status s) {
     case VS_ERR_WORKSPACE: return "VS_ERR_WORKSPACE: workspace missing, misaligned or too small";
     case VS_ERR_CUDA: return "VS_ERR_CUDA: CUDA launch or runtime error";
     case VS_ERR_TIMEOUT: return "VS_ERR_TIMEOUT: a bounded in-kernel wait gave up";
+    case VS_ERR_BOUNDS: return "VS_ERR_BOUNDS: a device bounds check failed (VS_DEBUG build)";
   }
   return "VS_ERR_UNKNOWN";
 }
@@ -133,6 +145,7 @@ size_t vs_workspace_bytes(const vs_params* p, int op) {
 }
 
 vs_status vs_rope(const vs_params* p, int32_t H, const void* x, void* y, int32_t transpose, void* stream) {
+  NvtxRange nvtx("vs_rope");
   if (!p || !x || !y || H <= 0 || p->L <= 0) return VS_ERR_INVALID_ARG;
   if (p->d != 64 && p->d != 128) return VS_ERR_UNSUPPORTED;
   if (!(p->rope_theta > 1.0) || !(p->yarn_factor >= 1.f)) return VS_ERR_INVALID_ARG;
@@ -167,6 +180,7 @@ vs_status vs_rope(const vs_params* p, int32_t H, const void* x, void* y, int32_t
 
 vs_status vs_index_build(const vs_params* p, const void* Q, const void* K, const vs_index* out, void* ws,
                          size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("vs_index_build");
   vs_status st = check_index_params(p);
   if (st != VS_OK) return st;
   if (!Q || !K || !aligned16(Q) || !aligned16(K)) return VS_ERR_INVALID_ARG;
@@ -258,6 +272,7 @@ extern "C" {
 
 vs_status vs_index_build_noalloc(const vs_params* p, const void* Q, const void* K, const vs_index* out,
                                  void* stream) {
+  NvtxRange nvtx("vs_index_build_noalloc");
   vs_status st = check_index_params(p);
   if (st != VS_OK) return st;
   if (!Q || !K || !aligned16(Q) || !aligned16(K)) return VS_ERR_INVALID_ARG;
@@ -270,6 +285,7 @@ vs_status vs_index_build_noalloc(const vs_params* p, const void* Q, const void* 
 
 vs_status vs_sparse_attn_fwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,
                              const void* V, void* O, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("vs_sparse_attn_fwd");
   vs_status st = check_params(p);
   if (st != VS_OK) return st;
   if ((st = check_index_ptrs(index)) != VS_OK) return st;
@@ -284,6 +300,7 @@ vs_status vs_sparse_attn_fwd(const vs_params* p, const vs_index* index, const vo
 vs_status vs_sparse_attn_fwd_rows(const vs_params* p, const vs_index* index, const void* Q, const void* K,
                                   const void* V, void* O, float* lse, void* ws, size_t ws_bytes, int32_t row_lo,
                                   int32_t row_hi, void* stream) {
+  NvtxRange nvtx("vs_sparse_attn_fwd_rows");
   vs_status st = check_params(p);
   if (st != VS_OK) return st;
   if (row_lo < 0 || row_hi > p->L || row_lo >= row_hi || row_lo % kBlock || row_hi % kBlock)
@@ -302,6 +319,7 @@ vs_status vs_sparse_attn_fwd_rows(const vs_params* p, const vs_index* index, con
 vs_status vs_sparse_attn_bwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,
                              const void* V, const void* O, const float* lse, const void* dO, void* dQ,
                              void* dK, void* dV, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("vs_sparse_attn_bwd");
   vs_status st = check_params(p);
   if (st != VS_OK) return st;
   if ((st = check_index_ptrs(index)) != VS_OK) return st;
@@ -319,6 +337,7 @@ vs_status vs_sparse_attn_bwd(const vs_params* p, const vs_index* index, const vo
 vs_status vs_striped_ring_fwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,
                               const void* V, void* O, float* lse, void* ws, size_t ws_bytes, void* const* step_events,
                               int32_t n_events, void* stream) {
+  NvtxRange nvtx("vs_striped_ring_fwd");
   vs_status st = check_params(p);
   if (st != VS_OK) return st;
   if ((st = check_index_ptrs(index)) != VS_OK) return st;
@@ -336,6 +355,7 @@ vs_status vs_striped_ring_bwd(const vs_params* p, const vs_index* index, const v
                               const void* V, const void* O, const float* lse, const void* dO, void* dQ, void* dK,
                               void* dV, void* ws, size_t ws_bytes, void* const* step_events, int32_t n_events,
                               void* stream) {
+  NvtxRange nvtx("vs_striped_ring_bwd");
   vs_status st = check_params(p);
   if (st != VS_OK) return st;
   if ((st = check_index_ptrs(index)) != VS_OK) return st;
@@ -354,6 +374,7 @@ vs_status vs_striped_ring_bwd(const vs_params* p, const vs_index* index, const v
 }
 
 vs_status vs_device_status(void* ws, void* stream) {
+  NvtxRange nvtx("vs_device_status");
   if (!ws) return VS_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaStreamSynchronize(s) != cudaSuccess) return VS_ERR_CUDA;
@@ -361,7 +382,7 @@ vs_status vs_device_status(void* ws, void* stream) {
   if (cudaMemcpy(&h, ws, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return VS_ERR_CUDA;
   if (h.code == VS_OK) return VS_OK;
   if (cudaMemset(ws, 0, sizeof(DevStatus)) != cudaSuccess) return VS_ERR_CUDA;
-  return h.code == VS_ERR_TIMEOUT ? VS_ERR_TIMEOUT : VS_ERR_CUDA;
+  return (h.code == VS_ERR_TIMEOUT || h.code == VS_ERR_BOUNDS) ? (vs_status)h.code : VS_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -629,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&mq_empty[t % kMQ]);
         float lse2 = 0.f, Dr = 0.f;
-        if (valid) {
+        if (valid && VS_BOUNDS(h < g.Hq && g.tq(tok) < g.L_glob, P.status, 2090)) {
           lse2 = P.lse[(size_t)h * g.L_glob + g.tq(tok)] * P.log2e;
           Dr = P.Dsum[(size_t)h * g.L_glob + g.tq(tok)];
         }
@@ -711,7 +711,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
               const int e = u.chunk * 64 + (int)col0 + jj;
-              if (e < u.cnt) {
+              if (e < u.cnt && VS_BOUNDS((size_t)u.split * u.stride + e < (size_t)g.L && u.vg < g.nvg, P.status, 2091)) {
                 const size_t o = ((size_t)u.vg * g.L + (size_t)u.split * u.stride + e) * D + dcol;
                 P.part_v[o] = __uint_as_float(av[jj]);
                 P.part_k[o] = __uint_as_float(ak[jj]);
@@ -732,6 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j < 0 || j >= 32) continue;  // the other group's key
                 float sk = 0.f, sv = 0.f;
                 for (int sp = 0; sp < R; ++sp) {
+                  if (!VS_BOUNDS((size_t)sp * stride + e < (size_t)g.L, P.status, 2092)) break;
                   const size_t o = ((size_t)vg * g.L + (size_t)sp * stride + e) * D + dcol;
                   sk += P.part_k[o];
                   sv += P.part_v[o];
@@ -748,6 +749,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               // a ring step: add into the fp32 sums of the keys' global rows
 #pragma unroll
               for (int jj = 0; jj < 32; ++jj) {
+                if (!VS_BOUNDS(g.tk(kb * kBlock + (int)col0 + jj) < g.L_glob && kvh < g.Hkv, P.status, 2093)) break;
                 const size_t o = ((size_t)g.tk(kb * kBlock + (int)col0 + jj) * g.Hkv + kvh) * D + dcol;
                 P.dv32[o] += __uint_as_float(av[jj]);
                 P.dk32[o] += __uint_as_float(ak[jj]) * P.scale;
@@ -755,6 +757,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
 #pragma unroll
               for (int jj = 0; jj < 32; ++jj) {
+                if (!VS_BOUNDS(kb * kBlock + (int)col0 + jj < g.L && kvh < g.Hkv, P.status, 2094)) break;
                 const size_t o = ((size_t)(kb * kBlock + (int)col0 + jj) * g.Hkv + kvh) * D + dcol;
                 P.dV[o] = __float2bfloat16_rn(__uint_as_float(av[jj]));
                 P.dK[o] = __float2bfloat16_rn(__uint_as_float(ak[jj]) * P.scale);

@@ -615,7 +615,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       const Item it = decode_item(g, id);
       const int tok = it.I[seg] * kBlock + rr;
       const int h = it.h[seg];
-      const bool valid = it.valid[seg];
+      // (a VS_DEBUG build checks the row's global position before any access)
+      const bool valid =
+          it.valid[seg] && VS_BOUNDS(h < g.Hq && (kRing ? g.tq(tok) : tok) < (kRing ? g.L_glob : g.L) &&
+                                         (!kRing || tok < g.L),
+                                     P.status, (kDQ ? kTagDq : kTagForward) * 100 + 90);
       float m_ref = kNegInf, l = 0.f;
       float lse2 = 0.f, Dr = 0.f;
       // global token of this row (a ring step views one shard of the layout)

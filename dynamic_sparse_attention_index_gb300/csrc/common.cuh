@@ -56,6 +56,24 @@ struct DevStatus {
 // ring-step instance only, so a plain call's code carries nothing for it).
 bool test_stall_requested();
 
+// Device bounds checks of a VS_DEBUG build (-DVS_DEBUG=1): VS_BOUNDS(cond,
+// st, site) is true when cond holds; otherwise it records VS_ERR_BOUNDS and
+// the site in the status block (once; no trap) and is false, so the caller
+// skips the access.  In a normal build it is the constant true and the check
+// compiles away.
+#ifndef VS_DEBUG
+#define VS_DEBUG 0
+#endif
+__device__ __forceinline__ bool report_bounds(DevStatus* st, int site) {
+  if (st && atomicCAS(&st->code, (int32_t)VS_OK, (int32_t)VS_ERR_BOUNDS) == (int32_t)VS_OK) atomicExch(&st->where, site);
+  return false;
+}
+#if VS_DEBUG
+#define VS_BOUNDS(cond, st, site) ((cond) ? true : ::vs::report_bounds((st), (site)))
+#else
+#define VS_BOUNDS(cond, st, site) true
+#endif
+
 // Records a wait that gave up: `where` = kernel tag * 100 + the kernel's
 // wait site (when several give up, one of them).
 __device__ __forceinline__ void report_timeout(DevStatus* st, int where) {

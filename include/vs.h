@@ -53,7 +53,8 @@ typedef enum vs_status {
   VS_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d not in {64,128}) */
   VS_ERR_WORKSPACE = 3,   /* ws too small or misaligned */
   VS_ERR_CUDA = 4,        /* a CUDA launch or runtime call failed */
-  VS_ERR_TIMEOUT = 5      /* a bounded in-kernel wait gave up (device-side) */
+  VS_ERR_TIMEOUT = 5,     /* a bounded in-kernel wait gave up (device-side) */
+  VS_ERR_BOUNDS = 6       /* a device bounds check failed (VS_DEBUG builds only; device-side) */
 } vs_status;
 
 /* Problem description.  Batch 1. */
@@ -234,7 +235,9 @@ VS_API vs_status vs_striped_ring_bwd(const vs_params* p, const vs_index* index, 
 
 /*
  * Reads the device-side status word of workspace `ws` (synchronises
- * `stream` first) and clears it.  Returns VS_OK or VS_ERR_TIMEOUT.
+ * `stream` first) and clears it.  Returns VS_OK, VS_ERR_TIMEOUT, or (in a
+ * library built with VS_DEBUG, whose kernels check their global-memory
+ * indices, record the first failure and skip the access) VS_ERR_BOUNDS.
  */
 VS_API vs_status vs_device_status(void* ws, void* stream);
 

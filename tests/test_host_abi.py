@@ -28,7 +28,7 @@ def test_exports_match_header(vs):
 
 
 def test_status_strings(vs):
-    for c in range(6):
+    for c in range(7):
         assert vs.vs_status_string(c).startswith("VS_")
 
 
