@@ -251,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       atomicAdd(&wcyc[where & (kWaitSites - 1)], (unsigned long long)(clock64() - w0));
     if (ok) return true;
     *abort_flag = 1;
-    report_timeout(P.status, (P.vertical ? kTagDkdvVertical : kTagDkdvSlash) * 100 + where);
+    report_timeout_first(P.status, (P.vertical ? kTagDkdvVertical : kTagDkdvSlash) * 100 + where);
     return false;
   };
   // the same, agreed across the warp (callers then issue warp-collective
@@ -597,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         } else if (clock64() - idle0 > idle_limit) {
           *abort_flag = 1;
-          report_timeout(P.status, (P.vertical ? kTagDkdvVertical : kTagDkdvSlash) * 100 + 12);
+          report_timeout_first(P.status, (P.vertical ? kTagDkdvVertical : kTagDkdvSlash) * 100 + 12);
           break;
         }
       }

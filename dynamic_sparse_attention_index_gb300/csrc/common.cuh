@@ -82,6 +82,12 @@ __device__ __forceinline__ void report_timeout(DevStatus* st, int where) {
     atomicExch(&st->where, where);
   }
 }
+// The same, keeping the first wait that gave up (the dK / dV kernel; the
+// query-major kernel's register budget has no room for the compare).
+__device__ __forceinline__ void report_timeout_first(DevStatus* st, int where) {
+  if (st && atomicCAS(&st->code, (int32_t)VS_OK, (int32_t)VS_ERR_TIMEOUT) == (int32_t)VS_OK)
+    atomicExch(&st->where, where);
+}
 // kernel tags of the status word's wait site
 enum : int { kTagForward = 1, kTagDq = 2, kTagDkdvVertical = 3, kTagDkdvSlash = 4 };
 
