@@ -92,8 +92,8 @@ struct Layout {
   static constexpr int kMeta = kVRing + kRV * kKBytes;
   static constexpr int kBars = (kMeta + kRK * (int)sizeof(TileMeta) + 15) / 16 * 16;  // mbarriers: 8-byte aligned
   // q_full[2], q_empty[2], k_full[RK], k_empty[RK], v_full[RV], v_empty[RV], meta_free[RK],
-  // s_full[2], p_ready[2], pv_done, o_free, dp_full, dp_free, ep_a, ep_b
-  static constexpr int kNumBars = 2 + 2 + 3 * kRK + 2 * kRV + 2 + 2 + 1 + 1 + 1 + 1 + 2;
+  // s_full[2], p_ready[2], pv_done, o_free, dp_full, dp_free, ep_a, ep_b, acc_done
+  static constexpr int kNumBars = 2 + 2 + 3 * kRK + 2 * kRV + 2 + 2 + 1 + 1 + 1 + 1 + 2 + 1;
   static constexpr int kMisc = kBars + kNumBars * 8;      // tmem slot, abort flag
   static constexpr int kWaitCyc = kMisc + 64;             // per-site wait cycle counters
   static constexpr int kXchg = kWaitCyc + kWaitSites * 8; // epilogue row exchange: 128 x 2 floats
@@ -165,6 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* dp_free = dp_full + 1;    // dQ: dP read by every row
   uint64_t* ep_a = dp_free + 1;       // forward epilogue: group 1 posted (m, l) of its rows
   uint64_t* ep_b = ep_a + 1;          // forward epilogue: group 0 posted the combination factors
+  uint64_t* acc_done = ep_b + 1;      // a row tile's last accumulate landed (once per row tile)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Ly::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Ly::kMisc + 4);
   unsigned long long* wcyc = reinterpret_cast<unsigned long long*>(sm + Ly::kWaitCyc);
@@ -192,6 +193,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&v_empty[i], 1);
     }
     mbar_init(pv_done, 1);
+    mbar_init(acc_done, 1);
     mbar_init(o_free, 8);
     mbar_init(ep_a, 4);
     mbar_init(ep_b, 4);
@@ -590,6 +592,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // now rather than behind the next row tile's first S
           if (last) {
             if (!issue_acc()) break;
+            umma_commit(acc_done);
             have_prev = false;
           }
           ++t;
@@ -767,11 +770,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kSmProfileQm) pk_ += clock64() - q1;
         if (last) {
           const long long pe0 = clock64();
-          // pv_done completes once per tile and a parity wait only tells the
-          // open phase from the one before it: the PV of tile t-1 may still be
-          // running here, so wait for its phase first, then for tile t's.
-          if (!wait_warp(pv_done, (t - 1) & 1, 25)) break;
-          if (!wait_warp(pv_done, t & 1, 23)) break;
+          // The accumulator is complete once the row tile's last accumulate
+          // landed.  pv_done cannot say so: at this point the accumulates of
+          // tiles t-1 and t may each have landed or not, three phases apart,
+          // and a parity wait tells only two apart.  acc_done completes once
+          // per row tile, and the next one needs this warp's next p_ready.
+          if (!wait_warp(acc_done, it_local & 1, 23)) break;
           tc_fence_after();
           __nv_bfloat16* orow = P.out + ((size_t)gtok * g.Hq + h) * D;
           // ring steps carry an fp32 row of local token tok between steps
