@@ -304,6 +304,9 @@ def run_gpu(args):
         balance = shard_balance(L, W, index_lists(ix_w, Hq), index_lists(ix1, Hq))
         balance["timed"] = ring_balance(vs, p1, ix1, Q, K, V, W, dev, step, step_ev, bwd)
         del ix1, ix_w
+    # the backward's status word says how dQ was formed (1: from the dS
+    # tiles stored in its workspace, 0: S and dP recomputed)
+    dq_stored = bool(ws_b is not None and not ring and int(ws_b[8:12].view(torch.int32).item()) == 1)
     assert vs.vs_device_status(ws_f) == vs.VS_OK
     assert ws_b is None or vs.vs_device_status(ws_b) == vs.VS_OK
 
@@ -401,6 +404,8 @@ def run_gpu(args):
     dom = ("vs_sparse_attn_bwd (dK/dV + dQ)", bwd_tf) if bwd else ("vs_sparse_attn_fwd", fwd_tf)
     peak, peak_s = pk["bf16_tflops"], pk["bf16_tflops_sustained"]
     kps = dict(KERNELS_PER_STEP if bwd else KERNELS_PER_STEP_FWD)
+    if dq_stored:
+        kps["bwd"] += 2  # the dS plan and the dQ kernel that reads the tiles (the recomputing one returns at once)
     if ring:
         # ring setup (shard lists, band bitmaps, a vertical union and packed
         # rows per shard) and W x W steps: one forward kernel per step; D, the
@@ -439,6 +444,7 @@ def run_gpu(args):
         "gpu_launches": sum(kps.values()) * args.steps,
         "clocks": clocks,
         "device_status": dev_status,
+        **({"dq_path": "stored dS tiles" if dq_stored else "recomputed S and dP"} if bwd and not ring else {}),
     }
     if rank == 0 and not args.no_cpu_baseline:
         rows = max(16, int(args.cpu_rows * (131072 / L) * (16 / Hq)))

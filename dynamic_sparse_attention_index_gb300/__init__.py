@@ -20,7 +20,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libvs.so")
 
 VS_OK, VS_ERR_INVALID_ARG, VS_ERR_UNSUPPORTED, VS_ERR_WORKSPACE, VS_ERR_CUDA, VS_ERR_TIMEOUT, VS_ERR_BOUNDS = range(7)
-VS_OP_INDEX, VS_OP_FWD, VS_OP_BWD, VS_OP_ROPE, VS_OP_RING_FWD, VS_OP_RING_BWD = range(6)
+VS_OP_INDEX, VS_OP_FWD, VS_OP_BWD, VS_OP_ROPE, VS_OP_RING_FWD, VS_OP_RING_BWD, VS_OP_BWD_MIN = range(7)
 
 #: every symbol the header declares
 EXPORTED = ("vs_workspace_bytes", "vs_status_string", "vs_rope", "vs_index_build",

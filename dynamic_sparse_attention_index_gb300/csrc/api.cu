@@ -20,8 +20,9 @@ cudaError_t launch_attn_fwd(const vs_params& p, const vs_index& ix, const void* 
 size_t attn_fwd_ws_bytes(const vs_params& p);
 cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
                             const void* O, const float* lse, const void* dO, void* dQ, void* dK, void* dV, void* ws,
-                            cudaStream_t s);
+                            size_t ws_bytes, cudaStream_t s);
 size_t attn_bwd_ws_bytes(const vs_params& p);
+size_t attn_bwd_ws_bytes_stored(const vs_params& p);
 size_t ring_ws_bytes(const vs_params& p, bool bwd);
 cudaError_t launch_ring_fwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
                             void* O, float* lse, void* ws, void* const* ev, int n_ev, cudaStream_t st);
@@ -138,7 +139,8 @@ size_t vs_workspace_bytes(const vs_params* p, int op) {
   }
   if (check_params(p) != VS_OK) return 0;
   if (op == VS_OP_FWD) return attn_fwd_ws_bytes(*p);
-  if (op == VS_OP_BWD) return p->d == 128 ? attn_bwd_ws_bytes(*p) : 0;
+  if (op == VS_OP_BWD) return p->d == 128 ? attn_bwd_ws_bytes_stored(*p) : 0;
+  if (op == VS_OP_BWD_MIN) return p->d == 128 ? attn_bwd_ws_bytes(*p) : 0;
   if (op == VS_OP_RING_FWD) return ring_ws_bytes(*p, false);
   if (op == VS_OP_RING_BWD) return p->d == 128 ? ring_ws_bytes(*p, true) : 0;
   return 0;
@@ -331,7 +333,8 @@ vs_status vs_sparse_attn_bwd(const vs_params* p, const vs_index* index, const vo
   if ((st = check_ws(ws, ws_bytes, attn_bwd_ws_bytes(*p))) != VS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
-  return launch_attn_bwd(*p, *index, Q, K, V, O, lse, dO, dQ, dK, dV, ws, s) == cudaSuccess ? VS_OK : VS_ERR_CUDA;
+  return launch_attn_bwd(*p, *index, Q, K, V, O, lse, dO, dQ, dK, dV, ws, ws_bytes, s) == cudaSuccess ? VS_OK
+                                                                                         : VS_ERR_CUDA;
 }
 
 vs_status vs_striped_ring_fwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,

@@ -79,6 +79,11 @@ struct BwdParams {
   DevStatus* status;
   int vertical;   // 1: vertical units, 0: slash units
   int stall;      // bounded-wait test: the planner emits nothing
+  // stored dS blocks (null ok: none): see DsPlan
+  const int32_t* ds_ok;
+  const int32_t* ds_rank;
+  const int32_t* ds_base_s;
+  const int32_t* ds_base_v;
 };
 
 struct SrcMeta {
@@ -89,8 +94,8 @@ struct SrcMeta {
   int32_t nsrc;
   int32_t first, last;
   int32_t kv0, kv1;     // the unit's stationary keys: packed row (vertical) or (kv head, first key) (slash)
+  int32_t blk[2];       // stored dS block of each source (-1: none)
   int32_t pad;
-  long long t_issue;    // unused (kept for the 16-byte multiple size)
 };
 
 // shared memory plan (bytes, 1024-aligned)
@@ -175,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     attn_dkdv_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mdO,
                      const __grid_constant__ CUtensorMap mK, const __grid_constant__ CUtensorMap mV,
                      const __grid_constant__ CUtensorMap mKp, const __grid_constant__ CUtensorMap mVp,
-                     const BwdParams P) {
+                     const __grid_constant__ CUtensorMap mDS, const BwdParams P) {
   constexpr int D = 128;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
@@ -190,7 +195,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // buffer (both indexed by tile parity), so one commit serves both waiters
   static_assert(kStages == 2, "P / dS buffers and Q / dO stages share the release barrier");
   uint64_t* pds_free = st_empty;
-  uint64_t* acc_done = pds_ready + 4;  // (the two slots after pds_ready are unused)
+  // stored dS: the loader's store of a tile's dS has read its buffer
+  uint64_t* ds_free = pds_ready + 2;
+  uint64_t* acc_done = pds_ready + 4;
   uint64_t* acc_free = acc_done + 1;
   uint64_t* mq_full = acc_free + 1;
   uint64_t* mq_empty = mq_full + kMQ;
@@ -207,6 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const AttnGeom& g = P.g;
   const int W = g.bs / kBlock;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool ds_on = P.ds_ok != nullptr && *P.ds_ok != 0;
 
   if (threadIdx.x == 0) {
     mbar_init(kvs_full, 1);
@@ -218,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sdp_full[i], 1);
       mbar_init(&pds_ready[i], 8);  // one arrival per P / dS warp
+      mbar_init(&ds_free[i], 1);
     }
     mbar_init(acc_done, 1);
     mbar_init(acc_free, 8);
@@ -322,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- the unit's sources, two per tile (warp-uniform registers)
       int nsrc = 0;
       bool first = true;
-      int th[2] = {0, 0}, tI[2] = {0, 0}, tdg[2] = {0, 0};
+      int th[2] = {0, 0}, tI[2] = {0, 0}, tdg[2] = {0, 0}, tb[2] = {-1, -1};
       uint32_t tm[2][2] = {{0u, 0u}, {0u, 0u}};
       auto emit = [&](bool last) {
         const int q = t % kMQ;
@@ -346,6 +355,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           m.last = last ? 1 : 0;
           m.kv0 = kv0;
           m.kv1 = kv1;
+          m.blk[0] = tb[0];
+          m.blk[1] = nsrc > 1 ? tb[1] : -1;
           mbar_arrive(&mq_full[q]);
         }
         __syncwarp();
@@ -353,30 +364,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         nsrc = 0;
         first = false;
       };
-      auto put = [&](int h, int I, uint32_t m0, uint32_t m1, int diag) {
+      auto put = [&](int h, int I, uint32_t m0, uint32_t m1, int diag, int blk) {
         if (nsrc == 0) {
           th[0] = h;
           tI[0] = I;
           tm[0][0] = m0;
           tm[0][1] = m1;
           tdg[0] = diag;
+          tb[0] = blk;
         } else {
           th[1] = h;
           tI[1] = I;
           tm[1][0] = m0;
           tm[1][1] = m1;
           tdg[1] = diag;
+          tb[1] = blk;
         }
         ++nsrc;
       };
       // to flag the last tile, a source is placed only once the next one is
       // known (one-source lookahead)
       bool have_look = false;
-      int look_h = 0, look_I = 0, look_diag = 0;
+      int look_h = 0, look_I = 0, look_diag = 0, look_blk = -1;
       uint32_t look_m0 = 0, look_m1 = 0;
-      auto push = [&](int h, int I, uint32_t m0, uint32_t m1, int diag) {
+      auto push = [&](int h, int I, uint32_t m0, uint32_t m1, int diag, int blk) {
         if (have_look) {
-          put(look_h, look_I, look_m0, look_m1, look_diag);
+          put(look_h, look_I, look_m0, look_m1, look_diag, look_blk);
           if (nsrc == 2) emit(false);
         }
         have_look = true;
@@ -385,6 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         look_m0 = m0;
         look_m1 = m1;
         look_diag = diag;
+        look_blk = blk;
       };
 
       if (!P.vertical) {
@@ -398,18 +412,34 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (j0 == 0) has0 = __shfl_sync(0xffffffffu, B, 0) == 0;
             // query blocks of band B for key block kb: I/W = kb/W + B, I >= kb
             const int lo = max(kb, (kb / W + B) * W), hi = min(g.nb - 1, (kb / W + B) * W + W - 1);
-            uint32_t live = __ballot_sync(0xffffffffu, B >= 0 && lo <= hi);
+            const bool on = B >= 0 && lo <= hi;
+            // stored dS: the band's rank and the first block of query block lo
+            int rk = 0, b_lo = 0;
+            if (ds_on && on) {
+              rk = B >= 1 ? P.ds_rank[(size_t)h * g.nbs + B] : 0;
+              b_lo = P.ds_base_s[(size_t)h * g.nb + lo];
+            }
+            uint32_t live = __ballot_sync(0xffffffffu, on);
             while (live) {
               const int k = __ffs(live) - 1;
               live &= live - 1;
               const int lk = __shfl_sync(0xffffffffu, lo, k), hk = __shfl_sync(0xffffffffu, hi, k);
-              for (int I = lk; I <= hk; ++I) push(h, I, 0xffffffffu, 0xffffffffu, I == kb ? 1 : 0);
+              const int Bk = __shfl_sync(0xffffffffu, B, k), rkk = __shfl_sync(0xffffffffu, rk, k);
+              const int bk = __shfl_sync(0xffffffffu, b_lo, k);
+              for (int I = lk; I <= hk; ++I) {
+                int blk = -1;
+                if (ds_on)
+                  blk = ds_slash_block(g, I == lk ? bk : P.ds_base_s[(size_t)h * g.nb + I], rkk, Bk, I, kb);
+                push(h, I, 0xffffffffu, 0xffffffffu, I == kb ? 1 : 0, blk);
+              }
             }
           }
           // band 0 is always active even if the index omits it
           if (!has0) {
             const int lo = kb, hi = min(g.nb - 1, (kb / W) * W + W - 1);
-            for (int I = lo; I <= hi; ++I) push(h, I, 0xffffffffu, 0xffffffffu, I == kb ? 1 : 0);
+            for (int I = lo; I <= hi; ++I)
+              push(h, I, 0xffffffffu, 0xffffffffu, I == kb ? 1 : 0,
+                   ds_on ? ds_slash_block(g, P.ds_base_s[(size_t)h * g.nb + I], 0, 0, I, kb) : -1);
           }
         }
       } else {
@@ -428,7 +458,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hi = 0; hi < nheads; ++hi) {
           const uint32_t* bm = hi ? bm1 : bm0;
           const int h = hs[hi];
+          int bv = 0;  // stored dS: first vertical-chunk block of query blocks I0 + lane
           for (int I = Ib; I < Ie && !*abort_flag; ++I) {
+            const int I0 = Ib + ((I - Ib) & ~31);
+            if (ds_on && I == I0) bv = (I0 + lane < Ie) ? P.ds_base_v[(size_t)h * g.nb + I0 + lane] : 0;
             auto act = [&](int m, uint32_t e) -> bool {
               if (m < 0 || !((e >> (kVFlagShift + hi)) & 1u)) return false;
               const int kbm = m / kBlock;
@@ -438,17 +471,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             };
             const uint32_t w0 = __ballot_sync(0xffffffffu, act(m0, e0));
             const uint32_t w1 = __ballot_sync(0xffffffffu, act(m1, e1));
-            if (w0 | w1) push(h, I, w0, w1, 0);
+            const int bvI = __shfl_sync(0xffffffffu, bv, I - I0);
+            if (w0 | w1) push(h, I, w0, w1, 0, ds_on ? bvI + chunk : -1);
           }
         }
       }
       // flush: the lookahead source is the unit's last
       if (have_look) {
-        put(look_h, look_I, look_m0, look_m1, look_diag);
+        put(look_h, look_I, look_m0, look_m1, look_diag, look_blk);
         emit(true);
       } else {
         // a vertical unit whose split has no active rows: one empty tile
-        put(P.vertical ? hs[0] : kvh * g.G, P.vertical ? g.nb - 1 : kb, 0u, 0u, 0);
+        put(P.vertical ? hs[0] : kvh * g.G, P.vertical ? g.nb - 1 : kb, 0u, 0u, 0, -1);
         emit(true);
       }
     }
@@ -457,6 +491,29 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ loader
     if (lane == 0) {
       int t = 0, un = 0;
+      // Stored dS: a tile's dS blocks are stored once its accumulate has
+      // released its stage (the wait below for tile t + 2), so the stores of
+      // tile t are issued after tile t + 2's loads; the last two tiles are
+      // stored at the end.  ds_free[t & 1] tells the P / dS warps that the
+      // buffer has been read.
+      int pblk[2][2] = {{-1, -1}, {-1, -1}};
+      // the stored blocks are read back once, after this kernel: evict
+      // them first so that the Q / dO tiles keep their place in L2
+      const uint64_t pol_stream = ds_on ? l2_policy_evict_first() : 0;
+      auto store_ds = [&](int u) {
+        const uint8_t* dbuf = sm + kPdS + (u & 1) * kPdSBytes + 128 * 128;
+        bool any = false;
+        for (int j = 0; j < 2; ++j)
+          if (pblk[u & 1][j] >= 0) {
+            tma_store_2d_hint(&mDS, dbuf + j * 8192, 0, pblk[u & 1][j] * 64, pol_stream);
+            any = true;
+          }
+        if (any) {
+          bulk_commit_group();
+          bulk_wait_read_all();
+        }
+        mbar_arrive(&ds_free[u & 1]);
+      };
       for (int uid = blockIdx.x; uid < nunits && !*abort_flag; uid += gridDim.x, ++un) {
         bool last = false;
         do {
@@ -464,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!wait(&mq_full[q], (t / kMQ) & 1, 3)) break;
           const int nsrc = mq[q].nsrc, kv0 = mq[q].kv0, kv1 = mq[q].kv1;
           const int h0 = mq[q].h[0], h1 = mq[q].h[1], I0 = mq[q].I[0], I1 = mq[q].I[1];
+          const int blk0 = mq[q].blk[0], blk1 = mq[q].blk[1];
           const bool first = mq[q].first != 0;
           last = mq[q].last != 0;
           mbar_arrive(&mq_empty[q]);
@@ -497,9 +555,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if (kWaitProfileKv) atomicAdd(&wcyc[27], (unsigned long long)(clock64() - e0));
+          if (ds_on) {
+            if (t >= 2) store_ds(t - 2);
+            pblk[t & 1][0] = blk0;
+            pblk[t & 1][1] = blk1;
+          }
           ++t;
         } while (!last && !*abort_flag);
       }
+      if (ds_on && !*abort_flag) {
+        // the last two tiles: wait for their accumulates, then store
+        for (int u = t >= 2 ? t - 2 : 0; u < t; ++u) {
+          if (!wait(&st_empty[u % kStages], (u / kStages) & 1, 5)) break;
+          store_ds(u);
+        }
+      }
+      if (ds_on) bulk_wait_all();
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -636,6 +707,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_warp(&sdp_full[t & 1], (t >> 1) & 1, 21)) break;
         const long long ph0 = kWaitProfileKv ? clock64() : 0;
         if (t >= 2 && !wait_warp(&pds_free[t & 1], ((t >> 1) - 1) & 1, 22)) break;
+        if (ds_on && t >= 2 && !wait_warp(&ds_free[t & 1], ((t >> 1) - 1) & 1, 24)) break;
         tc_fence_after();
         const float c = P.scale * P.log2e;
         uint8_t* pbuf = sm + kPdS + (t & 1) * kPdSBytes;
@@ -781,11 +853,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 struct BwdWs {
-  size_t status, prep_end, dsum, part_k, part_v, total;
+  size_t status, prep_end, dsum, part_k, part_v;
+  size_t ds_ok, ds_rank, ds_base_s, ds_base_v, ds;  // stored dS (cap > 0): after everything else
+  size_t total;
   PrepWs prep;
 };
 
-BwdWs bwd_layout(const AttnGeom& g) {
+// cap: stored dS blocks per head (0: none)
+BwdWs bwd_layout(const AttnGeom& g, long long cap) {
   WsLayout w;
   BwdWs o;
   o.status = w.take(sizeof(DevStatus));
@@ -793,13 +868,49 @@ BwdWs bwd_layout(const AttnGeom& g) {
   o.dsum = w.take((size_t)g.Hq * g.L * 4);
   o.part_k = w.take((size_t)g.nvg * g.L * g.d * 4);
   o.part_v = w.take((size_t)g.nvg * g.L * g.d * 4);
+  o.ds_ok = o.ds_rank = o.ds_base_s = o.ds_base_v = o.ds = w.off;
+  if (cap > 0) {
+    o.ds_ok = w.take(4);
+    o.ds_rank = w.take((size_t)g.Hq * g.nbs * 4);
+    o.ds_base_s = w.take((size_t)g.Hq * g.nb * 4);
+    o.ds_base_v = w.take((size_t)g.Hq * g.nb * 4);
+    o.ds = w.take((size_t)g.Hq * (size_t)cap * kDsBlockBytes);
+  }
   o.total = w.off;
   return o;
 }
 
+// Largest stored-dS capacity (blocks per head) that a workspace of ws_bytes
+// holds; block rows stay below 2^31 (tensor-map coordinates).
+long long ds_cap_for(const AttnGeom& g, size_t ws_bytes) {
+  const BwdWs one = bwd_layout(g, 1);
+  if (ws_bytes < one.total) return 0;
+  long long cap = (long long)((ws_bytes - one.ds) / ((size_t)g.Hq * kDsBlockBytes));
+  const long long row_cap = (2147483647LL / 64) / g.Hq;
+  return cap < row_cap ? cap : row_cap;
+}
+
+// Suggested capacity: a budget-fill index keeps about density x the causal
+// 64 x 64 blocks of each head; 1.5x that (2x for the group-shared index,
+// whose unions grow), plus four vertical chunks per query block.  None for
+// top-p selection (no density known in advance) or beyond 32 GiB.
+long long ds_cap_suggested(const vs_params& p, const AttnGeom& g) {
+  if (!(p.density > 0.f)) return 0;
+  const double f = p.index_mode == 1 ? 2.0 : 1.5;
+  const double head = f * p.density * (double)g.nb * (g.nb + 1) / 2.0 + 4.0 * g.nb;
+  if (head * g.Hq * kDsBlockBytes > 32.0 * 1024 * 1024 * 1024) return 0;
+  const long long cap = (long long)head + 1;
+  const long long row_cap = (2147483647LL / 64) / g.Hq;
+  return cap < row_cap ? cap : 0;
+}
+
 }  // namespace
 
-size_t attn_bwd_ws_bytes(const vs_params& p) { return bwd_layout(make_geom(p)).total; }
+size_t attn_bwd_ws_bytes(const vs_params& p) { return bwd_layout(make_geom(p), 0).total; }
+size_t attn_bwd_ws_bytes_stored(const vs_params& p) {
+  const AttnGeom g = make_geom(p);
+  return bwd_layout(g, ds_cap_suggested(p, g)).total;
+}
 
 cudaError_t launch_bwd_dsum(const void* O, const void* dO, float* Dsum, int L, int Hq, int d, cudaStream_t s) {
   const long long rows = (long long)L * Hq;
@@ -812,8 +923,8 @@ cudaError_t launch_bwd_dsum(const void* O, const void* dO, float* Dsum, int L, i
 cudaError_t launch_dkdv_core(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const vs_index& ix,
                              const void* Q, const void* K, const void* V, const void* dO, const float* lse,
                              const float* Dsum, void* dK, void* dV, float* part_k, float* part_v, float* dk32,
-                             float* dv32, DevStatus* st, cudaStream_t s) {
-  CUtensorMap mQ, mdO, mK, mV, mKp, mVp;
+                             float* dv32, DevStatus* st, const DsPlan* ds, cudaStream_t s) {
+  CUtensorMap mQ, mdO, mK, mV, mKp, mVp, mDS;
   if (!make_map_heads(&mQ, Q, g.L, g.Hq, 128, g.tq_mul, g.tq_add) ||
       !make_map_heads(&mdO, dO, g.L, g.Hq, 128, g.tq_mul, g.tq_add) ||
       !make_map_heads(&mK, K, g.L, g.Hkv, 128, g.tk_mul, g.tk_add) ||
@@ -821,6 +932,9 @@ cudaError_t launch_dkdv_core(const vs_params& p, const AttnGeom& g, const PrepPt
       !make_map_rows(&mKp, pp.Kp, (long long)g.nvg * g.L, 128) ||
       !make_map_rows(&mVp, pp.Vp, (long long)g.nvg * g.L, 128))
     return cudaErrorInvalidValue;
+  // the stored dS blocks (a map the kernel never touches when there are none)
+  if (ds ? !make_map_rows(&mDS, ds->ds, (long long)g.Hq * ds->cap * 64, 64) : false) return cudaErrorInvalidValue;
+  if (!ds) mDS = mKp;
   BwdParams P;
   P.g = g;
   P.inS = pp.inS;
@@ -840,6 +954,10 @@ cudaError_t launch_dkdv_core(const vs_params& p, const AttnGeom& g, const PrepPt
   P.log2e = 1.4426950408889634f;
   P.status = st;
   P.stall = test_stall_requested() ? 1 : 0;
+  P.ds_ok = ds ? ds->ok : nullptr;
+  P.ds_rank = ds ? ds->band_rank : nullptr;
+  P.ds_base_s = ds ? ds->base_s : nullptr;
+  P.ds_base_v = ds ? ds->base_v : nullptr;
   const size_t smem = kSmemBytes + 1024;
   cudaError_t e;
   if ((e = cudaFuncSetAttribute(attn_dkdv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
@@ -850,11 +968,11 @@ cudaError_t launch_dkdv_core(const vs_params& p, const AttnGeom& g, const PrepPt
   cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
   // vertical units first: their partials feed the slash units' epilogue
   P.vertical = 1;
-  attn_dkdv_kernel<<<nsm, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, P);
+  attn_dkdv_kernel<<<nsm, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, mDS, P);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   P.vertical = 0;
   const int nunits = g.Hkv * g.nb;
-  attn_dkdv_kernel<<<nunits < nsm ? nunits : nsm, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, P);
+  attn_dkdv_kernel<<<nunits < nsm ? nunits : nsm, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, mDS, P);
   return cudaGetLastError();
 }
 
@@ -862,10 +980,11 @@ size_t bwd_partials_bytes(const AttnGeom& g) { return (size_t)g.nvg * g.L * g.d 
 
 cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* Q, const void* K, const void* V,
                             const void* O, const float* lse, const void* dO, void* dQ, void* dK, void* dV, void* ws,
-                            cudaStream_t s) {
+                            size_t ws_bytes, cudaStream_t s) {
   if (p.d != 128) return cudaErrorNotSupported;
   const AttnGeom g = make_geom(p);
-  const BwdWs lay = bwd_layout(g);
+  const long long cap = ds_cap_for(g, ws_bytes);
+  const BwdWs lay = bwd_layout(g, cap);
   uint8_t* w = static_cast<uint8_t*>(ws);
   PrepPtrs pp;
   pp.inS = reinterpret_cast<uint32_t*>(w + lay.prep.inS);
@@ -879,10 +998,33 @@ cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* 
   cudaError_t e = launch_attn_prep(g, ix, K, V, pp, s);
   if (e != cudaSuccess) return e;
   if ((e = launch_bwd_dsum(O, dO, dsum, g.L, g.Hq, g.d, s)) != cudaSuccess) return e;
+  if (cap == 0) {
+    if ((e = launch_dkdv_core(p, g, pp, ix, Q, K, V, dO, lse, dsum, dK, dV,
+                              reinterpret_cast<float*>(w + lay.part_k), reinterpret_cast<float*>(w + lay.part_v),
+                              nullptr, nullptr, st, nullptr, s)) != cudaSuccess)
+      return e;
+    return launch_attn_dq(p, g, pp, Q, K, V, dO, lse, dsum, dQ, st, StepCtl(), s);
+  }
+  // Stored dS: the plan numbers every active block and checks that each
+  // head's fit its share of the workspace; the dK / dV kernels store them,
+  // the dQ kernel reads them back.  If a head's did not fit, the dK / dV
+  // kernels store nothing, the reading dQ kernel returns at once, and the
+  // recomputing one runs instead (each checks the plan's word).
+  DsPlan d;
+  d.ok = reinterpret_cast<int32_t*>(w + lay.ds_ok);
+  d.band_rank = reinterpret_cast<int32_t*>(w + lay.ds_rank);
+  d.base_s = reinterpret_cast<int32_t*>(w + lay.ds_base_s);
+  d.base_v = reinterpret_cast<int32_t*>(w + lay.ds_base_v);
+  d.ds = reinterpret_cast<__nv_bfloat16*>(w + lay.ds);
+  d.cap = (int)cap;
+  if ((e = launch_ds_plan(g, pp, d, s)) != cudaSuccess) return e;
   if ((e = launch_dkdv_core(p, g, pp, ix, Q, K, V, dO, lse, dsum, dK, dV, reinterpret_cast<float*>(w + lay.part_k),
-                            reinterpret_cast<float*>(w + lay.part_v), nullptr, nullptr, st, s)) != cudaSuccess)
+                            reinterpret_cast<float*>(w + lay.part_v), nullptr, nullptr, st, &d, s)) != cudaSuccess)
     return e;
-  return launch_attn_dq(p, g, pp, Q, K, V, dO, lse, dsum, dQ, st, StepCtl(), s);
+  if ((e = launch_dq_stored(p, g, pp, K, d, dQ, st, s)) != cudaSuccess) return e;
+  StepCtl ctl;
+  ctl.skip_if = d.ok;
+  return launch_attn_dq(p, g, pp, Q, K, V, dO, lse, dsum, dQ, st, ctl, s);
 }
 
 }  // namespace vs

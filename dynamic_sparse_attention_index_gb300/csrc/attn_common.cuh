@@ -171,6 +171,9 @@ struct StepCtl {
   float* carry_o = nullptr;     // [L][Hq][d] local rows
   float* carry_lse2 = nullptr;  // [Hq][L] (forward)
   int item_lo = 0, item_hi = -1;  // -1: every row tile
+  // the launch does nothing when this device word is non-zero (the stored
+  // dS tiles of the backward fit, so the dQ kernel that reads them runs)
+  const int32_t* skip_if = nullptr;
 };
 
 cudaError_t launch_fwd_core(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const void* Q, const void* K,
@@ -178,6 +181,39 @@ cudaError_t launch_fwd_core(const vs_params& p, const AttnGeom& g, const PrepPtr
 cudaError_t launch_attn_dq(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const void* Q, const void* K,
                            const void* V, const void* dO, const float* lse, const float* Dsum, void* dQ,
                            DevStatus* st, const StepCtl& ctl, cudaStream_t s);
+
+// Stored dS tiles of the backward.  When the caller's workspace has room,
+// the key-stationary dK / dV kernel writes every 64 x 64 dS block it forms
+// (dS = P (dP - D), bf16, 64 query rows x 64 keys, keys contiguous) and the
+// dQ kernel reads them back instead of recomputing S and dP.  The blocks of
+// (query head h, query block I) follow that row's key sources in order: the
+// slash key blocks active for h in descending key order (band 0, then each
+// kept band B >= 1 ascending), then the 64-entry chunks of the vertical
+// union list.  Head h owns blocks [h cap, (h + 1) cap).
+struct DsPlan {
+  int32_t* ok;         // device word: non-zero while every head's blocks fit in cap
+  int32_t* band_rank;  // [Hq][nbs]: kept bands of head h in [1, B]
+  int32_t* base_s;     // [Hq][nb]: first block of (h, I)
+  int32_t* base_v;     // [Hq][nb]: first vertical-chunk block of (h, I)
+  __nv_bfloat16* ds;   // [Hq cap][64][64] blocks
+  int cap;             // blocks per head
+};
+constexpr int kDsBlockBytes = 64 * 64 * 2;
+
+// Block of slash key block kb for query block I of a head, where kb lies in
+// band B (rank: the head's kept bands in [1, B]) and base is the first block
+// of (h, I): band 0 holds I, I-1, ..., (I / W) W, and every kept band B >= 1
+// the W blocks (I / W - B) W + W - 1 down to (I / W - B) W.
+__host__ __device__ inline int ds_slash_block(const AttnGeom& g, int base, int rank, int B, int I, int kb) {
+  const int W = g.bs / kBlock;
+  if (B == 0) return base + (I - kb);
+  const int Iw = I / W;
+  return base + (I - Iw * W + 1) + W * (rank - 1) + ((Iw - B) * W + W - 1 - kb);
+}
+
+cudaError_t launch_ds_plan(const AttnGeom& g, const PrepPtrs& pp, const DsPlan& d, cudaStream_t s);
+cudaError_t launch_dq_stored(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const void* K,
+                             const DsPlan& d, void* dQ, DevStatus* st, cudaStream_t s);
 
 // Tensor-map helpers (host): 3-D view (d, heads, tokens) of a [L][H][d] bf16
 // tensor with a (64, 1, 64) box, and a 2-D view (d, rows) with a (64, 64) box,

@@ -74,6 +74,7 @@ struct QmParams {
   float* carry_lse2;
   int item_lo, item_hi;  // row tiles [item_lo, item_hi) of the heaviest-first order
   int prod_item_hi;      // ring steps: the producers' bound, item_hi (item_lo in the bounded-wait test)
+  const int32_t* skip_if;  // non-zero device word: the launch does nothing
 };
 
 template <int D, bool kDQ>
@@ -147,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                        const __grid_constant__ CUtensorMap mKp, const __grid_constant__ CUtensorMap mVp,
                        const QmParams P) {
   using Ly = Layout<D, kDQ>;
+  if (P.skip_if != nullptr && *P.skip_if != 0) return;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + Ly::kBars);
@@ -1005,6 +1007,7 @@ void set_step(QmParams& P, const AttnGeom& g, const StepCtl& ctl) {
   P.item_lo = ctl.item_lo < 0 ? 0 : ctl.item_lo;
   P.item_hi = (ctl.item_hi < 0 || ctl.item_hi > g.nitems) ? g.nitems : ctl.item_hi;
   P.prod_item_hi = test_stall_requested() ? P.item_lo : P.item_hi;
+  P.skip_if = ctl.skip_if;
 }
 }  // namespace
 

@@ -22,6 +22,8 @@ constexpr int kMaxL = 1 << 20;                   // supported sequence length ce
 #define VS_WAIT_PROFILE 0
 #endif
 constexpr bool kWaitProfileKv = VS_WAIT_PROFILE == 1 || VS_WAIT_PROFILE == 2;
+// 7: the stored-dS dQ kernel's waits (producer, MMA issue, epilogue) and total cycles
+constexpr bool kWaitProfileDs = VS_WAIT_PROFILE == 7;
 // 4: only the dK/dV kernel's MMA-issue timers and total cycles (least intrusive)
 constexpr bool kMmaProfileKv = kWaitProfileKv || VS_WAIT_PROFILE == 4;
 constexpr bool kWaitProfileQm = VS_WAIT_PROFILE == 1 || VS_WAIT_PROFILE == 3;
@@ -35,7 +37,8 @@ constexpr int kWaitSites = 32;
 struct DevStatus {
   int32_t code;   // VS_OK or VS_ERR_TIMEOUT
   int32_t where;  // a wait that gave up: kernel tag * 100 + wait site
-  int32_t pad[2];
+  int32_t path;   // backward: 1 when dQ was formed from stored dS tiles
+  int32_t pad;
   // Cycles spent blocked at each wait site of the attention kernels, summed
   // over CTAs (lane 0 of each waiting warp), and the kernels' total cycles
   // per CTA in slot 31: a pipeline-balance diagnostic read by profiling tools.
@@ -89,7 +92,7 @@ __device__ __forceinline__ void report_timeout_first(DevStatus* st, int where) {
     atomicExch(&st->where, where);
 }
 // kernel tags of the status word's wait site
-enum : int { kTagForward = 1, kTagDq = 2, kTagDkdvVertical = 3, kTagDkdvSlash = 4 };
+enum : int { kTagForward = 1, kTagDq = 2, kTagDkdvVertical = 3, kTagDkdvSlash = 4, kTagDqStored = 5 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

@@ -29,7 +29,7 @@ cudaError_t launch_bwd_dsum(const void* O, const void* dO, float* Dsum, int L, i
 cudaError_t launch_dkdv_core(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const vs_index& ix,
                              const void* Q, const void* K, const void* V, const void* dO, const float* lse,
                              const float* Dsum, void* dK, void* dV, float* part_k, float* part_v, float* dk32,
-                             float* dv32, DevStatus* st, cudaStream_t s);
+                             float* dv32, DevStatus* st, const DsPlan* ds, cudaStream_t s);
 size_t bwd_partials_bytes(const AttnGeom& g);
 
 namespace {
@@ -255,7 +255,7 @@ cudaError_t launch_ring_bwd(const vs_params& p, const vs_index& ix, const void* 
       const PrepPtrs pp = shard_prep(c, s);
       if ((e = launch_dkdv_core(c.pl, g, pp, shard_index(c, ix, s), Q, K, V, dO, lse, dsum, dK, dV,
                                 reinterpret_cast<float*>(c.w + c.lay.part_k),
-                                reinterpret_cast<float*>(c.w + c.lay.part_v), dk32, dv32, status, st)) !=
+                                reinterpret_cast<float*>(c.w + c.lay.part_v), dk32, dv32, status, nullptr, st)) !=
           cudaSuccess)
         return e;
       ctl.acc_mode = step_mode(t, c.W);

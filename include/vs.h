@@ -26,7 +26,9 @@
  *     launch returns VS_ERR_CUDA.  Kernels that wait on an in-CTA barrier do
  *     so for a bounded time; on timeout they record VS_ERR_TIMEOUT in the
  *     workspace status word (first 16 bytes of `ws`) and return, which
- *     vs_device_status() reports after the stream is synchronised.
+ *     vs_device_status() reports after the stream is synchronised.  After
+ *     vs_sparse_attn_bwd, the status word's third int32 (bytes 8-11) is 1
+ *     when dQ was formed from stored dS tiles and 0 when it was recomputed.
  *   - No global state, except the static scratch of vs_index_build_noalloc
  *     (see there): other calls on different streams with different
  *     workspaces are independent.
@@ -94,7 +96,15 @@ typedef struct vs_index {
   int64_t* active_entries; /* optional [Hq] exact active (n, m) entries per head             */
 } vs_index;
 
-enum { VS_OP_INDEX = 0, VS_OP_FWD = 1, VS_OP_BWD = 2, VS_OP_ROPE = 3, VS_OP_RING_FWD = 4, VS_OP_RING_BWD = 5 };
+enum {
+  VS_OP_INDEX = 0,
+  VS_OP_FWD = 1,
+  VS_OP_BWD = 2,     /* the backward with room for its stored dS tiles (see vs_sparse_attn_bwd) */
+  VS_OP_ROPE = 3,
+  VS_OP_RING_FWD = 4,
+  VS_OP_RING_BWD = 5,
+  VS_OP_BWD_MIN = 6  /* the least workspace vs_sparse_attn_bwd accepts (dS recomputed for dQ)    */
+};
 
 /* Bytes of scratch `op` needs for problem `p` (0 if p is invalid). */
 VS_API size_t vs_workspace_bytes(const vs_params* p, int op);
@@ -190,6 +200,17 @@ VS_API vs_status vs_sparse_attn_fwd_rows(const vs_params* p, const vs_index* ind
  * dV = P^T dO, dS = P * (dO V^T - rowsum(dO * O)), dQ = scale dS K,
  * dK = scale dS^T Q; dK and dV sum over the Hq/Hkv query heads sharing a
  * key/value head and are written (not accumulated).
+ *
+ * Workspace: at least vs_workspace_bytes(p, VS_OP_BWD_MIN) bytes, else
+ * VS_ERR_WORKSPACE.  Bytes beyond that hold the dS tiles (bf16, 2 bytes per
+ * active 64 x 64 block entry): the dK / dV pass stores every active block it
+ * forms and dQ is computed from them, without forming S and dP a second
+ * time.  If the index needs more blocks than the workspace holds (decided on
+ * the device, per call), dQ recomputes them instead; the results agree
+ * within the stated tolerance either way.  vs_workspace_bytes(p, VS_OP_BWD)
+ * suggests room for a budget-fill index of density p->density (1.5x, 2x with
+ * index_mode 1), and the minimum for top-p selection or when that would
+ * exceed 32 GiB.
  */
 VS_API vs_status vs_sparse_attn_bwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,
                              const void* V, const void* O, const float* lse, const void* dO, void* dQ,

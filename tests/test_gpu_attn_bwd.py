@@ -11,6 +11,10 @@ same plus the arithmetic's own deviation at that element, with relative L2
 <= 1e-2.  Both use the same (oracle-built, injected) index.  The chained
 forward -> backward of a training step is checked at full size (below and
 in test_gpu_max_size.py), where no full oracle backward fits.
+
+Every case runs both ways of forming dQ: from the dS tiles that the dK / dV
+pass stores in a workspace with room for them, and by recomputing S and dP
+in the minimum workspace; the status word says which one ran.
 """
 import numpy as np
 import pytest
@@ -22,8 +26,32 @@ from _util import bf16_bits_of, f64, grad_close, inject_index, rel_l2, to_dev
 pytestmark = pytest.mark.gpu
 
 
-def _fwd_bwd(w, index, stripes=1, density=0.0, O_lse=None):
-    """GPU backward; O / LSE from the GPU forward, or injected (O_lse)."""
+# workspace of the backward: room for every dS block any index can have
+# (WS_ALL), room suggested for a budget-fill index of a given density (a
+# float), or the minimum (WS_MIN: dS recomputed)
+WS_ALL, WS_MIN = "all", None
+
+
+def _ws_bytes(vs, w, stripes, ws_density):
+    """Bytes of a backward workspace (see WS_*).  The dS blocks sit last, so
+    room for n blocks per head is the suggested size for density 1 less its
+    blocks plus n: nb^2 covers every slash block (nb (nb + 1) / 2) and every
+    vertical chunk (at most I per query block I)."""
+    mk = lambda dens: vs.make_params(w.L, w.Hq, w.Hkv, w.d, last_q=w.last_q, top_p=w.top_p, stripes=stripes,
+                                     density=dens)
+    if ws_density != WS_ALL:
+        return vs.vs_workspace_bytes(mk(ws_density), vs.VS_OP_BWD)
+    nb = w.L // 64
+    cap1 = int(1.5 * nb * (nb + 1) / 2 + 4 * nb) + 1
+    head = vs.vs_workspace_bytes(mk(1.0), vs.VS_OP_BWD) - w.Hq * cap1 * 8192
+    return head + w.Hq * nb * nb * 8192
+
+
+def _fwd_bwd(w, index, stripes=1, density=0.0, O_lse=None, ws_density=WS_ALL, want_path=None, ws_trim=0):
+    """GPU backward; O / LSE from the GPU forward, or injected (O_lse).
+    ws_density sizes the backward workspace (see WS_*), less ws_trim bytes
+    from its end (the dS blocks sit last); want_path, when given, is the dQ
+    path the status word must report (1 stored, 0 recomputed)."""
     import torch
     import dynamic_sparse_attention_index_gb300 as vs
     dev = torch.device("cuda:0")
@@ -46,11 +74,18 @@ def _fwd_bwd(w, index, stripes=1, density=0.0, O_lse=None):
         lse = torch.from_numpy(O_lse[1].astype(np.float32)).to(dev)
         wsf = None
     dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
-    wsb = vs.workspace(p, vs.VS_OP_BWD, dev)
+    if ws_density is WS_MIN:
+        wsb = vs.workspace(p, vs.VS_OP_BWD_MIN, dev)
+    else:
+        wsb = torch.empty(_ws_bytes(vs, w, stripes, ws_density) - ws_trim, dtype=torch.uint8, device=dev)
+        assert wsb.numel() > vs.vs_workspace_bytes(p, vs.VS_OP_BWD_MIN)
     vs.vs_sparse_attn_bwd(p, ix, Q, K, V, O, lse, dO, dQ, dK, dV, wsb)
     torch.cuda.synchronize()
+    path = int(wsb[8:12].view(torch.int32).item())
     assert wsf is None or vs.vs_device_status(wsf) == vs.VS_OK
     assert vs.vs_device_status(wsb) == vs.VS_OK
+    if want_path is not None:
+        assert path == want_path, ("dQ path", path, want_path)
     return ix, [f64(bf16_bits_of(t)) for t in (dQ, dK, dV)]
 
 
@@ -67,11 +102,12 @@ def _close(got, ref, name):
 def _check(w, index, stripes=1):
     q, k, v, do = f64(w.q), f64(w.k), f64(w.v), f64(w.do)
     O_lse = oracle.attention_forward(q, k, v, index, stripes=stripes)
-    _, got = _fwd_bwd(w, index, stripes, O_lse=O_lse)
     ref = oracle.attention_backward(q, k, v, do, index, stripes=stripes)
     emu = oracle.attention_backward_bf16_products(q, k, v, do, index, stripes=stripes)
-    for name, g, r, e in zip(("dQ", "dK", "dV"), got, ref, emu):
-        grad_close(name, g, r, e)
+    for ws_density, path in ((WS_ALL, 1), (WS_MIN, 0)):
+        _, got = _fwd_bwd(w, index, stripes, O_lse=O_lse, ws_density=ws_density, want_path=path)
+        for name, g, r, e in zip(("dQ", "dK", "dV"), got, ref, emu):
+            grad_close(name, g, r, e)
 
 
 CASES = [
@@ -134,6 +170,25 @@ def test_bwd_production_shape_element_wise():
     _check(w, index)
 
 
+def test_bwd_stored_ds_overflow_falls_back():
+    """A workspace with room for fewer dS blocks than the index needs: the
+    device-side plan finds that a head's blocks do not fit, nothing is
+    stored, and dQ is recomputed (status path 0) with the same results."""
+    w = synth.make_workload(3, L=2048, Hq=4, Hkv=2, d=128, backward=True)
+    index, _, _ = oracle.build_index(f64(w.q), f64(w.k), 64, 0.95, density=0.05)
+    q, k, v, do = f64(w.q), f64(w.k), f64(w.v), f64(w.do)
+    O_lse = oracle.attention_forward(q, k, v, index)
+    # room for density 1e-6 is four vertical chunks per query block and one
+    # block per head; trimmed to two blocks per head (band 0 alone needs 32)
+    nb = w.L // 64
+    trim = (4 * nb - 1) * w.Hq * 64 * 64 * 2
+    _, got = _fwd_bwd(w, index, O_lse=O_lse, ws_density=1e-6, want_path=0, ws_trim=trim)
+    ref = oracle.attention_backward(q, k, v, do, index)
+    emu = oracle.attention_backward_bf16_products(q, k, v, do, index)
+    for name, g, r, e in zip(("dQ", "dK", "dV"), got, ref, emu):
+        grad_close(name, g, r, e)
+
+
 def test_bwd_striped_32_shards():
     w = synth.make_workload(4, L=4096, Hq=2, Hkv=1, d=128, backward=True)
     index, _, _ = oracle.build_index(f64(w.q), f64(w.k), 64, 0.9, stripes=32)
@@ -148,9 +203,15 @@ def test_bwd_full_size_gqa_128k():
     rows, dK -> 0)."""
     w = synth.make_workload(3)
     index, _, _ = oracle.build_index(f64(w.q), f64(w.k), 64, 0.95, density=float(np.float32(0.05)))
-    ix, (dQ, dK, dV) = _fwd_bwd(w, index)
     rows = np.concatenate([np.arange(0, 64), np.arange(65536, 65536 + 64), np.arange(w.L - 64, w.L)])
     rQ = oracle.attention_backward_dq_rows(f64(w.q), f64(w.k), f64(w.v), f64(w.do), index, rows)
+    # the bench's workspace (room for the dS tiles of density 0.05), then the minimum
+    for ws_density, path in ((0.05, 1), (WS_MIN, 0)):
+        ix, (dQ, dK, dV) = _fwd_bwd(w, index, ws_density=ws_density, want_path=path)
+        _check_full(w, dQ, dK, dV, rows, rQ)
+
+
+def _check_full(w, dQ, dK, dV, rows, rQ):
     _close(dQ[rows], rQ, "dQ rows")
     G = w.Hq // w.Hkv
     dOf = f64(w.do)

@@ -109,3 +109,24 @@ def test_rope_rejects_bad_args(vs):
     assert L.vs_rope(ctypes.byref(p), 4, FAKE, FAKE, 0, None) == vs.VS_ERR_INVALID_ARG
     p = vs.make_params(4096, 4, 2, 64, yarn_factor=32.0, yarn_orig_len=0)
     assert L.vs_rope(ctypes.byref(p), 4, FAKE, FAKE, 0, None) == vs.VS_ERR_INVALID_ARG
+
+
+def test_bwd_workspace_sizes():
+    """The backward's minimum workspace, and the room it suggests for
+    stored dS tiles (64 x 64 bf16 blocks, per head 1.5 x the density's share
+    of the causal blocks plus four vertical chunks per query block; none for
+    top-p selection or beyond 32 GiB)."""
+    import dynamic_sparse_attention_index_gb300 as vs
+    L, Hq = 131072, 16
+    nb = L // 64
+    p0 = vs.make_params(L, Hq, 2, 128)
+    mn = vs.vs_workspace_bytes(p0, vs.VS_OP_BWD_MIN)
+    assert mn > 0 and vs.vs_workspace_bytes(p0, vs.VS_OP_BWD) == mn
+    p5 = vs.make_params(L, Hq, 2, 128, density=0.05)
+    assert vs.vs_workspace_bytes(p5, vs.VS_OP_BWD_MIN) == mn
+    extra = vs.vs_workspace_bytes(p5, vs.VS_OP_BWD) - mn
+    cap = int(1.5 * 0.05 * nb * (nb + 1) / 2 + 4 * nb) + 1
+    tables = Hq * (nb + 2 * nb) * 4  # band ranks (one per band, W = 1) and two block bases per query block
+    assert Hq * cap * 8192 + tables <= extra <= Hq * cap * 8192 + tables + 4 * 256
+    big = vs.make_params(1 << 20, 32, 8, 128, density=0.05)
+    assert vs.vs_workspace_bytes(big, vs.VS_OP_BWD) == vs.vs_workspace_bytes(big, vs.VS_OP_BWD_MIN)
