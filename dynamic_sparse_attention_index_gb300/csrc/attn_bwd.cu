@@ -491,16 +491,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ loader
     if (lane == 0) {
       int t = 0, un = 0;
-      // Stored dS: a tile's dS blocks are stored once its accumulate has
-      // released its stage (the wait below for tile t + 2), so the stores of
-      // tile t are issued after tile t + 2's loads; the last two tiles are
-      // stored at the end.  ds_free[t & 1] tells the P / dS warps that the
-      // buffer has been read.
+      // Stored dS: tile u's dS blocks are stored as soon as the P / dS warps
+      // have written them (pds_ready), which the loader meets at tile u + 2
+      // before it waits for u's stage; once tile u + 2's loads are issued,
+      // the store has read its buffer, and ds_free[u & 1] lets the P / dS
+      // warps write it again.  The last two tiles are stored at the end.
       int pblk[2][2] = {{-1, -1}, {-1, -1}};
       // the stored blocks are read back once, after this kernel: evict
       // them first so that the Q / dO tiles keep their place in L2
       const uint64_t pol_stream = ds_on ? l2_policy_evict_first() : 0;
-      auto store_ds = [&](int u) {
+      auto issue_store = [&](int u) -> bool {
         const uint8_t* dbuf = sm + kPdS + (u & 1) * kPdSBytes + 128 * 128;
         bool any = false;
         for (int j = 0; j < 2; ++j)
@@ -508,11 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_store_2d_hint(&mDS, dbuf + j * 8192, 0, pblk[u & 1][j] * 64, pol_stream);
             any = true;
           }
-        if (any) {
-          bulk_commit_group();
-          bulk_wait_read_all();
-        }
-        mbar_arrive(&ds_free[u & 1]);
+        if (any) bulk_commit_group();
+        return any;
       };
       for (int uid = blockIdx.x; uid < nunits && !*abort_flag; uid += gridDim.x, ++un) {
         bool last = false;
@@ -539,6 +536,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
+          bool stored = false;
+          if (ds_on && t >= 2) {
+            if (!wait(&pds_ready[t & 1], ((t - 2) >> 1) & 1, 6)) break;
+            stored = issue_store(t - 2);
+          }
           const int st = t % kStages;
           if (!wait(&st_empty[st], ((t / kStages) & 1) ^ 1, 4)) break;
           const long long e0 = kWaitProfileKv ? clock64() : 0;
@@ -556,7 +558,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (kWaitProfileKv) atomicAdd(&wcyc[27], (unsigned long long)(clock64() - e0));
           if (ds_on) {
-            if (t >= 2) store_ds(t - 2);
+            if (t >= 2) {
+              if (stored) bulk_wait_read_all();
+              mbar_arrive(&ds_free[t & 1]);
+            }
             pblk[t & 1][0] = blk0;
             pblk[t & 1][1] = blk1;
           }
@@ -564,10 +569,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         } while (!last && !*abort_flag);
       }
       if (ds_on && !*abort_flag) {
-        // the last two tiles: wait for their accumulates, then store
+        // the last two tiles: wait for their dS, then store
         for (int u = t >= 2 ? t - 2 : 0; u < t; ++u) {
-          if (!wait(&st_empty[u % kStages], (u / kStages) & 1, 5)) break;
-          store_ds(u);
+          if (!wait(&pds_ready[u & 1], (u >> 1) & 1, 5)) break;
+          issue_store(u);
         }
       }
       if (ds_on) bulk_wait_all();
@@ -707,7 +712,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wait_warp(&sdp_full[t & 1], (t >> 1) & 1, 21)) break;
         const long long ph0 = kWaitProfileKv ? clock64() : 0;
         if (t >= 2 && !wait_warp(&pds_free[t & 1], ((t >> 1) - 1) & 1, 22)) break;
-        if (ds_on && t >= 2 && !wait_warp(&ds_free[t & 1], ((t >> 1) - 1) & 1, 24)) break;
+        if (ds_on && t >= 2 && !wait_warp(&ds_free[t & 1], ((t >> 1) - 1) & 1, 9)) break;
         tc_fence_after();
         const float c = P.scale * P.log2e;
         uint8_t* pbuf = sm + kPdS + (t & 1) * kPdSBytes;
