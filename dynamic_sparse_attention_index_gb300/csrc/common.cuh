@@ -92,7 +92,7 @@ __device__ __forceinline__ void report_timeout_first(DevStatus* st, int where) {
     atomicExch(&st->where, where);
 }
 // kernel tags of the status word's wait site
-enum : int { kTagForward = 1, kTagDq = 2, kTagDkdvVertical = 3, kTagDkdvSlash = 4, kTagDqStored = 5 };
+enum : int { kTagForward = 1, kTagDq = 2, kTagDkdvVertical = 3, kTagDkdvSlash = 4, kTagDqStored = 5, kTagIndex = 6 };
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -147,6 +147,14 @@ struct IndexArgs {
   DevStatus* status;
 };
 cudaError_t launch_index(const IndexArgs& a, cudaStream_t s);
+// Key chunks and tiles of the tensor-core index passes (last_q = 64; the
+// workspace sizes their partials array from it).
+struct IxTcGrid {
+  int C;       // key chunks
+  int tpc;     // 128-key tiles per chunk
+  int npairs;  // head pairs per key/value head
+};
+IxTcGrid index_tc_grid(int L, int Hq, int Hkv);
 void index_grid(const vs_params& p, int* tiles_per_chunk, int* nchunk, int* row_splits);
 
 }  // namespace vs

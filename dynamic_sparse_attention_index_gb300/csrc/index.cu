@@ -355,7 +355,12 @@ void index_grid(const vs_params& p, int* tiles_per_chunk, int* nchunk, int* row_
   *row_splits = rs;
 }
 
+bool index_tc_supported(const IndexArgs& a);
+cudaError_t launch_index_scores_tc(const IndexArgs& a, cudaStream_t s);
+
 cudaError_t launch_index_scores(const IndexArgs& a, cudaStream_t s) {
+  // last_q = 64: the tensor-core passes (index_tc.cu); otherwise these
+  if (index_tc_supported(a)) return launch_index_scores_tc(a, s);
   dim3 grid(a.nchunk * a.row_splits, a.Hkv);
   if (a.d == 128) {
     index_scores_kernel<128, false><<<grid, kThreads, 0, s>>>(a);
