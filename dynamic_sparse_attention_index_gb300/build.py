@@ -37,7 +37,7 @@ def _flags() -> list:
     # counters (all, dK/dV only, query-major only, MMA issue of dK/dV or
     # query-major only)
     mode = os.environ.get("VS_WAIT_PROFILE", "")
-    extra = [f"-DVS_WAIT_PROFILE={mode}"] if mode in ("1", "2", "3", "4", "5", "6", "7") else []
+    extra = [f"-DVS_WAIT_PROFILE={mode}"] if mode in ("1", "2", "3", "4", "5", "6", "7", "8") else []
     # VS_DEBUG=1: device bounds checks (VS_ERR_BOUNDS in the status word)
     if os.environ.get("VS_DEBUG", "") == "1":
         extra.append("-DVS_DEBUG=1")

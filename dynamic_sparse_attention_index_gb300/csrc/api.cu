@@ -73,7 +73,7 @@ vs_status check_index_params(const vs_params* p) {
 }
 
 struct IndexWs {
-  size_t status, part, rowstat, v, T64, S, total;
+  size_t status, part, rowstat, v, T64, S, vhist, total;
 };
 
 IndexWs index_ws(const vs_params& p) {
@@ -94,6 +94,7 @@ IndexWs index_ws(const vs_params& p) {
   o.v = w.take((size_t)p.Hq * p.L * sizeof(float));
   o.T64 = w.take((size_t)p.Hq * p.last_q * ntile * sizeof(float));
   o.S = w.take((size_t)p.Hq * nbs * sizeof(float));
+  o.vhist = w.take((size_t)p.Hq * 2048 * sizeof(uint32_t));
   o.total = w.off;
   return o;
 }
@@ -231,6 +232,9 @@ vs_status vs_index_build(const vs_params* p, const void* Q, const void* K, const
   a.s_cnt = out->s_cnt;
   a.active = out->active_entries;
   a.status = reinterpret_cast<DevStatus*>(w + lay.status);
+  // cleared and filled by the tensor-core scoring passes; the others leave
+  // the counting to the selection
+  a.vhist = index_tc_supported(a) ? reinterpret_cast<uint32_t*>(w + lay.vhist) : nullptr;
   if (launch_index_scores(a, s) != cudaSuccess) return VS_ERR_CUDA;
   if (launch_select(a, s) != cudaSuccess) return VS_ERR_CUDA;
   if (p->index_mode == 1 && launch_group_union(*p, *out, s) != cudaSuccess) return VS_ERR_CUDA;

@@ -24,6 +24,8 @@ constexpr int kMaxL = 1 << 20;                   // supported sequence length ce
 constexpr bool kWaitProfileKv = VS_WAIT_PROFILE == 1 || VS_WAIT_PROFILE == 2;
 // 7: the stored-dS dQ kernel's waits (producer, MMA issue, epilogue) and total cycles
 constexpr bool kWaitProfileDs = VS_WAIT_PROFILE == 7;
+// 8: the selection kernel's phases (budget fill), per head summed
+constexpr bool kProfileSel = VS_WAIT_PROFILE == 8;
 // 4: only the dK/dV kernel's MMA-issue timers and total cycles (least intrusive)
 constexpr bool kMmaProfileKv = kWaitProfileKv || VS_WAIT_PROFILE == 4;
 constexpr bool kWaitProfileQm = VS_WAIT_PROFILE == 1 || VS_WAIT_PROFILE == 3;
@@ -144,6 +146,8 @@ struct IndexArgs {
   int32_t* s_idx;
   int32_t* s_cnt;
   int64_t* active;            // [Hq] or null
+  uint32_t* vhist;            // [Hq][2048] counts of v by key >> 20 (written by the tensor-core
+                              // pass 2), or null: the selection counts them itself
   DevStatus* status;
 };
 cudaError_t launch_index(const IndexArgs& a, cudaStream_t s);
@@ -155,6 +159,7 @@ struct IxTcGrid {
   int npairs;  // head pairs per key/value head
 };
 IxTcGrid index_tc_grid(int L, int Hq, int Hkv);
+bool index_tc_supported(const IndexArgs& a);
 void index_grid(const vs_params& p, int* tiles_per_chunk, int* nchunk, int* row_splits);
 
 }  // namespace vs

@@ -42,7 +42,8 @@ struct IxLayout {
   static constexpr int kMisc = kBar + kNumBars * 8;  // tensor memory slot, abort flag
   static constexpr int kRow = kMisc + 16;            // pass 2: (max, 1 / sum) of the 128 rows
   static constexpr int kRed = kRow + 128 * 8;        // pass 2: per-warp block sums, two buffers
-  static constexpr int kSmem = kRed + 2 * 4 * 2 * 4;
+  static constexpr int kHist = kRed + 2 * 4 * 2 * 4;  // pass 2: [2 heads][2048] counts of v by key >> 20
+  static constexpr int kSmem = kHist + 2 * 2048 * 4;
 };
 
 __device__ __forceinline__ float ix_exp2(float x) {
@@ -85,6 +86,7 @@ __global__ void __launch_bounds__(kIxThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Ly::kMisc + 4);
   float2* rowst = reinterpret_cast<float2*>(sm + Ly::kRow);
   float* red = reinterpret_cast<float*>(sm + Ly::kRed);  // [2][4 warps][2 heads]
+  uint32_t* hist = reinterpret_cast<uint32_t*>(sm + Ly::kHist);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x, pair = blockIdx.y, g = blockIdx.z;
   const int ha = g * a.G + 2 * pair;
@@ -111,6 +113,8 @@ __global__ void __launch_bounds__(kIxThreads, 1)
     tmem_alloc(tmem_slot, 256);  // two 128-column accumulators
     tmem_relinquish();
   }
+  if (kPass2)
+    for (int j = threadIdx.x; j < 2 * 2048; j += kIxThreads) hist[j] = 0u;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -289,7 +293,11 @@ __global__ void __launch_bounds__(kIxThreads, 1)
         const float va = va0 + va1, vb = vb0 + vb1;
         if (k < a.L) {
           a.v[(size_t)ha * a.L + k] = va;
-          if (has_b) a.v[(size_t)hb * a.L + k] = vb;
+          atomicAdd(&hist[min(__float_as_uint(va) >> 20, 2047u)], 1u);
+          if (has_b) {
+            a.v[(size_t)hb * a.L + k] = vb;
+            atomicAdd(&hist[2048 + min(__float_as_uint(vb) >> 20, 2047u)], 1u);
+          }
         }
         // 64-key block sums (keys beyond L hold zeros): warps 0-1 of the
         // group hold the tile's first block, warps 2-3 its second
@@ -319,6 +327,12 @@ __global__ void __launch_bounds__(kIxThreads, 1)
   __syncthreads();
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tbase, 256);
+  if (kPass2 && !*abort_flag)
+    // this CTA's counts into the heads' histograms (non-zero bins only)
+    for (int j = threadIdx.x; j < (has_b ? 2 : 1) * 2048; j += kIxThreads) {
+      const uint32_t cnt = hist[j];
+      if (cnt) atomicAdd(&a.vhist[(size_t)(j < 2048 ? ha : hb) * 2048 + (j & 2047)], cnt);
+    }
 }
 
 // S[h][B] = sum of the 64-key block masses of band B: key blocks
@@ -350,6 +364,7 @@ cudaError_t launch_tc(const IndexArgs& a, cudaStream_t s) {
                                 (int)smem)) != cudaSuccess)
     return e;
   const dim3 grid(c.C, c.npairs, a.Hkv);
+  if ((e = cudaMemsetAsync(a.vhist, 0, (size_t)a.Hq * 2048 * sizeof(uint32_t), s)) != cudaSuccess) return e;
   index_tc_kernel<D, false><<<grid, kIxThreads, smem, s>>>(mQ, mK, a, c);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   index_tc_kernel<D, true><<<grid, kIxThreads, smem, s>>>(mQ, mK, a, c);

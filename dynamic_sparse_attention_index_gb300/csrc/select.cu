@@ -342,6 +342,10 @@ __device__ unsigned long long slash_entries(const uint8_t* inS, int nbs, int bs,
 // Budget fill: verticals whose key reached the running threshold, gathered in
 // shared memory once they fit, so later threshold probes skip the full list.
 constexpr int kCandCap = 8192;
+// budget fill, fast path: verticals gathered above a histogram cut
+constexpr int kFastCap = 1024;
+// and the search warps' kept-band tables (bits and word prefixes)
+constexpr int kWarpTables = 32 * 1024;
 
 __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) {
   extern __shared__ __align__(16) uint8_t dyn[];
@@ -471,10 +475,17 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) 
       if (ncand >= 0 || nabove > (unsigned long long)kCandCap) return;
       if (threadIdx.x == 0) s.bcast_u32[0] = 0u;
       __syncthreads();
-      for (int m = threadIdx.x; m < L; m += kThreads) {
-        const uint32_t k = key_of(v[m]);
-        if (k >= tau) {
-          const unsigned i = atomicAdd(&s.bcast_u32[0], 1u);
+      for (int m0 = 0; m0 < L; m0 += kThreads) {
+        // one shared-memory atomic per warp (L is a multiple of 64)
+        const int m = m0 + (int)threadIdx.x;
+        const uint32_t k = m < L ? key_of(v[m]) : 0u;
+        const bool in = m < L && k >= tau;
+        const unsigned b = __ballot_sync(0xffffffffu, in);
+        unsigned i0 = 0;
+        if ((threadIdx.x & 31) == 0 && b) i0 = atomicAdd(&s.bcast_u32[0], (unsigned)__popc(b));
+        i0 = __shfl_sync(0xffffffffu, i0, 0);
+        if (in) {
+          const unsigned i = i0 + (unsigned)__popc(b & ((1u << (threadIdx.x & 31)) - 1u));
           ckey[i] = k;
           cblk[i] = m / bs;
         }
@@ -483,19 +494,292 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) 
       ncand = (int)s.bcast_u32[0];
       __syncthreads();
     };
-    uint32_t tau;
-    if (entries_at(0x7f800001u) >= target) {
-      tau = 0x7f800001u;  // nothing beyond band 0
-    } else if (entries_at(1u) < target) {
-      tau = 1u;  // every positive candidate
+    // Fast path.  A cut t_low from a histogram of the vertical keys (2048
+    // bins of key >> 20): the lowest bin edge with at most kFastCap
+    // verticals at or above it.  Those verticals are gathered in index
+    // order; if the set at t_low reaches the target, tau >= t_low and only
+    // they matter: seven warps finish the search three bits per round
+    // (warp_entries) and the kept verticals are compacted from them.
+    // Otherwise the bitwise search over the full list runs.
+    long long pf[8] = {};
+    const long long pf0 = kProfileSel ? clock64() : 0;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (a.vhist) {
+      // counted by the scoring pass
+      for (int b = threadIdx.x; b < 2048; b += kThreads) s.hcnt[b] = a.vhist[(size_t)h * 2048 + b];
     } else {
-      tau = 0u;
-      for (int bit = 30; bit >= 0; --bit) {
-        const uint32_t cand = tau | (1u << bit);
-        if (cand > 0x7f800000u) continue;
-        if (entries_at(cand) >= target) {
-          tau = cand;
-          gather(tau);
+      for (int b = threadIdx.x; b < 2048; b += kThreads) s.hcnt[b] = 0u;
+      __syncthreads();
+      // four keys per thread and step, the steps' loads issued together
+      const float4* v4 = reinterpret_cast<const float4*>(v);
+      const int L4 = L / 4;
+      for (int q0 = 0; q0 < L4; q0 += 4 * kThreads) {
+        float4 x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int q = q0 + u * kThreads + (int)threadIdx.x;
+          x[u] = q < L4 ? v4[q] : make_float4(-1.f, -1.f, -1.f, -1.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            // negative: past the end (keys of masses are below 2^31)
+            const int bin = xs[j] < 0.f ? -1 : (int)min(key_of(xs[j]) >> 20, 2047u);
+            const unsigned same = __match_any_sync(0xffffffffu, bin);
+            if (bin >= 0 && (__ffs(same) - 1) == lane) atomicAdd(&s.hcnt[bin], (unsigned)__popc(same));
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // suffix counts over the bins, 64 per lane from the top
+      unsigned c = 0;
+      for (int b = lane * 64; b < lane * 64 + 64; ++b) c += s.hcnt[b];
+      unsigned suf = c;
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned t = __shfl_down_sync(0xffffffffu, suf, o);
+        if (lane + o < 32) suf += t;
+      }
+      // lanes whose whole range fits: the one below the lowest of them
+      // refines bin by bin
+      const unsigned fits = __ballot_sync(0xffffffffu, suf <= (unsigned)kFastCap);
+      const int l0 = fits ? __ffs(fits) - 1 : 32;
+      int cut = l0 * 64;
+      if (l0 > 0 && lane == l0 - 1) {
+        unsigned acc = suf - c;  // bins above this lane's range
+        int b = lane * 64 + 64;
+        while (b > lane * 64 && acc + s.hcnt[b - 1] <= (unsigned)kFastCap) {
+          acc += s.hcnt[b - 1];
+          --b;
+        }
+        cut = b;
+      }
+      cut = __shfl_sync(0xffffffffu, cut, l0 > 0 ? l0 - 1 : 0);
+      if (lane == 0) s.bcast_u32[1] = (unsigned)cut << 20;
+    }
+    __syncthreads();
+    const uint32_t t_low = s.bcast_u32[1];
+    if (kProfileSel) pf[0] = clock64() - pf0;
+    // The verticals with key >= t_low (at most kFastCap by the cut) and the
+    // bands >= 1 with key >= t_low, gathered in any order.  Slots of the
+    // candidate arrays: [0, kFastCap) the verticals (key, token), then their
+    // working copy (key, band row x = nbs - 1 - key block), then the bands'
+    // working list (key, band).  After each search round the working lists
+    // keep only keys above tau: later thresholds are all above it.
+    uint32_t* ckey2 = ckey;
+    int32_t* cidx = cblk;
+    uint32_t* wkey = ckey + kFastCap;
+    int32_t* wx = cblk + kFastCap;
+    uint32_t* bkey = ckey + 2 * kFastCap;
+    int32_t* bidx = cblk + 2 * kFastCap;
+    constexpr int kBandCap = kCandCap - 2 * kFastCap;
+    int nw = 0, nbc = 0;
+    bool fast = false;
+    // warp-aggregated slot in a shared counter
+    auto slot = [&](bool in, unsigned* counter) -> unsigned {
+      const unsigned bal = __ballot_sync(0xffffffffu, in);
+      unsigned i0 = 0;
+      if (lane == 0 && bal) i0 = atomicAdd(counter, (unsigned)__popc(bal));
+      return __shfl_sync(0xffffffffu, i0, 0) + (unsigned)__popc(bal & ((1u << lane) - 1u));
+    };
+    if (t_low < 0x7f800000u) {
+      if (threadIdx.x == 0) {
+        s.bcast_u32[2] = 0u;
+        s.bcast_u32[3] = 0u;
+      }
+      __syncthreads();
+      // eight loads per thread in flight per step
+      for (int m0 = 0; m0 < L; m0 += 8 * kThreads) {
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int m = m0 + u * kThreads + (int)threadIdx.x;
+          x[u] = m < L ? v[m] : -1.f;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int m = m0 + u * kThreads + (int)threadIdx.x;
+          const bool in = x[u] >= 0.f && key_of(x[u]) >= t_low;
+          const unsigned i = slot(in, &s.bcast_u32[2]);
+          if (in && i < (unsigned)kFastCap) {
+            ckey2[i] = key_of(x[u]);
+            cidx[i] = m;
+            wkey[i] = key_of(x[u]);
+            wx[i] = nbs - 1 - m / bs;
+          }
+        }
+      }
+      for (int B0 = 0; B0 < nbs; B0 += kThreads) {
+        const int B = B0 + (int)threadIdx.x;
+        const uint32_t k = B < nbs ? key_of(S[B]) : 0u;
+        const bool in = B >= 1 && B < nbs && k >= t_low;
+        const unsigned i = slot(in, &s.bcast_u32[3]);
+        if (in && i < (unsigned)kBandCap) {
+          bkey[i] = k;
+          bidx[i] = B;
+        }
+      }
+      __syncthreads();
+      ncand = (int)s.bcast_u32[2];
+      nbc = (int)s.bcast_u32[3];
+      nw = ncand;
+      __syncthreads();
+      if (ncand > kFastCap || nbc > kBandCap) ncand = -1;  // cannot hold them: the full search
+    }
+    if (kProfileSel) {
+      pf[2] = clock64() - pf0 - pf[0];
+      pf[6] = ncand;
+    }
+    const int nwords = (nbs + 31) / 32;
+    // search warps: as many as the tables fit, up to 31 (2^nbr - 1 thresholds per round)
+    int nsw = kWarpTables / (8 * nwords);
+    if (nsw > 32) nsw = 32;
+    int nbr = 0;
+    while ((2 << nbr) - 1 <= nsw - 1 && nbr < 5) ++nbr;  // 2^nbr - 1 evaluators (warps 1..)
+    uint32_t* wbm = reinterpret_cast<uint32_t*>(cblk + kCandCap);  // [nsw][nwords] kept-band bits
+    int32_t* wpre = reinterpret_cast<int32_t*>(wbm + nsw * nwords);  // [nsw][nwords] kept bands in earlier words
+    const unsigned long long band0 = (unsigned long long)nbs * (unsigned long long)(bs * (bs + 1) / 2);
+    // active entries at threshold t, by one warp over the working lists
+    auto warp_entries = [&](uint32_t t) -> unsigned long long {
+      uint32_t* bm = wbm + warp * nwords;
+      int32_t* pre = wpre + warp * nwords;
+      unsigned long long se = 0;
+      // kept bands: the working ones with key >= t
+      for (int wd = lane; wd < nwords; wd += 32) bm[wd] = 0u;
+      __syncwarp();
+      for (int i = lane; i < nbc; i += 32)
+        if (bkey[i] >= t) {
+          const int B = bidx[i];
+          atomicOr(&bm[B >> 5], 1u << (B & 31));
+          se += (unsigned long long)(nbs - B) * (unsigned long long)bs * (unsigned long long)bs;
+        }
+      __syncwarp();
+      int carry = 0;
+      for (int base = 0; base < nwords; base += 32) {
+        const int wd = base + lane;
+        const int c = wd < nwords ? __popc(bm[wd]) : 0;
+        int incl = c;
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        if (wd < nwords) pre[wd] = carry + incl - c;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      __syncwarp();
+      unsigned long long ve = 0;
+      // not-kept bands in [1, x] for each vertical at or above t
+      for (int i = lane; i < nw; i += 32) {
+        const int x = wx[i];
+        if (wkey[i] < t || x < 1) continue;
+        const int w = x >> 5, j = x & 31;
+        const uint32_t msk = j == 31 ? 0xffffffffu : ((2u << j) - 1u);
+        ve += (unsigned long long)(x - (pre[w] + __popc(bm[w] & msk)));
+      }
+      for (int o = 16; o > 0; o >>= 1) {
+        se += __shfl_xor_sync(0xffffffffu, se, o);
+        ve += __shfl_xor_sync(0xffffffffu, ve, o);
+      }
+      return band0 + se + ve * (unsigned long long)bs;
+    };
+    uint32_t tau = 0u;
+    if (ncand >= 0 && nbr >= 1) {
+      fast = true;
+      bool first_round = true;
+      for (int hi = 30; hi >= 0; hi -= nbr) {
+        const int nbit = hi >= nbr - 1 ? nbr : hi + 1;
+        const int lo = hi - nbit + 1;
+        if (warp < (1 << nbit)) {
+          if (warp == 0) {
+            // the set at t_low must reach the target (checked beside round 1)
+            if (first_round) {
+              const bool ok = warp_entries(t_low) >= target;
+              if (lane == 0) s.bcast_u64[3] = ok ? 1ull : 0ull;  // a slot nothing else writes
+            }
+          } else {
+            const uint32_t cand = tau | ((uint32_t)warp << lo);
+            // monotone: every threshold at or below t_low reaches the target
+            const bool ok = cand <= 0x7f800000u && (cand <= t_low || warp_entries(cand) >= target);
+            if (lane == 0) s.wcnt[warp] = ok ? 1u : 0u;
+          }
+        }
+        __syncthreads();
+        if (first_round && s.bcast_u64[3] == 0ull) {
+          fast = false;  // (read by every thread before the next barrier; the slot is not reused)
+          break;
+        }
+        first_round = false;
+        unsigned k = 0;
+        for (int w = 1; w < (1 << nbit); ++w)
+          if (s.wcnt[w]) k = (unsigned)w;
+        tau |= k << lo;
+        // working lists: keys above tau only (one vertical, up to six bands per thread)
+        uint32_t vk = 0u, bk[6];
+        int vx = 0, bb[6];
+        const int i = (int)threadIdx.x;
+        if (i < nw) {
+          vk = wkey[i];
+          vx = wx[i];
+        }
+#pragma unroll
+        for (int u = 0; u < 6; ++u) {
+          const int j = u * kThreads + i;
+          bk[u] = j < nbc ? bkey[j] : 0u;
+          bb[u] = j < nbc ? bidx[j] : 0;
+        }
+        if (threadIdx.x == 0) {
+          s.bcast_u32[2] = 0u;
+          s.bcast_u32[3] = 0u;
+        }
+        __syncthreads();
+        {
+          const bool in = i < nw && vk > tau;
+          const unsigned p = slot(in, &s.bcast_u32[2]);
+          if (in) {
+            wkey[p] = vk;
+            wx[p] = vx;
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < 6; ++u) {
+          const bool in = u * kThreads + i < nbc && bk[u] > tau;
+          const unsigned p = slot(in, &s.bcast_u32[3]);
+          if (in) {
+            bkey[p] = bk[u];
+            bidx[p] = bb[u];
+          }
+        }
+        __syncthreads();
+        nw = (int)s.bcast_u32[2];
+        nbc = (int)s.bcast_u32[3];
+        __syncthreads();
+      }
+      if (tau == 0u) tau = 1u;  // every positive candidate
+      if (kProfileSel) {
+        pf[3] = clock64() - pf0 - pf[0] - pf[2];
+        pf[5] = fast ? 1 : 0;
+      }
+    }
+    if (!fast) {
+      // the bitwise search, probing the whole vertical list until its
+      // candidates fit the gathered list
+      ncand = -1;
+      if (entries_at(0x7f800001u) >= target) {
+        tau = 0x7f800001u;  // nothing beyond band 0
+      } else if (entries_at(1u) < target) {
+        tau = 1u;  // every positive candidate
+      } else {
+        tau = 0u;
+        for (int bit = 30; bit >= 0; --bit) {
+          const uint32_t cand = tau | (1u << bit);
+          if (cand > 0x7f800000u) continue;
+          if (entries_at(cand) >= target) {
+            tau = cand;
+            gather(tau);
+          }
         }
       }
     }
@@ -513,7 +797,37 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) 
     }
     __syncthreads();
     ++ns;
-    nv = compact_above(v, L, tau - 1u, vout, notS, nbs, bs, &vert_e, s);
+    if (fast) {
+      // the kept verticals are gathered candidates (any order): each is
+      // placed by the number of kept tokens below it
+      int32_t* kept = wx;  // free after the search
+      if (threadIdx.x == 0) s.bcast_u32[2] = 0u;
+      __syncthreads();
+      for (int c0 = 0; c0 < ncand; c0 += kThreads) {
+        const int i = c0 + (int)threadIdx.x;
+        const bool in = i < ncand && ckey2[i] >= tau;
+        const unsigned p = slot(in, &s.bcast_u32[2]);
+        if (in) kept[p] = cidx[i];
+      }
+      __syncthreads();
+      const int K = (int)s.bcast_u32[2];
+      unsigned long long ve = 0;
+      for (int i = threadIdx.x; i < K; i += kThreads) {
+        const int e = kept[i];
+        int pos = 0;
+        for (int j = 0; j < K; ++j) pos += kept[j] < e ? 1 : 0;
+        vout[pos] = e;
+        ve += (unsigned long long)bs * (unsigned long long)notS[nbs - 1 - e / bs];
+      }
+      vert_e = block_sum_u64(ve, s);
+      nv = K;
+    } else {
+      nv = compact_above(v, L, tau - 1u, vout, notS, nbs, bs, &vert_e, s);
+    }
+    if (kProfileSel && threadIdx.x == 0 && a.status) {
+      pf[4] = clock64() - pf0;
+      for (int k = 0; k < 7; ++k) atomicAdd(&a.status->wait_cycles[k], (unsigned long long)pf[k]);
+    }
   }
   if (threadIdx.x == 0) {
     a.v_cnt[h] = nv;
@@ -525,7 +839,10 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) 
 }  // namespace
 
 // kept-band flags, band prefix table, budget-fill candidate list (key, block)
-size_t select_smem_bytes(int nbs) { return align_up(nbs, 16) + align_up((size_t)nbs * 4, 16) + (size_t)kCandCap * 8; }
+// (and, after them, each search warp's kept-band bits and word prefixes)
+size_t select_smem_bytes(int nbs) {
+  return align_up(nbs, 16) + align_up((size_t)nbs * 4, 16) + (size_t)kCandCap * 8 + kWarpTables + (size_t)kFastCap * 2;
+}
 
 cudaError_t launch_select(const IndexArgs& a, cudaStream_t s) {
   const size_t smem = select_smem_bytes(a.nbs);
