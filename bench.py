@@ -50,8 +50,12 @@ WORKLOADS = {
 }
 DENSITY = 0.05     # budget fill: 95 % sparsity (fixed in the pages' experiments)
 LAST_Q, TOP_P = 64, 0.95
-KERNELS_PER_STEP = {"rope": 4, "index": 5, "fwd": 4, "bwd": 8}
-KERNELS_PER_STEP_FWD = {"rope": 2, "index": 5, "fwd": 4}
+# library kernels per step: RoPE of Q and K (and the adjoint on dQ and dK);
+# the index (two tensor-core scoring passes, slash sums, selection); the
+# forward (three prep kernels, attention); the backward (three prep kernels,
+# D, dK / dV for the vertical and the slash units, the recomputing dQ kernel)
+KERNELS_PER_STEP = {"rope": 4, "index": 4, "fwd": 4, "bwd": 7}
+KERNELS_PER_STEP_FWD = {"rope": 2, "index": 4, "fwd": 4}
 # ex2.approx issue rate of one SM per clock (the index's exponentials;
 # measured with a standalone microbenchmark on this GPU)
 MUFU_EX2_PER_CLK_SM = 32
@@ -61,7 +65,8 @@ N_SM = 152
 # profile summary together with the SHA-256 of the kernel sources it was taken
 # on: when the sources have changed since, the figure no longer applies and
 # the line reports null.
-TRAFFIC_SOURCES = ("attn_bwd.cu", "attn_fwd.cu", "attn_prep.cu", "attn_common.cuh", "ptx.cuh", "common.cuh")
+TRAFFIC_SOURCES = ("attn_bwd.cu", "attn_fwd.cu", "attn_prep.cu", "attn_dq_stored.cu", "attn_common.cuh", "ptx.cuh",
+                   "common.cuh")
 
 
 def kernel_sources_sha() -> str:

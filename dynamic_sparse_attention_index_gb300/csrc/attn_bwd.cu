@@ -853,8 +853,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 2) tmem_dealloc(tbase, 512);
   if (kMmaProfileKv && threadIdx.x < kWaitSites - 1 && wcyc[threadIdx.x])
     atomicAdd(&P.status->wait_cycles[threadIdx.x], wcyc[threadIdx.x]);
-  if (kMmaProfileKv && threadIdx.x == kWaitSites - 1)
-    atomicAdd(&P.status->wait_cycles[kWaitSites - 1], (unsigned long long)(clock64() - kernel_t0));
+  if (kMmaProfileKv && threadIdx.x == kWaitSites - 1) {
+    const unsigned long long dt = (unsigned long long)(clock64() - kernel_t0);
+    atomicAdd(&P.status->wait_cycles[kWaitSites - 1], dt);
+    // the slowest CTA of the slash launch (the tail of the grid)
+    if (!P.vertical) atomicMax(&P.status->wait_cycles[kWaitSites - 2], dt);
+  }
 }
 
 struct BwdWs {
