@@ -104,6 +104,65 @@ def test_index_budget_fill(wid, L, Hq, Hkv, d, W, density):
         assert ok, bad[:5]
 
 
+# The selection kernel's budget fill first gathers the verticals above a
+# histogram cut (bins of the fp32 bit pattern >> 20, at most 1024 verticals
+# above the cut) and the bands above it (at most 6144); when the set at that
+# cut reaches the target it finishes on those lists, otherwise it searches
+# bit by bit over the full list.  _select_path repeats that decision on the
+# host from the kernel's own masses so a test can show which branch ran.
+_FAST_CAP, _BAND_CAP = 1024, 6144
+
+
+def _select_path(v32, S32, L, bs, density):
+    kv = np.asarray(v32, np.float32).view(np.uint32).astype(np.int64)
+    ks = np.asarray(S32, np.float32).view(np.uint32).astype(np.int64)
+    hist = np.bincount(np.minimum(kv >> 20, 2047), minlength=2048)
+    suf = np.append(np.cumsum(hist[::-1])[::-1], 0)
+    t_low = int(np.flatnonzero(suf <= _FAST_CAP)[0]) << 20
+    Vs = np.flatnonzero(kv >= t_low)
+    Ss = np.concatenate([[0], 1 + np.flatnonzero(ks[1:] >= t_low)])
+    if len(Ss) - 1 > _BAND_CAP:
+        return "bitwise"
+    reach = oracle.active_entries(L, Vs, Ss, bs) >= density * oracle.total_causal_entries(L)
+    return "fast" if reach else "bitwise"
+
+
+def _concentrated_workload(L, Hq, Hkv, d, n_heavy, gain):
+    """The last queries attend to the first n_heavy keys: a shared direction
+    of norm ``gain`` is added to those keys and to the last 64 queries.  The
+    slash bands that meet only the other keys then carry almost no mass."""
+    w = synth.make_workload(1, L=L, Hq=Hq, Hkv=Hkv, d=d)
+    q, k = synth.bf16_bits_to_f64(w.q), synth.bf16_bits_to_f64(w.k)
+    u = np.full(d, gain / np.sqrt(d))
+    k[:n_heavy] += u
+    q[-64:] += u
+    w.q, w.k = synth.f64_to_bf16_bits(q), synth.f64_to_bf16_bits(k)
+    return w
+
+
+@pytest.mark.parametrize("density,path", [(0.01, "fast"), (0.2, "fast"), (0.6, "bitwise"),
+                                          (0.9, "bitwise")])
+def test_index_budget_fill_paths(density, path):
+    """Both branches of the budget fill, on an input whose far bands are
+    nearly empty: the kept sets equal the oracle's selection on the kernel's
+    fp32 masses and the active counts are exact."""
+    w = _concentrated_workload(4096, 2, 1, 64, 1200, 10.0)
+    p, ix = _run(w, density=density)
+    lists = gpu_index_lists(ix, w.Hq)
+    act = ix.active_entries.cpu().numpy()
+    dens32 = float(np.float32(density))
+    for h in range(w.Hq):
+        v32 = ix.v_score[h].cpu().numpy().astype(np.float64)
+        S32 = ix.s_score[h].cpu().numpy().astype(np.float64)
+        assert _select_path(v32, S32, w.L, 64, dens32) == path
+        Vo, So = oracle.select_budget(v32, S32, w.L, 64, dens32)
+        np.testing.assert_array_equal(lists[h][0], Vo)
+        np.testing.assert_array_equal(lists[h][1], So)
+        assert act[h] == oracle.active_entries(w.L, Vo, So, 64)
+        if density == 0.01:
+            assert len(Vo) == 0 and So.tolist() == [0]  # band 0 alone reaches 1 %
+
+
 def test_index_full_size_gqa_128k():
     """The 128K GQA workload (16 query heads, 2 KV heads, d=128) at full size."""
     w = synth.make_workload(3, backward=False)
