@@ -206,6 +206,41 @@ def index_roofline(w, A_index_time_ms, kept, pk, sm_mhz):
                                      else " ex2 rate x SMs x max SM clock")}
 
 
+def xattn_ablation(vs, torch, w, Q, K, dev, stream, pk, stride: int, threshold: float, iters: int = 5):
+    """The anti-diagonal block index (the pages' "w/ XAttn Idx." ablation) on
+    the same RoPE'd Q and K, timed alone after the step's timed region: ms per
+    call, and its tensor work against the bf16 burst peak.  Counted work: the
+    causal strided cells of both passes, 2 x 2 S d FLOP each per head."""
+    W = w.stripes
+    bs = 64 * W
+    S = stride if bs // stride <= 128 else bs // 128
+    px = vs.make_params(w.L, w.Hq, w.Hkv, w.d, stripes=W)
+    xi = vs.XattnBuffers.allocate(px, dev)
+    ws = vs.workspace(px, vs.VS_OP_XATTN, dev)
+    for _ in range(3):
+        vs.vs_xattn_index_build(px, S, threshold, Q, K, xi, ws)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(iters):
+        vs.vs_xattn_index_build(px, S, threshold, Q, K, xi, ws)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / iters
+    R = w.L // S
+    flop = 2.0 * (R * (R + 1) // 2) * 2 * S * w.d * w.Hq
+    tf = flop / (ms * 1e-3) / 1e12
+    act = int(xi.active_entries.sum().item())
+    st = vs.vs_device_status(ws)
+    del xi, ws
+    return {"kernel": "vs_xattn_index_build (two tcgen05 scoring passes, block selection)", "stride": S,
+            "block": bs, "threshold": threshold, "ms": round(ms, 4), "achieved": round(tf, 2), "unit": "TFLOP/s",
+            "bound": "tensor", "peak": pk["bf16_tflops"], "frac": round(tf / pk["bf16_tflops"], 4),
+            "peak_src": pk["src"] + " bf16 burst", "flop": flop,
+            "sparsity": round(1 - act / (w.Hq * w.L * (w.L + 1) / 2), 5),
+            "device_status": vs.vs_status_string(st), "launches_per_call": 3}
+
+
 def run_gpu(args):
     import torch
 
@@ -401,6 +436,10 @@ def run_gpu(args):
     flops = (14.0 if bwd else 4.0) * d * A
     value, e2e_val, ms, e2e_ms = replica_throughput(dist, world, flops, ms, e2e_ms, dev)
     pk = _peaks()
+    xattn = None
+    if args.xattn_stride > 0:
+        # after the timed regions: Q and K hold the last step's rotated inputs
+        xattn = xattn_ablation(vs, torch, w, Q, K, dev, stream, pk, args.xattn_stride, args.xattn_threshold)
     fwd_tf = 4.0 * d * A / (phase["fwd"] * 1e-3) / 1e12
     bwd_tf = 10.0 * d * A / (phase["bwd"] * 1e-3) / 1e12 if bwd else None
     # dominant call: the backward (dK/dV + dQ kernels, 10 d A) when there is
@@ -450,6 +489,7 @@ def run_gpu(args):
         "clocks": clocks,
         "device_status": dev_status,
         **({"dq_path": "stored dS tiles" if dq_stored else "recomputed S and dP"} if bwd and not ring else {}),
+        **({"xattn_index": xattn} if xattn else {}),
     }
     if rank == 0 and not args.no_cpu_baseline:
         rows = max(16, int(args.cpu_rows * (131072 / L) * (16 / Hq)))
@@ -649,6 +689,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--index-mode", default="head", choices=["head", "group"],
                     help="one index per query head (the method) or one per GQA group (union)")
+    ap.add_argument("--xattn-stride", type=int, default=8,
+                    help="stride of the anti-diagonal block index timed after the step (0: skip)")
+    ap.add_argument("--xattn-threshold", type=float, default=0.9)
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)

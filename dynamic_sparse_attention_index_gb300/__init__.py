@@ -8,7 +8,7 @@ library is missing or fails to load, every call raises.
 Entry points mirror the C names: ``vs_workspace_bytes``, ``vs_rope``,
 ``vs_index_build``, ``vs_index_build_noalloc``, ``vs_sparse_attn_fwd``, ``vs_sparse_attn_bwd``,
 ``vs_sparse_attn_fwd_rows``, ``vs_striped_ring_fwd``, ``vs_striped_ring_bwd``, ``vs_device_status``,
-``vs_status_string``.
+``vs_status_string``, ``vs_xattn_index_build``.
 """
 from __future__ import annotations
 
@@ -20,12 +20,12 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libvs.so")
 
 VS_OK, VS_ERR_INVALID_ARG, VS_ERR_UNSUPPORTED, VS_ERR_WORKSPACE, VS_ERR_CUDA, VS_ERR_TIMEOUT, VS_ERR_BOUNDS = range(7)
-VS_OP_INDEX, VS_OP_FWD, VS_OP_BWD, VS_OP_ROPE, VS_OP_RING_FWD, VS_OP_RING_BWD, VS_OP_BWD_MIN = range(7)
+VS_OP_INDEX, VS_OP_FWD, VS_OP_BWD, VS_OP_ROPE, VS_OP_RING_FWD, VS_OP_RING_BWD, VS_OP_BWD_MIN, VS_OP_XATTN = range(8)
 
 #: every symbol the header declares
 EXPORTED = ("vs_workspace_bytes", "vs_status_string", "vs_rope", "vs_index_build",
             "vs_index_build_noalloc", "vs_sparse_attn_fwd", "vs_sparse_attn_bwd", "vs_device_status",
-            "vs_striped_ring_fwd", "vs_striped_ring_bwd", "vs_sparse_attn_fwd_rows")
+            "vs_striped_ring_fwd", "vs_striped_ring_bwd", "vs_sparse_attn_fwd_rows", "vs_xattn_index_build")
 
 #: size of the static scratch behind vs_index_build_noalloc (VS_INDEX_NOALLOC_SCRATCH_BYTES)
 INDEX_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -51,6 +51,13 @@ class vs_index(ctypes.Structure):
     _fields_ = [
         ("v_idx", ctypes.c_void_p), ("v_cnt", ctypes.c_void_p), ("s_idx", ctypes.c_void_p),
         ("s_cnt", ctypes.c_void_p), ("v_score", ctypes.c_void_p), ("s_score", ctypes.c_void_p),
+        ("active_entries", ctypes.c_void_p),
+    ]
+
+
+class vs_xattn_index(ctypes.Structure):
+    _fields_ = [
+        ("block_score", ctypes.c_void_p), ("block_mask", ctypes.c_void_p), ("block_cnt", ctypes.c_void_p),
         ("active_entries", ctypes.c_void_p),
     ]
 
@@ -81,9 +88,11 @@ def lib() -> ctypes.CDLL:
         L.vs_striped_ring_fwd.argtypes = [P, I, VP, VP, VP, VP, VP, VP, SZ, EV, i32, VP]
         L.vs_sparse_attn_fwd_rows.argtypes = [P, I, VP, VP, VP, VP, VP, VP, SZ, i32, i32, VP]
         L.vs_striped_ring_bwd.argtypes = [P, I, VP, VP, VP, VP, VP, VP, VP, VP, VP, VP, SZ, EV, i32, VP]
+        L.vs_xattn_index_build.argtypes = [P, i32, ctypes.c_float, VP, VP, ctypes.POINTER(vs_xattn_index), VP,
+                                           SZ, VP]
         for f in ("vs_rope", "vs_index_build", "vs_index_build_noalloc", "vs_sparse_attn_fwd",
                   "vs_sparse_attn_bwd", "vs_device_status", "vs_striped_ring_fwd", "vs_striped_ring_bwd",
-                  "vs_sparse_attn_fwd_rows"):
+                  "vs_sparse_attn_fwd_rows", "vs_xattn_index_build"):
             getattr(L, f).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -150,6 +159,38 @@ class IndexBuffers:
         return vs_index(*[(t.data_ptr() if t is not None else None) for t in
                           (self.v_idx, self.v_cnt, self.s_idx, self.s_cnt, self.v_score, self.s_score,
                            self.active_entries)])
+
+
+@dataclass
+class XattnBuffers:
+    """Device arrays of one anti-diagonal block index (``vs_xattn_index``)."""
+    block_score: object
+    block_mask: object
+    block_cnt: object = None
+    active_entries: object = None
+
+    @classmethod
+    def allocate(cls, p: vs_params, device):
+        import torch
+        nb = p.L // (p.block * p.stripes)
+        nw = (nb + 31) // 32
+        return cls(block_score=torch.empty((p.Hq, nb, nb), dtype=torch.float32, device=device),
+                   block_mask=torch.empty((p.Hq, nb, nw), dtype=torch.int32, device=device),
+                   block_cnt=torch.empty((p.Hq, nb), dtype=torch.int32, device=device),
+                   active_entries=torch.zeros(p.Hq, dtype=torch.int64, device=device))
+
+    def c(self) -> vs_xattn_index:
+        return vs_xattn_index(*[(t.data_ptr() if t is not None else None) for t in
+                                (self.block_score, self.block_mask, self.block_cnt, self.active_entries)])
+
+    def kept_blocks(self):
+        """Host lists: per head, per block row I, the ascending kept block
+        columns (decoded from the mask words)."""
+        import numpy as np
+        m = self.block_mask.cpu().numpy().view(np.uint32)
+        Hq, nb, nw = m.shape
+        bits = ((m[..., :, None] >> np.arange(32, dtype=np.uint32)) & 1).reshape(Hq, nb, nw * 32)[..., :nb]
+        return [[np.flatnonzero(bits[h, I]).astype(np.int64) for I in range(nb)] for h in range(Hq)]
 
 
 def workspace(p: vs_params, op: int, device):
@@ -229,3 +270,10 @@ def vs_striped_ring_bwd(p: vs_params, index: IndexBuffers, Q, K, V, O, lse, dO, 
 
 def vs_device_status(ws, stream=None) -> int:
     return int(lib().vs_device_status(_ptr(ws), _stream(stream)))
+
+
+def vs_xattn_index_build(p: vs_params, stride: int, threshold: float, Q, K, index: XattnBuffers, ws, stream=None):
+    ix = index.c()
+    _check(lib().vs_xattn_index_build(ctypes.byref(p), int(stride), float(threshold), _ptr(Q), _ptr(K),
+                                      ctypes.byref(ix), _ptr(ws), ws.numel(), _stream(stream)),
+           "vs_xattn_index_build")

@@ -30,6 +30,8 @@ cudaError_t launch_ring_bwd(const vs_params& p, const vs_index& ix, const void* 
                             const void* O, const float* lse, const void* dO, void* dQ, void* dK, void* dV, void* ws,
                             void* const* ev, int n_ev, cudaStream_t st);
 
+size_t xattn_select_smem(int nb);
+
 bool test_stall_requested() {
   const char* v = std::getenv("VS_TEST_STALL_PRODUCERS");
   return v && std::atoi(v) == 1;
@@ -99,6 +101,23 @@ IndexWs index_ws(const vs_params& p) {
   return o;
 }
 
+struct XattnWs {
+  size_t status, rs, cnt, active, total;
+};
+
+// Sized for any stride (stride 1 has the most strided rows, L per head).
+XattnWs xattn_ws(const vs_params& p) {
+  const size_t nb = (size_t)p.L / ((size_t)kBlock * p.stripes);
+  WsLayout w;
+  XattnWs o;
+  o.status = w.take(sizeof(DevStatus));
+  o.rs = w.take((size_t)p.Hq * p.L * sizeof(float2));
+  o.cnt = w.take((size_t)p.Hq * nb * sizeof(int32_t));
+  o.active = w.take((size_t)p.Hq * sizeof(unsigned long long));
+  o.total = w.off;
+  return o;
+}
+
 vs_status check_ws(const void* ws, size_t ws_bytes, size_t need) {
   if (!ws) return VS_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return VS_ERR_WORKSPACE;
@@ -147,6 +166,7 @@ size_t vs_workspace_bytes(const vs_params* p, int op) {
   if (op == VS_OP_BWD_MIN) return p->d == 128 ? attn_bwd_ws_bytes(*p) : 0;
   if (op == VS_OP_RING_FWD) return ring_ws_bytes(*p, false);
   if (op == VS_OP_RING_BWD) return p->d == 128 ? ring_ws_bytes(*p, true) : 0;
+  if (op == VS_OP_XATTN) return xattn_ws(*p).total;
   return 0;
 }
 
@@ -239,6 +259,58 @@ vs_status vs_index_build(const vs_params* p, const void* Q, const void* K, const
   if (launch_select(a, s) != cudaSuccess) return VS_ERR_CUDA;
   if (p->index_mode == 1 && launch_group_union(*p, *out, s) != cudaSuccess) return VS_ERR_CUDA;
   return VS_OK;
+}
+
+vs_status vs_xattn_index_build(const vs_params* p, int32_t stride, float threshold, const void* Q, const void* K,
+                               const vs_xattn_index* out, void* ws, size_t ws_bytes, void* stream) {
+  NvtxRange nvtx("vs_xattn_index_build");
+  vs_status st = check_params(p);
+  if (st != VS_OK) return st;
+  if (!Q || !K || !aligned16(Q) || !aligned16(K)) return VS_ERR_INVALID_ARG;
+  if (!out || !out->block_score || !out->block_mask) return VS_ERR_INVALID_ARG;
+  const void* ptrs[] = {out->block_score, out->block_mask, out->block_cnt, out->active_entries};
+  for (const void* q : ptrs)
+    if (q && !aligned16(q)) return VS_ERR_INVALID_ARG;
+  if (!(threshold > 0.f && threshold <= 1.f)) return VS_ERR_INVALID_ARG;
+  const int bs = kBlock * p->stripes;
+  // the stride divides the block edge; a block has 4 .. 128 strided rows
+  if (stride < 1 || (stride & (stride - 1)) != 0 || bs % stride != 0) return VS_ERR_INVALID_ARG;
+  const int bsS = bs / stride;
+  if (bsS < 4 || bsS > 128 || (bsS & (bsS - 1)) != 0) return VS_ERR_UNSUPPORTED;
+  const int nb = p->L / bs;
+  if (xattn_select_smem(nb) > 227 * 1024 - 8192) return VS_ERR_UNSUPPORTED;
+  const XattnWs lay = xattn_ws(*p);
+  if ((st = check_ws(ws, ws_bytes, lay.total)) != VS_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  if (cudaMemsetAsync(w + lay.status, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
+  XaArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.Q = Q;
+  a.K = K;
+  a.L = p->L;
+  a.Hq = p->Hq;
+  a.Hkv = p->Hkv;
+  a.G = p->Hq / p->Hkv;
+  a.d = p->d;
+  a.S = stride;
+  a.R = p->L / stride;
+  a.nrt = (a.R + 127) / 128;
+  a.bs = bs;
+  a.bsS = bsS;
+  a.nb = nb;
+  a.nw = (nb + 31) / 32;
+  a.c2 = default_scale(*p) * 1.4426950408889634f / (float)stride;
+  a.inv_bsS = 1.0f / (float)bsS;
+  a.threshold = threshold;
+  a.rs = reinterpret_cast<float2*>(w + lay.rs);
+  a.X = out->block_score;
+  a.mask = out->block_mask;
+  a.cnt = out->block_cnt ? out->block_cnt : reinterpret_cast<int32_t*>(w + lay.cnt);
+  a.active = out->active_entries ? reinterpret_cast<unsigned long long*>(out->active_entries)
+                                 : reinterpret_cast<unsigned long long*>(w + lay.active);
+  a.status = reinterpret_cast<DevStatus*>(w + lay.status);
+  return launch_xattn(a, s) == cudaSuccess ? VS_OK : VS_ERR_CUDA;
 }
 
 // ---------------------------------------------------------------------------

@@ -222,5 +222,9 @@ cudaError_t launch_dq_stored(const vs_params& p, const AttnGeom& g, const PrepPt
 // shard of the striped layout) as L consecutive rows.
 bool make_map_heads(CUtensorMap* m, const void* base, int L, int H, int d, int tok_mul = 1, int tok_add = 0);
 bool make_map_rows(CUtensorMap* m, const void* base, long long rows, int d);
+// make_map_strided views [L][H][d] with token t = c * S + j as element
+// (channel, j * H + h, c): row c of the box at middle coordinate j * H + h is
+// head h's token c * S + j (R = L / S rows).
+bool make_map_strided(CUtensorMap* m, const void* base, int R, int H, int d, int S);
 
 }  // namespace vs

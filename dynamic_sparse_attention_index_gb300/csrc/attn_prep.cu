@@ -162,6 +162,19 @@ bool make_map_heads(CUtensorMap* m, const void* base, int L, int H, int d, int t
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_map_strided(CUtensorMap* m, const void* base, int R, int H, int d, int S) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  // element (x, j * H + h, c) is channel x of head h at token c * S + j
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)S * H, (cuuint64_t)R};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)S * H * d * 2};
+  cuuint32_t box[3] = {64, 1, 64};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool make_map_rows(CUtensorMap* m, const void* base, long long rows, int d) {
   auto enc = encode_fn();
   if (!enc) return false;

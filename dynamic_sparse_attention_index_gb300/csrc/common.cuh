@@ -94,7 +94,10 @@ __device__ __forceinline__ void report_timeout_first(DevStatus* st, int where) {
     atomicExch(&st->where, where);
 }
 // kernel tags of the status word's wait site
-enum : int { kTagForward = 1, kTagDq = 2, kTagDkdvVertical = 3, kTagDkdvSlash = 4, kTagDqStored = 5, kTagIndex = 6 };
+enum : int {
+  kTagForward = 1, kTagDq = 2, kTagDkdvVertical = 3, kTagDkdvSlash = 4, kTagDqStored = 5, kTagIndex = 6,
+  kTagXattn = 7
+};
 
 __host__ __device__ constexpr size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
@@ -161,5 +164,24 @@ struct IxTcGrid {
 IxTcGrid index_tc_grid(int L, int Hq, int Hkv);
 bool index_tc_supported(const IndexArgs& a);
 void index_grid(const vs_params& p, int* tiles_per_chunk, int* nchunk, int* row_splits);
+
+// Anti-diagonal block scorer (vs_xattn_index_build).
+struct XaArgs {
+  const void* Q;
+  const void* K;
+  int32_t L, Hq, Hkv, G, d;
+  int32_t S, R, nrt;           // stride, strided rows L / S, 128-row tiles of them
+  int32_t bs, bsS, nb, nw;     // block edge, strided rows per block, blocks per row, mask words per row
+  float c2;                    // softmax scale * log2(e) / S
+  float inv_bsS;
+  float threshold;
+  float2* rs;                  // [Hq][R] (max, sum) per strided row, log2 domain
+  float* X;                    // [Hq][nb][nb] block scores
+  uint32_t* mask;              // [Hq][nb][nw] kept-block bits
+  int32_t* cnt;                // [Hq][nb] kept blocks per block row
+  unsigned long long* active;  // [Hq] causal entries inside the kept blocks
+  DevStatus* status;
+};
+cudaError_t launch_xattn(const XaArgs& a, cudaStream_t s);
 
 }  // namespace vs

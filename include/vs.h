@@ -96,6 +96,19 @@ typedef struct vs_index {
   int64_t* active_entries; /* optional [Hq] exact active (n, m) entries per head             */
 } vs_index;
 
+/*
+ * Block index of the anti-diagonal scorer (vs_xattn_index_build), per query
+ * head h, with bs = block * stripes, nb = L / bs blocks per row and
+ * nw = (nb + 31) / 32 mask words per block row (all DEVICE pointers,
+ * caller-owned, 16-byte aligned).
+ */
+typedef struct vs_xattn_index {
+  float* block_score;      /* [Hq][nb][nb] X[h][I][J]; zero above the diagonal (J > I)               */
+  uint32_t* block_mask;    /* [Hq][nb][nw] bit J & 31 of word J >> 5 of row I: block (I, J) kept     */
+  int32_t* block_cnt;      /* optional [Hq][nb] kept blocks of each block row (diagonal included)    */
+  int64_t* active_entries; /* optional [Hq] causal (n, m) entries inside the kept blocks              */
+} vs_xattn_index;
+
 enum {
   VS_OP_INDEX = 0,
   VS_OP_FWD = 1,
@@ -103,7 +116,8 @@ enum {
   VS_OP_ROPE = 3,
   VS_OP_RING_FWD = 4,
   VS_OP_RING_BWD = 5,
-  VS_OP_BWD_MIN = 6  /* the least workspace vs_sparse_attn_bwd accepts (dS recomputed for dQ)    */
+  VS_OP_BWD_MIN = 6, /* the least workspace vs_sparse_attn_bwd accepts (dS recomputed for dQ)   */
+  VS_OP_XATTN = 7    /* vs_xattn_index_build (any stride)                                       */
 };
 
 /* Bytes of scratch `op` needs for problem `p` (0 if p is invalid). */
@@ -137,6 +151,33 @@ VS_API vs_status vs_rope(const vs_params* p, int32_t H, const void* x, void* y, 
  */
 VS_API vs_status vs_index_build(const vs_params* p, const void* Q, const void* K, const vs_index* out, void* ws,
                          size_t ws_bytes, void* stream);
+
+/*
+ * Anti-diagonal block index, an alternative to the vertical-slash index (the
+ * ablation row "MTraining w/ XAttn Idx." of the MTraining review, section
+ * 五 "实验结果", table "训练效率结果"; the pages only name it: this is the
+ * published XAttention block scorer).  With S = stride, strided row r groups
+ * query tokens rS .. rS+S-1 and strided column c key tokens cS .. cS+S-1;
+ *   z[r, c] = scale / S * sum_j q[rS + j] . k[cS + S-1-j]   (the mean logit on
+ *             the anti-diagonal of the S x S sub-block), cells c > r masked,
+ *   P = softmax of z over each strided row,
+ *   X[h][I][J] = (S / bs) * sum of P over the cells of block (I, J)
+ *             (bs-token blocks; every block row sums to 1),
+ * and each block row I keeps the smallest descending prefix of
+ * X[h][I][0..I] (ties: lower J first) reaching `threshold` of the row's
+ * total, plus the diagonal block I (threshold = 1 keeps every block of
+ * positive score).  Uses L, Hq, Hkv, d, stripes (bs = 64 * stripes, the tile
+ * of the striped-layout emulation) and softmax_scale of *p; Q [L][Hq][d] and
+ * K [L][Hkv][d] bf16 as elsewhere.
+ * Errors: VS_ERR_INVALID_ARG for a stride that is not a power of two
+ * dividing bs, a threshold outside (0, 1] or a missing output;
+ * VS_ERR_UNSUPPORTED unless 4 <= bs / stride <= 128.  Workspace:
+ * vs_workspace_bytes(p, VS_OP_XATTN) bytes (any stride).  Fills every
+ * non-NULL field of *out.
+ */
+VS_API vs_status vs_xattn_index_build(const vs_params* p, int32_t stride, float threshold, const void* Q,
+                                      const void* K, const vs_xattn_index* out, void* ws, size_t ws_bytes,
+                                      void* stream);
 
 /*
  * Variant of vs_index_build that allocates nothing and takes no workspace.

@@ -130,3 +130,41 @@ def test_bwd_workspace_sizes():
     assert Hq * cap * 8192 + tables <= extra <= Hq * cap * 8192 + tables + 4 * 256
     big = vs.make_params(1 << 20, 32, 8, 128, density=0.05)
     assert vs.vs_workspace_bytes(big, vs.VS_OP_BWD) == vs.vs_workspace_bytes(big, vs.VS_OP_BWD_MIN)
+
+
+def _call_xattn(vs, p, stride=8, thr=0.9, q=FAKE, k=FAKE, ws=FAKE, ws_bytes=1 << 40, out=None):
+    if out is None:
+        out = vs.vs_xattn_index(FAKE, FAKE, None, None)
+    return vs.lib().vs_xattn_index_build(ctypes.byref(p), stride, thr, q, k, ctypes.byref(out), ws, ws_bytes, None)
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(stride=3), "VS_ERR_INVALID_ARG"),        # not a power of two
+    (dict(stride=0), "VS_ERR_INVALID_ARG"),
+    (dict(stride=128), "VS_ERR_INVALID_ARG"),      # does not divide bs = 64
+    (dict(stride=32), "VS_ERR_UNSUPPORTED"),       # two strided rows per block
+    (dict(thr=0.0), "VS_ERR_INVALID_ARG"),
+    (dict(thr=1.5), "VS_ERR_INVALID_ARG"),
+    (dict(q=None), "VS_ERR_INVALID_ARG"),
+    (dict(k=FAKE + 8), "VS_ERR_INVALID_ARG"),
+    (dict(ws=None), "VS_ERR_WORKSPACE"),
+    (dict(ws_bytes=1024), "VS_ERR_WORKSPACE"),
+])
+def test_xattn_rejects_bad_args(vs, kw, code):
+    p = vs.make_params(4096, 4, 2, 128)
+    assert _call_xattn(vs, p, **kw) == getattr(vs, code)
+
+
+def test_xattn_rejects_missing_outputs_and_sizes_workspace(vs):
+    p = vs.make_params(4096, 4, 2, 128)
+    assert _call_xattn(vs, p, out=vs.vs_xattn_index(None, FAKE, None, None)) == vs.VS_ERR_INVALID_ARG
+    assert _call_xattn(vs, p, out=vs.vs_xattn_index(FAKE, None, None, None)) == vs.VS_ERR_INVALID_ARG
+    assert _call_xattn(vs, p, out=vs.vs_xattn_index(FAKE, FAKE, FAKE + 4, None)) == vs.VS_ERR_INVALID_ARG
+    # stride 1 (full-resolution cells, 64 rows per block) is accepted up to the argument checks
+    n = vs.vs_workspace_bytes(p, vs.VS_OP_XATTN)
+    assert n >= 4 * 4096 * 8  # a (max, sum) per strided row at stride 1
+    assert _call_xattn(vs, p, stride=1, ws_bytes=n - 256) == vs.VS_ERR_WORKSPACE
+    # striped tiles: bs = 64 W, the stride must keep 4 .. 128 strided rows per block
+    p32 = vs.make_params(65536, 2, 1, 128, stripes=32)
+    assert _call_xattn(vs, p32, stride=8) == vs.VS_ERR_UNSUPPORTED  # 256 rows per block
+    assert vs.vs_workspace_bytes(vs.make_params(4096, 4, 3, 128), vs.VS_OP_XATTN) == 0
