@@ -30,8 +30,6 @@ cudaError_t launch_ring_bwd(const vs_params& p, const vs_index& ix, const void* 
                             const void* O, const float* lse, const void* dO, void* dQ, void* dK, void* dV, void* ws,
                             void* const* ev, int n_ev, cudaStream_t st);
 
-size_t xattn_select_smem(int nb);
-
 bool test_stall_requested() {
   const char* v = std::getenv("VS_TEST_STALL_PRODUCERS");
   return v && std::atoi(v) == 1;
@@ -278,7 +276,6 @@ vs_status vs_xattn_index_build(const vs_params* p, int32_t stride, float thresho
   const int bsS = bs / stride;
   if (bsS < 4 || bsS > 128 || (bsS & (bsS - 1)) != 0) return VS_ERR_UNSUPPORTED;
   const int nb = p->L / bs;
-  if (xattn_select_smem(nb) > 227 * 1024 - 8192) return VS_ERR_UNSUPPORTED;
   const XattnWs lay = xattn_ws(*p);
   if ((st = check_ws(ws, ws_bytes, lay.total)) != VS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

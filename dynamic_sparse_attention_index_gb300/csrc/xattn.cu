@@ -34,9 +34,10 @@
 // One CTA per (128-row tile, head), heaviest tiles first; a loader warp
 // streams (Q' 64-feature slab, K' 64-feature slab) stages through a
 // four-deep ring, one thread issues the MMAs, four warps read TMEM.
-// The selection kernel sorts each block row's scores (bitonic, in shared
-// memory), sums them as exact 64-bit fixed-point integers in the sorted
-// order, and keeps the shortest prefix reaching the threshold.
+// The selection kernel gives each block row one warp, which finds the
+// row's threshold score by a radix descent over exact 64-bit fixed-point
+// sums (no sort) and keeps the scores above it, then ties in index order,
+// up to the threshold's share.
 #include "attn_common.cuh"
 #include "ptx.cuh"
 
@@ -60,8 +61,14 @@ __device__ __forceinline__ float xa_exp2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+__device__ __forceinline__ float xa_log2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
-template <int D, bool kPass2>
+// kBsS: strided rows per block (pass 2 only; 0 in pass 1)
+template <int D, bool kPass2, int kBsS>
 __global__ void __launch_bounds__(kXaThreads, 1)
     xattn_score_kernel(const __grid_constant__ CUtensorMap mQ, const __grid_constant__ CUtensorMap mK,
                        const XaArgs a) {
@@ -186,7 +193,7 @@ __global__ void __launch_bounds__(kXaThreads, 1)
     const float c2 = a.c2;
     // columns c < climit hold this row's causal cells (none for rows past R)
     const int climit = r < a.R ? r + 1 : 0;
-    if (!kPass2) {
+    if constexpr (!kPass2) {
       float m = kXaNegInf, l = 0.f;
       for (int st = 0; st < nst; ++st) {
         if (!wait_warp(&acc_full[st & 1], (st >> 1) & 1, 4)) break;
@@ -228,17 +235,15 @@ __global__ void __launch_bounds__(kXaThreads, 1)
       }
       if (r < a.R && !*abort_flag) a.rs[(size_t)h * a.R + r] = make_float2(m, l);
     } else {
-      // the row's (max, 1 / sum) from pass 1
-      float M = 0.f, inv = 0.f;
+      // the row's log2 normaliser from pass 1: p = exp2(z c2 - (max + log2 sum))
+      float Mn = 0.f;
       if (r < a.R) {
         const float2 t = a.rs[(size_t)h * a.R + r];
-        M = t.x;
-        inv = t.y > 0.f ? 1.0f / t.y : 0.f;
+        Mn = t.x + xa_log2(t.y);
       }
-      const int bsS = a.bsS;
-      int lb = 0;
-      while ((1 << lb) < bsS) ++lb;
-      float* Xrow = a.X + ((size_t)h * a.nb + (r < a.R ? r >> lb : 0)) * a.nb;
+      constexpr int kLb = kBsS <= 4 ? 2 : kBsS <= 8 ? 3 : kBsS <= 16 ? 4 : kBsS <= 32 ? 5 : kBsS <= 64 ? 6 : 7;
+      constexpr int kNb = 128 / kBsS;  // block columns per 128-column half
+      float* Xrow = a.X + ((size_t)h * a.nb + (r < a.R ? r >> kLb : 0)) * a.nb;
       int rb = 0;
       // Every epilogue warp runs all nst x 2 iterations (a failed wait only
       // skips the work), so the named barrier of the 64- and 128-row blocks
@@ -249,8 +254,9 @@ __global__ void __launch_bounds__(kXaThreads, 1)
 #pragma unroll 1
         for (int half = 0; half < 2; ++half) {
           const int c0 = st * 256 + half * 128;
-          uint32_t x[128];
+          float v[kNb];
           if (ok) {
+            uint32_t x[128];
 #pragma unroll
             for (int cc = 0; cc < 128; cc += 32)
               tmem_ld32(tbase + (uint32_t)((st & 1) * 256 + half * 128 + cc) + lane_off, x + cc);
@@ -261,36 +267,61 @@ __global__ void __launch_bounds__(kXaThreads, 1)
               if (lane == 0) mbar_arrive(&acc_free[st & 1]);
             }
             const int lim = climit - c0;
+            if (__all_sync(0xffffffffu, lim >= 128)) {
 #pragma unroll
-            for (int j = 0; j < 128; ++j)
-              x[j] = __float_as_uint(j < lim ? xa_exp2(fmaf(__uint_as_float(x[j]), c2, -M)) * inv : 0.f);
+              for (int j = 0; j < 128; ++j) x[j] = __float_as_uint(xa_exp2(fmaf(__uint_as_float(x[j]), c2, -Mn)));
+            } else {
+#pragma unroll
+              for (int j = 0; j < 128; ++j)
+                x[j] = __float_as_uint(j < lim ? xa_exp2(fmaf(__uint_as_float(x[j]), c2, -Mn)) : 0.f);
+            }
             // block-column sums: after level t, x[j] (j a multiple of 2^(t+1))
             // holds the sum of columns j .. j + 2^(t+1) - 1
 #pragma unroll
-            for (int t = 0; t < 7; ++t)
-              if (t < lb) {
+            for (int t = 0; t < kLb; ++t)
 #pragma unroll
-                for (int j = 0; j < 128; j += 2 << t)
-                  x[j] = __float_as_uint(__uint_as_float(x[j]) + __uint_as_float(x[j + (1 << t)]));
-              }
+              for (int j = 0; j < 128; j += 2 << t)
+                x[j] = __float_as_uint(__uint_as_float(x[j]) + __uint_as_float(x[j + (1 << t)]));
+#pragma unroll
+            for (int b = 0; b < kNb; ++b) v[b] = __uint_as_float(x[b * kBsS]);
           }
-          const int jb0 = c0 >> lb;  // block column of this half's first block
-          if (bsS <= 32) {
-            // a block's rows are bsS consecutive lanes
+          const int jb0 = c0 >> kLb;  // block column of this half's first block
+          if constexpr (kBsS <= 32) {
+            // a block's rows are kBsS consecutive lanes: reduce-scatter the
+            // kNb block sums across them, halving the list per exchange
             if (ok) {
+              int base = 0;  // first block column held by this lane
+              constexpr int kSteps = kLb < (kNb > 1 ? __builtin_ctz(kNb) : 0) ? kLb : (kNb > 1 ? __builtin_ctz(kNb) : 0);
 #pragma unroll
-              for (int j = 0; j < 128; j += 4)
-                if ((j & (bsS - 1)) == 0) {
-                  float v = __uint_as_float(x[j]);
-                  for (int o = 1; o < bsS; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-                  const int J = jb0 + (j >> lb);
-                  if ((lane & (bsS - 1)) == 0 && r < a.R && J < a.nb) Xrow[J] = v * a.inv_bsS;
+              for (int sstep = 0; sstep < kSteps; ++sstep) {
+                const int o = kBsS >> (sstep + 1);
+                const int cnt = kNb >> sstep, hlf = cnt >> 1;
+                const bool upper = (lane & o) != 0;
+#pragma unroll
+                for (int i = 0; i < hlf; ++i) {
+                  const float send = upper ? v[i] : v[i + hlf];
+                  const float keep = upper ? v[i + hlf] : v[i];
+                  v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
                 }
+                if (upper) base += hlf;
+              }
+              constexpr int kLeft = kNb >> kSteps;  // block sums held per lane
+              // lanes still sharing those blocks: the lower offsets not used
+              constexpr int kRest = kBsS >> kSteps;
+#pragma unroll
+              for (int o = kRest >> 1; o > 0; o >>= 1)
+#pragma unroll
+                for (int i = 0; i < kLeft; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+              if ((lane & (kRest - 1)) == 0 && r < a.R) {
+#pragma unroll
+                for (int i = 0; i < kLeft; ++i)
+                  if (jb0 + base + i < a.nb) Xrow[jb0 + base + i] = v[i] * a.inv_bsS;
+              }
             }
           } else {
             // 64 rows (two warps) or 128 rows (four warps) per block: warp
             // sums through shared memory, added in warp order by warp 4
-            float v0 = ok ? __uint_as_float(x[0]) : 0.f, v1 = ok ? __uint_as_float(x[64]) : 0.f;
+            float v0 = ok ? v[0] : 0.f, v1 = (ok && kNb > 1) ? v[kNb > 1 ? 1 : 0] : 0.f;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
               v0 += __shfl_xor_sync(0xffffffffu, v0, o);
@@ -303,15 +334,15 @@ __global__ void __launch_bounds__(kXaThreads, 1)
             }
             asm volatile("bar.sync 1, 128;" ::: "memory");
             if (ok && q == 0) {
-              if (bsS == 64 && lane < 4) {
+              if (kBsS == 64 && lane < 4) {
                 const int br = lane >> 1, bc = lane & 1;  // block row in the tile, block column in the half
-                const float v = rbuf[(2 * br) * 2 + bc] + rbuf[(2 * br + 1) * 2 + bc];
+                const float sum = rbuf[(2 * br) * 2 + bc] + rbuf[(2 * br + 1) * 2 + bc];
                 const int Ib = (r0 >> 6) + br, Jb = jb0 + bc;
-                if (Ib * 64 < a.R && Jb < a.nb) a.X[((size_t)h * a.nb + Ib) * a.nb + Jb] = v * a.inv_bsS;
-              } else if (bsS == 128 && lane == 0) {
-                const float v = ((rbuf[0] + rbuf[2]) + rbuf[4]) + rbuf[6];
+                if (Ib * 64 < a.R && Jb < a.nb) a.X[((size_t)h * a.nb + Ib) * a.nb + Jb] = sum * a.inv_bsS;
+              } else if (kBsS == 128 && lane == 0) {
+                const float sum = ((rbuf[0] + rbuf[2]) + rbuf[4]) + rbuf[6];
                 const int Ib = r0 >> 7, Jb = jb0;
-                if (Ib * 128 < a.R && Jb < a.nb) a.X[((size_t)h * a.nb + Ib) * a.nb + Jb] = v * a.inv_bsS;
+                if (Ib * 128 < a.R && Jb < a.nb) a.X[((size_t)h * a.nb + Ib) * a.nb + Jb] = sum * a.inv_bsS;
               }
             }
             rb ^= 1;
@@ -327,117 +358,193 @@ __global__ void __launch_bounds__(kXaThreads, 1)
   if (warp == 2) tmem_dealloc(tbase, 512);
 }
 
-// Block-wide sum and exclusive scan of 64-bit integers (256 threads).
-__device__ unsigned long long xa_block_sum(unsigned long long v, unsigned long long* wbuf) {
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  __syncthreads();
-  if (lane == 0) wbuf[warp] = v;
-  __syncthreads();
-  unsigned long long t = 0;
-  for (int w = 0; w < kXaThreads / 32; ++w) t += wbuf[w];
-  return t;
-}
-__device__ unsigned long long xa_block_exscan(unsigned long long v, unsigned long long* wbuf) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  unsigned long long inc = v;
-  for (int o = 1; o < 32; o <<= 1) {
-    const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += y;
-  }
-  __syncthreads();
-  if (lane == 31) wbuf[warp] = inc;
-  __syncthreads();
-  unsigned long long before = 0;
-  for (int w = 0; w < warp; ++w) before += wbuf[w];
-  return before + inc - v;
+// A score as an exact fixed-point integer: x * 2^60, truncated (a block
+// row's scores sum to about 1, so every partial sum stays below 2^62).
+__device__ __forceinline__ unsigned long long xa_quant(uint32_t key) {
+  return (unsigned long long)__float2ull_rz(ldexpf(__uint_as_float(key), 60));
 }
 
-// One CTA per (block row I, head h): the kept block columns of row I.
-// Sort keys: (score bits << 32) | (2^32 - 1 - J), sorted descending, so equal
-// scores come lower J first; scores are non-negative fp32, whose bit
-// patterns order like the values.
+__device__ __forceinline__ unsigned long long xa_warp_sum(unsigned long long v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+constexpr int kSelWarps = kXaThreads / 32;  // block rows per CTA, one per warp
+
+// Per-warp histogram of one radix level (8-bit digits).
+struct XaWarpHist {
+  unsigned long long sum[256];
+  uint32_t cnt[256];
+  uint32_t key[256];  // a key that fell into the bin (exact when the bin holds one)
+};
+
+// One warp per (block row I, head h): the kept block columns of row I.
+// Scores are non-negative fp32, so their bit patterns order like the
+// values.  A most-significant-digit-first radix descent (four 8-bit digits)
+// over per-warp histograms of counts and fixed-point sums finds the
+// threshold key t: the scores above t sum to less than the target and those
+// at or above it reach it.  All scores above t are kept, then the scores
+// equal to t in index order until the target is reached (the lower block
+// column first among equal scores, as in a stable descending sort).  The
+// row is read from global memory (L2) at every level; no block barriers.
 __global__ void __launch_bounds__(kXaThreads) xattn_select_kernel(const XaArgs a) {
-  extern __shared__ unsigned long long xa_keys[];
-  __shared__ unsigned long long wbuf[kXaThreads / 32];
-  __shared__ uint32_t words[512];
-  __shared__ int kfirst;
-  const int I = blockIdx.x, h = blockIdx.y;
+  __shared__ XaWarpHist hist[kSelWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int I = blockIdx.x * kSelWarps + warp, h = blockIdx.y;
+  if (I >= a.nb) return;
+  XaWarpHist& H = hist[warp];
   const int n = I + 1;
-  int npad = 1;
-  while (npad < n) npad <<= 1;
-  const float* row = a.X + ((size_t)h * a.nb + I) * a.nb;
-  for (int j = threadIdx.x; j < npad; j += kXaThreads)
-    xa_keys[j] = j < n ? ((unsigned long long)__float_as_uint(row[j]) << 32) | (unsigned long long)(0xffffffffu - (uint32_t)j)
-                       : 0ull;
-  for (int w = threadIdx.x; w < a.nw; w += kXaThreads) words[w] = 0u;
-  if (threadIdx.x == 0) kfirst = n;
-  __syncthreads();
-  // bitonic sort, descending
-  for (int k = 2; k <= npad; k <<= 1)
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      for (int i = threadIdx.x; i < npad; i += kXaThreads) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const unsigned long long u = xa_keys[i], v = xa_keys[ixj];
-          if ((i & k) == 0 ? (u < v) : (u > v)) {
-            xa_keys[i] = v;
-            xa_keys[ixj] = u;
-          }
-        }
-      }
-      __syncthreads();
-    }
-  // scores as exact fixed-point integers: x * 2^60, truncated (a block row's
-  // scores sum to about 1, so every partial sum stays below 2^62)
-  auto quant = [](unsigned long long key) -> unsigned long long {
-    return (unsigned long long)__float2ull_rz(ldexpf(__uint_as_float((uint32_t)(key >> 32)), 60));
-  };
-  // each thread owns a run of consecutive sorted positions
-  const int seg = (npad + kXaThreads - 1) / kXaThreads;
-  const int b0 = (int)threadIdx.x * seg, b1 = min(b0 + seg, n);
-  unsigned long long mine = 0, npos = 0;
-  for (int p = b0; p < b1; ++p) {
-    mine += quant(xa_keys[p]);
-    npos += (xa_keys[p] >> 32) != 0ull;
-  }
-  int kc;
-  if (a.threshold >= 1.f) {
-    kc = (int)xa_block_sum(npos, wbuf);  // every positive score (they sort first)
-  } else {
-    const unsigned long long tot = xa_block_sum(mine, wbuf);
+  const uint32_t* row = reinterpret_cast<const uint32_t*>(a.X) + ((size_t)h * a.nb + I) * a.nb;
+  unsigned long long mine = 0;
+#pragma unroll 4
+  for (int j = lane; j < n; j += 32) mine += xa_quant(__ldg(row + j));
+  const unsigned long long tot = xa_warp_sum(mine);
+  uint32_t t = 0u;     // threshold key: keep key > t, and ties == t as below
+  bool all_ties = false;
+  uint32_t ntie = 0u;  // ties kept in index order when not all_ties
+  const bool sel = a.threshold < 1.f && tot > 0;  // else every block of positive score
+  if (sel) {
     unsigned long long target = (unsigned long long)((double)a.threshold * (double)tot);
     if ((double)target < (double)a.threshold * (double)tot) ++target;
     if (target < 1) target = 1;
-    unsigned long long run = xa_block_exscan(mine, wbuf);
-    for (int p = b0; p < b1; ++p) {
-      run += quant(xa_keys[p]);
-      if (run >= target) {
-        atomicMin(&kfirst, p + 1);
+    unsigned long long need = target;  // mass still to reach within the current prefix
+    uint32_t prefix = 0u, cnt_eq = 0u;
+    int lev = 0;
+#pragma unroll 1
+    for (; lev < 4; ++lev) {
+      const int shift = 24 - 8 * lev;
+#pragma unroll
+      for (int b = lane; b < 256; b += 32) {
+        H.sum[b] = 0ull;
+        H.cnt[b] = 0u;
+      }
+      __syncwarp();
+      for (int j00 = 0; j00 < n; j00 += 128) {
+        // four loads in flight, then the four groups of 32
+        uint32_t kb[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) kb[u] = j00 + 32 * u + lane < n ? __ldg(row + j00 + 32 * u + lane) : 0u;
+#pragma unroll 1
+        for (int u = 0; u < 4; ++u) {
+          const int j = j00 + 32 * u + lane;
+          const uint32_t k = kb[u];
+          const bool in = j < n && (uint32_t)((unsigned long long)k >> (shift + 8)) == prefix;
+          const int d = in ? (int)((k >> shift) & 255u) : -1;
+          const unsigned long long q = in ? xa_quant(k) : 0ull;
+          // scores of a row often share their leading bits: at most four
+          // digits in this group of 32 are reduced across the warp and added
+          // once each (a loop every lane runs), more are added one by one
+          const unsigned same = __match_any_sync(0xffffffffu, d);
+          const unsigned leaders = __ballot_sync(0xffffffffu, in && (__ffs(same) - 1) == lane);
+          if (__popc(leaders) > 4) {
+            if (in) {
+              atomicAdd(&H.sum[d], q);
+              atomicAdd(&H.cnt[d], 1u);
+              H.key[d] = k;
+            }
+          } else {
+            for (unsigned rest = leaders; rest; rest &= rest - 1) {
+              const int src = __ffs(rest) - 1;
+              const int dl = __shfl_sync(0xffffffffu, d, src);
+              const unsigned long long v = xa_warp_sum((in && d == dl) ? q : 0ull);
+              if (lane == src) {
+                atomicAdd(&H.sum[dl], v);
+                atomicAdd(&H.cnt[dl], (uint32_t)__popc(same));
+                H.key[dl] = k;
+              }
+            }
+          }
+          __syncwarp();
+        }
+      }
+      // lane u owns bins [8u, 8u + 8); the mass above its range comes from
+      // a suffix scan over the lanes; the lane holding the crossing finds
+      // the digit d with S(d + 1) < need <= S(d), S the suffix sum
+      unsigned long long own = 0;
+#pragma unroll
+      for (int b = 0; b < 8; ++b) own += H.sum[8 * lane + b];
+      unsigned long long inc = own;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_down_sync(0xffffffffu, inc, o);
+        if (lane + o < 32) inc += y;
+      }
+      const unsigned long long above = inc - own;
+      const bool mine_x = above < need && above + own >= need;
+      uint32_t dg = 0u, ce = 0u, kk = 0u;
+      unsigned long long nd = 0ull;
+      if (mine_x) {
+        unsigned long long acc = above;
+        for (int b = 8 * lane + 7; b >= 8 * lane; --b) {
+          if (acc + H.sum[b] >= need) {
+            dg = (uint32_t)b;
+            nd = need - acc;
+            ce = H.cnt[b];
+            kk = H.key[b];
+            break;
+          }
+          acc += H.sum[b];
+        }
+      }
+      const int src = __ffs(__ballot_sync(0xffffffffu, mine_x)) - 1;
+      dg = __shfl_sync(0xffffffffu, dg, src);
+      nd = __shfl_sync(0xffffffffu, nd, src);
+      ce = __shfl_sync(0xffffffffu, ce, src);
+      kk = __shfl_sync(0xffffffffu, kk, src);
+      __syncwarp();
+      prefix = (prefix << 8) | dg;
+      need = nd;
+      cnt_eq = ce;
+      if (ce == 1u) {
+        // one score in the bin: it is the threshold key
+        t = kk;
         break;
       }
     }
-    __syncthreads();
-    kc = kfirst;
+    if (lev == 4) t = prefix;
+    const unsigned long long qt = xa_quant(t);
+    unsigned long long k = qt ? (need + qt - 1) / qt : 1;
+    if (k < 1) k = 1;
+    if (k > cnt_eq) k = cnt_eq;
+    ntie = (uint32_t)k;
+    all_ties = ntie == cnt_eq;
   }
-  for (int p = threadIdx.x; p < kc; p += kXaThreads) {
-    const uint32_t J = 0xffffffffu - (uint32_t)xa_keys[p];
-    atomicOr(&words[J >> 5], 1u << (J & 31));
-  }
-  if (threadIdx.x == 0) atomicOr(&words[I >> 5], 1u << (I & 31));  // the diagonal block
-  __syncthreads();
+  // mask words from ballots over the row in index order (word w covers
+  // block columns 32 w .. 32 w + 31); ties beyond the first ntie dropped
   uint32_t* out = a.mask + ((size_t)h * a.nb + I) * a.nw;
-  int c = 0;
-  for (int w = threadIdx.x; w < a.nw; w += kXaThreads) {
-    out[w] = words[w];
-    c += __popc(words[w]);
+  uint32_t run = 0, c = 0;
+  const bool rank_ties = sel && !all_ties;
+#pragma unroll 4
+  for (int w = 0; w < a.nw; ++w) {
+    const int j = w * 32 + lane;
+    const uint32_t k = j < n ? __ldg(row + j) : 0u;
+    bool keep = j < n && (k > t || j == I || (sel && all_ties && k == t));
+    if (rank_ties) {
+      const bool tie = j < n && k == t;
+      const unsigned bt = __ballot_sync(0xffffffffu, tie);
+      if (tie && run + (uint32_t)__popc(bt & ((1u << lane) - 1u)) < ntie) keep = true;
+      run += (uint32_t)__popc(bt);
+    }
+    const uint32_t word = __ballot_sync(0xffffffffu, keep);
+    if (lane == 0) out[w] = word;
+    c += (uint32_t)__popc(word);
   }
-  const int cnt = (int)xa_block_sum((unsigned long long)c, wbuf);
-  if (threadIdx.x == 0) {
-    a.cnt[(size_t)h * a.nb + I] = cnt;
+  if (lane == 0) {
+    a.cnt[(size_t)h * a.nb + I] = (int)c;
     const unsigned long long bs = (unsigned long long)a.bs;
-    atomicAdd(&a.active[h], (unsigned long long)(cnt - 1) * bs * bs + bs * (bs + 1) / 2);
+    atomicAdd(&a.active[h], (unsigned long long)(c - 1) * bs * bs + bs * (bs + 1) / 2);
   }
+}
+
+template <int D, int kBsS>
+cudaError_t launch_pass2(const CUtensorMap& mQ, const CUtensorMap& mK, const XaArgs& a, int grid, size_t smem,
+                         cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(xattn_score_kernel<D, true, kBsS>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  xattn_score_kernel<D, true, kBsS><<<grid, kXaThreads, smem, s>>>(mQ, mK, a);
+  return cudaGetLastError();
 }
 
 template <int D>
@@ -447,26 +554,24 @@ cudaError_t launch_scores(const XaArgs& a, cudaStream_t s) {
     return cudaErrorInvalidValue;
   const size_t smem = kXaSmem + 1024;
   cudaError_t e;
-  if ((e = cudaFuncSetAttribute(xattn_score_kernel<D, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)smem)) != cudaSuccess)
-    return e;
-  if ((e = cudaFuncSetAttribute(xattn_score_kernel<D, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if ((e = cudaFuncSetAttribute(xattn_score_kernel<D, false, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 (int)smem)) != cudaSuccess)
     return e;
   const int grid = a.nrt * a.Hq;
-  xattn_score_kernel<D, false><<<grid, kXaThreads, smem, s>>>(mQ, mK, a);
+  xattn_score_kernel<D, false, 0><<<grid, kXaThreads, smem, s>>>(mQ, mK, a);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  xattn_score_kernel<D, true><<<grid, kXaThreads, smem, s>>>(mQ, mK, a);
-  return cudaGetLastError();
+  switch (a.bsS) {
+    case 4: return launch_pass2<D, 4>(mQ, mK, a, grid, smem, s);
+    case 8: return launch_pass2<D, 8>(mQ, mK, a, grid, smem, s);
+    case 16: return launch_pass2<D, 16>(mQ, mK, a, grid, smem, s);
+    case 32: return launch_pass2<D, 32>(mQ, mK, a, grid, smem, s);
+    case 64: return launch_pass2<D, 64>(mQ, mK, a, grid, smem, s);
+    case 128: return launch_pass2<D, 128>(mQ, mK, a, grid, smem, s);
+  }
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace
-
-size_t xattn_select_smem(int nb) {
-  size_t npad = 1;
-  while (npad < (size_t)nb) npad <<= 1;
-  return npad * sizeof(unsigned long long);
-}
 
 cudaError_t launch_xattn(const XaArgs& a, cudaStream_t s) {
   cudaError_t e;
@@ -474,11 +579,7 @@ cudaError_t launch_xattn(const XaArgs& a, cudaStream_t s) {
   if ((e = cudaMemsetAsync(a.X, 0, (size_t)a.Hq * a.nb * a.nb * sizeof(float), s)) != cudaSuccess) return e;
   if ((e = cudaMemsetAsync(a.active, 0, (size_t)a.Hq * sizeof(unsigned long long), s)) != cudaSuccess) return e;
   if ((e = (a.d == 128 ? launch_scores<128>(a, s) : launch_scores<64>(a, s))) != cudaSuccess) return e;
-  const size_t smem = xattn_select_smem(a.nb);
-  if ((e = cudaFuncSetAttribute(xattn_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) !=
-      cudaSuccess)
-    return e;
-  xattn_select_kernel<<<dim3(a.nb, a.Hq), kXaThreads, smem, s>>>(a);
+  xattn_select_kernel<<<dim3((a.nb + kSelWarps - 1) / kSelWarps, a.Hq), kXaThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
