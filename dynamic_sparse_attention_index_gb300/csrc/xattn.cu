@@ -430,6 +430,8 @@ __global__ void __launch_bounds__(kXaThreads) xattn_select_kernel(const XaArgs a
           const int j = j00 + 32 * u + lane;
           const uint32_t k = kb[u];
           const bool in = j < n && (uint32_t)((unsigned long long)k >> (shift + 8)) == prefix;
+          // below the first level most groups hold no score of the prefix
+          if (__ballot_sync(0xffffffffu, in) == 0u) continue;
           const int d = in ? (int)((k >> shift) & 255u) : -1;
           const unsigned long long q = in ? xa_quant(k) : 0ull;
           // scores of a row often share their leading bits: at most four
