@@ -59,6 +59,8 @@ CASES = [
     (3, 2048, 1, 1, 128, 1, 2, 0.9),    # 128-row blocks
     (4, 4096, 2, 1, 128, 8, 4, 0.9),    # striped tiles, bs = 256
     (3, 4096, 2, 1, 128, 8, 1, 1.0),    # threshold 1: every block of positive score
+    (4, 8192, 2, 1, 128, 16, 32, 0.9),  # the 32-stripe tile, bs = 2048: 128 strided rows per block
+    (4, 8192, 2, 1, 64, 32, 32, 0.9),   # 64 per block
 ]
 
 
