@@ -694,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) 
         const int lo = hi - nbit + 1;
         if (warp < (1 << nbit)) {
           if (warp == 0) {
-            // the set at t_low must reach the target (checked beside round 1)
+            // the set at t_low must reach the target (checked beside the first search round)
             if (first_round) {
               const bool ok = warp_entries(t_low) >= target;
               if (lane == 0) s.bcast_u64[3] = ok ? 1ull : 0ull;  // a slot nothing else writes
