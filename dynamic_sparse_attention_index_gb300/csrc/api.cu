@@ -79,8 +79,9 @@ struct IndexWs {
 IndexWs index_ws(const vs_params& p) {
   int tpc, nchunk, rs;
   index_grid(p, &tpc, &nchunk, &rs);
-  // the tensor-core passes' key chunks (last_q = 64) share the partials array
-  const int ctc = index_tc_grid(p.L, p.Hq, p.Hkv).C;
+  // the tensor-core passes' key chunks (last_q = 64; two partials per chunk)
+  // share the partials array
+  const int ctc = 2 * index_tc_grid(p.L, p.Hq, p.Hkv).C;
   if (ctc > nchunk) nchunk = ctc;
   const size_t qpad = (size_t)(p.last_q + 15) / 16 * 16;
   const size_t bs = (size_t)kBlock * p.stripes;

@@ -11,22 +11,25 @@
 // Two passes over K, both tcgen05 products of a pair of query heads (128
 // rows: two heads x 64 rows, one head and zeros when the group has an odd
 // head left) with 128-key tiles:
-//   pass 1, rows on M: S = Q K^T; each epilogue thread owns one row and keeps
-//     its running (max, sum) in the log2 domain, written per key chunk;
-//   pass 2, keys on M: S^T = K Q^T; each epilogue thread owns one key, forms
-//     p for the 128 rows from the rows' (max, 1 / sum) combined over the
-//     chunks, and sums them per head into v; the 64-key block sums of v go
-//     to a small table that the slash kernel adds up per band.
+//   pass 1, rows on M: S = Q K^T; each epilogue thread owns one row and half
+//     of the keys and keeps their running (max, sum) in the log2 domain,
+//     written per key chunk and half;
+//   pass 2, keys on M: S^T = K Q^T; each epilogue thread owns one key and one
+//     head of the pair, forms p for the head's 64 rows from the rows' (max,
+//     1 / sum) combined over the partials, and sums them into v; the 64-key
+//     block sums of v go to a small table that the slash kernel adds up per
+//     band.
 // One CTA per (key chunk, head pair, key/value head); a loader warp stages
 // the pair's Q rows once and streams K tiles through a three-deep ring, one
-// thread issues the MMAs into two TMEM accumulators, four warps read them.
+// thread issues the MMAs into two TMEM accumulators, eight warps read them
+// (two per lane quadrant, each 64 of the tile's 128 columns).
 #include "attn_common.cuh"
 #include "ptx.cuh"
 
 namespace vs {
 namespace {
 
-constexpr int kIxThreads = 256;  // warp 0 loader, 1 MMA issuer, 2 tensor memory, 4..7 epilogue
+constexpr int kIxThreads = 384;  // warp 0 loader, 1 MMA issuer, 2 tensor memory, 4..11 epilogue
 constexpr int kIxStages = 3;
 constexpr float kIxNegInf = -__builtin_huge_valf();
 
@@ -41,7 +44,7 @@ struct IxLayout {
   static constexpr int kNumBars = 1 + 2 * kIxStages + 4;
   static constexpr int kMisc = kBar + kNumBars * 8;  // tensor memory slot, abort flag
   static constexpr int kRow = kMisc + 16;            // pass 2: (max, 1 / sum) of the 128 rows
-  static constexpr int kRed = kRow + 128 * 8;        // pass 2: per-warp block sums, two buffers
+  static constexpr int kRed = kRow + 128 * 8;        // pass 2: per-warp block sums [2 buffers][2 heads][4]
   static constexpr int kHist = kRed + 2 * 4 * 2 * 4;  // pass 2: [2 heads][2048] counts of v by key >> 20
   static constexpr int kSmem = kHist + 2 * 2048 * 4;
 };
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(kIxThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + Ly::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + Ly::kMisc + 4);
   float2* rowst = reinterpret_cast<float2*>(sm + Ly::kRow);
-  float* red = reinterpret_cast<float*>(sm + Ly::kRed);  // [2][4 warps][2 heads]
+  float* red = reinterpret_cast<float*>(sm + Ly::kRed);  // [2 buffers][2 heads][4 warps]
   uint32_t* hist = reinterpret_cast<uint32_t*>(sm + Ly::kHist);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int chunk = blockIdx.x, pair = blockIdx.y, g = blockIdx.z;
@@ -104,7 +107,7 @@ __global__ void __launch_bounds__(kIxThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&acc_full[i], 1);
-      mbar_init(&acc_free[i], 4);  // one arrival per epilogue warp
+      mbar_init(&acc_free[i], 8);  // one arrival per epilogue warp
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -194,30 +197,36 @@ __global__ void __launch_bounds__(kIxThreads, 1)
     __syncwarp();
   } else if (warp >= 4) {
     // ------------------------------------------------------------ epilogue
-    const int q = warp - 4;  // tensor memory lane quadrant
+    // two warps per tensor memory lane quadrant, each reading half of the
+    // tile's 128 columns: pass 1 keys 64 hc .. 64 hc + 63, pass 2 the rows
+    // of one head of the pair (hc = 0: head a, 1: head b)
+    const int q = (warp - 4) & 3;  // lane quadrant
+    const int hc = (warp - 4) >> 2;
     const int i = q * 32 + lane;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     const float c2 = a.scale_log2;
     const int nq = a.L - 64;  // token of the first index row
     if (!kPass2) {
       // thread = row i of the pair: running max / sum over this chunk's keys
+      // in its column half, written as one of the chunk's two partials
       const int n = nq + (i & 63);
       float m = kIxNegInf, l = 0.f;
       for (int t = 0; t < nt; ++t) {
         if (!wait_warp(&acc_full[t & 1], (t >> 1) & 1, 5)) break;
         tc_fence_after();
-        uint32_t x[128];
-#pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32(tbase + (uint32_t)((t & 1) * 128) + lane_off + c0, x + c0);
+        uint32_t x[64];
+        const uint32_t ta = tbase + (uint32_t)((t & 1) * 128 + 64 * hc) + lane_off;
+        tmem_ld32(ta, x);
+        tmem_ld32(ta + 32, x + 32);
         tmem_ld_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&acc_free[t & 1]);
-        const int k0 = (t0 + t) * 128;
-        const bool masked = k0 + 127 > nq;  // the chunk reaches the index rows' own block
+        const int k0 = (t0 + t) * 128 + 64 * hc;
+        const bool masked = k0 + 63 > nq;  // the half reaches the index rows' own block
         float mx = kIxNegInf;
 #pragma unroll
-        for (int j = 0; j < 128; ++j) {
+        for (int j = 0; j < 64; ++j) {
           float v = __uint_as_float(x[j]) * c2;
           if (masked && k0 + j > n) v = kIxNegInf;
           x[j] = __float_as_uint(v);
@@ -227,7 +236,7 @@ __global__ void __launch_bounds__(kIxThreads, 1)
         if (mn != kIxNegInf) {
           float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
 #pragma unroll
-          for (int j = 0; j < 128; j += 4) {
+          for (int j = 0; j < 64; j += 4) {
             s0 += ix_exp2(__uint_as_float(x[j]) - mn);
             s1 += ix_exp2(__uint_as_float(x[j + 1]) - mn);
             s2 += ix_exp2(__uint_as_float(x[j + 2]) - mn);
@@ -240,84 +249,83 @@ __global__ void __launch_bounds__(kIxThreads, 1)
       const bool valid = i < 64 || has_b;
       if (valid) {
         const int h = i < 64 ? ha : hb;
-        a.part[(size_t)chunk * a.Hq * 64 + (size_t)h * 64 + (i & 63)] = make_float2(m, l);
+        a.part[(size_t)(2 * chunk + hc) * a.Hq * 64 + (size_t)h * 64 + (i & 63)] = make_float2(m, l);
       }
     } else {
-      // the pair's 128 rows: (max, 1 / sum) combined over the pass-1 chunks
-      {
+      // the pair's 128 rows: (max, 1 / sum) combined over the pass-1
+      // partials (two per key chunk)
+      if (hc == 0) {
         const bool valid = i < 64 || has_b;
         const size_t prow = (size_t)(i < 64 ? ha : hb) * 64 + (i & 63);
         float M = kIxNegInf, l = 0.f;
         if (valid) {
-          for (int ch = 0; ch < c.C; ++ch) M = fmaxf(M, a.part[(size_t)ch * a.Hq * 64 + prow].x);
-          for (int ch = 0; ch < c.C; ++ch) {
+          for (int ch = 0; ch < 2 * c.C; ++ch) M = fmaxf(M, a.part[(size_t)ch * a.Hq * 64 + prow].x);
+          for (int ch = 0; ch < 2 * c.C; ++ch) {
             const float2 pt = a.part[(size_t)ch * a.Hq * 64 + prow];
             if (pt.x != kIxNegInf) l += pt.y * ix_exp2(pt.x - M);
           }
         }
         rowst[i] = (valid && l > 0.f) ? make_float2(M, 1.0f / l) : make_float2(0.f, 0.f);
       }
-      asm volatile("bar.sync 1, 128;" ::: "memory");
-      // thread = key i of the tile: p over the 128 rows, summed per head
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      // thread = key i of the tile: p over this warp's head's 64 rows.  Every
+      // warp runs all nt iterations (a failed wait only skips the work), so
+      // the per-head named barrier always sees the head's four warps.
+      const bool head_on = hc == 0 || has_b;
+      const int h = hc ? hb : ha;
+      const float2* rs = rowst + 64 * hc;
       for (int t = 0; t < nt; ++t) {
-        if (!wait_warp(&acc_full[t & 1], (t >> 1) & 1, 5)) break;
-        tc_fence_after();
-        uint32_t x[128];
-#pragma unroll
-        for (int c0 = 0; c0 < 128; c0 += 32) tmem_ld32(tbase + (uint32_t)((t & 1) * 128) + lane_off + c0, x + c0);
-        tmem_ld_wait();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&acc_free[t & 1]);
+        const bool ok = wait_warp(&acc_full[t & 1], (t >> 1) & 1, 5);
         const int k0 = (t0 + t) * 128;
         const int k = k0 + i;
-        const bool masked = k0 + 127 > nq;
-        float va0 = 0.f, va1 = 0.f, vb0 = 0.f, vb1 = 0.f;
+        float va = 0.f;
+        if (ok) {
+          tc_fence_after();
+          uint32_t x[64];
+          const uint32_t ta = tbase + (uint32_t)((t & 1) * 128 + 64 * hc) + lane_off;
+          tmem_ld32(ta, x);
+          tmem_ld32(ta + 32, x + 32);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&acc_free[t & 1]);
+          const bool masked = k0 + 127 > nq;
+          float v0 = 0.f, v1 = 0.f, v2 = 0.f, v3 = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 64; cc += 2) {
-          const float2 sa = rowst[cc], sa1 = rowst[cc + 1], sb = rowst[64 + cc], sb1 = rowst[64 + cc + 1];
-          float pa = ix_exp2(fmaf(__uint_as_float(x[cc]), c2, -sa.x)) * sa.y;
-          float pa1 = ix_exp2(fmaf(__uint_as_float(x[cc + 1]), c2, -sa1.x)) * sa1.y;
-          float pb = ix_exp2(fmaf(__uint_as_float(x[64 + cc]), c2, -sb.x)) * sb.y;
-          float pb1 = ix_exp2(fmaf(__uint_as_float(x[64 + cc + 1]), c2, -sb1.x)) * sb1.y;
-          if (masked) {
-            // causal: row cc of either head is token nq + cc
-            if (k > nq + cc) pa = pb = 0.f;
-            if (k > nq + cc + 1) pa1 = pb1 = 0.f;
+          for (int cc = 0; cc < 64; cc += 4) {
+            float p0 = ix_exp2(fmaf(__uint_as_float(x[cc]), c2, -rs[cc].x)) * rs[cc].y;
+            float p1 = ix_exp2(fmaf(__uint_as_float(x[cc + 1]), c2, -rs[cc + 1].x)) * rs[cc + 1].y;
+            float p2 = ix_exp2(fmaf(__uint_as_float(x[cc + 2]), c2, -rs[cc + 2].x)) * rs[cc + 2].y;
+            float p3 = ix_exp2(fmaf(__uint_as_float(x[cc + 3]), c2, -rs[cc + 3].x)) * rs[cc + 3].y;
+            if (masked) {
+              // causal: row cc of the head is token nq + cc
+              if (k > nq + cc) p0 = 0.f;
+              if (k > nq + cc + 1) p1 = 0.f;
+              if (k > nq + cc + 2) p2 = 0.f;
+              if (k > nq + cc + 3) p3 = 0.f;
+            }
+            v0 += p0;
+            v1 += p1;
+            v2 += p2;
+            v3 += p3;
           }
-          va0 += pa;
-          va1 += pa1;
-          vb0 += pb;
-          vb1 += pb1;
-        }
-        const float va = va0 + va1, vb = vb0 + vb1;
-        if (k < a.L) {
-          a.v[(size_t)ha * a.L + k] = va;
-          atomicAdd(&hist[min(__float_as_uint(va) >> 20, 2047u)], 1u);
-          if (has_b) {
-            a.v[(size_t)hb * a.L + k] = vb;
-            atomicAdd(&hist[2048 + min(__float_as_uint(vb) >> 20, 2047u)], 1u);
+          va = (v0 + v1) + (v2 + v3);
+          if (k < a.L && head_on) {
+            a.v[(size_t)h * a.L + k] = va;
+            atomicAdd(&hist[hc * 2048 + min(__float_as_uint(va) >> 20, 2047u)], 1u);
           }
         }
-        // 64-key block sums (keys beyond L hold zeros): warps 0-1 of the
-        // group hold the tile's first block, warps 2-3 its second
-        float wa = va, wb = vb;
+        // 64-key block sums (keys beyond L hold zeros): warps of quadrants
+        // 0-1 hold the tile's first block, 2-3 its second
+        float wa = va;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-          wa += __shfl_xor_sync(0xffffffffu, wa, o);
-          wb += __shfl_xor_sync(0xffffffffu, wb, o);
-        }
-        float* rb = red + (t & 1) * 8;
-        if (lane == 0) {
-          rb[q * 2] = wa;
-          rb[q * 2 + 1] = wb;
-        }
-        asm volatile("bar.sync 1, 128;" ::: "memory");
-        if (q == 0 && lane < 4) {
-          const int b = lane >> 1, hh = lane & 1;
-          const int blk = k0 / 64 + b;
-          if (blk < a.ntile && (hh == 0 || has_b))
-            a.T64[(size_t)(hh ? hb : ha) * a.ntile + blk] = rb[(2 * b) * 2 + hh] + rb[(2 * b + 1) * 2 + hh];
+        for (int o = 16; o > 0; o >>= 1) wa += __shfl_xor_sync(0xffffffffu, wa, o);
+        float* rb = red + (t & 1) * 8 + hc * 4;
+        if (lane == 0) rb[q] = wa;
+        asm volatile("bar.sync %0, 128;" ::"r"(2 + hc) : "memory");
+        if (ok && head_on && q == 0 && lane < 2) {
+          const int blk = k0 / 64 + lane;
+          if (blk < a.ntile) a.T64[(size_t)h * a.ntile + blk] = rb[2 * lane] + rb[2 * lane + 1];
         }
       }
     }
