@@ -591,24 +591,32 @@ __global__ void __launch_bounds__(kThreads, 1) select_kernel(const IndexArgs a) 
         s.bcast_u32[3] = 0u;
       }
       __syncthreads();
-      // eight loads per thread in flight per step
-      for (int m0 = 0; m0 < L; m0 += 8 * kThreads) {
-        float x[8];
+      // four 16-byte loads (16 verticals) per thread in flight per step (v is
+      // 16-byte aligned and L a multiple of 64)
+      const float4* v4 = reinterpret_cast<const float4*>(v);
+      const int L4 = L / 4;
+      for (int q0 = 0; q0 < L4; q0 += 4 * kThreads) {
+        float4 x[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int m = m0 + u * kThreads + (int)threadIdx.x;
-          x[u] = m < L ? v[m] : -1.f;
+        for (int u = 0; u < 4; ++u) {
+          const int q = q0 + u * kThreads + (int)threadIdx.x;
+          x[u] = q < L4 ? v4[q] : make_float4(-1.f, -1.f, -1.f, -1.f);
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const int m = m0 + u * kThreads + (int)threadIdx.x;
-          const bool in = x[u] >= 0.f && key_of(x[u]) >= t_low;
-          const unsigned i = slot(in, &s.bcast_u32[2]);
-          if (in && i < (unsigned)kFastCap) {
-            ckey2[i] = key_of(x[u]);
-            cidx[i] = m;
-            wkey[i] = key_of(x[u]);
-            wx[i] = nbs - 1 - m / bs;
+        for (int u = 0; u < 4; ++u) {
+          const int m4 = 4 * (q0 + u * kThreads + (int)threadIdx.x);
+          const float xs[4] = {x[u].x, x[u].y, x[u].z, x[u].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            // negative: past the end (keys of masses are below 2^31)
+            const bool in = xs[j] >= 0.f && key_of(xs[j]) >= t_low;
+            const unsigned i = slot(in, &s.bcast_u32[2]);
+            if (in && i < (unsigned)kFastCap) {
+              ckey2[i] = key_of(xs[j]);
+              cidx[i] = m4 + j;
+              wkey[i] = key_of(xs[j]);
+              wx[i] = nbs - 1 - (m4 + j) / bs;
+            }
           }
         }
       }
