@@ -50,11 +50,13 @@ WORKLOADS = {
 }
 DENSITY = 0.05     # budget fill: 95 % sparsity (fixed in the pages' experiments)
 LAST_Q, TOP_P = 64, 0.95
-# library kernels per step: RoPE of Q and K (and the adjoint on dQ and dK);
-# the index (two tensor-core scoring passes, slash sums, selection); the
-# forward (three prep kernels, attention); the backward (three prep kernels,
-# D, dK / dV for the vertical and the slash units, the recomputing dQ kernel)
-KERNELS_PER_STEP = {"rope": 4, "index": 4, "fwd": 4, "bwd": 7}
+# library kernels per step: RoPE of Q and K; the index (two tensor-core
+# scoring passes, slash sums, selection); the forward (three prep kernels,
+# attention); the backward (three prep kernels, D, dK / dV for the vertical
+# and the slash units, the recomputing dQ kernel, and with rope_mode = 1 the
+# RoPE adjoint on dK and the one on dQ, which returns at once when the dQ
+# kernel of the stored dS tiles applied it in its epilogue)
+KERNELS_PER_STEP = {"rope": 2, "index": 4, "fwd": 4, "bwd": 9}
 KERNELS_PER_STEP_FWD = {"rope": 2, "index": 4, "fwd": 4}
 # ex2.approx issue rate of one SM per clock (the index's exponentials;
 # measured with a standalone microbenchmark on this GPU)
@@ -258,8 +260,9 @@ def run_gpu(args):
     bwd = w.backward
     rope_kw = dict(rope_theta=w.rope_theta, yarn_factor=w.yarn_factor, yarn_orig_len=w.yarn_orig_len)
     imode = 1 if args.index_mode == "group" else 0
+    # the backward returns the gradients of the un-rotated Q and K (rope_mode = 1)
     p = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=DENSITY, stripes=W, index_mode=imode,
-                       **rope_kw)
+                       rope_mode=1 if bwd else 0, **rope_kw)
     p_nat = vs.make_params(L, Hq, Hkv, d, last_q=LAST_Q, top_p=TOP_P, density=0.0, stripes=W, index_mode=imode,
                            **rope_kw)
 
@@ -315,8 +318,6 @@ def run_gpu(args):
             else:
                 vs.vs_sparse_attn_bwd(p, ix, Q, K, v_, O, lse, ins[3], dq, dk, dv, ws_b)
             rec("bwd", 1)
-            vs.vs_rope(p, Hq, dq, dq, True)
-            vs.vs_rope(p, Hkv, dk, dk, True)
 
     # natural top-p sparsity (reported; not the timed operating point)
     vs.vs_rope(p, Hq, Qr, Q, False)
@@ -453,10 +454,11 @@ def run_gpu(args):
     if ring:
         # ring setup (shard lists, band bitmaps, a vertical union and packed
         # rows per shard) and W x W steps: one forward kernel per step; D, the
-        # two dK / dV kernels and the dQ kernel per step, two final casts
+        # two dK / dV kernels and the dQ kernel per step, two final casts, the
+        # RoPE adjoint on dQ and dK
         kps["fwd"] = 2 + 2 * W + W * W
         if bwd:
-            kps["bwd"] = 1 + 2 + 2 * W + 3 * W * W + 2
+            kps["bwd"] = 1 + 2 + 2 * W + 3 * W * W + 2 + 2
     out = {
         "metric": "VS sparse attn fwd+bwd ms and effective TFLOP/s at 128K (% bf16 peak)",
         "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,

@@ -43,7 +43,7 @@ class vs_params(ctypes.Structure):
         ("last_q", ctypes.c_int32), ("top_p", ctypes.c_float), ("block", ctypes.c_int32),
         ("stripes", ctypes.c_int32), ("softmax_scale", ctypes.c_float), ("density", ctypes.c_float),
         ("rope_theta", ctypes.c_double), ("yarn_factor", ctypes.c_float), ("yarn_orig_len", ctypes.c_int32),
-        ("index_mode", ctypes.c_int32),
+        ("index_mode", ctypes.c_int32), ("rope_mode", ctypes.c_int32),
     ]
 
 
@@ -103,9 +103,10 @@ VS_INDEX_PER_HEAD, VS_INDEX_GROUP_SHARED = 0, 1
 
 
 def make_params(L, Hq, Hkv, d, last_q=64, top_p=0.95, stripes=1, softmax_scale=0.0, density=0.0,
-                rope_theta=10000.0, yarn_factor=1.0, yarn_orig_len=0, block=64, index_mode=0) -> vs_params:
+                rope_theta=10000.0, yarn_factor=1.0, yarn_orig_len=0, block=64, index_mode=0,
+                rope_mode=0) -> vs_params:
     return vs_params(L, Hq, Hkv, d, last_q, top_p, block, stripes, softmax_scale, density,
-                     rope_theta, yarn_factor, yarn_orig_len, index_mode)
+                     rope_theta, yarn_factor, yarn_orig_len, index_mode, rope_mode)
 
 
 def _ptr(t):

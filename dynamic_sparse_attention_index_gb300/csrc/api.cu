@@ -62,6 +62,10 @@ vs_status check_params(const vs_params* p) {
   if (!(p->density >= 0.f && p->density <= 1.f)) return VS_ERR_INVALID_ARG;
   if (!(p->softmax_scale >= 0.f) || !std::isfinite(p->softmax_scale)) return VS_ERR_INVALID_ARG;
   if (p->index_mode != 0 && p->index_mode != 1) return VS_ERR_INVALID_ARG;
+  if (p->rope_mode != 0 && p->rope_mode != 1) return VS_ERR_INVALID_ARG;
+  if (p->rope_mode == 1 &&
+      (!(p->rope_theta > 1.0) || !(p->yarn_factor >= 1.f) || (p->yarn_factor > 1.f && p->yarn_orig_len <= 0)))
+    return VS_ERR_INVALID_ARG;
   return VS_OK;
 }
 
@@ -184,22 +188,7 @@ vs_status vs_rope(const vs_params* p, int32_t H, const void* x, void* y, int32_t
   a.H = H;
   a.d = p->d;
   a.transpose = transpose ? 1 : 0;
-  // theta_i = base^(-2i/d); YaRN NTK-by-parts: gamma_i = clip((r_i - 1)/(32 - 1), 0, 1),
-  // r_i = orig_len * theta_i / (2 pi); theta'_i = theta_i (gamma_i + (1 - gamma_i)/s)
-  const double s = p->yarn_factor;
-  for (int i = 0; i < p->d / 2; ++i) {
-    double f = std::pow(p->rope_theta, -2.0 * i / p->d);
-    if (s > 1.0) {
-      const double r = p->yarn_orig_len * f / (2.0 * 3.14159265358979323846);
-      double g = (r - 1.0) / (32.0 - 1.0);
-      g = g < 0.0 ? 0.0 : (g > 1.0 ? 1.0 : g);
-      f = f * (g + (1.0 - g) / s);
-    }
-    // f / (2 pi) < 1; its double value scaled by 2^64 converts to uint64 exactly
-    const double turns = f / (2.0 * 3.14159265358979323846);
-    a.turn[i] = turns < 1.0 ? (uint64_t)(turns * 18446744073709551616.0) : ~0ull;
-  }
-  a.mscale = s > 1.0 ? (float)(0.1 * std::log(s) + 1.0) : 1.0f;
+  rope_fill(*p, a);
   return launch_rope(a, static_cast<cudaStream_t>(stream)) == cudaSuccess ? VS_OK : VS_ERR_CUDA;
 }
 
@@ -448,9 +437,11 @@ vs_status vs_striped_ring_bwd(const vs_params* p, const vs_index* index, const v
   if ((st = check_ws(ws, ws_bytes, ring_ws_bytes(*p, true))) != VS_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, sizeof(DevStatus), s) != cudaSuccess) return VS_ERR_CUDA;
-  return launch_ring_bwd(*p, *index, Q, K, V, O, lse, dO, dQ, dK, dV, ws, step_events, n_events, s) == cudaSuccess
-             ? VS_OK
-             : VS_ERR_CUDA;
+  if (launch_ring_bwd(*p, *index, Q, K, V, O, lse, dO, dQ, dK, dV, ws, step_events, n_events, s) != cudaSuccess)
+    return VS_ERR_CUDA;
+  // rope_mode = 1: the ring's dQ and dK back through the RoPE adjoint
+  if (p->rope_mode == 1 && launch_rope_adjoint(*p, dQ, dK, nullptr, s) != cudaSuccess) return VS_ERR_CUDA;
+  return VS_OK;
 }
 
 vs_status vs_device_status(void* ws, void* stream) {

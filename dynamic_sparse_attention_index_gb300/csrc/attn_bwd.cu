@@ -1012,7 +1012,8 @@ cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* 
                               reinterpret_cast<float*>(w + lay.part_k), reinterpret_cast<float*>(w + lay.part_v),
                               nullptr, nullptr, st, nullptr, s)) != cudaSuccess)
       return e;
-    return launch_attn_dq(p, g, pp, Q, K, V, dO, lse, dsum, dQ, st, StepCtl(), s);
+    if ((e = launch_attn_dq(p, g, pp, Q, K, V, dO, lse, dsum, dQ, st, StepCtl(), s)) != cudaSuccess) return e;
+    return p.rope_mode == 1 ? launch_rope_adjoint(p, dQ, dK, nullptr, s) : cudaSuccess;
   }
   // Stored dS: the plan numbers every active block and checks that each
   // head's fit its share of the workspace; the dK / dV kernels store them,
@@ -1033,7 +1034,11 @@ cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* 
   if ((e = launch_dq_stored(p, g, pp, K, d, dQ, st, s)) != cudaSuccess) return e;
   StepCtl ctl;
   ctl.skip_if = d.ok;
-  return launch_attn_dq(p, g, pp, Q, K, V, dO, lse, dsum, dQ, st, ctl, s);
+  if ((e = launch_attn_dq(p, g, pp, Q, K, V, dO, lse, dsum, dQ, st, ctl, s)) != cudaSuccess) return e;
+  // rope_mode = 1: the stored-dS dQ kernel applied the RoPE adjoint in its
+  // epilogue; the recomputing one did not, so dQ's pass runs only when the
+  // plan chose that path (its word is then zero)
+  return p.rope_mode == 1 ? launch_rope_adjoint(p, dQ, dK, d.ok, s) : cudaSuccess;
 }
 
 }  // namespace vs

@@ -109,6 +109,11 @@ struct DqsParams {
   __nv_bfloat16* dq;
   float scale;
   DevStatus* status;
+  // RoPE adjoint fused into the epilogue (rope_mode = 1): channel i pairs
+  // with i + 64 and is rotated by -t theta_i, t the row's token
+  int32_t rope;
+  float rope_mscale;
+  uint64_t rope_turn[64];  // theta_i / (2 pi) as 0.64 fixed-point fractions
 };
 
 constexpr int kQsThreads = 256;  // warp 0 planner, 1 MMA, 2 tensor memory, 3 loader, 4..7 epilogue
@@ -518,18 +523,62 @@ __global__ void __launch_bounds__(kQsThreads, 1)
       const bool valid = it.valid[seg];
       const int tok = it.I[seg] * kBlock + rr;
       __nv_bfloat16* orow = P.dq + ((size_t)tok * g.Hq + it.h[seg]) * 128;
-      for (int c0 = 0; c0 < 128; c0 += 32) {
-        uint32_t o[32];
-        tmem_ld32(tbase + (uint32_t)(b * 128) + lane_off + c0, o);
-        tmem_ld_wait();
-        if (valid) {
-          uint32_t q16[16];
+      if (P.rope) {
+        // dQ of the un-rotated queries: y_i = c (x_i cos phi + x_{i+64} sin phi),
+        // y_{i+64} = c (x_{i+64} cos phi - x_i sin phi), phi = tok theta_i
+        // reduced to a turn as the RoPE kernel reduces it
+        const float kTurnToRad = 1.4629180792671596e-09f;  // 2 pi / 2^32
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
-            q16[k] = pack_bf16(__uint_as_float(o[2 * k]) * P.scale, __uint_as_float(o[2 * k + 1]) * P.scale);
-          uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+        for (int c0 = 0; c0 < 64; c0 += 32) {
+          uint32_t lo[32], hi[32];
+          tmem_ld32(tbase + (uint32_t)(b * 128) + lane_off + c0, lo);
+          tmem_ld32(tbase + (uint32_t)(b * 128) + lane_off + c0 + 64, hi);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t ql[16], qh[16];
 #pragma unroll
-          for (int k = 0; k < 4; ++k) dst[k] = make_uint4(q16[4 * k], q16[4 * k + 1], q16[4 * k + 2], q16[4 * k + 3]);
+            for (int k = 0; k < 16; ++k) {
+              float yl[2], yh[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const uint64_t frac = (uint64_t)tok * P.rope_turn[c0 + 2 * k + e];  // modulo 2^64
+                const float phi = (float)(int32_t)(uint32_t)(frac >> 32) * kTurnToRad;
+                // phi is already in [-pi, pi): the hardware sine and cosine
+                // (absolute error below 4e-7 there) are far inside the bf16
+                // rounding of the result
+                const float sn = __sinf(phi), cs = __cosf(phi);
+                const float x = __uint_as_float(lo[2 * k + e]) * P.scale;
+                const float y = __uint_as_float(hi[2 * k + e]) * P.scale;
+                yl[e] = P.rope_mscale * (x * cs + y * sn);
+                yh[e] = P.rope_mscale * (y * cs - x * sn);
+              }
+              ql[k] = pack_bf16(yl[0], yl[1]);
+              qh[k] = pack_bf16(yh[0], yh[1]);
+            }
+            uint4* dl = reinterpret_cast<uint4*>(orow + c0);
+            uint4* dh = reinterpret_cast<uint4*>(orow + c0 + 64);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              dl[k] = make_uint4(ql[4 * k], ql[4 * k + 1], ql[4 * k + 2], ql[4 * k + 3]);
+              dh[k] = make_uint4(qh[4 * k], qh[4 * k + 1], qh[4 * k + 2], qh[4 * k + 3]);
+            }
+          }
+        }
+      } else {
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          uint32_t o[32];
+          tmem_ld32(tbase + (uint32_t)(b * 128) + lane_off + c0, o);
+          tmem_ld_wait();
+          if (valid) {
+            uint32_t q16[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              q16[k] = pack_bf16(__uint_as_float(o[2 * k]) * P.scale, __uint_as_float(o[2 * k + 1]) * P.scale);
+            uint4* dst = reinterpret_cast<uint4*>(orow + c0);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              dst[k] = make_uint4(q16[4 * k], q16[4 * k + 1], q16[4 * k + 2], q16[4 * k + 3]);
+          }
         }
       }
       tc_fence_before();
@@ -575,6 +624,15 @@ cudaError_t launch_dq_stored(const vs_params& p, const AttnGeom& g, const PrepPt
   P.dq = static_cast<__nv_bfloat16*>(dQ);
   P.scale = default_scale(p);
   P.status = st;
+  P.rope = p.rope_mode == 1 ? 1 : 0;
+  P.rope_mscale = 1.f;
+  for (int i = 0; i < 64; ++i) P.rope_turn[i] = 0;
+  if (P.rope) {
+    RopeArgs ra;
+    rope_fill(p, ra);
+    P.rope_mscale = ra.mscale;
+    for (int i = 0; i < 64; ++i) P.rope_turn[i] = ra.turn[i];
+  }
   const size_t smem = kQsSmem + 1024;
   cudaError_t e = cudaFuncSetAttribute(dq_stored_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

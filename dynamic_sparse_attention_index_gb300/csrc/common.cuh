@@ -124,9 +124,16 @@ struct RopeArgs {
   int32_t L, H, d;
   int32_t transpose;
   float mscale;
-  uint64_t turn[64];  // theta_i / (2 pi) as a 0.64 fixed-point fraction, d/2 <= 64 (host-computed in fp64)
+  uint64_t turn[64];       // theta_i / (2 pi) as a 0.64 fixed-point fraction, d/2 <= 64 (host-computed in fp64)
+  const int32_t* skip_if;  // device word or null: the kernel returns at once when it is non-zero
 };
+// The frequencies (rope_theta, YaRN) and temperature of p into a (x, y, L,
+// H, transpose and skip_if are the caller's).
+void rope_fill(const vs_params& p, RopeArgs& a);
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s);
+// rope_mode = 1: the RoPE adjoint in place on dK [L][Hkv][d] and on dQ
+// [L][Hq][d] (the dQ pass returns at once when *dq_skip_if != 0).
+cudaError_t launch_rope_adjoint(const vs_params& p, void* dQ, void* dK, const int32_t* dq_skip_if, cudaStream_t s);
 
 struct IndexArgs {
   const void* Q;

@@ -16,6 +16,9 @@
 // cosine are taken in fp32.
 #include <cuda_bf16.h>
 
+#include <cmath>
+#include <cstring>
+
 #include "common.cuh"
 
 namespace vs {
@@ -23,6 +26,7 @@ namespace vs {
 __global__ void __launch_bounds__(256) rope_kernel(const __nv_bfloat16* x, __nv_bfloat16* y,
                                                    int L, int H, int d, int transpose, float mscale,
                                                    RopeArgs freqs) {
+  if (freqs.skip_if != nullptr && *freqs.skip_if != 0) return;
   const int half = d >> 1, ng = half >> 3;
   const long long idx = (long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (idx >= (long long)L * ng) return;
@@ -62,6 +66,25 @@ __global__ void __launch_bounds__(256) rope_kernel(const __nv_bfloat16* x, __nv_
   }
 }
 
+void rope_fill(const vs_params& p, RopeArgs& a) {
+  // theta_i = base^(-2i/d); YaRN NTK-by-parts: gamma_i = clip((r_i - 1)/(32 - 1), 0, 1),
+  // r_i = orig_len * theta_i / (2 pi); theta'_i = theta_i (gamma_i + (1 - gamma_i)/s)
+  const double s = p.yarn_factor;
+  for (int i = 0; i < p.d / 2; ++i) {
+    double f = std::pow(p.rope_theta, -2.0 * i / p.d);
+    if (s > 1.0) {
+      const double r = p.yarn_orig_len * f / (2.0 * 3.14159265358979323846);
+      double g = (r - 1.0) / (32.0 - 1.0);
+      g = g < 0.0 ? 0.0 : (g > 1.0 ? 1.0 : g);
+      f = f * (g + (1.0 - g) / s);
+    }
+    // f / (2 pi) < 1; its double value scaled by 2^64 converts to uint64 exactly
+    const double turns = f / (2.0 * 3.14159265358979323846);
+    a.turn[i] = turns < 1.0 ? (uint64_t)(turns * 18446744073709551616.0) : ~0ull;
+  }
+  a.mscale = s > 1.0 ? (float)(0.1 * std::log(s) + 1.0) : 1.0f;
+}
+
 cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s) {
   const long long n = (long long)a.L * (a.d / 16);
   const int threads = 256;
@@ -70,6 +93,25 @@ cudaError_t launch_rope(const RopeArgs& a, cudaStream_t s) {
                                                    static_cast<__nv_bfloat16*>(a.y), a.L, a.H, a.d, a.transpose,
                                                    a.mscale, a);
   return cudaGetLastError();
+}
+
+cudaError_t launch_rope_adjoint(const vs_params& p, void* dQ, void* dK, const int32_t* dq_skip_if, cudaStream_t s) {
+  RopeArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.L = p.L;
+  a.d = p.d;
+  a.transpose = 1;
+  rope_fill(p, a);
+  a.x = dK;
+  a.y = dK;
+  a.H = p.Hkv;
+  cudaError_t e = launch_rope(a, s);
+  if (e != cudaSuccess) return e;
+  a.x = dQ;
+  a.y = dQ;
+  a.H = p.Hq;
+  a.skip_if = dq_skip_if;
+  return launch_rope(a, s);
 }
 
 }  // namespace vs

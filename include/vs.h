@@ -79,6 +79,13 @@ typedef struct vs_params {
                          /* 1: shared by each GQA group: every head of a key/value   */
                          /*    group uses the union of the group's per-head sets     */
                          /*    (vs_index_build; the attention calls read the arrays) */
+  int32_t rope_mode;     /* 0: the backward's dQ, dK are gradients of the Q, K it    */
+                         /*    was given (the rotated ones);                         */
+                         /* 1: it maps them back through the RoPE adjoint of         */
+                         /*    rope_theta / YaRN above: gradients of the un-rotated  */
+                         /*    queries and keys (vs_sparse_attn_bwd and              */
+                         /*    vs_striped_ring_bwd; Q and K are always passed        */
+                         /*    rotated)                                               */
 } vs_params;
 
 /*

@@ -21,7 +21,7 @@ import pytest
 
 import oracle
 import synth
-from _util import bf16_bits_of, f64, grad_close, inject_index, rel_l2, to_dev
+from _util import bf16_bits_of, f64, grad_close, inject_index, rel_l2, to_dev, ulp_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -47,16 +47,18 @@ def _ws_bytes(vs, w, stripes, ws_density):
     return head + w.Hq * nb * nb * 8192
 
 
-def _fwd_bwd(w, index, stripes=1, density=0.0, O_lse=None, ws_density=WS_ALL, want_path=None, ws_trim=0):
+def _fwd_bwd(w, index, stripes=1, density=0.0, O_lse=None, ws_density=WS_ALL, want_path=None, ws_trim=0,
+             params_kw=None):
     """GPU backward; O / LSE from the GPU forward, or injected (O_lse).
     ws_density sizes the backward workspace (see WS_*), less ws_trim bytes
     from its end (the dS blocks sit last); want_path, when given, is the dQ
-    path the status word must report (1 stored, 0 recomputed)."""
+    path the status word must report (1 stored, 0 recomputed); params_kw
+    adds fields of vs_params (e.g. rope_mode)."""
     import torch
     import dynamic_sparse_attention_index_gb300 as vs
     dev = torch.device("cuda:0")
     p = vs.make_params(w.L, w.Hq, w.Hkv, w.d, last_q=w.last_q, top_p=w.top_p, stripes=stripes,
-                       density=density)
+                       density=density, **(params_kw or {}))
     if index is None:
         ix = vs.IndexBuffers.allocate(p, dev)
     else:
@@ -127,6 +129,53 @@ def test_bwd_topp_index(wid, L, Hq, Hkv, p_):
     w = synth.make_workload(wid, L=L, Hq=Hq, Hkv=Hkv, d=128, top_p=p_, backward=True)
     index, _, _ = oracle.build_index(f64(w.q), f64(w.k), w.last_q, p_)
     _check(w, index)
+
+
+def _rope_adjoint(g, kw):
+    return oracle.rope(g, kw["rope_theta"], transpose=True, yarn_factor=kw["yarn_factor"],
+                       yarn_orig_len=kw["yarn_orig_len"])
+
+
+def _rope_pair_ulps(src):
+    """bf16 ulps of the two channels a rotation mixes into each output
+    element: channel i and i + d/2 of the same row."""
+    u = ulp_bf16(src)
+    h = src.shape[-1] // 2
+    both = u[..., :h] + u[..., h:]
+    return np.concatenate([both, both], axis=-1)
+
+
+@pytest.mark.parametrize("yarn", [False, True])
+def test_bwd_rope_mode_maps_gradients_back(yarn):
+    """rope_mode = 1 returns the gradients of the un-rotated queries and
+    keys.  On the stored-dS path the RoPE adjoint of dQ is fused into the dQ
+    kernel's epilogue (one rounding); the recomputing path's dQ and every dK
+    take the RoPE kernel after the backward.  Each output equals the same
+    kernels' rope_mode = 0 gradient rotated back in fp64 (the oracle's RoPE
+    adjoint) to the bf16 rounding of the output, plus, for the fused dQ, the
+    rotated rounding of its two source channels; dV is unchanged bit for bit;
+    relative L2 to the rotated exact gradient <= 1e-2."""
+    w = synth.make_workload(3, L=1024, Hq=4, Hkv=2, d=128, backward=True)
+    index, _, _ = oracle.build_index(f64(w.q), f64(w.k), 64, 0.95, density=0.1)
+    q, k, v, do = f64(w.q), f64(w.k), f64(w.v), f64(w.do)
+    O_lse = oracle.attention_forward(q, k, v, index)
+    ref = oracle.attention_backward(q, k, v, do, index)
+    kw = dict(rope_theta=1e4, yarn_factor=4.0 if yarn else 1.0, yarn_orig_len=256 if yarn else 0)
+    m = oracle.rope_mscale(kw["yarn_factor"])
+    for ws_density, path in ((WS_ALL, 1), (WS_MIN, 0)):
+        _, g0 = _fwd_bwd(w, index, O_lse=O_lse, ws_density=ws_density, want_path=path, params_kw=kw)
+        _, g1 = _fwd_bwd(w, index, O_lse=O_lse, ws_density=ws_density, want_path=path,
+                         params_kw=dict(kw, rope_mode=1))
+        for name, a, b, fused in (("dQ", g0[0], g1[0], path == 1), ("dK", g0[1], g1[1], False)):
+            want = _rope_adjoint(a, kw)
+            bound = 0.5 * ulp_bf16(want) + 2e-6 * m * np.abs(a).max()
+            if fused:
+                bound = bound + 0.5 * m * _rope_pair_ulps(a)
+            err = np.abs(b - want)
+            assert (err <= bound).all(), (name, path, float((err - bound).max()))
+        np.testing.assert_array_equal(g1[2], g0[2])
+        for name, got, r in (("dQ", g1[0], ref[0]), ("dK", g1[1], ref[1])):
+            assert rel_l2(got, _rope_adjoint(r, kw)) <= 1e-2, (name, path)
 
 
 def test_bwd_budget_fill_index():

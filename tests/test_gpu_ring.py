@@ -14,16 +14,16 @@ import pytest
 
 import oracle
 import synth
-from _util import bf16_bits_of, f64, grad_close, inject_index, rel_l2, to_dev
+from _util import bf16_bits_of, f64, grad_close, inject_index, rel_l2, to_dev, ulp_bf16
 
 pytestmark = pytest.mark.gpu
 
 
-def _ring(w, W, index, O_lse=None, events=False):
+def _ring(w, W, index, O_lse=None, events=False, params_kw=None):
     import torch
     import dynamic_sparse_attention_index_gb300 as vs
     dev = torch.device("cuda:0")
-    p = vs.make_params(w.L, w.Hq, w.Hkv, w.d, last_q=64, top_p=w.top_p, stripes=W)
+    p = vs.make_params(w.L, w.Hq, w.Hkv, w.d, last_q=64, top_p=w.top_p, stripes=W, **(params_kw or {}))
     ix = inject_index(vs, p, index, dev)
     Q, K, V = to_dev(w.q, dev), to_dev(w.k, dev), to_dev(w.v, dev)
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(W * W + 1)] if events else None
@@ -79,6 +79,26 @@ def test_ring_forward_backward(wid, L, Hq, Hkv, d, W, p_, dens):
     emu = oracle.attention_backward_bf16_products(q, k, v, do, index, stripes=W)
     for name, a, r, e in zip(("dQ", "dK", "dV"), g, ref, emu):
         grad_close(name, a, r, e)
+
+
+def test_ring_backward_rope_mode():
+    """rope_mode = 1 on the ring: dQ and dK come back through the RoPE
+    adjoint (the RoPE kernel after the ring), equal to the rope_mode = 0
+    gradients rotated back in fp64 to the bf16 rounding of the output; dV
+    unchanged bit for bit."""
+    w = synth.make_workload(4, L=2048, Hq=4, Hkv=2, d=128, top_p=0.9, backward=True)
+    q, k, v = f64(w.q), f64(w.k), f64(w.v)
+    index, _, _ = oracle.build_index(q, k, 64, 0.9, stripes=4)
+    O_lse = oracle.attention_forward(q, k, v, index, stripes=4)
+    kw = dict(rope_theta=1e4, yarn_factor=1.0, yarn_orig_len=0)
+    g0 = _ring(w, 4, index, O_lse=O_lse, params_kw=kw)["grads"]
+    g1 = _ring(w, 4, index, O_lse=O_lse, params_kw=dict(kw, rope_mode=1))["grads"]
+    for name, a, b in (("dQ", g0[0], g1[0]), ("dK", g0[1], g1[1])):
+        want = oracle.rope(a, 1e4, transpose=True)
+        err = np.abs(b - want)
+        bound = 0.5 * ulp_bf16(want) + 2e-6 * np.abs(a).max()
+        assert (err <= bound).all(), (name, float((err - bound).max()))
+    np.testing.assert_array_equal(g1[2], g0[2])
 
 
 def test_ring_forward_d64():

@@ -62,6 +62,9 @@ def _call_index(vs, p, q=FAKE, k=FAKE, ws=FAKE, ws_bytes=1 << 40, ix=None):
     (dict(stripes=3), "VS_ERR_INVALID_ARG"),
     (dict(density=-0.1), "VS_ERR_INVALID_ARG"),
     (dict(index_mode=2), "VS_ERR_INVALID_ARG"),
+    (dict(rope_mode=2), "VS_ERR_INVALID_ARG"),
+    (dict(rope_mode=1, rope_theta=1.0), "VS_ERR_INVALID_ARG"),          # the adjoint needs the frequencies
+    (dict(rope_mode=1, yarn_factor=32.0, yarn_orig_len=0), "VS_ERR_INVALID_ARG"),
 ])
 def test_index_rejects_bad_params(vs, kw, code):
     args = dict(L=4096, Hq=4, Hkv=2, d=64, last_q=64, top_p=0.9)
