@@ -46,6 +46,7 @@ CASES = [
     (3, 512, 2, 1, 64, 1, 0.9, 1),
     (3, 768, 8, 1, 128, 200, 0.9, 2),
     (4, 4096, 2, 1, 128, 64, 0.9, 32),   # the striped workload's 32 shards
+    (3, 2048, 6, 2, 128, 64, 0.9, 1),    # tensor-core scoring, a group of three: one pair holds one head
 ]
 
 

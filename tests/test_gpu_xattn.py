@@ -57,6 +57,7 @@ CASES = [
     (1, 2048, 3, 1, 64, 16, 1, 0.95),   # 4 per block, odd group
     (3, 1024, 2, 1, 128, 1, 1, 0.9),    # stride 1: exact block masses, 64-row blocks
     (3, 2048, 1, 1, 128, 1, 2, 0.9),    # 128-row blocks
+    (3, 1024, 2, 2, 64, 1, 1, 0.9),     # d = 64 with 64-row blocks
     (4, 4096, 2, 1, 128, 8, 4, 0.9),    # striped tiles, bs = 256
     (3, 4096, 2, 1, 128, 8, 1, 1.0),    # threshold 1: every block of positive score
     (4, 8192, 2, 1, 128, 16, 32, 0.9),  # the 32-stripe tile, bs = 2048: 128 strided rows per block
