@@ -349,8 +349,10 @@ def run_gpu(args):
         balance["timed"] = ring_balance(vs, p1, ix1, Q, K, V, W, dev, step, step_ev, bwd)
         del ix1, ix_w
     # the backward's status word says how dQ was formed (1: from the dS
-    # tiles stored in its workspace, 0: S and dP recomputed)
+    # tiles stored in its workspace, 0: S and dP recomputed) and in how many
+    # passes over key/value head groups
     dq_stored = bool(ws_b is not None and not ring and int(ws_b[8:12].view(torch.int32).item()) == 1)
+    dq_passes = int(ws_b[12:16].view(torch.int32).item()) if dq_stored else 0
     assert vs.vs_device_status(ws_f) == vs.VS_OK
     assert ws_b is None or vs.vs_device_status(ws_b) == vs.VS_OK
 
@@ -499,7 +501,8 @@ def run_gpu(args):
         "gpu_launches": sum(kps.values()) * args.steps,
         "clocks": clocks,
         "device_status": dev_status,
-        **({"dq_path": "stored dS tiles" if dq_stored else "recomputed S and dP"} if bwd and not ring else {}),
+        **({"dq_path": (f"stored dS tiles ({dq_passes} passes)" if dq_passes > 1 else "stored dS tiles")
+                        if dq_stored else "recomputed S and dP"} if bwd and not ring else {}),
         **({"xattn_index": xattn} if xattn else {}),
     }
     if rank == 0 and not args.no_cpu_baseline:

@@ -78,6 +78,7 @@ struct BwdParams {
   float log2e;
   DevStatus* status;
   int vertical;   // 1: vertical units, 0: slash units
+  int kv_lo, kv_n;  // this launch's key/value heads [kv_lo, kv_lo + kv_n) (one pass)
   int stall;      // bounded-wait test: the planner emits nothing
   // stored dS blocks (null ok: none): see DsPlan
   const int32_t* ds_ok;
@@ -151,12 +152,14 @@ __device__ __forceinline__ void vsplit(const AttnGeom& g, int cnt, int* R, int* 
   *stride = r64;
 }
 
-// Vertical unit enumeration: units (vg, chunk, split), vg-major.
+// Vertical unit enumeration: units (vg, chunk, split), vg-major, over the
+// union groups [vg_lo, vg_hi) of one pass.
 struct VUnit {
   int vg, chunk, split, R, stride, cnt;
 };
-__device__ bool decode_vunit(const AttnGeom& g, const int32_t* vcnt, int id, VUnit* u) {
-  for (int vg = 0; vg < g.nvg; ++vg) {
+__device__ __forceinline__ int vg_per_kv(const AttnGeom& g) { return g.pair_heads ? g.G / 2 : g.G; }
+__device__ bool decode_vunit(const AttnGeom& g, const int32_t* vcnt, int vg_lo, int vg_hi, int id, VUnit* u) {
+  for (int vg = vg_lo; vg < vg_hi; ++vg) {
     const int cnt = vcnt[(size_t)vg * (g.nb + 1) + g.nb];
     int R, stride;
     vsplit(g, cnt, &R, &stride);
@@ -270,17 +273,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // number of units of this launch
+  const int vg_lo = P.kv_lo * vg_per_kv(g), vg_hi = (P.kv_lo + P.kv_n) * vg_per_kv(g);
   int nunits;
   if (P.vertical) {
     nunits = 0;
-    for (int vg = 0; vg < g.nvg; ++vg) {
+    for (int vg = vg_lo; vg < vg_hi; ++vg) {
       const int cnt = P.vcnt[(size_t)vg * (g.nb + 1) + g.nb];
       int R, stride;
       vsplit(g, cnt, &R, &stride);
       nunits += ((cnt + 63) / 64) * R;
     }
   } else {
-    nunits = g.Hkv * g.nb;
+    nunits = P.kv_n * g.nb;
   }
 
   if (warp == 0 && P.stall) {
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int nheads, kv0, kv1 = 0;
       if (P.vertical) {
         VUnit u;
-        decode_vunit(g, P.vcnt, uid, &u);
+        decode_vunit(g, P.vcnt, vg_lo, vg_hi, uid, &u);
         vg = u.vg;
         chunk = u.chunk;
         split = u.split;
@@ -321,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         kv0 = vg * g.L + chunk * 64;
       } else {
         // key blocks in ascending order (more causal rows first)
-        kvh = uid / g.nb;
+        kvh = P.kv_lo + uid / g.nb;
         kb = uid % g.nb;
         nheads = g.G;
         kv0 = kvh;
@@ -784,7 +788,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) mbar_arrive(acc_free);
           if (P.vertical) {
             VUnit u;
-            decode_vunit(g, P.vcnt, uid, &u);
+            decode_vunit(g, P.vcnt, vg_lo, vg_hi, uid, &u);
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) {
               const int e = u.chunk * 64 + (int)col0 + jj;
@@ -795,11 +799,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           } else {
-            const int kvh = uid / g.nb, kb = uid % g.nb;
+            const int kvh = P.kv_lo + uid / g.nb, kb = uid % g.nb;
             // add the vertical partials of tokens in this key block (all union groups of kvh)
-            const int vg_per_kv = g.pair_heads ? g.G / 2 : g.G;
-            for (int q = 0; q < vg_per_kv; ++q) {
-              const int vg = kvh * vg_per_kv + q;
+            for (int q = 0; q < vg_per_kv(g); ++q) {
+              const int vg = kvh * vg_per_kv(g) + q;
               const int cnt = P.vcnt[(size_t)vg * (g.nb + 1) + g.nb];
               int R, stride;
               vsplit(g, cnt, &R, &stride);
@@ -868,8 +871,8 @@ struct BwdWs {
   PrepWs prep;
 };
 
-// cap: stored dS blocks per head (0: none)
-BwdWs bwd_layout(const AttnGeom& g, long long cap) {
+// cap: stored dS blocks per head (0: none), hpp: query heads per pass
+BwdWs bwd_layout(const AttnGeom& g, long long cap, int hpp) {
   WsLayout w;
   BwdWs o;
   o.status = w.take(sizeof(DevStatus));
@@ -883,42 +886,83 @@ BwdWs bwd_layout(const AttnGeom& g, long long cap) {
     o.ds_rank = w.take((size_t)g.Hq * g.nbs * 4);
     o.ds_base_s = w.take((size_t)g.Hq * g.nb * 4);
     o.ds_base_v = w.take((size_t)g.Hq * g.nb * 4);
-    o.ds = w.take((size_t)g.Hq * (size_t)cap * kDsBlockBytes);
+    o.ds = w.take((size_t)hpp * (size_t)cap * kDsBlockBytes);
   }
   o.total = w.off;
   return o;
 }
 
-// Largest stored-dS capacity (blocks per head) that a workspace of ws_bytes
-// holds; block rows stay below 2^31 (tensor-map coordinates).
-long long ds_cap_for(const AttnGeom& g, size_t ws_bytes) {
-  const BwdWs one = bwd_layout(g, 1);
-  if (ws_bytes < one.total) return 0;
-  long long cap = (long long)((ws_bytes - one.ds) / ((size_t)g.Hq * kDsBlockBytes));
-  const long long row_cap = (2147483647LL / 64) / g.Hq;
-  return cap < row_cap ? cap : row_cap;
+// How the stored dS blocks are split: blocks per head and key/value head
+// groups per pass (the call runs ceil(Hkv / gpp) passes).
+struct DsSplit {
+  long long cap = 0;
+  int gpp = 1;
+};
+
+// Blocks per head that a budget-fill index of density p.density is expected
+// to need: density x the causal 64 x 64 blocks of each head, x 1.5 (x 2 for
+// the group-shared index, whose unions grow), plus four vertical chunks per
+// query block.  0 for top-p selection (no density known in advance).
+double ds_blocks_expected(const vs_params& p, const AttnGeom& g) {
+  if (!(p.density > 0.f)) return 0.0;
+  const double f = p.index_mode == 1 ? 2.0 : 1.5;
+  return f * p.density * (double)g.nb * (g.nb + 1) / 2.0 + 4.0 * g.nb;
 }
 
-// Suggested capacity: a budget-fill index keeps about density x the causal
-// 64 x 64 blocks of each head; 1.5x that (2x for the group-shared index,
-// whose unions grow), plus four vertical chunks per query block.  None for
-// top-p selection (no density known in advance) or beyond 32 GiB.
-long long ds_cap_suggested(const vs_params& p, const AttnGeom& g) {
-  if (!(p.density > 0.f)) return 0;
-  const double f = p.index_mode == 1 ? 2.0 : 1.5;
-  const double head = f * p.density * (double)g.nb * (g.nb + 1) / 2.0 + 4.0 * g.nb;
-  if (head * g.Hq * kDsBlockBytes > 32.0 * 1024 * 1024 * 1024) return 0;
-  const long long cap = (long long)head + 1;
-  const long long row_cap = (2147483647LL / 64) / g.Hq;
-  return cap < row_cap ? cap : 0;
+// Block rows of the dS tensor map stay below 2^31 (TMA coordinates).
+long long ds_row_cap(int hpp) { return (2147483647LL / 64) / hpp; }
+
+// The split a workspace of ws_bytes allows: one pass over every head when
+// the expected blocks fit (or when none are expected: top-p), else the
+// fewest passes whose heads each get the expected room, else one key/value
+// head group per pass (the most room per head).  The device still checks
+// the real counts and recomputes dQ when a head's blocks do not fit.
+DsSplit ds_split_for(const vs_params& p, const AttnGeom& g, size_t ws_bytes) {
+  DsSplit sp;
+  const BwdWs one = bwd_layout(g, 1, 1);
+  if (ws_bytes < one.total) return sp;
+  const size_t room = ws_bytes - one.ds;
+  const double want = ds_blocks_expected(p, g);
+  for (int n = 1; n <= g.Hkv; ++n) {
+    const int gpp = (g.Hkv + n - 1) / n;
+    if (n > 1 && gpp == (g.Hkv + n - 2) / (n - 1)) continue;  // the same split as n - 1 passes
+    const int hpp = gpp * g.G;
+    long long cap = (long long)(room / ((size_t)hpp * kDsBlockBytes));
+    if (cap > ds_row_cap(hpp)) cap = ds_row_cap(hpp);
+    sp.cap = cap;
+    sp.gpp = gpp;
+    if (want == 0.0 || (double)cap >= want) break;
+  }
+  return sp;
+}
+
+// Suggested split: every head in one pass up to 32 GiB of blocks; beyond
+// that the fewest passes whose blocks take at most 96 GiB; none past that.
+DsSplit ds_split_suggested(const vs_params& p, const AttnGeom& g) {
+  DsSplit sp;
+  const double want = ds_blocks_expected(p, g);
+  if (want == 0.0) return sp;
+  const long long cap = (long long)want + 1;
+  for (int n = 1; n <= g.Hkv; ++n) {
+    const int gpp = (g.Hkv + n - 1) / n;
+    const int hpp = gpp * g.G;
+    const double limit = (n == 1 ? 32.0 : 96.0) * 1024 * 1024 * 1024;
+    if ((double)cap * hpp * kDsBlockBytes <= limit && cap <= ds_row_cap(hpp)) {
+      sp.cap = cap;
+      sp.gpp = gpp;
+      return sp;
+    }
+  }
+  return sp;
 }
 
 }  // namespace
 
-size_t attn_bwd_ws_bytes(const vs_params& p) { return bwd_layout(make_geom(p), 0).total; }
+size_t attn_bwd_ws_bytes(const vs_params& p) { return bwd_layout(make_geom(p), 0, 1).total; }
 size_t attn_bwd_ws_bytes_stored(const vs_params& p) {
   const AttnGeom g = make_geom(p);
-  return bwd_layout(g, ds_cap_suggested(p, g)).total;
+  const DsSplit sp = ds_split_suggested(p, g);
+  return bwd_layout(g, sp.cap, sp.gpp * g.G).total;
 }
 
 cudaError_t launch_bwd_dsum(const void* O, const void* dO, float* Dsum, int L, int Hq, int d, cudaStream_t s) {
@@ -929,11 +973,14 @@ cudaError_t launch_bwd_dsum(const void* O, const void* dO, float* Dsum, int L, i
   return cudaGetLastError();
 }
 
-cudaError_t launch_dkdv_core(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const vs_index& ix,
-                             const void* Q, const void* K, const void* V, const void* dO, const float* lse,
-                             const float* Dsum, void* dK, void* dV, float* part_k, float* part_v, float* dk32,
-                             float* dv32, DevStatus* st, const DsPlan* ds, cudaStream_t s) {
+// dK / dV of the key/value heads [kv_lo, kv_lo + kv_n): the vertical
+// launch, then the slash launch
+cudaError_t launch_dkdv_heads(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const vs_index& ix,
+                              const void* Q, const void* K, const void* V, const void* dO, const float* lse,
+                              const float* Dsum, void* dK, void* dV, float* part_k, float* part_v, float* dk32,
+                              float* dv32, DevStatus* st, const DsPlan* ds, int kv_lo, int kv_n, cudaStream_t s) {
   CUtensorMap mQ, mdO, mK, mV, mKp, mVp, mDS;
+  if (kv_lo < 0 || kv_n < 1 || kv_lo + kv_n > g.Hkv) return cudaErrorInvalidValue;
   if (!make_map_heads(&mQ, Q, g.L, g.Hq, 128, g.tq_mul, g.tq_add) ||
       !make_map_heads(&mdO, dO, g.L, g.Hq, 128, g.tq_mul, g.tq_add) ||
       !make_map_heads(&mK, K, g.L, g.Hkv, 128, g.tk_mul, g.tk_add) ||
@@ -942,7 +989,7 @@ cudaError_t launch_dkdv_core(const vs_params& p, const AttnGeom& g, const PrepPt
       !make_map_rows(&mVp, pp.Vp, (long long)g.nvg * g.L, 128))
     return cudaErrorInvalidValue;
   // the stored dS blocks (a map the kernel never touches when there are none)
-  if (ds ? !make_map_rows(&mDS, ds->ds, (long long)g.Hq * ds->cap * 64, 64) : false) return cudaErrorInvalidValue;
+  if (ds ? !make_map_rows(&mDS, ds->ds, (long long)ds->hpp * ds->cap * 64, 64) : false) return cudaErrorInvalidValue;
   if (!ds) mDS = mKp;
   BwdParams P;
   P.g = g;
@@ -962,6 +1009,8 @@ cudaError_t launch_dkdv_core(const vs_params& p, const AttnGeom& g, const PrepPt
   P.scale = default_scale(p);
   P.log2e = 1.4426950408889634f;
   P.status = st;
+  P.kv_lo = kv_lo;
+  P.kv_n = kv_n;
   P.stall = test_stall_requested() ? 1 : 0;
   P.ds_ok = ds ? ds->ok : nullptr;
   P.ds_rank = ds ? ds->band_rank : nullptr;
@@ -980,9 +1029,17 @@ cudaError_t launch_dkdv_core(const vs_params& p, const AttnGeom& g, const PrepPt
   attn_dkdv_kernel<<<nsm, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, mDS, P);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   P.vertical = 0;
-  const int nunits = g.Hkv * g.nb;
+  const int nunits = kv_n * g.nb;
   attn_dkdv_kernel<<<nunits < nsm ? nunits : nsm, kThreads, smem, s>>>(mQ, mdO, mK, mV, mKp, mVp, mDS, P);
   return cudaGetLastError();
+}
+
+cudaError_t launch_dkdv_core(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const vs_index& ix,
+                             const void* Q, const void* K, const void* V, const void* dO, const float* lse,
+                             const float* Dsum, void* dK, void* dV, float* part_k, float* part_v, float* dk32,
+                             float* dv32, DevStatus* st, const DsPlan* ds, cudaStream_t s) {
+  return launch_dkdv_heads(p, g, pp, ix, Q, K, V, dO, lse, Dsum, dK, dV, part_k, part_v, dk32, dv32, st, ds, 0,
+                           g.Hkv, s);
 }
 
 size_t bwd_partials_bytes(const AttnGeom& g) { return (size_t)g.nvg * g.L * g.d * 4; }
@@ -992,8 +1049,9 @@ cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* 
                             size_t ws_bytes, cudaStream_t s) {
   if (p.d != 128) return cudaErrorNotSupported;
   const AttnGeom g = make_geom(p);
-  const long long cap = ds_cap_for(g, ws_bytes);
-  const BwdWs lay = bwd_layout(g, cap);
+  const DsSplit sp = ds_split_for(p, g, ws_bytes);
+  const long long cap = sp.cap;
+  const BwdWs lay = bwd_layout(g, cap, sp.gpp * g.G);
   uint8_t* w = static_cast<uint8_t*>(ws);
   PrepPtrs pp;
   pp.inS = reinterpret_cast<uint32_t*>(w + lay.prep.inS);
@@ -1016,10 +1074,11 @@ cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* 
     return p.rope_mode == 1 ? launch_rope_adjoint(p, dQ, dK, nullptr, s) : cudaSuccess;
   }
   // Stored dS: the plan numbers every active block and checks that each
-  // head's fit its share of the workspace; the dK / dV kernels store them,
-  // the dQ kernel reads them back.  If a head's did not fit, the dK / dV
-  // kernels store nothing, the reading dQ kernel returns at once, and the
-  // recomputing one runs instead (each checks the plan's word).
+  // head's fit its share of the workspace; per pass (a range of key/value
+  // head groups) the dK / dV kernels store them and the dQ kernel reads
+  // them back.  If a head's did not fit, the dK / dV kernels store nothing,
+  // the reading dQ kernel returns at once, and the recomputing one runs
+  // instead (each checks the plan's word).
   DsPlan d;
   d.ok = reinterpret_cast<int32_t*>(w + lay.ds_ok);
   d.band_rank = reinterpret_cast<int32_t*>(w + lay.ds_rank);
@@ -1027,11 +1086,16 @@ cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* 
   d.base_v = reinterpret_cast<int32_t*>(w + lay.ds_base_v);
   d.ds = reinterpret_cast<__nv_bfloat16*>(w + lay.ds);
   d.cap = (int)cap;
+  d.hpp = sp.gpp * g.G;
   if ((e = launch_ds_plan(g, pp, d, s)) != cudaSuccess) return e;
-  if ((e = launch_dkdv_core(p, g, pp, ix, Q, K, V, dO, lse, dsum, dK, dV, reinterpret_cast<float*>(w + lay.part_k),
-                            reinterpret_cast<float*>(w + lay.part_v), nullptr, nullptr, st, &d, s)) != cudaSuccess)
-    return e;
-  if ((e = launch_dq_stored(p, g, pp, K, d, dQ, st, s)) != cudaSuccess) return e;
+  for (int kv_lo = 0; kv_lo < g.Hkv; kv_lo += sp.gpp) {
+    const int kv_n = g.Hkv - kv_lo < sp.gpp ? g.Hkv - kv_lo : sp.gpp;
+    if ((e = launch_dkdv_heads(p, g, pp, ix, Q, K, V, dO, lse, dsum, dK, dV,
+                               reinterpret_cast<float*>(w + lay.part_k), reinterpret_cast<float*>(w + lay.part_v),
+                               nullptr, nullptr, st, &d, kv_lo, kv_n, s)) != cudaSuccess)
+      return e;
+    if ((e = launch_dq_stored(p, g, pp, K, d, dQ, st, kv_lo, kv_n, s)) != cudaSuccess) return e;
+  }
   StepCtl ctl;
   ctl.skip_if = d.ok;
   if ((e = launch_attn_dq(p, g, pp, Q, K, V, dO, lse, dsum, dQ, st, ctl, s)) != cudaSuccess) return e;

@@ -94,11 +94,12 @@ struct Item {
 };
 
 // Items are numbered heaviest-first: larger block index = more causal keys.
-__host__ __device__ inline Item decode_item(const AttnGeom& g, int id) {
+// decode_item_at takes the item's row position (0 = heaviest) and its place
+// pr in the row (0 .. items_per_row - 1).
+__host__ __device__ inline Item decode_item_at(const AttnGeom& g, int row, int pr) {
   Item it;
   if (g.pair_heads) {
-    const int I = g.nb - 1 - id / g.items_per_row;
-    const int pr = id % g.items_per_row;
+    const int I = g.nb - 1 - row;
     const int kv = pr / (g.G / 2), hp = pr % (g.G / 2);
     it.g = kv;
     it.h[0] = kv * g.G + 2 * hp;
@@ -108,8 +109,8 @@ __host__ __device__ inline Item decode_item(const AttnGeom& g, int id) {
     it.vg = pr;
   } else {
     const int npair = (g.nb + 1) / 2;
-    const int u = npair - 1 - id / g.items_per_row;
-    const int h = id % g.items_per_row;
+    const int u = npair - 1 - row;
+    const int h = pr;
     it.g = h / g.G;
     it.h[0] = it.h[1] = h;
     it.I[0] = 2 * u;
@@ -119,6 +120,16 @@ __host__ __device__ inline Item decode_item(const AttnGeom& g, int id) {
     it.vg = h;
   }
   return it;
+}
+__host__ __device__ inline Item decode_item(const AttnGeom& g, int id) {
+  return decode_item_at(g, id / g.items_per_row, id % g.items_per_row);
+}
+// Items of the key/value heads [kv_lo, kv_lo + kv_n) alone, numbered the same
+// way (id < rows x kv_n x items_per_row / Hkv).
+__host__ __device__ inline int items_per_kv(const AttnGeom& g) { return g.items_per_row / g.Hkv; }
+__host__ __device__ inline Item decode_item_kv(const AttnGeom& g, int id, int kv_lo, int kv_n) {
+  const int n = kv_n * items_per_kv(g);
+  return decode_item_at(g, id / n, kv_lo * items_per_kv(g) + id % n);
 }
 
 // Workspace regions written by the prep kernels (offsets from ws base).
@@ -189,14 +200,19 @@ cudaError_t launch_attn_dq(const vs_params& p, const AttnGeom& g, const PrepPtrs
 // (query head h, query block I) follow that row's key sources in order: the
 // slash key blocks active for h in descending key order (band 0, then each
 // kept band B >= 1 ascending), then the 64-entry chunks of the vertical
-// union list.  Head h owns blocks [h cap, (h + 1) cap).
+// union list.  The backward runs in passes over whole key/value head groups
+// (hpp = heads per pass, a multiple of Hq / Hkv; one pass when everything
+// fits): the blocks of one pass's heads are stored and read back before the
+// next pass reuses the room, and head h owns blocks [(h mod hpp) cap,
+// (h mod hpp + 1) cap).
 struct DsPlan {
   int32_t* ok;         // device word: non-zero while every head's blocks fit in cap
   int32_t* band_rank;  // [Hq][nbs]: kept bands of head h in [1, B]
   int32_t* base_s;     // [Hq][nb]: first block of (h, I)
   int32_t* base_v;     // [Hq][nb]: first vertical-chunk block of (h, I)
-  __nv_bfloat16* ds;   // [Hq cap][64][64] blocks
+  __nv_bfloat16* ds;   // [hpp cap][64][64] blocks
   int cap;             // blocks per head
+  int hpp;             // query heads per pass
 };
 constexpr int kDsBlockBytes = 64 * 64 * 2;
 
@@ -212,8 +228,9 @@ __host__ __device__ inline int ds_slash_block(const AttnGeom& g, int base, int r
 }
 
 cudaError_t launch_ds_plan(const AttnGeom& g, const PrepPtrs& pp, const DsPlan& d, cudaStream_t s);
+// dQ of the row tiles of key/value heads [kv_lo, kv_lo + kv_n) (one pass)
 cudaError_t launch_dq_stored(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const void* K,
-                             const DsPlan& d, void* dQ, DevStatus* st, cudaStream_t s);
+                             const DsPlan& d, void* dQ, DevStatus* st, int kv_lo, int kv_n, cudaStream_t s);
 
 // Tensor-map helpers (host): 3-D view (d, heads, tokens) of a [L][H][d] bf16
 // tensor with a (64, 1, 64) box, and a 2-D view (d, rows) with a (64, 64) box,

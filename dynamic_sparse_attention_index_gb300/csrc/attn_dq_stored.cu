@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(1024) ds_plan_kernel(AttnGeom g, const uint32_
   __syncthreads();
   if (threadIdx.x == 0) carry = 0;
   __syncthreads();
-  const long long head0 = (long long)h * d.cap;
+  const long long head0 = (long long)(h % d.hpp) * d.cap;
   for (int base = 0; base < g.nb; base += blockDim.x) {
     const int I = base + threadIdx.x;
     int n = 0, ns = 0;
@@ -107,6 +107,8 @@ struct DqsParams {
   const int32_t* base_v;
   const int32_t* ok;
   __nv_bfloat16* dq;
+  int kv_lo, kv_n;  // this pass: the row tiles of key/value heads [kv_lo, kv_lo + kv_n)
+  int nitems;       // their number
   float scale;
   DevStatus* status;
   // RoPE adjoint fused into the epilogue (rope_mode = 1): channel i pairs
@@ -148,7 +150,11 @@ __global__ void __launch_bounds__(kQsThreads, 1)
                      const __grid_constant__ CUtensorMap mKp, const DqsParams P) {
   // the stored tiles did not fit: the recomputing dQ kernel runs instead
   if (*P.ok == 0) return;
-  if (blockIdx.x == 0 && threadIdx.x == 0 && P.status) P.status->path = 1;
+  // one thread of one launch at a time (the passes run in stream order)
+  if (blockIdx.x == 0 && threadIdx.x == 0 && P.status) {
+    P.status->path = 1;
+    P.status->passes += 1;
+  }
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBarOff);
@@ -237,10 +243,10 @@ __global__ void __launch_bounds__(kQsThreads, 1)
       ++t;
       return __shfl_sync(0xffffffffu, ok, 0);
     };
-    for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x) {
+    for (int id = blockIdx.x; id < P.nitems && !*abort_flag; id += gridDim.x) {
       const long long h0 = tick();
       // the item in scalars (an indexed struct would live in local memory)
-      const Item it = decode_item(g, id);
+      const Item it = decode_item_kv(g, id, P.kv_lo, P.kv_n);
       const int I0 = it.I[0], I1 = it.I[1], kvh = it.g, vg = it.vg;
       const bool val0 = it.valid[0], val1 = it.valid[1];
       const uint32_t* bm0 = P.inS + (size_t)it.h[0] * g.nw;
@@ -472,7 +478,7 @@ __global__ void __launch_bounds__(kQsThreads, 1)
     if (lane == 0) {
       constexpr uint32_t kIdesc = idesc_bf16(128, 128, false, true);  // A = dS K-major, B = K MN-major
       int t = 0, it_local = 0;
-      for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
+      for (int id = blockIdx.x; id < P.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
         const int b = it_local & 1;
         const uint32_t tacc = tbase + (uint32_t)(b * 128);
         const long long f0 = tick();
@@ -512,14 +518,14 @@ __global__ void __launch_bounds__(kQsThreads, 1)
     const int r = q * 32 + lane, seg = r >> 6, rr = r & 63;
     const uint32_t lane_off = (uint32_t)(q * 32) << 16;
     int it_local = 0;
-    for (int id = blockIdx.x; id < g.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
+    for (int id = blockIdx.x; id < P.nitems && !*abort_flag; id += gridDim.x, ++it_local) {
       const int b = it_local & 1;
       const long long a0 = tick();
       if (!wait_warp(&acc_done[b], (it_local >> 1) & 1, 23)) break;
       const long long a1 = tick();
       if (kWaitProfileDs) pc[0] += a1 - a0;
       tc_fence_after();
-      const Item it = decode_item(g, id);
+      const Item it = decode_item_kv(g, id, P.kv_lo, P.kv_n);
       const bool valid = it.valid[seg];
       const int tok = it.I[seg] * kBlock + rr;
       __nv_bfloat16* orow = P.dq + ((size_t)tok * g.Hq + it.h[seg]) * 128;
@@ -608,9 +614,10 @@ cudaError_t launch_ds_plan(const AttnGeom& g, const PrepPtrs& pp, const DsPlan& 
 }
 
 cudaError_t launch_dq_stored(const vs_params& p, const AttnGeom& g, const PrepPtrs& pp, const void* K,
-                             const DsPlan& d, void* dQ, DevStatus* st, cudaStream_t s) {
+                             const DsPlan& d, void* dQ, DevStatus* st, int kv_lo, int kv_n, cudaStream_t s) {
   CUtensorMap mDS, mK, mKp;
-  if (!make_map_rows(&mDS, d.ds, (long long)g.Hq * d.cap * 64, 64) ||
+  if (kv_lo < 0 || kv_n < 1 || kv_lo + kv_n > g.Hkv) return cudaErrorInvalidValue;
+  if (!make_map_rows(&mDS, d.ds, (long long)d.hpp * d.cap * 64, 64) ||
       !make_map_heads(&mK, K, g.L, g.Hkv, 128) || !make_map_rows(&mKp, pp.Kp, (long long)g.nvg * g.L, 128))
     return cudaErrorInvalidValue;
   DqsParams P;
@@ -622,6 +629,9 @@ cudaError_t launch_dq_stored(const vs_params& p, const AttnGeom& g, const PrepPt
   P.base_v = d.base_v;
   P.ok = d.ok;
   P.dq = static_cast<__nv_bfloat16*>(dQ);
+  P.kv_lo = kv_lo;
+  P.kv_n = kv_n;
+  P.nitems = g.nitems / g.Hkv * kv_n;
   P.scale = default_scale(p);
   P.status = st;
   P.rope = p.rope_mode == 1 ? 1 : 0;
@@ -639,7 +649,7 @@ cudaError_t launch_dq_stored(const vs_params& p, const AttnGeom& g, const PrepPt
   int dev = 0, nsm = 152;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  const int grid = g.nitems < nsm ? g.nitems : nsm;
+  const int grid = P.nitems < nsm ? P.nitems : nsm;
   dq_stored_kernel<<<grid, kQsThreads, smem, s>>>(mDS, mK, mKp, P);
   return cudaGetLastError();
 }

@@ -40,7 +40,7 @@ struct DevStatus {
   int32_t code;   // VS_OK or VS_ERR_TIMEOUT
   int32_t where;  // a wait that gave up: kernel tag * 100 + wait site
   int32_t path;   // backward: 1 when dQ was formed from stored dS tiles
-  int32_t pad;
+  int32_t passes; // backward: the stored-dS passes that ran (key/value head groups split)
   // Cycles spent blocked at each wait site of the attention kernels, summed
   // over CTAs (lane 0 of each waiting warp), and the kernels' total cycles
   // per CTA in slot 31: a pipeline-balance diagnostic read by profiling tools.

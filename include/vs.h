@@ -253,12 +253,18 @@ VS_API vs_status vs_sparse_attn_fwd_rows(const vs_params* p, const vs_index* ind
  * VS_ERR_WORKSPACE.  Bytes beyond that hold the dS tiles (bf16, 2 bytes per
  * active 64 x 64 block entry): the dK / dV pass stores every active block it
  * forms and dQ is computed from them, without forming S and dP a second
- * time.  If the index needs more blocks than the workspace holds (decided on
- * the device, per call), dQ recomputes them instead; the results agree
- * within the stated tolerance either way.  vs_workspace_bytes(p, VS_OP_BWD)
- * suggests room for a budget-fill index of density p->density (1.5x, 2x with
- * index_mode 1), and the minimum for top-p selection or when that would
- * exceed 32 GiB.
+ * time.  When the room cannot hold every head's expected blocks (a
+ * budget-fill index of density p->density: 1.5x its share of the causal
+ * blocks, 2x with index_mode 1, plus four vertical chunks per query block),
+ * the call runs in passes over whole key/value head groups, as few as give
+ * each head that room; the blocks of one pass are stored and read back
+ * before the next reuses the room.  For top-p selection (density 0) it runs
+ * one pass.  If the index needs more blocks per head than the room gives
+ * (decided on the device, per call), dQ recomputes them instead; the
+ * results agree within the stated tolerance either way (and are the same
+ * bits for any number of passes).  vs_workspace_bytes(p, VS_OP_BWD) suggests
+ * room for the expected blocks of every head in one pass up to 32 GiB, else
+ * for the fewest passes whose blocks take at most 96 GiB, else the minimum.
  */
 VS_API vs_status vs_sparse_attn_bwd(const vs_params* p, const vs_index* index, const void* Q, const void* K,
                              const void* V, const void* O, const float* lse, const void* dO, void* dQ,

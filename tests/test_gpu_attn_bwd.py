@@ -48,12 +48,13 @@ def _ws_bytes(vs, w, stripes, ws_density):
 
 
 def _fwd_bwd(w, index, stripes=1, density=0.0, O_lse=None, ws_density=WS_ALL, want_path=None, ws_trim=0,
-             params_kw=None):
+             params_kw=None, want_passes=None):
     """GPU backward; O / LSE from the GPU forward, or injected (O_lse).
     ws_density sizes the backward workspace (see WS_*), less ws_trim bytes
     from its end (the dS blocks sit last); want_path, when given, is the dQ
-    path the status word must report (1 stored, 0 recomputed); params_kw
-    adds fields of vs_params (e.g. rope_mode)."""
+    path the status word must report (1 stored, 0 recomputed), want_passes
+    the number of stored-dS passes; params_kw adds fields of vs_params (e.g.
+    rope_mode)."""
     import torch
     import dynamic_sparse_attention_index_gb300 as vs
     dev = torch.device("cuda:0")
@@ -84,10 +85,12 @@ def _fwd_bwd(w, index, stripes=1, density=0.0, O_lse=None, ws_density=WS_ALL, wa
     vs.vs_sparse_attn_bwd(p, ix, Q, K, V, O, lse, dO, dQ, dK, dV, wsb)
     torch.cuda.synchronize()
     path = int(wsb[8:12].view(torch.int32).item())
+    passes = int(wsb[12:16].view(torch.int32).item())
     assert wsf is None or vs.vs_device_status(wsf) == vs.VS_OK
     assert vs.vs_device_status(wsb) == vs.VS_OK
     if want_path is not None:
         assert path == want_path, ("dQ path", path, want_path)
+    assert passes == (0 if path == 0 else (want_passes or 1)), ("passes", passes, want_passes)
     return ix, [f64(bf16_bits_of(t)) for t in (dQ, dK, dV)]
 
 
@@ -236,6 +239,32 @@ def test_bwd_stored_ds_overflow_falls_back():
     emu = oracle.attention_backward_bf16_products(q, k, v, do, index)
     for name, g, r, e in zip(("dQ", "dK", "dV"), got, ref, emu):
         grad_close(name, g, r, e)
+
+
+@pytest.mark.parametrize("Hq,Hkv,hpp,passes", [(8, 4, 2, 4), (6, 3, 4, 2), (3, 3, 1, 3), (16, 2, 8, 2)])
+def test_bwd_stored_ds_in_passes(Hq, Hkv, hpp, passes):
+    """A workspace whose dS room holds the expected blocks of hpp heads
+    only: the backward runs in passes over key/value head groups (4, 2 with
+    an uneven last pass, 3 with unpaired heads, 2), every pass on the stored
+    path; gradients against the oracle, and the same bits as one pass with
+    room for every head."""
+    dens = 0.3
+    w = synth.make_workload(3, L=2048, Hq=Hq, Hkv=Hkv, d=128, backward=True)
+    index, _, _ = oracle.build_index(f64(w.q), f64(w.k), 64, 0.95, density=dens)
+    q, k, v, do = f64(w.q), f64(w.k), f64(w.v), f64(w.do)
+    O_lse = oracle.attention_forward(q, k, v, index)
+    # the suggested room gives every head cap blocks; keep hpp heads' worth
+    nb = w.L // 64
+    cap = int(1.5 * dens * nb * (nb + 1) / 2 + 4 * nb) + 1
+    trim = (w.Hq - hpp) * cap * 64 * 64 * 2
+    _, got = _fwd_bwd(w, index, density=dens, O_lse=O_lse, ws_density=dens, want_path=1, ws_trim=trim,
+                      want_passes=passes)
+    _, one = _fwd_bwd(w, index, density=dens, O_lse=O_lse, ws_density=dens, want_path=1)
+    ref = oracle.attention_backward(q, k, v, do, index)
+    emu = oracle.attention_backward_bf16_products(q, k, v, do, index)
+    for name, g, o, r, e in zip(("dQ", "dK", "dV"), got, one, ref, emu):
+        grad_close(name, g, r, e)
+        np.testing.assert_array_equal(g, o, err_msg=name)
 
 
 def test_bwd_striped_32_shards():
