@@ -461,7 +461,10 @@ def run_gpu(args):
     peak, peak_s = pk["bf16_tflops"], pk["bf16_tflops_sustained"]
     kps = dict(KERNELS_PER_STEP if bwd else KERNELS_PER_STEP_FWD)
     if dq_stored:
-        kps["bwd"] += 2  # the dS plan and the dQ kernel that reads the tiles (the recomputing one returns at once)
+        # the dS plan and, per pass over KV-head groups, the dQ kernel that
+        # reads the tiles (the recomputing one returns at once) and, after
+        # the first pass, the two dK / dV kernels again
+        kps["bwd"] += 1 + dq_passes + 2 * (dq_passes - 1)
     if ring:
         # ring setup (shard lists, band bitmaps, a vertical union and packed
         # rows per shard) and W x W steps: one forward kernel per step; D, the
