@@ -47,7 +47,8 @@ __all__ = [
     "bf16_round", "rope_inv_freq", "rope_mscale", "rope", "index_scores",
     "select_top_p", "select_budget", "build_index", "active_entries",
     "sparsity_ratio", "explicit_mask", "attention_forward", "attention_backward",
-    "attention_forward_rows", "attention_backward_dq_rows", "total_causal_entries",
+    "attention_forward_rows", "attention_backward_dq_rows", "attention_backward_dkdv_keys",
+    "total_causal_entries",
     "attention_backward_bf16_products", "striped_ring_forward", "striped_ring_backward",
     "group_shared_index",
 ]
@@ -378,6 +379,52 @@ def attention_backward(Q, K, V, dO, index, scale=None, stripes=1, block=64):
             dQ[r, h, :] = scale * (dS @ kh)
             dK[:, g, :] += scale * (dS.T @ Q[r, h, :])
     return dQ, dK, dV
+
+
+def attention_backward_dkdv_keys(Q, K, V, dO, index, keys, scale=None, stripes=1, block=64):
+    """dK and dV of the listed key rows only (same definitions as
+    ``attention_backward``): each query row n whose mask reaches one of the
+    keys takes its full masked softmax P_n, dP_n = dO_n V^T and
+    dS_n = P_n * (dP_n - P_n . dP_n), and adds P_nm dO_n to dV_m and
+    scale dS_nm q_n to dK_m, summed over the query heads of the key's group.
+    The rows visited are a superset of those reaching the keys (rows outside
+    a key's mask add zero there): the row tiles ``t + B`` for each listed
+    key's tile t and kept band B, and, when a listed key is a kept vertical,
+    every row from that key on.  Returns dK, dV [len(keys), Hkv, d]."""
+    Q = np.asarray(Q, np.float64)
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    dO = np.asarray(dO, np.float64)
+    L, Hq, d = Q.shape
+    Hkv = K.shape[1]
+    G = Hq // Hkv
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    bs = block * stripes
+    nbs = L // bs
+    keys = np.asarray(keys, np.int64)
+    dK = np.zeros((keys.size, Hkv, d))
+    dV = np.zeros((keys.size, Hkv, d))
+    for h in range(Hq):
+        Vh, Sh = index[h]
+        g = h // G
+        kh, vh = K[:, g, :], V[:, g, :]
+        tiles = (np.unique(keys // bs)[:, None] + np.asarray(Sh, np.int64)[None, :]).ravel()
+        tiles = np.unique(tiles[tiles < nbs])
+        rows = (tiles[:, None] * bs + np.arange(bs)[None, :]).ravel()
+        vert = keys[np.isin(keys, np.asarray(Vh, np.int64))]
+        if vert.size:
+            rows = np.union1d(rows, np.arange(vert.min(), L))
+        for r in _chunks(L, rows):
+            msk = _row_mask(r, L, Vh, Sh, bs)
+            s = np.where(msk, scale * (Q[r, h, :] @ kh.T), -np.inf)
+            p = np.exp(s - s.max(axis=1, keepdims=True))
+            p /= p.sum(axis=1, keepdims=True)
+            dP = dO[r, h, :] @ vh.T
+            dS = p * (dP - (p * dP).sum(axis=1, keepdims=True))
+            dV[:, g, :] += p[:, keys].T @ dO[r, h, :]
+            dK[:, g, :] += scale * (dS[:, keys].T @ Q[r, h, :])
+    return dK, dV
 
 
 def attention_backward_bf16_products(Q, K, V, dO, index, scale=None, stripes=1, block=64):

@@ -140,6 +140,30 @@ def test_dq_rows_matches_full_backward():
     np.testing.assert_allclose(attention_backward_dq_rows(Q, K, V, dO, index, rows), dQ[rows], atol=1e-13)
 
 
+@pytest.mark.parametrize("stripes", [1, 2])
+def test_dkdv_keys_matches_full_backward(stripes):
+    """dK / dV of listed keys against the full backward: keys in the first,
+    a middle and the last tile, kept verticals among them (rows from the
+    vertical on), GQA 4 / 2, and the striped tiles."""
+    from oracle import attention_backward_dkdv_keys
+    L, Hq, Hkv, d = 512, 4, 2, 8
+    Q, K, V, dO = _inputs(L, Hq, Hkv, d, 41 + stripes)
+    rng = np.random.default_rng(6)
+    nbs = L // (64 * stripes)
+    index = [(np.sort(np.union1d(rng.choice(L, 9, replace=False), [200])),
+              np.union1d(rng.choice(nbs, 2, replace=False), [0])) for _ in range(Hq)]
+    _, dK, dV = attention_backward(Q, K, V, dO, index, stripes=stripes)
+    verts = np.unique(np.concatenate([V_ for V_, _ in index]))
+    plain = np.setdiff1d([0, 3, 63, 201, 330, 448, 500, 511], verts)
+    # keys that are no head's vertical (rows only from the kept bands), then
+    # with two verticals among them (rows from the earlier one on)
+    assert verts[0] < 200
+    for keys in (plain, np.union1d(plain, [verts[0], 200])):
+        gK, gV = attention_backward_dkdv_keys(Q, K, V, dO, index, keys, stripes=stripes)
+        np.testing.assert_allclose(gK, dK[keys], atol=1e-13)
+        np.testing.assert_allclose(gV, dV[keys], atol=1e-13)
+
+
 def test_gradient_column_identities():
     """Identities used for full-size checks: summed over keys, dV equals the
     sum of dO over the rows of the group's heads (softmax rows sum to 1), and
