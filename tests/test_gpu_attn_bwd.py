@@ -276,17 +276,25 @@ def test_bwd_striped_32_shards():
 def test_bwd_full_size_gqa_128k():
     """The 128K GQA training workload at full size under the oracle's
     budget-fill index (forward then backward on the GPU, as in a training
-    step): dQ on sampled rows against the oracle, dK / dV through identities
-    that hold for any mask (keys summed: dV -> sum of dO over the group's
-    rows, dK -> 0)."""
+    step): dQ on sampled rows and dK / dV of the keys of two blocks near the
+    end against the oracle, all keys' dK / dV through identities that hold
+    for any mask (keys summed: dV -> sum of dO over the group's rows,
+    dK -> 0)."""
     w = synth.make_workload(3)
     index, _, _ = oracle.build_index(f64(w.q), f64(w.k), 64, 0.95, density=float(np.float32(0.05)))
     rows = np.concatenate([np.arange(0, 64), np.arange(65536, 65536 + 64), np.arange(w.L - 64, w.L)])
-    rQ = oracle.attention_backward_dq_rows(f64(w.q), f64(w.k), f64(w.v), f64(w.do), index, rows)
+    q, k, v, do = f64(w.q), f64(w.k), f64(w.v), f64(w.do)
+    rQ = oracle.attention_backward_dq_rows(q, k, v, do, index, rows)
+    # dK / dV of the keys of two blocks near the end (few rows reach them)
+    nb = w.L // 64
+    keys = np.concatenate([np.arange((nb - 8) * 64, (nb - 7) * 64), np.arange((nb - 1) * 64, nb * 64)])
+    rK, rV = oracle.attention_backward_dkdv_keys(q, k, v, do, index, keys)
     # the bench's workspace (room for the dS tiles of density 0.05), then the minimum
     for ws_density, path in ((0.05, 1), (WS_MIN, 0)):
         ix, (dQ, dK, dV) = _fwd_bwd(w, index, ws_density=ws_density, want_path=path)
         _check_full(w, dQ, dK, dV, rows, rQ)
+        _close(dK[keys], rK, "dK keys")
+        _close(dV[keys], rV, "dV keys")
 
 
 def _check_full(w, dQ, dK, dV, rows, rQ):
