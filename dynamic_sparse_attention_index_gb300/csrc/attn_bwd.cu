@@ -886,7 +886,7 @@ BwdWs bwd_layout(const AttnGeom& g, long long cap, int hpp) {
     o.ds_rank = w.take((size_t)g.Hq * g.nbs * 4);
     o.ds_base_s = w.take((size_t)g.Hq * g.nb * 4);
     o.ds_base_v = w.take((size_t)g.Hq * g.nb * 4);
-    o.ds = w.take((size_t)hpp * (size_t)cap * kDsBlockBytes);
+    o.ds = w.take(((size_t)hpp * (size_t)cap + 1) * kDsBlockBytes);  // and the zero block
   }
   o.total = w.off;
   return o;
@@ -909,8 +909,9 @@ double ds_blocks_expected(const vs_params& p, const AttnGeom& g) {
   return f * p.density * (double)g.nb * (g.nb + 1) / 2.0 + 4.0 * g.nb;
 }
 
-// Block rows of the dS tensor map stay below 2^31 (TMA coordinates).
-long long ds_row_cap(int hpp) { return (2147483647LL / 64) / hpp; }
+// Block rows of the dS tensor map (hpp cap blocks and the zero block) stay
+// below 2^31 (TMA coordinates).
+long long ds_row_cap(int hpp) { return (2147483647LL / 64 - 1) / hpp; }
 
 // The split a workspace of ws_bytes allows: one pass over every head when
 // the expected blocks fit (or when none are expected: top-p), else the
@@ -921,7 +922,7 @@ DsSplit ds_split_for(const vs_params& p, const AttnGeom& g, size_t ws_bytes) {
   DsSplit sp;
   const BwdWs one = bwd_layout(g, 1, 1);
   if (ws_bytes < one.total) return sp;
-  const size_t room = ws_bytes - one.ds;
+  const size_t room = ws_bytes - one.ds - kDsBlockBytes;  // less the zero block
   const double want = ds_blocks_expected(p, g);
   for (int n = 1; n <= g.Hkv; ++n) {
     const int gpp = (g.Hkv + n - 1) / n;
@@ -989,7 +990,8 @@ cudaError_t launch_dkdv_heads(const vs_params& p, const AttnGeom& g, const PrepP
       !make_map_rows(&mVp, pp.Vp, (long long)g.nvg * g.L, 128))
     return cudaErrorInvalidValue;
   // the stored dS blocks (a map the kernel never touches when there are none)
-  if (ds ? !make_map_rows(&mDS, ds->ds, (long long)ds->hpp * ds->cap * 64, 64) : false) return cudaErrorInvalidValue;
+  if (ds ? !make_map_rows(&mDS, ds->ds, ((long long)ds->hpp * ds->cap + 1) * 64, 64) : false)
+    return cudaErrorInvalidValue;
   if (!ds) mDS = mKp;
   BwdParams P;
   P.g = g;
@@ -1087,6 +1089,8 @@ cudaError_t launch_attn_bwd(const vs_params& p, const vs_index& ix, const void* 
   d.ds = reinterpret_cast<__nv_bfloat16*>(w + lay.ds);
   d.cap = (int)cap;
   d.hpp = sp.gpp * g.G;
+  d.zero_blk = d.hpp * d.cap;
+  if ((e = cudaMemsetAsync(d.ds + (size_t)d.zero_blk * 64 * 64, 0, kDsBlockBytes, s)) != cudaSuccess) return e;
   if ((e = launch_ds_plan(g, pp, d, s)) != cudaSuccess) return e;
   for (int kv_lo = 0; kv_lo < g.Hkv; kv_lo += sp.gpp) {
     const int kv_n = g.Hkv - kv_lo < sp.gpp ? g.Hkv - kv_lo : sp.gpp;

@@ -204,15 +204,16 @@ cudaError_t launch_attn_dq(const vs_params& p, const AttnGeom& g, const PrepPtrs
 // (hpp = heads per pass, a multiple of Hq / Hkv; one pass when everything
 // fits): the blocks of one pass's heads are stored and read back before the
 // next pass reuses the room, and head h owns blocks [(h mod hpp) cap,
-// (h mod hpp + 1) cap).
+// (h mod hpp + 1) cap); one more block after them holds zeros.
 struct DsPlan {
   int32_t* ok;         // device word: non-zero while every head's blocks fit in cap
   int32_t* band_rank;  // [Hq][nbs]: kept bands of head h in [1, B]
   int32_t* base_s;     // [Hq][nb]: first block of (h, I)
   int32_t* base_v;     // [Hq][nb]: first vertical-chunk block of (h, I)
-  __nv_bfloat16* ds;   // [hpp cap][64][64] blocks
+  __nv_bfloat16* ds;   // [hpp cap + 1][64][64] blocks
   int cap;             // blocks per head
   int hpp;             // query heads per pass
+  int zero_blk;        // hpp cap: a block of zeros (the rows of a segment a source does not reach)
 };
 constexpr int kDsBlockBytes = 64 * 64 * 2;
 

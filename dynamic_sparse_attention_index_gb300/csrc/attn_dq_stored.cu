@@ -107,6 +107,7 @@ struct DqsParams {
   const int32_t* base_v;
   const int32_t* ok;
   __nv_bfloat16* dq;
+  int zero_blk;     // the block of zeros
   int kv_lo, kv_n;  // this pass: the row tiles of key/value heads [kv_lo, kv_lo + kv_n)
   int nitems;       // their number
   float scale;
@@ -392,8 +393,8 @@ __global__ void __launch_bounds__(kQsThreads, 1)
     }
   } else if (warp == 3) {
     // ------------------------------------------------------------ loader
-    // One tile per record: zeros for the inactive (source, segment) dS
-    // blocks, then the TMA loads of the active ones and of the K tiles.
+    // One tile per record: the TMA loads of its dS blocks (the block of
+    // zeros for a segment the source does not reach) and of its K tiles.
     if (lane == 0) {
       tma_prefetch_desc(&mDS);
       tma_prefetch_desc(&mK);
@@ -424,35 +425,24 @@ __global__ void __launch_bounds__(kQsThreads, 1)
       if (kWaitProfileDs) pc[3] += e1 - r0;
       uint8_t* a = sm + st * kStageBytes + kStageA;
       uint8_t* bb = sm + st * kStageBytes + kStageB;
-      // zeros where a segment has no entries of the source
-      auto zero8k = [&](uint8_t* z) {
-        uint4* zz = reinterpret_cast<uint4*>(z);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) zz[k * 32 + lane] = make_uint4(0u, 0u, 0u, 0u);
-      };
-      const bool z00 = b00 < 0, z01 = b01 < 0, z10 = nsrc > 1 && b10 < 0, z11 = nsrc > 1 && b11 < 0;
-      if (z00) zero8k(a);
-      if (z01) zero8k(a + 8192);
-      if (z10) zero8k(a + kHalf);
-      if (z11) zero8k(a + kHalf + 8192);
-      if (z00 || z01 || z10 || z11) fence_proxy_async_smem();
-      if (kWaitProfileDs) pc[5] += (int)z00 + (int)z01 + (int)z10 + (int)z11;
+      if (kWaitProfileDs) pc[5] += (int)(b00 < 0) + (int)(b01 < 0) + (nsrc > 1 ? (int)(b10 < 0) + (int)(b11 < 0) : 0);
       if (lane == 0) {
-        const int nload = (int)!z00 + (int)!z01 + (nsrc > 1 ? (int)!z10 + (int)!z11 : 0);
         word[st] = wd;
-        mbar_arrive_expect_tx(&full[st], (uint32_t)(2 * nsrc + nload) * 8192u);
+        mbar_arrive_expect_tx(&full[st], (uint32_t)(4 * nsrc) * 8192u);
       }
       __syncwarp();
       // one copy per lane: lanes 0-3 the dS blocks (source l / 2, segment
       // l % 2), lanes 4-7 the K tiles (source (l - 4) / 2, d half l % 2)
-      // the dS blocks are read once (evict first); K tiles are re-read by
-      // every row tile whose sources include them (evict last)
+      // the dS blocks are read once (evict first); K tiles, re-read by
+      // every row tile whose sources include them, and the block of zeros
+      // stay (evict last)
       if (lane < 8) {
         const int j = (lane >> 1) & 1, k = lane & 1;
         if (j < nsrc) {
           if (lane < 4) {
             const int blk = j ? (k ? b11 : b10) : (k ? b01 : b00);
-            if (blk >= 0) tma_load_2d_hint(a + j * kHalf + k * 8192, &mDS, &full[st], 0, blk * 64, pol_stream);
+            tma_load_2d_hint(a + j * kHalf + k * 8192, &mDS, &full[st], 0, (blk >= 0 ? blk : P.zero_blk) * 64,
+                             blk >= 0 ? pol_stream : pol_keep);
           } else {
             const int src = j ? s1 : s0;
             uint8_t* kd = bb + k * kHalf + j * 8192;
@@ -617,7 +607,7 @@ cudaError_t launch_dq_stored(const vs_params& p, const AttnGeom& g, const PrepPt
                              const DsPlan& d, void* dQ, DevStatus* st, int kv_lo, int kv_n, cudaStream_t s) {
   CUtensorMap mDS, mK, mKp;
   if (kv_lo < 0 || kv_n < 1 || kv_lo + kv_n > g.Hkv) return cudaErrorInvalidValue;
-  if (!make_map_rows(&mDS, d.ds, (long long)d.hpp * d.cap * 64, 64) ||
+  if (!make_map_rows(&mDS, d.ds, ((long long)d.hpp * d.cap + 1) * 64, 64) ||
       !make_map_heads(&mK, K, g.L, g.Hkv, 128) || !make_map_rows(&mKp, pp.Kp, (long long)g.nvg * g.L, 128))
     return cudaErrorInvalidValue;
   DqsParams P;
@@ -629,6 +619,7 @@ cudaError_t launch_dq_stored(const vs_params& p, const AttnGeom& g, const PrepPt
   P.base_v = d.base_v;
   P.ok = d.ok;
   P.dq = static_cast<__nv_bfloat16*>(dQ);
+  P.zero_blk = d.zero_blk;
   P.kv_lo = kv_lo;
   P.kv_n = kv_n;
   P.nitems = g.nitems / g.Hkv * kv_n;
