@@ -267,6 +267,25 @@ def test_bwd_stored_ds_in_passes(Hq, Hkv, hpp, passes):
         np.testing.assert_array_equal(g, o, err_msg=name)
 
 
+def test_bwd_stored_ds_passes_rope_mode_striped():
+    """Four stored-dS passes with rope_mode = 1 (the RoPE adjoint of dQ in
+    the epilogue of every pass's dQ kernel, dK's after the last pass) on
+    striped tiles (W = 2): the same bits as one pass."""
+    dens = 0.3
+    w = synth.make_workload(4, L=2048, Hq=8, Hkv=4, d=128, backward=True)
+    index, _, _ = oracle.build_index(f64(w.q), f64(w.k), 64, 0.95, stripes=2, density=dens)
+    q, k, v = f64(w.q), f64(w.k), f64(w.v)
+    O_lse = oracle.attention_forward(q, k, v, index, stripes=2)
+    nb = w.L // 64
+    cap = int(1.5 * dens * nb * (nb + 1) / 2 + 4 * nb) + 1
+    kw = dict(rope_mode=1, rope_theta=1e4)
+    _, got = _fwd_bwd(w, index, stripes=2, density=dens, O_lse=O_lse, ws_density=dens, want_path=1,
+                      ws_trim=(w.Hq - 2) * cap * 64 * 64 * 2, params_kw=kw, want_passes=4)
+    _, one = _fwd_bwd(w, index, stripes=2, density=dens, O_lse=O_lse, ws_density=dens, want_path=1, params_kw=kw)
+    for name, g, o in zip(("dQ", "dK", "dV"), got, one):
+        np.testing.assert_array_equal(g, o, err_msg=name)
+
+
 def test_bwd_striped_32_shards():
     w = synth.make_workload(4, L=4096, Hq=2, Hkv=1, d=128, backward=True)
     index, _, _ = oracle.build_index(f64(w.q), f64(w.k), 64, 0.9, stripes=32)
