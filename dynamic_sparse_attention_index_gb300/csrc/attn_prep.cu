@@ -3,6 +3,8 @@
 // and per-block prefix counts, and the packed K/V rows of those verticals.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+
 #include "attn_common.cuh"
 
 namespace vs {
@@ -100,33 +102,26 @@ __global__ void __launch_bounds__(1024) prep_vunion_kernel(AttnGeom g, const int
 __global__ void prep_pack_kernel(AttnGeom g, const __nv_bfloat16* __restrict__ K, const __nv_bfloat16* __restrict__ V,
                                  const uint32_t* __restrict__ vlist, const int32_t* __restrict__ vcnt,
                                  __nv_bfloat16* __restrict__ Kp, __nv_bfloat16* __restrict__ Vp) {
-  const int lanes_per_row = g.d / 8;  // 16-byte pieces
-  const long long gtid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  // blockIdx.y: the union group; its rows up to the end of the last 64-row
+  // chunk, 16 bytes a thread
+  const int vg = blockIdx.y;
+  const int lanes_per_row = g.d / 8;
+  const int cnt = vcnt[(size_t)vg * (g.nb + 1) + g.nb];
+  const long long total = (long long)((cnt + 63) & ~63) * lanes_per_row;
+  const int kv = g.pair_heads ? vg / (g.G / 2) : vg / g.G;
   const long long stride = (long long)gridDim.x * blockDim.x;
-  const long long total = (long long)g.nvg * g.L * lanes_per_row;
-  for (long long t = gtid; t < total; t += stride) {
+  for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += stride) {
     const int piece = (int)(t % lanes_per_row);
-    const long long row = t / lanes_per_row;
-    const int vg = (int)(row / g.L);
-    const int u = (int)(row % g.L);
-    const int cnt = vcnt[(size_t)vg * (g.nb + 1) + g.nb];
+    const int u = (int)(t / lanes_per_row);
     const size_t dst = ((size_t)vg * g.L + u) * g.d + piece * 8;
     if (u >= cnt) {
       // zero the tail of the last 64-row chunk: masked columns there are
       // multiplied by P = 0 and must hold finite values
-      if (u < ((cnt + 63) & ~63)) {
-        *reinterpret_cast<uint4*>(Kp + dst) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(Vp + dst) = make_uint4(0, 0, 0, 0);
-      }
+      *reinterpret_cast<uint4*>(Kp + dst) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(Vp + dst) = make_uint4(0, 0, 0, 0);
       continue;
     }
     const int m = (int)(vlist[(size_t)vg * g.L + u] & kVTokenMask);
-    int kv;
-    if (g.pair_heads) {
-      kv = vg / (g.G / 2);
-    } else {
-      kv = vg / g.G;
-    }
     const size_t src = ((size_t)g.tk(m) * g.Hkv + kv) * g.d + piece * 8;
     *reinterpret_cast<uint4*>(Kp + dst) = *reinterpret_cast<const uint4*>(K + src);
     *reinterpret_cast<uint4*>(Vp + dst) = *reinterpret_cast<const uint4*>(V + src);
@@ -209,7 +204,9 @@ cudaError_t launch_prep_verticals(const AttnGeom& g, const vs_index& ix, const v
   prep_vunion_kernel<<<g.nvg, 1024, sm, s>>>(g, ix.v_idx, ix.v_cnt, pp.vlist, pp.vcnt, pp.vbits);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  prep_pack_kernel<<<152 * 8, 256, 0, s>>>(g, static_cast<const __nv_bfloat16*>(K),
+  // about eight 256-thread blocks per SM over all union groups
+  const dim3 grid((unsigned)std::max(1, 152 * 8 / g.nvg), (unsigned)g.nvg);
+  prep_pack_kernel<<<grid, 256, 0, s>>>(g, static_cast<const __nv_bfloat16*>(K),
                                            static_cast<const __nv_bfloat16*>(V), pp.vlist, pp.vcnt, pp.Kp, pp.Vp);
   return cudaGetLastError();
 }
